@@ -1,0 +1,200 @@
+"""The CPU oracle for the forward 2-D convolution -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and this
+package never imports the library: the two share no code.
+
+Contents
+  * ``conv2d`` / ``conv2d_at``: the plain nested-loop definition (C, built with
+    gcc into ``oracle/_build``), double accumulation, float32 epilogue.  See the
+    header of ``conv_oracle.c`` for the passages it follows.
+  * ``im2col.py``: a second, independent brute force (unfold, then one matrix
+    product per group), written in numpy ("Convolutions", sections 2.4 and 3).
+  * ``arith.py``: output size, MAC and parameter counts as closed forms
+    ("Convolutions", sections 2.1 and 2.3).
+  * number-format helpers: exact half / bfloat16 decoding and round-to-even
+    encoding, used by the parity checks.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_lock = threading.Lock()
+_libs: dict[int, ctypes.CDLL] = {}
+
+ACTIVATIONS = ("identity", "relu", "silu", "sigmoid", "tanh", "hard_swish",
+               "hard_sigmoid", "clip", "leaky_relu")
+_ACT_CODE = {name: i for i, name in enumerate(ACTIVATIONS)}
+DTYPES = ("f32", "f16", "bf16")
+_DT_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def library_path(mutant: int = 0) -> str:
+    name = "libconv_oracle.so" if mutant == 0 else f"libconv_oracle_mutant{mutant}.so"
+    return os.path.join(_BUILD, name)
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the C oracle with gcc (no fused multiply-add, so the float32
+    epilogue rounds each step on every host).  ``mutant`` > 0 plants one
+    deliberate mistake; the pin tests use those builds to show they catch it."""
+    out = library_path(mutant)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-pthread", f"-DORACLE_MUTANT={mutant}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _load(mutant: int = 0) -> ctypes.CDLL:
+    with _lock:
+        if mutant in _libs:
+            return _libs[mutant]
+        lib = ctypes.CDLL(build(mutant))
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        vp = ctypes.c_void_p
+        lib.oracle_conv2d.argtypes = [i64p, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
+        lib.oracle_conv2d.restype = ctypes.c_int
+        lib.oracle_conv2d_at.argtypes = [i64p, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                         ctypes.c_int, vp, vp, vp, vp, i64p, ctypes.c_int64,
+                                         vp, vp, vp, vp, ctypes.c_int]
+        lib.oracle_conv2d_at.restype = ctypes.c_int
+        lib.oracle_output_extent.argtypes = [ctypes.c_int64] * 6
+        lib.oracle_output_extent.restype = ctypes.c_int64
+        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_half_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_half.restype = ctypes.c_uint16
+        lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_activation.argtypes = [ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                          ctypes.c_float]
+        lib.oracle_activation.restype = ctypes.c_float
+        lib.oracle_mutant.restype = ctypes.c_int
+        _libs[mutant] = lib
+        return lib
+
+
+class Oracle:
+    """Handle on one build of the C oracle (the real one, or a planted mutant)."""
+
+    def __init__(self, mutant: int = 0):
+        self.lib = _load(mutant)
+        self.mutant = mutant
+
+    # --- closed forms -------------------------------------------------------
+    def output_extent(self, size, k, pad_begin, pad_end, stride=1, dilation=1) -> int:
+        return int(self.lib.oracle_output_extent(size, k, pad_begin, pad_end, stride, dilation))
+
+    def activation(self, act: str, t: float, alpha: float = 0.0, beta: float = 0.0) -> float:
+        return float(self.lib.oracle_activation(_ACT_CODE[act], t, alpha, beta))
+
+    def half_to_double(self, bits: int) -> float:
+        return float(self.lib.oracle_half_to_double(bits))
+
+    def bf16_to_double(self, bits: int) -> float:
+        return float(self.lib.oracle_bf16_to_double(bits))
+
+    def float_to_half(self, f: float) -> int:
+        return int(self.lib.oracle_float_to_half(f))
+
+    def float_to_bf16(self, f: float) -> int:
+        return int(self.lib.oracle_float_to_bf16(f))
+
+    # --- the convolution ----------------------------------------------------
+    def conv2d(self, x, w, bias=None, residual=None, *, dtype="f32", stride=(1, 1),
+               pads=(0, 0, 0, 0), dilation=(1, 1), groups=1, act="identity",
+               alpha=0.0, beta=0.0, nthreads=None, index=None):
+        """Evaluate the definition.
+
+        x: (N, Cin, H, W) and w: (Cout, Cin/groups, kh, kw) numpy arrays --
+        float32 for dtype "f32", uint16 bit patterns for "f16" / "bf16".
+        bias: (Cout,), residual: (N, Cout, Ho, Wo), same element type.
+        pads are ONNX order (top, left, bottom, right).
+        index: optional 1-D int64 array of NCHW linear output indices; then
+        only those outputs are computed (flat arrays of len(index) returned).
+
+        Returns dict(y=..., t=float32 epilogue result, acc=double sum,
+        scale=double sum of |w x|) with shape (N, Cout, Ho, Wo) or (len(index),).
+        """
+        geom, ho, wo = self.geometry(x.shape, w.shape, stride, pads, dilation, groups)
+        want = np.float32 if dtype == "f32" else np.uint16
+        arrs = [np.ascontiguousarray(a) if a is not None else None
+                for a in (x, w, bias, residual)]
+        for a in arrs:
+            if a is not None and a.dtype != want:
+                raise TypeError(f"oracle operand dtype {a.dtype}, expected {want} for {dtype}")
+        n, cout = x.shape[0], w.shape[0]
+        if arrs[2] is not None and arrs[2].shape != (cout,):
+            raise ValueError("bias shape")
+        if arrs[3] is not None and arrs[3].shape != (n, cout, ho, wo):
+            raise ValueError("residual shape")
+        shape = (n, cout, ho, wo) if index is None else (len(index),)
+        y = np.empty(shape, dtype=want)
+        t = np.empty(shape, dtype=np.float32)
+        acc = np.empty(shape, dtype=np.float64)
+        scale = np.empty(shape, dtype=np.float64)
+        nthreads = nthreads or os.cpu_count() or 1
+        g = (ctypes.c_int64 * 16)(*geom)
+        ptr = lambda a: a.ctypes.data if a is not None else None
+        common = (g, _ACT_CODE[act], alpha, beta, _DT_CODE[dtype],
+                  ptr(arrs[0]), ptr(arrs[1]), ptr(arrs[2]), ptr(arrs[3]))
+        if index is None:
+            rc = self.lib.oracle_conv2d(*common, ptr(y), ptr(t), ptr(acc), ptr(scale), nthreads)
+        else:
+            idx = np.ascontiguousarray(index, dtype=np.int64)
+            rc = self.lib.oracle_conv2d_at(
+                *common, idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(idx),
+                ptr(y), ptr(t), ptr(acc), ptr(scale), nthreads)
+        if rc != 0:
+            raise ValueError("geometry outside the definition")
+        return {"y": y, "t": t, "acc": acc, "scale": scale}
+
+    def geometry(self, xshape, wshape, stride, pads, dilation, groups):
+        n, cin, h, w_ = xshape
+        cout, cin_g, kh, kw = wshape
+        if cin_g * groups != cin:
+            raise ValueError("weight channels x groups != input channels")
+        pt, pl, pb, pr = pads
+        ho = self.output_extent(h, kh, pt, pb, stride[0], dilation[0])
+        wo = self.output_extent(w_, kw, pl, pr, stride[1], dilation[1])
+        geom = [n, cin, h, w_, cout, kh, kw, pt, pl, pb, pr,
+                stride[0], stride[1], dilation[0], dilation[1], groups]
+        return geom, ho, wo
+
+
+def to_float64(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact decode of an operand array to float64 (half / bfloat16 bit
+    patterns by their IEEE / bfloat16 definitions)."""
+    if dtype == "f32":
+        return a.astype(np.float64)
+    if dtype == "f16":
+        return a.view(np.float16).astype(np.float64)
+    bits = a.astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
+def ulp(y: np.ndarray, dtype: str) -> np.ndarray:
+    """One unit in the last place of the element type at |y| (the spacing of
+    representable values there; the subnormal spacing below the normal range)."""
+    mant_bits, min_exp = {"f32": (23, -126), "f16": (10, -14), "bf16": (7, -126)}[dtype]
+    a = np.abs(np.asarray(y, dtype=np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, min_exp)
+    return np.ldexp(1.0, (e - mant_bits).astype(np.int64))
