@@ -1,0 +1,448 @@
+// conv_api.cu -- the C ABI of libconv: validation, planning and dispatch.
+//
+// "Convolution, pooling and resize" (Layout and operands; Variants; split k)
+// describes the host side this follows: a problem struct carrying the shape,
+// explicit pads, dilation, groups and the fused activation; sizes checked with
+// checked arithmetic and the device's limits before anything is recorded; a
+// scratch query; a variant chosen from the problem and the device; a k split
+// that depends only on the shape; an error for scratch that overlaps an
+// operand.  Everything here runs on the host; conv_forward only enqueues.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "conv_internal.h"
+
+namespace conv {
+size_t tc_smem_bytes(int bn, int k_pad, int stages, int tap_major, long long stg_bytes);
+}
+
+using namespace conv;
+
+namespace {
+
+constexpr long long kI32 = 2147483647LL;
+constexpr int kMaxDevices = 64;
+constexpr size_t kMaxDynSmem = 232448;  // 227 KB per block on sm_100-class devices
+
+bool mul_ok(long long a, long long b, long long* out) {
+  return !__builtin_mul_overflow(a, b, out);
+}
+
+struct Shape {
+  long long ho, wo, cg, mg, K, npix, x_elems, w_elems, y_elems;
+};
+
+conv_status validate(const conv_problem* p, Shape* s) {
+  if (!p) return CONV_ERR_NULL;
+  if (p->dtype < CONV_F32 || p->dtype > CONV_BF16) return CONV_ERR_DTYPE;
+  if (p->act < CONV_ACT_IDENTITY || p->act > CONV_ACT_LEAKY_RELU) return CONV_ERR_ACT;
+  const long long pos[] = {p->n, p->c_in, p->h, p->w, p->c_out, p->kh, p->kw,
+                           p->stride_h, p->stride_w, p->dil_h, p->dil_w, p->groups};
+  for (long long v : pos)
+    if (v < 1) return CONV_ERR_SHAPE;
+  if (p->pad_top < 0 || p->pad_left < 0 || p->pad_bottom < 0 || p->pad_right < 0) return CONV_ERR_SHAPE;
+  if (p->c_in % p->groups || p->c_out % p->groups) return CONV_ERR_SHAPE;
+  long long span_h, span_w, ext_h, ext_w;
+  if (!mul_ok(p->dil_h, p->kh - 1, &span_h) || !mul_ok(p->dil_w, p->kw - 1, &span_w))
+    return CONV_ERR_OVERFLOW;
+  if (__builtin_add_overflow(p->h, p->pad_top, &ext_h) || __builtin_add_overflow(ext_h, p->pad_bottom, &ext_h) ||
+      __builtin_add_overflow(p->w, p->pad_left, &ext_w) || __builtin_add_overflow(ext_w, p->pad_right, &ext_w))
+    return CONV_ERR_OVERFLOW;
+  if (ext_h - 1 < span_h || ext_w - 1 < span_w) return CONV_ERR_SHAPE;  // no output position
+  s->ho = (ext_h - span_h - 1) / p->stride_h + 1;
+  s->wo = (ext_w - span_w - 1) / p->stride_w + 1;
+  s->cg = p->c_in / p->groups;
+  s->mg = p->c_out / p->groups;
+  long long t;
+  if (!mul_ok(s->cg, p->kh, &t) || !mul_ok(t, p->kw, &s->K)) return CONV_ERR_OVERFLOW;
+  if (!mul_ok(p->n, s->ho, &t) || !mul_ok(t, s->wo, &s->npix)) return CONV_ERR_OVERFLOW;
+  if (!mul_ok(p->n, p->c_in, &t) || !mul_ok(t, p->h, &t) || !mul_ok(t, p->w, &s->x_elems))
+    return CONV_ERR_OVERFLOW;
+  if (!mul_ok(p->c_out, s->K, &s->w_elems)) return CONV_ERR_OVERFLOW;
+  if (!mul_ok(s->npix, p->c_out, &s->y_elems)) return CONV_ERR_OVERFLOW;
+  if (!mul_ok(s->x_elems, 4, &t) || !mul_ok(s->y_elems, 4 * 64, &t) || !mul_ok(s->w_elems, 4, &t))
+    return CONV_ERR_OVERFLOW;  // byte counts (and split planes) fit int64
+  // kernel limits: per-image sizes and window offsets fit their 32-bit fields
+  long long per_img_in, per_img_out;
+  if (!mul_ok(p->c_in, p->h * p->w, &per_img_in) || per_img_in > kI32) return CONV_ERR_SHAPE;
+  if (!mul_ok(p->c_out, s->ho * s->wo, &per_img_out) || per_img_out > kI32) return CONV_ERR_SHAPE;
+  if (s->K > kI32 || p->h > kI32 || p->w > kI32 || p->pad_top > kI32 || p->pad_left > kI32 ||
+      p->stride_h > kI32 || p->stride_w > kI32 || p->n > kI32 || p->c_out > kI32)
+    return CONV_ERR_SHAPE;
+  if (span_h > 32767 || span_w > 32767) return CONV_ERR_SHAPE;  // packed window table fields
+  if (s->ho > kI32 || s->wo > kI32) return CONV_ERR_SHAPE;
+  return CONV_OK;
+}
+
+int occupancy_estimate(const FfmaCfg& c, size_t smem) {
+  const int t = c.threads();
+  const int regs = c.tm * c.tn + 48;
+  int occ = 2048 / t;
+  occ = std::min(occ, static_cast<int>(kMaxDynSmem / std::max<size_t>(smem, 1)));
+  occ = std::min(occ, 65536 / (t * regs));
+  return std::max(occ, 1);
+}
+
+void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
+  // Per-SM time model: an SM runs ceil(blocks / SMs) tiles of bm x bn outputs
+  // (padding included) at a rate set by the register tile, slowed when fewer
+  // than 8 warps are resident to hide latency.  Lowest time wins; ties go to
+  // the earlier (larger) tile.
+  double best = 0.0;
+  int bi = -1;
+  for (int i = 0; i < kNumFfmaCfgs; ++i) {
+    const FfmaCfg& c = kFfmaCfgs[i];
+    const long long tm = (s.mg + c.bm - 1) / c.bm, tn = (s.npix + c.bn - 1) / c.bn;
+    const long long ctas = tm * tn * p->groups;
+    if (tm * p->groups > 65535) continue;
+    const long long per_sm = (ctas + sm - 1) / sm;
+    const int occ = occupancy_estimate(c, ffma_smem_bytes(i, p->dtype));
+    const double warps = static_cast<double>(std::min<long long>(per_sm, occ)) * c.threads() / 32.0;
+    const double speed = ((c.tm == 8 && c.tn == 8) ? 1.0 : (c.tm * c.tn == 32 ? 0.85 : 0.6)) *
+                         std::min(1.0, warps / 8.0);
+    const double t = static_cast<double>(per_sm) * c.bm * c.bn / speed;
+    if (bi < 0 || t < best * (1.0 - 1e-9)) { best = t; bi = i; }
+  }
+  if (bi < 0) bi = 0;
+  const FfmaCfg& c = kFfmaCfgs[bi];
+  const long long ctas = ((s.mg + c.bm - 1) / c.bm) * ((s.npix + c.bn - 1) / c.bn) * p->groups;
+  // split k ("Convolution, pooling and resize", split k for small grids): a
+  // grid smaller than the device whose k has at least 256 terms runs k in at
+  // most 16 ranges of at least 128 terms, each a whole number of 8-term stages,
+  // aiming at about two blocks per SM; the cut is a function of (shape, SM
+  // count) only.
+  int split = 1;
+  const int forced = static_cast<int>((p->flags & CONV_FLAG_SPLIT_K_MASK) >> CONV_FLAG_SPLIT_K_SHIFT);
+  if (!(p->flags & CONV_FLAG_NO_SPLIT_K)) {
+    if (forced > 0) {
+      split = forced;
+    } else if (ctas < sm && s.K >= 256) {
+      const long long want = (2LL * sm + ctas - 1) / ctas;  // about two blocks per SM
+      split = static_cast<int>(std::min<long long>({16, s.K / 128, want}));
+    }
+  }
+  long long len = s.K;
+  if (split > 1) {
+    len = ((s.K + split - 1) / split + kFfmaBK - 1) / kFfmaBK * kFfmaBK;
+    split = static_cast<int>((s.K + len - 1) / len);
+  }
+  if (split <= 1) { split = 1; len = s.K; }
+  out->ffma_cfg = bi;
+  out->info.variant = split > 1 ? CONV_VARIANT_IGEMM_FFMA_SPLIT : CONV_VARIANT_IGEMM_FFMA;
+  out->info.split_k = split;
+  out->info.tile_m = c.bm;
+  out->info.tile_n = c.bn;
+  out->info.ctas = ctas * split;
+  out->info.scratch_bytes = split > 1 ? static_cast<uint64_t>(split) * s.y_elems * sizeof(float) : 0;
+  out->k_per_split = static_cast<int>(len);
+}
+
+bool plan_depthwise(const conv_problem* p, const Shape& s, Plan* out) {
+  constexpr int QW = 4;
+  DwPlan d;
+  d.lm = static_cast<int>((p->pad_left + 3) / 4 * 4);
+  const long long strips = (s.wo + QW - 1) / QW;
+  const long long need = d.lm - p->pad_left + (strips * QW - 1) * p->stride_w + (p->kw - 1) * p->dil_w + 1;
+  long long row = std::max<long long>(d.lm + p->w, need);
+  row = (row + 3) / 4 * 4;
+  const long long wfl = (s.mg * p->kh * p->kw + 3) / 4 * 4;
+  const long long budget = 40 * 1024 / 4 - wfl;  // floats
+  if (row > 1 << 20 || budget <= 0) return false;
+  long long th = s.ho;
+  auto in_rows = [&](long long t) { return (t - 1) * p->stride_h + (p->kh - 1) * p->dil_h + 1; };
+  while (th > 1 && in_rows(th) * row > budget) th = (th + 1) / 2;
+  if (in_rows(th) * row > budget) return false;
+  d.th = static_cast<int>(th);
+  d.in_rows = static_cast<int>(in_rows(th));
+  d.row = static_cast<int>(row);
+  d.vec = 0;
+  d.threads = 256;
+  out->dw = d;
+  out->info.variant = CONV_VARIANT_DEPTHWISE;
+  out->info.split_k = 1;
+  out->info.tile_m = static_cast<int>(s.mg);
+  out->info.tile_n = static_cast<int>(th * s.wo);
+  out->info.ctas = p->n * p->groups * ((s.ho + th - 1) / th);
+  out->info.scratch_bytes = 0;
+  return true;
+}
+
+bool plan_tc(const conv_problem* p, const Shape& s, int sm, Plan* out) {
+  if (p->dtype == CONV_F32) return false;
+  static const int bns[] = {256, 128, 64, 48, 32};
+  int bn = 0;
+  long long best = -1;
+  for (int cand : bns) {  // least padded channels; ties go to the wider tile
+    const long long padded = (s.mg + cand - 1) / cand * cand;
+    if (best < 0 || padded < best) { best = padded; bn = cand; }
+  }
+  TcPlan t;
+  t.bn = bn;
+  t.k_pad = static_cast<int>((s.K + 63) / 64 * 64);
+  t.tap_major = (s.cg % 8 == 0) ? 1 : 0;
+  t.co_tiles = static_cast<int>((s.mg + bn - 1) / bn);
+  const long long pix_tiles = (s.npix + 127) / 128;
+  if (pix_tiles > kI32) return false;
+  t.pix_tiles = static_cast<int>(pix_tiles);
+  const long long stg = std::min<long long>(bn, s.mg) * s.K * 2;
+  t.stages = 0;
+  for (int st = 4; st >= 2; --st) {
+    if (tc_smem_bytes(bn, t.k_pad, st, t.tap_major, stg) <= kMaxDynSmem) { t.stages = st; break; }
+  }
+  if (!t.stages) return false;
+  t.smem = tc_smem_bytes(bn, t.k_pad, t.stages, t.tap_major, stg);
+  const long long combos = p->groups * t.co_tiles;
+  long long cpc = combos >= sm ? 1 : std::min<long long>(pix_tiles, sm / combos);
+  if (cpc < 1) cpc = 1;
+  if (combos * cpc > kI32) return false;
+  t.ctas = static_cast<int>(combos * cpc);
+  out->tc = t;
+  out->info.variant = CONV_VARIANT_IGEMM_TC;
+  out->info.split_k = 1;
+  out->info.tile_m = bn;
+  out->info.tile_n = 128;
+  out->info.ctas = t.ctas;
+  out->info.scratch_bytes = 0;
+  return true;
+}
+
+conv_status make_plan(const conv_problem* p, int sm, Plan* out, Shape* shape) {
+  if (sm < 1) return CONV_ERR_ARG;
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  memset(out, 0, sizeof(*out));
+  out->info.ho = s.ho;
+  out->info.wo = s.wo;
+  out->info.gemm_m = s.mg;
+  out->info.gemm_n = s.npix;
+  out->info.gemm_k = s.K;
+  const bool force_ffma = (p->flags & CONV_FLAG_FORCE_FFMA) != 0;
+  bool done = false;
+  if (!force_ffma && s.cg == 1) done = plan_depthwise(p, s, out);
+  if (!done && !force_ffma) done = plan_tc(p, s, sm, out);
+  if (!done) plan_ffma(p, s, sm, out);
+  if (shape) *shape = s;
+  return CONV_OK;
+}
+
+struct DevInfo {
+  int sm = 0;
+  int ok = 0;  // 1 usable, -1 not an sm_103 device
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[kMaxDevices];
+
+conv_status device_info(int* dev_out, int* sm_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return CONV_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.ok == 0) {
+    int major = 0, minor = 0, sm = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return CONV_ERR_DEVICE;
+    }
+    d.sm = sm;
+    d.ok = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (d.ok != 1) return CONV_ERR_DEVICE;
+  *dev_out = dev;
+  *sm_out = d.sm;
+  return CONV_OK;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || !na || !nb) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+const char* variant_name(int v) {
+  switch (v) {
+    case CONV_VARIANT_IGEMM_FFMA: return "igemm_ffma";
+    case CONV_VARIANT_IGEMM_FFMA_SPLIT: return "igemm_ffma_split_k";
+    case CONV_VARIANT_DEPTHWISE: return "depthwise_halo";
+    case CONV_VARIANT_IGEMM_TC: return "igemm_tcgen05";
+    case CONV_VARIANT_IGEMM_TC_1X1: return "igemm_tcgen05_1x1";
+    default: return "unknown";
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t conv_abi_version(void) { return CONV_ABI_VERSION; }
+
+const char* conv_status_string(conv_status s) {
+  switch (s) {
+    case CONV_OK: return "ok";
+    case CONV_ERR_SHAPE: return "invalid shape";
+    case CONV_ERR_OVERFLOW: return "size overflow";
+    case CONV_ERR_DTYPE: return "unknown element type";
+    case CONV_ERR_ACT: return "unknown activation";
+    case CONV_ERR_NULL: return "required pointer is NULL";
+    case CONV_ERR_SCRATCH: return "scratch too small or misaligned";
+    case CONV_ERR_ALIAS: return "overlapping operands";
+    case CONV_ERR_DEVICE: return "no usable sm_103 device";
+    case CONV_ERR_CUDA: return "CUDA launch failed";
+    case CONV_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+  }
+}
+
+conv_status conv_output_shape(const conv_problem* p, int64_t* ho, int64_t* wo) {
+  if (!ho || !wo) return CONV_ERR_NULL;
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  *ho = s.ho;
+  *wo = s.wo;
+  return CONV_OK;
+}
+
+conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_plan_info* out) {
+  if (!out) return CONV_ERR_NULL;
+  Plan plan;
+  conv_status st = make_plan(p, sm_count, &plan, nullptr);
+  if (st == CONV_OK) *out = plan.info;
+  return st;
+}
+
+conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes) {
+  if (!bytes) return CONV_ERR_NULL;
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  int dev, sm;
+  st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  Plan plan;
+  st = make_plan(p, sm, &plan, nullptr);
+  if (st == CONV_OK) *bytes = static_cast<size_t>(plan.info.scratch_bytes);
+  return st;
+}
+
+conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) {
+  if (!buf || !len) return CONV_ERR_NULL;
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  int dev, sm;
+  st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  Plan plan;
+  st = make_plan(p, sm, &plan, nullptr);
+  if (st != CONV_OK) return st;
+  const conv_plan_info& i = plan.info;
+  if (i.variant == CONV_VARIANT_IGEMM_TC) {
+    snprintf(buf, len, "%s tile=128px x %dco k=%lld (padded %d, %s order) stages=%d blocks=%lld sms=%d",
+             variant_name(i.variant), plan.tc.bn, static_cast<long long>(i.gemm_k), plan.tc.k_pad,
+             plan.tc.tap_major ? "tap-major" : "channel-major", plan.tc.stages,
+             static_cast<long long>(i.ctas), sm);
+  } else if (i.variant == CONV_VARIANT_DEPTHWISE) {
+    snprintf(buf, len, "%s rows/block=%d staged=%dx%d blocks=%lld sms=%d", variant_name(i.variant),
+             plan.dw.th, plan.dw.in_rows, plan.dw.row, static_cast<long long>(i.ctas), sm);
+  } else {
+    snprintf(buf, len, "%s tile=%dco x %dpx split_k=%d blocks=%lld scratch=%llu sms=%d",
+             variant_name(i.variant), i.tile_m, i.tile_n, i.split_k, static_cast<long long>(i.ctas),
+             static_cast<unsigned long long>(i.scratch_bytes), sm);
+  }
+  return CONV_OK;
+}
+
+conv_status conv_forward(const conv_problem* p, const void* x, const void* w, const void* bias,
+                         const void* residual, void* y, void* scratch, size_t scratch_bytes,
+                         void* stream) {
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  if (!x || !w || !y) return CONV_ERR_NULL;
+  if (p->has_bias && !bias) return CONV_ERR_NULL;
+  if (p->has_residual && !residual) return CONV_ERR_NULL;
+  const size_t es = p->dtype == CONV_F32 ? 4 : 2;
+  const size_t xb = s.x_elems * es, wb = s.w_elems * es, yb = s.y_elems * es;
+  const size_t bb = p->has_bias ? p->c_out * es : 0, rb = p->has_residual ? yb : 0;
+  const void* in_ptr[] = {x, w, p->has_bias ? bias : nullptr, p->has_residual ? residual : nullptr};
+  const size_t in_len[] = {xb, wb, bb, rb};
+  for (int i = 0; i < 4; ++i)
+    if (overlap(y, yb, in_ptr[i], in_len[i])) return CONV_ERR_ALIAS;
+  int dev, sm;
+  st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  Plan plan;
+  st = make_plan(p, sm, &plan, nullptr);
+  if (st != CONV_OK) return st;
+  const size_t need = plan.info.scratch_bytes;
+  if (need) {
+    if (!scratch || scratch_bytes < need || reinterpret_cast<uintptr_t>(scratch) % 16) return CONV_ERR_SCRATCH;
+    for (int i = 0; i < 4; ++i)
+      if (overlap(scratch, need, in_ptr[i], in_len[i])) return CONV_ERR_ALIAS;
+    if (overlap(scratch, need, y, yb)) return CONV_ERR_ALIAS;
+  }
+
+  ConvArgs a;
+  memset(&a, 0, sizeof(a));
+  a.n = static_cast<int>(p->n); a.c_in = static_cast<int>(p->c_in);
+  a.h = static_cast<int>(p->h); a.w = static_cast<int>(p->w);
+  a.c_out = static_cast<int>(p->c_out); a.kh = static_cast<int>(p->kh); a.kw = static_cast<int>(p->kw);
+  a.pt = static_cast<int>(p->pad_top); a.pl = static_cast<int>(p->pad_left);
+  a.sh = static_cast<int>(p->stride_h); a.sw = static_cast<int>(p->stride_w);
+  a.dh = static_cast<int>(p->dil_h); a.dw = static_cast<int>(p->dil_w);
+  a.groups = static_cast<int>(p->groups); a.cg = static_cast<int>(s.cg); a.mg = static_cast<int>(s.mg);
+  a.ho = static_cast<int>(s.ho); a.wo = static_cast<int>(s.wo);
+  a.K = static_cast<int>(s.K);
+  a.hw = p->h * p->w; a.howo = s.ho * s.wo; a.npix = s.npix;
+  a.act = p->act; a.alpha = p->act_alpha; a.beta = p->act_beta;
+  a.x = x; a.wt = w; a.y = y;
+  a.bias = p->has_bias ? bias : nullptr;
+  a.residual = p->has_residual ? residual : nullptr;
+  a.vec_out = (reinterpret_cast<uintptr_t>(y) % 16 == 0) ? 1 : 0;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaSuccess;
+  switch (plan.info.variant) {
+    case CONV_VARIANT_DEPTHWISE: {
+      const int rt = static_cast<int>((s.ho + plan.dw.th - 1) / plan.dw.th);
+      plan.dw.vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && ((a.hw * es) % 16 == 0) &&
+                    (((p->w * es) % 16 == 0) || rt == 1);
+      err = launch_depthwise(plan, a, p->dtype, cs);
+      break;
+    }
+    case CONV_VARIANT_IGEMM_TC:
+      err = launch_tc(plan, a, p->dtype, cs);
+      break;
+    default: {
+      a.split = plan.info.split_k;
+      a.k_per_split = plan.k_per_split;
+      a.partial = static_cast<float*>(scratch);
+      err = launch_ffma(plan, a, p->dtype, cs);
+      if (err == cudaSuccess && a.split > 1) err = launch_split_reduce(a, p->dtype, cs);
+      break;
+    }
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return CONV_ERR_CUDA;
+  }
+  return CONV_OK;
+}
+
+conv_status conv_device_error(uint32_t* word, int32_t reset) {
+  if (!word) return CONV_ERR_NULL;
+  int dev, sm;
+  conv_status st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  return tc_error_word(word, reset) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+}  // extern "C"

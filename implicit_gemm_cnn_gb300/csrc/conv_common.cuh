@@ -1,0 +1,92 @@
+// conv_common.cuh -- types and device helpers shared by the convolution kernels.
+//
+// The fused epilogue follows "Convolution, pooling and resize", Layout and
+// operands: sum, bias, residual addition, activation, in that order, each step
+// rounded to float32.  The adds and multiplies below use the _rn intrinsics so
+// that the compiler cannot contract them into fused multiply-adds: every step
+// is rounded as written.  The activations are the ONNX operator definitions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace conv {
+
+// Everything a kernel needs to know about one launch.  Per-image sizes are
+// validated on the host to fit int32; batch-level offsets use int64.
+struct ConvArgs {
+  int n, c_in, h, w, c_out, kh, kw;
+  int pt, pl, sh, sw, dh, dw;
+  int groups, cg, mg;      // input / output channels per group
+  int ho, wo;
+  int K;                   // terms per output: cg * kh * kw
+  long long hw, howo;      // h*w, ho*wo
+  long long npix;          // n * ho * wo (GEMM columns across the batch)
+  int act;
+  float alpha, beta;
+  const void* x;
+  const void* wt;
+  const void* bias;        // nullptr when absent
+  const void* residual;    // nullptr when absent
+  void* y;
+  float* partial;          // split k: [split][n][c_out][ho][wo] float32 planes
+  int split;               // ranges of k (1 = whole)
+  int k_per_split;         // terms per range (a multiple of the k chunk)
+  int vec_out;             // y (and scratch) 16-byte aligned: vector stores allowed
+};
+
+enum Act {
+  ACT_IDENTITY = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_SIGMOID = 3, ACT_TANH = 4,
+  ACT_HARD_SWISH = 5, ACT_HARD_SIGMOID = 6, ACT_CLIP = 7, ACT_LEAKY_RELU = 8
+};
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float sigmoid_f32(float t) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-t)));
+}
+
+__device__ __forceinline__ float activate(float t, int act, float alpha, float beta) {
+  switch (act) {
+    case ACT_RELU: return t > 0.0f ? t : 0.0f;
+    case ACT_SILU: return __fmul_rn(t, sigmoid_f32(t));
+    case ACT_SIGMOID: return sigmoid_f32(t);
+    case ACT_TANH: return tanhf(t);
+    case ACT_HARD_SWISH: {
+      float s = __fadd_rn(__fmul_rn(t, 1.0f / 6.0f), 0.5f);
+      return __fmul_rn(t, fmaxf(0.0f, fminf(1.0f, s)));
+    }
+    case ACT_HARD_SIGMOID: {
+      float s = __fadd_rn(__fmul_rn(alpha, t), beta);
+      return fmaxf(0.0f, fminf(1.0f, s));
+    }
+    case ACT_CLIP: return fminf(fmaxf(t, alpha), beta);
+    case ACT_LEAKY_RELU: return t >= 0.0f ? t : __fmul_rn(alpha, t);
+    default: return t;
+  }
+}
+
+// t = acc; t += bias[co]; t += residual[out_index]; t = act(t); round to T.
+template <typename T>
+__device__ __forceinline__ T epilogue(float acc, int co, long long out_index, const ConvArgs& a) {
+  float t = acc;
+  if (a.bias) t = __fadd_rn(t, to_f32(static_cast<const T*>(a.bias)[co]));
+  if (a.residual) t = __fadd_rn(t, to_f32(static_cast<const T*>(a.residual)[out_index]));
+  return from_f32<T>(activate(t, a.act, a.alpha, a.beta));
+}
+
+}  // namespace conv

@@ -1,0 +1,392 @@
+// conv_ffma.cu -- implicit-GEMM convolution on CUDA cores (float32 FFMA), with
+// an optional split of k into ranges and the ordered reduction that finishes it.
+//
+// The method ("Convolution, pooling and resize", Variants: the implicit GEMM
+// tile kernel that gathers the input window while it loads the tile, and
+// "Convolutions", section 2.4: Y = W cols per group).  Per group g the output
+// is the product of W_g (Cout/G x K) and the column matrix (K x N*Ho*Wo), with
+// K = Cin/G * kh * kw ordered (channel, kernel row, kernel column) as OIHW
+// weights lie.  The column matrix is never written: each k row of a pixel tile
+// is gathered from x while the tile is staged into shared memory, with a
+// zero for every tap outside the image.  A block computes BM output channels
+// x BN pixels (pixels of several images may share a tile: batch is part of the
+// GEMM's N).  Bias, residual and activation are applied as the tile is stored,
+// so y is written once.
+//
+// Split k ("Convolution, pooling and resize", RTX 4070 split k): when the grid
+// is too small to fill the device, k is cut into ranges; each range's block
+// writes its raw float32 sums into its own plane of scratch, and
+// split_reduce adds the planes in range order, then applies the epilogue.
+// No atomics: every output's sum has an order fixed by the shape.
+//
+// Pipeline: fp32 tiles arrive by cp.async (4-byte copies with zero fill for
+// padded taps) kFfmaStages deep; 16-bit operands (the fallback for shapes the
+// tensor-core kernel does not take) are converted to fp32 as they are staged.
+// The window offsets of the block's k range are decoded once into a table in
+// shared memory (offset in the input plane set, row and column displacement).
+#include "conv_internal.h"
+
+namespace conv {
+namespace {
+
+__device__ __forceinline__ void cp_async4(float* smem, const void* gmem, bool pred) {
+  unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  int n = pred ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ void stage_elem(float* dst, const T* src, bool ok) {
+  if constexpr (sizeof(T) == 4) {
+    cp_async4(dst, src, ok);
+  } else {
+    *dst = ok ? to_f32(*src) : 0.0f;
+  }
+}
+
+// Store 4 consecutive outputs (same image, same channel) starting at out.
+template <typename T>
+__device__ __forceinline__ void store4(T* y, long long out, const float v[4]) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(y + out) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    T h[4] = {from_f32<T>(v[0]), from_f32<T>(v[1]), from_f32<T>(v[2]), from_f32<T>(v[3])};
+    *reinterpret_cast<uint2*>(y + out) = *reinterpret_cast<const uint2*>(h);
+  }
+}
+
+__host__ __device__ constexpr int pow2_floor(int v) {
+  int p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+
+template <typename T, int BM, int BN, int TM, int TN>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+    igemm_ffma(const ConvArgs a) {
+  constexpr int NT = (BM / TM) * (BN / TN);
+  constexpr int BK = kFfmaBK;
+  constexpr int S = kFfmaStages;
+  constexpr int AS = BM + 4;  // padded weight-tile row: conflict-free transposed stores
+  static_assert(TM == 4 || TM == 8, "TM");
+  static_assert(TN == 4 || TN == 8, "TN");
+  extern __shared__ __align__(16) float smem[];
+  float* As = smem;                                       // [S][BK][AS]
+  float* Bs = As + S * BK * AS;                           // [S][BK][BN]
+  int2* ktab = reinterpret_cast<int2*>(Bs + S * BK * BN);  // [kFfmaKTab]
+
+  const T* __restrict__ x = static_cast<const T*>(a.x);
+  const T* __restrict__ wt = static_cast<const T*>(a.wt);
+  const int tid = threadIdx.x;
+  const long long pix0 = static_cast<long long>(blockIdx.x) * BN;
+  const int co_tiles = (a.mg + BM - 1) / BM;
+  const int g = blockIdx.y / co_tiles;
+  const int m0 = (blockIdx.y % co_tiles) * BM;
+  const int k_begin = blockIdx.z * a.k_per_split;
+  const int k_end = min(a.K, k_begin + a.k_per_split);
+  const int khw = a.kh * a.kw;
+
+  // ---- the pixel columns this thread stages --------------------------------
+  // LB threads gather the input tile: RSTEP rows at a time of BN pixels each
+  // (LB >= BN), or PCOLS pixel columns each over all BK rows (LB < BN).
+  constexpr int LB = NT >= BN ? pow2_floor(NT / BN < BK ? NT / BN : BK) * BN : pow2_floor(NT);
+  constexpr int PCOLS = LB >= BN ? 1 : BN / LB;
+  constexpr int RSTEP = LB >= BN ? LB / BN : 1;
+  constexpr int BROWS = BK / RSTEP;
+  static_assert(BK % RSTEP == 0 && (LB >= BN ? LB % BN == 0 : BN % LB == 0), "loader mapping");
+  const bool bloader = tid < LB;
+  const int r0 = LB >= BN ? tid / BN : 0;
+  const int cbase = LB >= BN ? tid % BN : tid;
+  long long pbase[PCOLS];
+  int ih0[PCOLS], iw0[PCOLS];
+  bool pval[PCOLS];
+#pragma unroll
+  for (int j = 0; j < PCOLS; ++j) {
+    const int col = cbase + j * LB;
+    const long long p = pix0 + col;
+    pval[j] = bloader && p < a.npix;
+    const long long pp = pval[j] ? p : 0;
+    const int n = static_cast<int>(pp / a.howo);
+    const int rem = static_cast<int>(pp - static_cast<long long>(n) * a.howo);
+    const int oh = rem / a.wo, ow = rem - (rem / a.wo) * a.wo;
+    ih0[j] = oh * a.sh - a.pt;
+    iw0[j] = ow * a.sw - a.pl;
+    pbase[j] = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
+               static_cast<long long>(ih0[j]) * a.w + iw0[j];
+  }
+
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+  const int tx = tid % (BN / TN);
+  const int ty = tid / (BN / TN);
+
+  for (int kseg = k_begin; kseg < k_end; kseg += kFfmaKTab) {
+    const int seg_end = min(k_end, kseg + kFfmaKTab);
+    __syncthreads();  // the previous segment's table and stages are free
+    for (int k = kseg + tid; k < seg_end; k += NT) {
+      const int c = k / khw;
+      const int tap = k - c * khw;
+      const int u = tap / a.kw, v = tap - (tap / a.kw) * a.kw;
+      const int dy = u * a.dh, dx = v * a.dw;
+      ktab[k - kseg] = make_int2(c * static_cast<int>(a.hw) + dy * a.w + dx, (dy << 16) | dx);
+    }
+    __syncthreads();
+
+    auto load_stage = [&](int st, int k0) {
+      float* as = As + st * BK * AS;
+      float* bs = Bs + st * BK * BN;
+      constexpr int AE = (BM * BK + NT - 1) / NT;
+#pragma unroll
+      for (int i = 0; i < AE; ++i) {
+        const int e = tid + i * NT;
+        if (e < BM * BK) {
+          const int kk = e % BK, m = e / BK;
+          const int k = k0 + kk;
+          const bool ok = (m0 + m < a.mg) && (k < seg_end);
+          const T* src = ok ? wt + static_cast<long long>(g * a.mg + m0 + m) * a.K + k : wt;
+          stage_elem<T>(as + kk * AS + m, src, ok);
+        }
+      }
+      if (bloader) {
+#pragma unroll
+        for (int i = 0; i < BROWS; ++i) {
+          const int kk = r0 + i * RSTEP;
+          const int k = k0 + kk;
+          const bool kok = k < seg_end;
+          const int2 e = kok ? ktab[k - kseg] : make_int2(0, 0);
+          const int dy = e.y >> 16, dx = e.y & 0xffff;
+#pragma unroll
+          for (int j = 0; j < PCOLS; ++j) {
+            const int col = cbase + j * LB;
+            const int ih = ih0[j] + dy, iw = iw0[j] + dx;
+            const bool ok = kok && pval[j] && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
+                            static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
+            const T* src = ok ? x + pbase[j] + e.x : x;
+            stage_elem<T>(bs + kk * BN + col, src, ok);
+          }
+        }
+      }
+    };
+
+    const int nch = (seg_end - kseg + BK - 1) / BK;
+#pragma unroll
+    for (int st = 0; st < S - 1; ++st) {
+      if (st < nch) load_stage(st, kseg + st * BK);
+      cp_async_commit();
+    }
+    for (int c = 0; c < nch; ++c) {
+      cp_async_wait<S - 2>();
+      __syncthreads();
+      const int nxt = c + S - 1;
+      if (nxt < nch) load_stage(nxt % S, kseg + nxt * BK);
+      cp_async_commit();
+      const float* as = As + (c % S) * BK * AS;
+      const float* bs = Bs + (c % S) * BK * BN;
+#pragma unroll
+      for (int kk = 0; kk < BK; ++kk) {
+        float ra[TM], rb[TN];
+        const float4 a0 = *reinterpret_cast<const float4*>(as + kk * AS + ty * 4);
+        ra[0] = a0.x; ra[1] = a0.y; ra[2] = a0.z; ra[3] = a0.w;
+        if constexpr (TM == 8) {
+          const float4 a1 = *reinterpret_cast<const float4*>(as + kk * AS + BM / 2 + ty * 4);
+          ra[4] = a1.x; ra[5] = a1.y; ra[6] = a1.z; ra[7] = a1.w;
+        }
+        const float4 b0 = *reinterpret_cast<const float4*>(bs + kk * BN + tx * 4);
+        rb[0] = b0.x; rb[1] = b0.y; rb[2] = b0.z; rb[3] = b0.w;
+        if constexpr (TN == 8) {
+          const float4 b1 = *reinterpret_cast<const float4*>(bs + kk * BN + BN / 2 + tx * 4);
+          rb[4] = b1.x; rb[5] = b1.y; rb[6] = b1.z; rb[7] = b1.w;
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+          for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(ra[i], rb[j], acc[i][j]);
+      }
+    }
+    cp_async_wait<0>();
+  }
+
+  // ---- store: raw partial planes (split k) or the fused epilogue -----------
+  const long long total = static_cast<long long>(a.n) * a.c_out * a.howo;
+  T* y = static_cast<T*>(a.y);
+#pragma unroll
+  for (int jg = 0; jg < TN / 4; ++jg) {
+    const long long p = pix0 + jg * (BN / 2) + tx * 4;
+    if (p >= a.npix) continue;
+    const int n = static_cast<int>(p / a.howo);
+    const long long rem = p - static_cast<long long>(n) * a.howo;
+    const bool whole4 = a.vec_out && (p + 3 < a.npix) && (rem + 3 < a.howo) && ((a.howo & 3) == 0);
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+      if (m >= a.mg) continue;
+      const int co = g * a.mg + m;
+      const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo + rem;
+      if (a.split > 1) {
+        float* part = a.partial + static_cast<long long>(blockIdx.z) * total;
+        if (whole4) {
+          *reinterpret_cast<float4*>(part + out) =
+              make_float4(acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const long long pq = p + q;
+            if (pq >= a.npix) break;
+            const int nq = static_cast<int>(pq / a.howo);
+            part[(static_cast<long long>(nq) * a.c_out + co) * a.howo + (pq - nq * a.howo)] =
+                acc[i][jg * 4 + q];
+          }
+        }
+      } else {
+        if (whole4) {
+          float v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = to_f32(epilogue<T>(acc[i][jg * 4 + q], co, out + q, a));
+          store4<T>(y, out, v);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const long long pq = p + q;
+            if (pq >= a.npix) break;
+            const int nq = static_cast<int>(pq / a.howo);
+            const long long oq = (static_cast<long long>(nq) * a.c_out + co) * a.howo + (pq - nq * a.howo);
+            y[oq] = epilogue<T>(acc[i][jg * 4 + q], co, oq, a);
+          }
+        }
+      }
+    }
+  }
+}
+
+// Sum the split planes in range order, then the fused epilogue.  Four
+// consecutive outputs per thread when the plane length allows vector loads.
+template <typename T>
+__global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
+  const long long total = static_cast<long long>(a.n) * a.c_out * a.howo;
+  T* y = static_cast<T*>(a.y);
+  const float* part = a.partial;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  if ((total & 3) == 0) {
+    const long long q = total >> 2;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < q; i += stride) {
+      float4 s = reinterpret_cast<const float4*>(part)[i];
+      for (int z = 1; z < a.split; ++z) {
+        const float4 t = reinterpret_cast<const float4*>(part + z * total)[i];
+        s.x = __fadd_rn(s.x, t.x); s.y = __fadd_rn(s.y, t.y);
+        s.z = __fadd_rn(s.z, t.z); s.w = __fadd_rn(s.w, t.w);
+      }
+      const long long o = i * 4;
+      const int co = static_cast<int>((o / a.howo) % a.c_out);
+      float v[4] = {s.x, s.y, s.z, s.w};
+      if (a.vec_out && (a.howo & 3) == 0) {  // the 4 outputs share a channel
+        float r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = to_f32(epilogue<T>(v[k], co, o + k, a));
+        store4<T>(y, o, r);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ck = static_cast<int>(((o + k) / a.howo) % a.c_out);
+          y[o + k] = epilogue<T>(v[k], ck, o + k, a);
+        }
+      }
+    }
+  } else {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total; i += stride) {
+      float s = part[i];
+      for (int z = 1; z < a.split; ++z) s = __fadd_rn(s, part[z * total + i]);
+      const int co = static_cast<int>((i / a.howo) % a.c_out);
+      y[i] = epilogue<T>(s, co, i, a);
+    }
+  }
+}
+
+template <typename T, int CFG>
+cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
+  constexpr FfmaCfg c = kFfmaCfgs[CFG];
+  auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn>;
+  const size_t smem = ffma_smem_bytes(CFG, sizeof(T) == 4 ? CONV_F32 : CONV_F16);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !configured[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    configured[dev] = 1;
+  }
+  const long long gx = (a.npix + c.bn - 1) / c.bn;
+  const int co_tiles = (a.mg + c.bm - 1) / c.bm;
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(co_tiles * a.groups),
+            static_cast<unsigned>(a.split));
+  kern<<<grid, c.threads(), smem, s>>>(a);
+  (void)plan;
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
+  switch (plan.ffma_cfg) {
+    case 0: return launch_cfg<T, 0>(plan, a, s);
+    case 1: return launch_cfg<T, 1>(plan, a, s);
+    case 2: return launch_cfg<T, 2>(plan, a, s);
+    case 3: return launch_cfg<T, 3>(plan, a, s);
+    case 4: return launch_cfg<T, 4>(plan, a, s);
+    case 5: return launch_cfg<T, 5>(plan, a, s);
+    case 6: return launch_cfg<T, 6>(plan, a, s);
+    case 7: return launch_cfg<T, 7>(plan, a, s);
+    case 8: return launch_cfg<T, 8>(plan, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_reduce_typed(const ConvArgs& a, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.n) * a.c_out * a.howo;
+  const long long work = (total & 3) == 0 ? total / 4 : total;
+  long long blocks = (work + 255) / 256;
+  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  split_reduce<T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t ffma_smem_bytes(int cfg, int dtype) {
+  (void)dtype;
+  const FfmaCfg c = kFfmaCfgs[cfg];
+  return static_cast<size_t>(kFfmaStages) * kFfmaBK * (c.bm + 4 + c.bn) * sizeof(float) +
+         static_cast<size_t>(kFfmaKTab) * sizeof(int2);
+}
+
+cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s) {
+  switch (dtype) {
+    case CONV_F32: return launch_typed<float>(plan, a, s);
+    case CONV_F16: return launch_typed<__half>(plan, a, s);
+    case CONV_BF16: return launch_typed<__nv_bfloat16>(plan, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_split_reduce(const ConvArgs& a, int dtype, cudaStream_t s) {
+  switch (dtype) {
+    case CONV_F32: return launch_reduce_typed<float>(a, s);
+    case CONV_F16: return launch_reduce_typed<__half>(a, s);
+    case CONV_BF16: return launch_reduce_typed<__nv_bfloat16>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace conv

@@ -1,0 +1,66 @@
+// conv_internal.h -- host-side plan and launch interfaces between the C ABI
+// (conv_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "conv.h"
+#include "conv_common.cuh"
+
+namespace conv {
+
+// CUDA-core implicit GEMM tiles: output channels (BM) x pixels (BN) per block,
+// TM x TN outputs per thread.
+struct FfmaCfg {
+  int bm, bn, tm, tn;
+  int threads() const { return (bm / tm) * (bn / tn); }
+};
+constexpr int kFfmaBK = 8;          // k terms per pipeline stage
+constexpr int kFfmaStages = 4;      // pipeline depth
+constexpr int kFfmaKTab = 2304;     // k entries of the window table per segment
+constexpr int kNumFfmaCfgs = 9;
+constexpr FfmaCfg kFfmaCfgs[kNumFfmaCfgs] = {
+    {128, 128, 8, 8}, {64, 128, 8, 8}, {128, 64, 8, 8}, {64, 64, 4, 4}, {32, 256, 4, 8},
+    {16, 256, 4, 8},  {40, 128, 8, 4}, {16, 64, 4, 4},  {40, 64, 8, 4}};
+
+size_t ffma_smem_bytes(int cfg, int dtype);
+
+// Depthwise (one input channel per group) halo-tiled direct kernel.
+struct DwPlan {
+  int th;        // output rows per block
+  int in_rows;   // input rows staged per block
+  int lm;        // left margin (columns before input column 0)
+  int row;       // staged row length in elements (>= lm + needed columns)
+  int vec;       // bytes per vector copy of an input row (0: element copies)
+  int threads;
+};
+
+// tcgen05 implicit GEMM: 128 pixels x BN output channels per tile.
+struct TcPlan {
+  int bn;          // N tile (output channels), a multiple of 16
+  int k_pad;       // k padded to a multiple of 64
+  int tap_major;   // k ordered (tap, channel) with 8-channel chunks; else (channel, tap)
+  int stages;      // A-operand pipeline depth
+  int co_tiles;    // output-channel tiles per group
+  int pix_tiles;   // 128-pixel tiles
+  int ctas;        // persistent blocks
+  size_t smem;     // dynamic shared memory bytes
+};
+
+struct Plan {
+  conv_plan_info info;
+  int ffma_cfg;
+  int k_per_split;  // terms per k range of the split variant
+  DwPlan dw;
+  TcPlan tc;
+};
+
+cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_split_reduce(const ConvArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_depthwise(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_tc(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
+cudaError_t tc_error_word(uint32_t* word, int reset);
+
+}  // namespace conv

@@ -1,0 +1,207 @@
+/*
+ * conv.h -- C ABI of libconv: the forward 2-D convolution (ONNX Conv
+ * semantics) on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Convolution, pooling and resize", Layout and operands;
+ * "Convolutions", sections 2.1 and 3):
+ *
+ *   Ho = floor((H + pad_top + pad_bottom - dil_h*(kh-1) - 1) / stride_h) + 1
+ *   Wo = floor((W + pad_left + pad_right - dil_w*(kw-1) - 1) / stride_w) + 1
+ *   y[n,co,oh,ow] = act( ( sum_{c,u,v} x[n, g*Cin/G + c, oh*sh - pt + u*dh,
+ *                                                 ow*sw - pl + v*dw] * w[co,c,u,v] )
+ *                        + bias[co] + residual[n,co,oh,ow] )
+ *   with g = co / (Cout/G), zero outside the image, and the epilogue applied
+ *   in that order -- sum, bias, residual, activation -- each step rounded to
+ *   float32, the result rounded once to the element type (nearest even).
+ *
+ * Layouts: x is NCHW [n][c_in][h][w], w is OIHW [c_out][c_in/groups][kh][kw],
+ * bias is [c_out], residual and y are NCHW [n][c_out][Ho][Wo]; all dense and
+ * contiguous.  A one-dimensional convolution is h = 1 (with kh = 1).
+ * One element type covers every operand; sums accumulate in float32.
+ *
+ * Ownership: every pointer is caller-owned memory.  conv_forward takes device
+ * pointers; the library allocates nothing per call (it keeps a small
+ * per-device cache of device attributes).  Pointers from a CUDA allocator
+ * (256-byte aligned) take every fast path; other alignments are legal and
+ * may run a slower variant of the same kernels.
+ *
+ * Asynchrony: conv_forward only enqueues kernels on `stream` (a cudaStream_t;
+ * NULL is the legacy default stream) and returns; it never synchronises and
+ * copies nothing to the host.  Results are bit-identical from run to run on
+ * one device: no kernel uses atomics, and every sum has a fixed order.
+ *
+ * Errors: every function returns a conv_status.  Validation runs on the host
+ * before anything is enqueued, so a call that returns an error other than
+ * CONV_ERR_CUDA enqueued nothing.
+ */
+#ifndef CONV_GB300_H
+#define CONV_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CONV_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define CONV_API __attribute__((visibility("default")))
+#else
+#define CONV_API
+#endif
+
+typedef enum conv_dtype {
+  CONV_F32 = 0,  /* float32 operands and output                             */
+  CONV_F16 = 1,  /* IEEE binary16 operands and output, float32 accumulation */
+  CONV_BF16 = 2  /* bfloat16 operands and output, float32 accumulation      */
+} conv_dtype;
+
+/* Activations fused into the store ("Convolution, pooling and resize",
+ * Layout and operands), with the ONNX operator definitions:
+ *   relu max(t,0); sigmoid 1/(1+exp(-t)); tanh; silu t*sigmoid(t);
+ *   hard_sigmoid max(0,min(1, alpha*t + beta));
+ *   hard_swish t*max(0,min(1, t/6 + 1/2))   (alpha, beta unused);
+ *   clip min(max(t, alpha), beta)            (alpha = min, beta = max);
+ *   leaky_relu t >= 0 ? t : alpha*t. */
+typedef enum conv_act {
+  CONV_ACT_IDENTITY = 0,
+  CONV_ACT_RELU = 1,
+  CONV_ACT_SILU = 2,
+  CONV_ACT_SIGMOID = 3,
+  CONV_ACT_TANH = 4,
+  CONV_ACT_HARD_SWISH = 5,
+  CONV_ACT_HARD_SIGMOID = 6,
+  CONV_ACT_CLIP = 7,
+  CONV_ACT_LEAKY_RELU = 8
+} conv_act;
+
+/* conv_problem.flags: testing and measurement switches.  0 = automatic. */
+#define CONV_FLAG_FORCE_FFMA 0x1u   /* the CUDA-core implicit GEMM for every shape   */
+#define CONV_FLAG_NO_SPLIT_K 0x2u   /* never split k                                 */
+#define CONV_FLAG_SPLIT_K_SHIFT 8   /* bits 8..13: force this many ranges of k (1-63) */
+#define CONV_FLAG_SPLIT_K_MASK 0x3f00u
+
+/* The problem ("Convolution, pooling and resize", Layout and operands: a
+ * problem struct with the shape, explicit pads, dilation, groups and the fused
+ * activation).  Sizes are element counts. */
+typedef struct conv_problem {
+  int64_t n, c_in, h, w;            /* input NCHW                              */
+  int64_t c_out, kh, kw;            /* weights OIHW [c_out][c_in/groups][kh][kw] */
+  int64_t pad_top, pad_left, pad_bottom, pad_right; /* ONNX pads [t, l, b, r]  */
+  int64_t stride_h, stride_w;       /* >= 1                                    */
+  int64_t dil_h, dil_w;             /* >= 1                                    */
+  int64_t groups;                   /* divides c_in and c_out                  */
+  int32_t act;                      /* conv_act                                */
+  float act_alpha, act_beta;        /* see conv_act                            */
+  int32_t dtype;                    /* conv_dtype of x, w, bias, residual, y   */
+  int32_t has_bias;                 /* bias pointer is read iff nonzero        */
+  int32_t has_residual;             /* residual pointer is read iff nonzero    */
+  uint32_t flags;                   /* CONV_FLAG_*                             */
+} conv_problem;
+
+typedef enum conv_status {
+  CONV_OK = 0,
+  CONV_ERR_SHAPE = 1,    /* a size < 1 (pads < 0), groups not dividing the
+                            channels, no output position, or a size past a
+                            kernel limit                                     */
+  CONV_ERR_OVERFLOW = 2, /* an element count or offset overflows int64      */
+  CONV_ERR_DTYPE = 3,    /* unknown conv_dtype                               */
+  CONV_ERR_ACT = 4,      /* unknown conv_act                                 */
+  CONV_ERR_NULL = 5,     /* a required pointer is NULL                       */
+  CONV_ERR_SCRATCH = 6,  /* scratch smaller than conv_scratch_bytes reports  */
+  CONV_ERR_ALIAS = 7,    /* y overlaps an input, or scratch overlaps an operand
+                            ("Convolution, pooling and resize": scratch may
+                            share a buffer with the operands only if its range
+                            overlaps none of theirs)                          */
+  CONV_ERR_DEVICE = 8,   /* no usable CUDA device, or not sm_103-class        */
+  CONV_ERR_CUDA = 9,     /* a CUDA call or kernel launch failed               */
+  CONV_ERR_ARG = 10      /* another invalid argument (e.g. a zero-length buffer) */
+} conv_status;
+
+/* What conv_forward runs for a problem ("Convolution, pooling and resize",
+ * Variants: the variant a device runs is a function of the problem). */
+typedef enum conv_variant {
+  CONV_VARIANT_IGEMM_FFMA = 0,     /* implicit GEMM on CUDA cores, fused epilogue */
+  CONV_VARIANT_IGEMM_FFMA_SPLIT = 1, /* the same with k split into ranges, each
+                                      into a float32 plane of scratch, then an
+                                      ordered sum + epilogue pass            */
+  CONV_VARIANT_DEPTHWISE = 2,      /* direct halo-tiled kernel (one input channel
+                                      per group, any channel multiplier)     */
+  CONV_VARIANT_IGEMM_TC = 3,       /* implicit GEMM on tcgen05 tensor cores,
+                                      input window gathered into shared memory */
+  CONV_VARIANT_IGEMM_TC_1X1 = 4    /* tcgen05 implicit GEMM for 1x1 / stride 1 /
+                                      no pad: input tiles read as they lie, by TMA */
+} conv_variant;
+
+/* The host-side plan of a problem for a device with `sm_count` SMs. */
+typedef struct conv_plan_info {
+  int32_t variant;        /* conv_variant                                     */
+  int32_t split_k;        /* ranges of k (1 = the whole sum in one pass)       */
+  int64_t ho, wo;         /* output size                                      */
+  int64_t gemm_m;         /* output channels per group (Cout / groups)        */
+  int64_t gemm_n;         /* output pixels (n * Ho * Wo)                      */
+  int64_t gemm_k;         /* terms of each sum (Cin/groups * kh * kw)         */
+  int64_t ctas;           /* thread blocks of the main kernel                 */
+  int32_t tile_m, tile_n; /* output channels x pixels per thread block        */
+  uint64_t scratch_bytes; /* device scratch conv_forward needs                */
+} conv_plan_info;
+
+/* Library ABI version (CONV_ABI_VERSION). */
+CONV_API int32_t conv_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+CONV_API const char* conv_status_string(conv_status status);
+
+/* Output size of `p` ("Convolutions", section 2.1, boxed equation, with the
+ * two pads of an axis added separately).  Host only; validates `p` (all of
+ * the checks of conv_forward that do not involve pointers).
+ * Errors: CONV_ERR_NULL (p, ho or wo NULL), CONV_ERR_SHAPE, CONV_ERR_OVERFLOW,
+ * CONV_ERR_DTYPE, CONV_ERR_ACT. */
+CONV_API conv_status conv_output_shape(const conv_problem* p, int64_t* ho, int64_t* wo);
+
+/* The plan for a device with `sm_count` SMs: variant, k split, tile, grid and
+ * scratch bytes.  Host only and a pure function of (p, sm_count), so split
+ * decisions -- and with them the summation order -- depend only on the shape
+ * and the device ("Convolution, pooling and resize", split k: the cut depends
+ * only on the shape).  Assumes 256-byte aligned operands.
+ * Errors: as conv_output_shape, and CONV_ERR_ARG for sm_count < 1. */
+CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_plan_info* out);
+
+/* Scratch bytes conv_forward needs for `p` on the current CUDA device
+ * ("Convolution, pooling and resize", Layout and operands: the scratch
+ * query): the float32 partial planes of split k (ranges x output elements),
+ * 0 for every variant that keeps its sums on chip.
+ * Errors: as conv_plan, and CONV_ERR_DEVICE without a usable device. */
+CONV_API conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes);
+
+/* Writes a one-line description of what conv_forward runs for `p` on the
+ * current device into buf (NUL-terminated, truncated to len). */
+CONV_API conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len);
+
+/* Enqueue y = conv(x, w) + bias + residual, activated, on `stream`.
+ *   x, w, y     device pointers (required);
+ *   bias        device pointer, read iff p->has_bias (then required);
+ *   residual    device pointer, read iff p->has_residual (then required);
+ *   scratch     device memory of scratch_bytes bytes, at least
+ *               conv_scratch_bytes(p); may be NULL when that is 0.  Its range
+ *               must overlap no operand; y must overlap no input.
+ *   stream      cudaStream_t (NULL: legacy default stream).
+ * Errors: those of conv_plan; CONV_ERR_NULL, CONV_ERR_SCRATCH, CONV_ERR_ALIAS
+ * before anything is enqueued; CONV_ERR_DEVICE; CONV_ERR_CUDA when a launch
+ * fails (the error is the launch's; nothing is synchronised). */
+CONV_API conv_status conv_forward(const conv_problem* p, const void* x, const void* w,
+                         const void* bias, const void* residual, void* y,
+                         void* scratch, size_t scratch_bytes, void* stream);
+
+/* Reads (and, if `reset`, clears) the current device's error word: nonzero
+ * when a tensor-core kernel gave up a bounded wait (its output is then
+ * incomplete).  Synchronises the device; for tests and diagnostics. */
+CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV_GB300_H */

@@ -1,0 +1,187 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every
+symbol include/conv.h declares, validates problems with checked arithmetic,
+and plans deterministically.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import implicit_gemm_cnn_gb300 as conv
+import oracle
+from implicit_gemm_cnn_gb300 import build as conv_build
+from workloads import LAYERS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    conv_build.build()
+    return conv.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "conv.h")).read()
+    return re.findall(r"CONV_API\s+[\w\s\*]+?\b(conv_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) == 8, names
+    for name in names:
+        assert hasattr(lib, name), name           # dlsym succeeds
+    assert conv.conv_abi_version() == 1
+
+
+def test_struct_layout_matches_header():
+    # int64 x 16, then int32, float, float, int32 x 3, uint32 -> 156 -> padded 160
+    assert ctypes.sizeof(conv.ConvProblem) == 160
+    assert conv.ConvProblem.act.offset == 128 and conv.ConvProblem.flags.offset == 152
+    assert ctypes.sizeof(conv.ConvPlanInfo) == 72
+
+
+def test_status_strings(lib):
+    for code in range(11):
+        assert conv.conv_status_string(code)
+
+
+@pytest.mark.parametrize("case", [
+    # (x_shape, w_shape, stride, pads, dilation)
+    ((1, 1, 4, 4), (1, 1, 3, 3), 1, 0, 1),
+    ((8, 3, 224, 224), (64, 3, 7, 7), 2, 3, 1),
+    ((1, 1, 10, 10), (1, 1, 3, 3), 1, 0, 2),
+    ((2, 4, 13, 9), (6, 4, 4, 2), (3, 2), (2, 0, 1, 3), (1, 3)),
+    ((1, 2, 1, 50), (3, 2, 1, 5), 1, (0, 2, 0, 2), 1),      # one-dimensional (h = 1)
+    ((1, 2, 5, 5), (2, 2, 5, 5), 1, 0, 1),                    # single output position
+])
+def test_output_shape_matches_oracle(lib, case):
+    xs, ws, stride, pads, dil = case
+    p = conv.make_problem(xs, ws, stride=stride, pads=pads, dilation=dil)
+    o = oracle.Oracle()
+    pt, pl, pb, pr = conv._pads(pads)
+    sh, sw = conv._pair(stride)
+    dh, dw = conv._pair(dil)
+    want = (o.output_extent(xs[2], ws[2], pt, pb, sh, dh), o.output_extent(xs[3], ws[3], pl, pr, sw, dw))
+    assert conv.conv_output_shape(p) == want
+
+
+def _status(fn, *args):
+    try:
+        fn(*args)
+    except conv.ConvError as e:
+        return e.name
+    return "CONV_OK"
+
+
+def test_validation_errors(lib):
+    ok = dict(x_shape=(2, 4, 8, 8), w_shape=(6, 2, 3, 3), groups=2, pads=1)
+    assert _status(conv.conv_output_shape, conv.make_problem(**ok)) == "CONV_OK"
+    bad = [
+        (dict(ok, x_shape=(0, 4, 8, 8)), "CONV_ERR_SHAPE"),
+        (dict(ok, groups=3), "CONV_ERR_SHAPE"),                         # 4 % 3
+        (dict(ok, w_shape=(5, 2, 3, 3)), "CONV_ERR_SHAPE"),             # 5 % 2
+        (dict(ok, pads=0, w_shape=(6, 2, 9, 9)), "CONV_ERR_SHAPE"),     # no output position
+        (dict(ok, pads=(-1, 0, 0, 0)), "CONV_ERR_SHAPE"),
+        (dict(ok, stride=0), "CONV_ERR_SHAPE"),
+        (dict(ok, dilation=0), "CONV_ERR_SHAPE"),
+        (dict(ok, x_shape=(2 ** 40, 4, 2 ** 20, 2 ** 20)), "CONV_ERR_OVERFLOW"),
+        (dict(ok, dilation=2 ** 62), "CONV_ERR_OVERFLOW"),
+        (dict(ok, x_shape=(1, 4, 70000, 70000)), "CONV_ERR_SHAPE"),     # per-image > int32
+    ]
+    for kw, want in bad:
+        assert _status(conv.conv_output_shape, conv.make_problem(**kw)) == want, (kw, want)
+    p = conv.make_problem(**ok)
+    p.dtype = 7
+    assert _status(conv.conv_output_shape, p) == "CONV_ERR_DTYPE"
+    p = conv.make_problem(**ok)
+    p.act = 42
+    assert _status(conv.conv_output_shape, p) == "CONV_ERR_ACT"
+    assert lib.conv_output_shape(None, None, None) == 5  # CONV_ERR_NULL
+
+
+def test_forward_host_side_errors(lib):
+    """Errors conv_forward reports before it touches a device (fake addresses
+    are never dereferenced on these paths)."""
+    p = conv.make_problem((1, 4, 8, 8), (4, 4, 3, 3), pads=1, has_bias=True)
+    x, w, b, y = 0x10000, 0x20000, 0x30000, 0x40000
+    assert lib.conv_forward(ctypes.byref(p), None, w, b, None, y, None, 0, None) == 5
+    assert lib.conv_forward(ctypes.byref(p), x, w, None, None, y, None, 0, None) == 5  # bias
+    # y overlapping the input
+    assert lib.conv_forward(ctypes.byref(p), x, w, b, None, x + 64, None, 0, None) == 7
+    p.has_residual = 1
+    assert lib.conv_forward(ctypes.byref(p), x, w, b, None, y, None, 0, None) == 5
+    assert lib.conv_forward(ctypes.byref(p), x, w, b, y, y, None, 0, None) == 7        # in-place
+    # no GPU in this process: the device query fails cleanly
+    import torch
+    if not torch.cuda.is_available():
+        p.has_residual = 0
+        assert lib.conv_forward(ctypes.byref(p), x, w, b, None, y, None, 0, None) == 8
+        assert _status(conv.conv_scratch_bytes, p) == "CONV_ERR_DEVICE"
+        assert _status(conv.conv_device_error, True) == "CONV_ERR_DEVICE"
+
+
+def _layer_problem(L, flags=0):
+    return conv.make_problem((L.n, L.c_in, L.h, L.w), (L.c_out, L.c_in // L.groups, L.kh, L.kw),
+                             dtype=L.dtype, stride=L.stride, pads=L.pads, dilation=L.dilation,
+                             groups=L.groups, act=L.act, alpha=L.alpha, has_bias=L.bias,
+                             has_residual=L.residual_shape is not None, flags=flags)
+
+
+EXPECTED_VARIANT = {
+    "small_3x3_f32": "igemm_ffma", "resnet50_stem_f16": "igemm_tcgen05",
+    "resnet50_3x3_f16": "igemm_tcgen05", "resnet50_1x1_res_f16": "igemm_tcgen05",
+    "mbv3_dw5x5_f32": "depthwise_halo", "mbv3_dw5x5_f16": "depthwise_halo",
+    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05",
+    "grouped_dil2_f32": "igemm_ffma", "late_1x1_splitk_f32": "igemm_ffma_split_k",
+    "strided_3x3_s2_f32": "igemm_ffma",
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAYERS))
+def test_plans_of_the_workloads(lib, name):
+    L = LAYERS[name]
+    p = _layer_problem(L)
+    plan = conv.conv_plan(p, 152)
+    assert plan["variant_name"] == EXPECTED_VARIANT[name], plan
+    assert (plan["ho"], plan["wo"]) == conv.conv_output_shape(p)
+    assert plan["gemm_k"] == (L.c_in // L.groups) * L.kh * L.kw
+    assert plan["gemm_n"] == L.n * plan["ho"] * plan["wo"]
+    y_elems = L.n * L.c_out * plan["ho"] * plan["wo"]
+    if plan["split_k"] > 1:
+        assert plan["scratch_bytes"] == plan["split_k"] * y_elems * 4
+        assert plan["ctas"] <= 2 * 152
+    else:
+        assert plan["scratch_bytes"] == 0
+    assert conv.conv_plan(p, 152) == plan      # a pure function of (problem, SMs)
+
+
+def test_split_k_rule(lib):
+    L = LAYERS["late_1x1_splitk_f32"]
+    p = _layer_problem(L)
+    a, b = conv.conv_plan(p, 152), conv.conv_plan(p, 148)
+    assert a["split_k"] > 1 and b["split_k"] > 1
+    # every range but the last is a multiple of the 8-term stage; ranges cover k
+    K = a["gemm_k"]
+    per = -(-K // a["split_k"])
+    assert a["split_k"] <= 16 and K / a["split_k"] >= 128
+    # forcing: none, or an exact count
+    q = _layer_problem(L, flags=conv.FLAG_NO_SPLIT_K)
+    assert conv.conv_plan(q, 152)["split_k"] == 1 and conv.conv_plan(q, 152)["scratch_bytes"] == 0
+    q = _layer_problem(L, flags=4 << conv.SPLIT_K_SHIFT)
+    assert conv.conv_plan(q, 152)["split_k"] == 4
+    # a grid that already fills the device does not split
+    big = LAYERS["strided_3x3_s2_f32"]
+    assert conv.conv_plan(_layer_problem(big), 152)["split_k"] == 1
+    assert per >= 128
+
+
+def test_force_ffma_flag(lib):
+    for name in ("resnet50_stem_f16", "mbv3_dw5x5_f32"):
+        p = _layer_problem(LAYERS[name], flags=conv.FLAG_FORCE_FFMA)
+        assert conv.conv_plan(p, 152)["variant_name"].startswith("igemm_ffma")
+
+
+def test_plan_rejects_bad_sm_count(lib):
+    p = _layer_problem(LAYERS["small_3x3_f32"])
+    assert _status(conv.conv_plan, p, 0) == "CONV_ERR_ARG"
