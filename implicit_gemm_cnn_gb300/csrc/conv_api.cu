@@ -140,32 +140,37 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   out->k_per_split = static_cast<int>(len);
 }
 
-bool plan_depthwise(const conv_problem* p, const Shape& s, Plan* out) {
-  constexpr int QW = 4;
+bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
+  constexpr int QW = 8;                       // outputs per thread along a row
+  const int es = p->dtype == CONV_F32 ? 4 : 2;
+  const int al = 16 / es;                     // elements per 16 bytes
   DwPlan d;
-  d.lm = static_cast<int>((p->pad_left + 3) / 4 * 4);
+  d.lm = static_cast<int>((p->pad_left + al - 1) / al * al);  // image column 0 on a 16-byte boundary
   const long long strips = (s.wo + QW - 1) / QW;
-  const long long need = d.lm - p->pad_left + (strips * QW - 1) * p->stride_w + (p->kw - 1) * p->dil_w + 1;
+  // columns the last strip's windows reach (+1 for the paired loads)
+  const long long need = d.lm - p->pad_left + (strips * QW - 1) * p->stride_w + (p->kw - 1) * p->dil_w + 2;
   long long row = std::max<long long>(d.lm + p->w, need);
-  row = (row + 3) / 4 * 4;
-  const long long wfl = (s.mg * p->kh * p->kw + 3) / 4 * 4;
-  const long long budget = 40 * 1024 / 4 - wfl;  // floats
-  if (row > 1 << 20 || budget <= 0) return false;
-  long long th = s.ho;
+  row = (row + al - 1) / al * al;
+  const long long wbytes = 2 * ((s.mg * p->kh * p->kw + 3) / 4 * 4) * 4;
+  const long long per_elem = 2LL * es + (es == 4 ? 0 : 4);  // two staging buffers (+ fp32 tile)
+  const long long budget = 16 * 1024 - wbytes;              // bytes: ~12 blocks per SM
+  if (row > (1 << 20) || wbytes > 64 * 1024) return false;
   auto in_rows = [&](long long t) { return (t - 1) * p->stride_h + (p->kh - 1) * p->dil_h + 1; };
-  while (th > 1 && in_rows(th) * row > budget) th = (th + 1) / 2;
-  if (in_rows(th) * row > budget) return false;
+  long long th = s.ho;
+  while (th > 1 && in_rows(th) * row * per_elem > budget) th = (th + 1) / 2;
+  if (in_rows(th) * row * per_elem + wbytes > 200 * 1024) return false;
   d.th = static_cast<int>(th);
   d.in_rows = static_cast<int>(in_rows(th));
   d.row = static_cast<int>(row);
   d.vec = 0;
-  d.threads = 256;
+  d.sm = sm;
   out->dw = d;
   out->info.variant = CONV_VARIANT_DEPTHWISE;
   out->info.split_k = 1;
   out->info.tile_m = static_cast<int>(s.mg);
   out->info.tile_n = static_cast<int>(th * s.wo);
-  out->info.ctas = p->n * p->groups * ((s.ho + th - 1) / th);
+  const long long items = p->n * p->groups * ((s.ho + th - 1) / th);
+  out->info.ctas = std::min<long long>(items, 12LL * sm);
   out->info.scratch_bytes = 0;
   return true;
 }
@@ -222,7 +227,7 @@ conv_status make_plan(const conv_problem* p, int sm, Plan* out, Shape* shape) {
   out->info.gemm_k = s.K;
   const bool force_ffma = (p->flags & CONV_FLAG_FORCE_FFMA) != 0;
   bool done = false;
-  if (!force_ffma && s.cg == 1) done = plan_depthwise(p, s, out);
+  if (!force_ffma && s.cg == 1) done = plan_depthwise(p, s, sm, out);
   if (!done && !force_ffma) done = plan_tc(p, s, sm, out);
   if (!done) plan_ffma(p, s, sm, out);
   if (shape) *shape = s;
@@ -412,9 +417,14 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
   cudaError_t err = cudaSuccess;
   switch (plan.info.variant) {
     case CONV_VARIANT_DEPTHWISE: {
-      const int rt = static_cast<int>((s.ho + plan.dw.th - 1) / plan.dw.th);
-      plan.dw.vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && ((a.hw * es) % 16 == 0) &&
-                    (((p->w * es) % 16 == 0) || rt == 1);
+      // widest cp.async copy that keeps every plane and row start aligned
+      plan.dw.vec = 0;
+      for (int cb = 16; cb >= 4; cb /= 2) {
+        if (reinterpret_cast<uintptr_t>(x) % cb == 0 && (a.hw * es) % cb == 0 && (p->w * es) % cb == 0) {
+          plan.dw.vec = cb;
+          break;
+        }
+      }
       err = launch_depthwise(plan, a, p->dtype, cs);
       break;
     }

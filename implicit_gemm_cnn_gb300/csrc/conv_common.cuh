@@ -80,6 +80,17 @@ __device__ __forceinline__ float activate(float t, int act, float alpha, float b
   }
 }
 
+// The epilogue on values already in registers (bias and residual converted to
+// float32 exactly): the same steps and roundings as epilogue() below.
+template <typename T>
+__device__ __forceinline__ T epilogue_vals(float acc, float bias, float res, bool has_bias,
+                                           bool has_res, int act, float alpha, float beta) {
+  float t = acc;
+  if (has_bias) t = __fadd_rn(t, bias);
+  if (has_res) t = __fadd_rn(t, res);
+  return from_f32<T>(activate(t, act, alpha, beta));
+}
+
 // t = acc; t += bias[co]; t += residual[out_index]; t = act(t); round to T.
 template <typename T>
 __device__ __forceinline__ T epilogue(float acc, int co, long long out_index, const ConvArgs& a) {

@@ -29,13 +29,14 @@ size_t ffma_smem_bytes(int cfg, int dtype);
 
 // Depthwise (one input channel per group) halo-tiled direct kernel.
 struct DwPlan {
-  int th;        // output rows per block
-  int in_rows;   // input rows staged per block
-  int lm;        // left margin (columns before input column 0)
+  int th;        // output rows per work item
+  int in_rows;   // input rows staged per work item
+  int lm;        // left margin (columns before input column 0), 16-byte aligned
   int row;       // staged row length in elements (>= lm + needed columns)
-  int vec;       // bytes per vector copy of an input row (0: element copies)
-  int threads;
+  int vec;       // bytes per cp.async copy of input rows (16/8/4; 0: element copies)
+  int sm;        // SMs of the device (blocks loop over the work items)
 };
+size_t depthwise_smem_bytes(const DwPlan& d, int mg, int kh, int kw, int dtype);
 
 // tcgen05 implicit GEMM: 128 pixels x BN output channels per tile.
 struct TcPlan {

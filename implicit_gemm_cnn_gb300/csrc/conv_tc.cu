@@ -171,7 +171,7 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
 }
 
 struct TcLayout {
-  uint32_t b_off, stg_off, a_off, tab_off, bar_off, slot_off, end;
+  uint32_t b_off, stg_off, a_off, tab_off, bias_off, bar_off, slot_off, end;
 };
 
 __host__ __device__ inline TcLayout tc_layout(int bn, int k_pad, int stages, int tap_major,
@@ -182,7 +182,8 @@ __host__ __device__ inline TcLayout tc_layout(int bn, int k_pad, int stages, int
   L.stg_off = L.a_off + static_cast<uint32_t>(stages) * kStageBytes;
   L.tab_off = L.stg_off + static_cast<uint32_t>((stg_bytes + 15) / 16 * 16);
   const int ntab = tap_major ? k_pad / 8 : k_pad;
-  L.bar_off = L.tab_off + static_cast<uint32_t>(ntab) * 16;
+  L.bias_off = L.tab_off + static_cast<uint32_t>(ntab) * 16;
+  L.bar_off = L.bias_off + static_cast<uint32_t>(bn) * 4;
   L.slot_off = L.bar_off + static_cast<uint32_t>(2 * stages + 7) * 8;
   L.end = L.slot_off + 16;
   return L;
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
   uint8_t* sA = tsm + L.a_off;
   uint16_t* stg = reinterpret_cast<uint16_t*>(tsm + L.stg_off);
   int4* tab = reinterpret_cast<int4*>(tsm + L.tab_off);
+  float* sbias = reinterpret_cast<float*>(tsm + L.bias_off);
   const uint32_t bar0 = smem_u32(tsm + L.bar_off);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
@@ -315,9 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       fence_proxy_async();
       mbar_arrive(wready_bar);
     }
-    // epilogue
+    // epilogue: bias of the block's channel tile staged once in shared memory
+    for (int c = tid; c < BN; c += kEpiWarps * 32)
+      sbias[c] = (a.bias && c < rows_valid) ? to_f32(static_cast<const T*>(a.bias)[g * a.mg + co0 + c]) : 0.0f;
+    asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiWarps * 32) : "memory");  // epilogue warps only
     const int row = warp * 32 + lane;
-    T* y = static_cast<T*>(a.y);
+    T* __restrict__ y = static_cast<T*>(a.y);
+    const T* __restrict__ res = static_cast<const T*>(a.residual);
+    const bool has_bias = a.bias != nullptr, has_res = res != nullptr;
     for (int t = 0; ok && t < ntiles; ++t) {
       const int b = t & 1;
       const uint32_t u = static_cast<uint32_t>(t >> 1);
@@ -332,18 +339,34 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
         obase = (n * a.c_out + static_cast<long long>(g) * a.mg + co0) * a.howo + (pix - n * a.howo);
       }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + b * BN;
+      // residual values of the next 16 channels are requested before this
+      // chunk's stores, so their latency overlaps the chunk's work
+      float rnext[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        rnext[jj] = (has_res && valid && jj < rows_valid)
+                        ? to_f32(__ldg(res + obase + static_cast<long long>(jj) * a.howo)) : 0.0f;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 16) {
+        float rcur[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) rcur[jj] = rnext[jj];
+        if (has_res && valid && c + 16 < BN) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int col = c + 16 + jj;
+            rnext[jj] = col < rows_valid ? to_f32(__ldg(res + obase + static_cast<long long>(col) * a.howo)) : 0.0f;
+          }
+        }
         uint32_t r[16];
         tmem_ld16(tbase + c, r);
         if (valid) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int col = c + jj;
-            if (col < rows_valid) {
-              const long long o = obase + static_cast<long long>(col) * a.howo;
-              y[o] = epilogue<T>(__uint_as_float(r[jj]), g * a.mg + co0 + col, o, a);
-            }
+            if (col < rows_valid)
+              y[obase + static_cast<long long>(col) * a.howo] = epilogue_vals<T>(
+                  __uint_as_float(r[jj]), sbias[col], rcur[jj], has_bias, has_res, a.act, a.alpha, a.beta);
           }
         }
       }
