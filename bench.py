@@ -1,0 +1,536 @@
+"""Benchmark of the forward convolution on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--layer NAME | --layers all]
+
+One step is one conv_forward over one batch of the workload layer: the
+ResNet-50 stem (N=8, 3->64, 7x7, stride 2, pad 3, 224->112, bias + ReLU,
+fp16) by default.  Inputs are seeded synthetic tensors of the layer's shapes
+and distributions, resident in HBM; the step rotates over enough independent
+input sets that their total exceeds twice the L2, so every step reads its
+operands from HBM.  The K timed steps are replayed from CUDA graphs of
+back-to-back launches; the region is bracketed by a barrier and device
+synchronisation, timed with CUDA events, and the max over ranks is taken.
+
+The JSON line also carries: the roofline of the main kernel (algorithmic bytes
+or FLOPs of one launch over the launch's duration measured with CUDA events
+captured in the same graphs, against the measured peaks), the end-to-end rate
+through the public API with pinned host buffers, the CPU oracle's rate on a
+bounded sample (test infrastructure, timed only here), the kernel launch
+count and the SM clocks seen.
+
+--impl reference times the CPU oracle itself on the same workload and metric,
+one bounded sample per step.  --layers all prints one line per workload layer.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "conv TFLOP/s (2·N·Ho·Wo·Co·Ci·k²/g) and depthwise GB/s, % of roofline"
+HEADLINE = "resnet50_stem_f16"
+L2_BYTES = 129 * 1024 * 1024
+# float32 FFMA peak: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
+FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+# ---- layer arithmetic (closed forms; no convolution is evaluated here) -----
+def out_hw(L):
+    ho = (L.h + L.pads[0] + L.pads[2] - L.dilation[0] * (L.kh - 1) - 1) // L.stride[0] + 1
+    wo = (L.w + L.pads[1] + L.pads[3] - L.dilation[1] * (L.kw - 1) - 1) // L.stride[1] + 1
+    return ho, wo
+
+
+def layer_flops(L) -> int:
+    ho, wo = out_hw(L)
+    return 2 * L.n * ho * wo * L.c_out * (L.c_in // L.groups) * L.kh * L.kw
+
+
+def layer_bytes(L) -> int:
+    """Algorithmic bytes: every operand read once, the output written once."""
+    ho, wo = out_hw(L)
+    es = 4 if L.dtype == "f32" else 2
+    y = L.n * L.c_out * ho * wo
+    elems = (L.n * L.c_in * L.h * L.w + L.c_out * (L.c_in // L.groups) * L.kh * L.kw
+             + (L.c_out if L.bias else 0) + (y if L.residual_shape else 0) + y)
+    return elems * es
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def roofline_bound(L, variant: str, pk: dict) -> tuple[str, float, str]:
+    """(bound, peak, unit) of the layer's binding roofline: HBM when its
+    arithmetic intensity is below the ridge of its compute path."""
+    intensity = layer_flops(L) / layer_bytes(L)
+    if variant.startswith("depthwise"):
+        compute, kind = FFMA_PEAK_TFLOPS, "alu"
+    elif variant.startswith("igemm_tcgen05"):
+        compute, kind = pk["bf16_tflops"], "tensor"  # fp16 and bf16 share the dense rate
+    else:
+        compute, kind = FFMA_PEAK_TFLOPS, "alu"
+    ridge = compute * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if intensity < ridge:
+        return "hbm", pk["hbm_gbs"], "GB/s"
+    return kind, compute, "TFLOP/s"
+
+
+def kernel_source(variant: str) -> str:
+    name = {"igemm_tcgen05": "conv_tc.cu", "depthwise_halo": "conv_depthwise.cu"}.get(
+        variant.split()[0], "conv_ffma.cu")
+    return os.path.join(ROOT, "implicit_gemm_cnn_gb300", "csrc", name)
+
+
+def profiled_traffic(layer_name: str, variant: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if the kernel source is unchanged since the capture."""
+    src = kernel_source(variant)
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    prof_dir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof_dir):
+        return None
+    for fn in sorted(os.listdir(prof_dir)):
+        if layer_name not in fn:
+            continue
+        text = open(os.path.join(prof_dir, fn)).read()
+        m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+        t = re.search(r"dram_bytes_per_launch:\s*([0-9.e+]+)", text)
+        if m and t and m.group(1) == digest:
+            return float(t.group(1))
+    return None
+
+
+# ---- distributed helpers (also exercised by the CPU gloo tests) ----------
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(per_rank_units: float, world: int, seconds_max: float) -> float:
+    """Whole-job rate: units of all ranks over the slowest rank's time."""
+    return per_rank_units * world / seconds_max
+
+
+# ---- clocks --------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---- our implementation --------------------------------------------------
+def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
+             with_cpu_baseline: bool, with_e2e: bool, quick: bool = False) -> dict:
+    import torch
+
+    import implicit_gemm_cnn_gb300 as conv
+    from workloads import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    geo = dict(stride=L.stride, pads=L.pads, dilation=L.dilation, groups=L.groups, act=L.act,
+               alpha=L.alpha, beta=L.beta)
+    p = conv.make_problem((L.n, L.c_in, L.h, L.w), (L.c_out, L.c_in // L.groups, L.kh, L.kw),
+                          dtype=L.dtype, has_bias=L.bias, has_residual=L.residual_shape is not None,
+                          **geo)
+    ho, wo = conv.conv_output_shape(p)
+    variant = conv.conv_describe_variant(p)
+    need = conv.conv_scratch_bytes(p)
+    plan = conv.conv_plan(p, torch.cuda.get_device_properties(local_rank).multi_processor_count)
+    launches_per_step = 2 if plan["split_k"] > 1 else 1
+    set_bytes = layer_bytes(L)
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    sets = []
+    for s in range(nsets):
+        inp = make_inputs(L, seed_offset=s + 1000 * rank)
+        t = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+        t["y"] = torch.empty((L.n, L.c_out, ho, wo), dtype=t["x"].dtype, device=dev)
+        t["scratch"] = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        sets.append(t)
+
+    def step(i):
+        t = sets[i % nsets]
+        conv.conv_forward(p, t["x"], t["w"], t["bias"], t["residual"], t["y"], t["scratch"], need)
+
+    # W untimed warm-up steps through the public call
+    for i in range(max(warmup, nsets)):
+        step(i)
+    torch.cuda.synchronize()
+
+    # graphs of back-to-back launches, with external events around each launch
+    chunk = max(1, min(steps, max(nsets, 500)))
+
+    def capture(n, with_events=True):
+        evs = None
+        if with_events:
+            try:
+                evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                        torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
+            except TypeError:  # a torch without external events
+                evs = None
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        try:
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n):
+                    if evs:
+                        evs[i][0].record()
+                    step(i)
+                    if evs:
+                        evs[i][1].record()
+        except RuntimeError:
+            if not evs:
+                raise
+            torch.cuda.synchronize()
+            return capture(n, with_events=False)
+        torch.cuda.synchronize()
+        return g, evs
+
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if quick:
+        # eager launches, no graphs or clock settling: for profiler captures
+        sampler = ClockSampler(local_rank).start()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        clocks = sampler.stop()
+        ev_full, full_reps = None, 0
+    else:
+        g_full, ev_full = capture(chunk)
+        full_reps, rem = divmod(steps, chunk)
+        g_rem = capture(rem)[0] if rem else None
+        # settle clocks under load (untimed); clocks are sampled through the timed region
+        sampler = ClockSampler(local_rank).start()
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            g_full.replay()
+            torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(full_reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        clocks = sampler.stop()
+    secs = e0.elapsed_time(e1) / 1e3
+    secs_max = max_over_ranks(secs, world)
+
+    # per-launch durations: the events captured in the full-chunk graph, as
+    # recorded by its last replay inside the timed region
+    launch_ms = None
+    if ev_full and full_reps > 0:
+        try:
+            d = [a.elapsed_time(b) for a, b in ev_full]
+            launch_ms = statistics.mean(d)
+        except RuntimeError:
+            launch_ms = None
+    if launch_ms is None:
+        launch_ms = secs * 1e3 / steps
+
+    flops = layer_flops(L)
+    value = aggregate(flops * steps, world, secs_max) / 1e12
+    pk = peaks()
+    bound, peak, unit = roofline_bound(L, variant, pk)
+    per_launch = layer_bytes(L) if bound == "hbm" else flops
+    achieved = per_launch / (launch_ms / 1e3) / (1e9 if unit == "GB/s" else 1e12)
+    roof = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(L.name, variant),
+            "peak_source": pk["source"], "algorithmic_per_launch": per_launch,
+            "launch_us": round(launch_ms * 1e3, 3),
+            "tensor_or_alu_frac": round(flops / (launch_ms / 1e3) / 1e12 / (
+                pk["bf16_tflops"] if variant.startswith("igemm_tcgen05") else FFMA_PEAK_TFLOPS), 4)}
+
+    out = {"value": value, "secs": secs_max, "variant": variant, "roofline": roof,
+           "clocks": clocks, "launches": launches_per_step * steps, "nsets": nsets,
+           "set_bytes": set_bytes, "chunk": chunk}
+
+    if with_e2e:
+        out["e2e"] = e2e_rate(L, p, sets[0], need, min(steps, 200), dev)
+    if with_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(L, target_s=10.0)
+    return out
+
+
+def e2e_rate(L, p, t, need, steps, dev) -> dict:
+    """Through the public API: pinned host input -> device, conv2d, result ->
+    pinned host, every step."""
+    import torch
+
+    import implicit_gemm_cnn_gb300 as conv
+    x_host = t["x"].cpu().pin_memory()
+    y_host = torch.empty(t["y"].shape, dtype=t["y"].dtype).pin_memory()
+    x_dev = torch.empty_like(t["x"])
+    geo = dict(stride=L.stride, pads=L.pads, dilation=L.dilation, groups=L.groups, act=L.act,
+               alpha=L.alpha, beta=L.beta)
+    scratch = t["scratch"] if need else None
+
+    def step():
+        x_dev.copy_(x_host, non_blocking=True)
+        conv.conv2d(x_dev, t["w"], t["bias"], t["residual"], out=t["y"], scratch=scratch, **geo)
+        y_host.copy_(t["y"], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) / 1e3
+    return {"value": layer_flops(L) * steps / secs / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+            "d2h_bytes_per_step": y_host.numel() * y_host.element_size(), "steps": steps}
+
+
+# ---- the CPU oracle (reported baseline / reference arm) -------------------
+def _oracle_setup(L):
+    import numpy as np
+
+    import oracle
+    from workloads import make_inputs, to_numpy_operand
+    inp = make_inputs(L)
+    ops = [to_numpy_operand(inp[k], L.dtype) for k in ("x", "w", "bias", "residual")]
+    o = oracle.Oracle()
+    kw = dict(dtype=L.dtype, stride=L.stride, pads=L.pads, dilation=L.dilation, groups=L.groups,
+              act=L.act, alpha=L.alpha, beta=L.beta)
+    ho, wo = out_hw(L)
+    total = L.n * L.c_out * ho * wo
+    per_out_flops = 2 * (L.c_in // L.groups) * L.kh * L.kw
+    return o, ops, kw, total, per_out_flops, np
+
+
+def cpu_baseline(L, target_s: float = 10.0) -> dict:
+    """The oracle as it stands on this host's cores, on a bounded sample of
+    the workload's outputs (about target_s seconds of CPU work)."""
+    o, ops, kw, total, per_out, np = _oracle_setup(L)
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(total, min(total, 20000), replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    o.conv2d(*ops, index=probe, nthreads=cores, **kw)
+    rate = len(probe) / max(time.perf_counter() - t0, 1e-6)   # outputs / s
+    count = int(min(total, max(len(probe), rate * target_s)))
+    idx = np.sort(rng.choice(total, count, replace=False)).astype(np.int64) if count < total else None
+    t0 = time.perf_counter()
+    o.conv2d(*ops, index=idx, nthreads=cores, **kw)
+    secs = time.perf_counter() - t0
+    return {"value": count * per_out / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "seconds": round(secs, 2),
+            "sample": f"{count} of {total} outputs ({'all' if idx is None else 'random'}) of one "
+                      f"batch, float64 sums, {cores} threads"}
+
+
+def run_reference(L, steps: int, warmup: int) -> dict:
+    """The reference arm: the CPU oracle, each step a bounded sample of the
+    workload, sized so that the whole run takes about a minute."""
+    o, ops, kw, total, per_out, np = _oracle_setup(L)
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(1)
+    probe = np.sort(rng.choice(total, min(total, 20000), replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    o.conv2d(*ops, index=probe, nthreads=cores, **kw)
+    rate = len(probe) / max(time.perf_counter() - t0, 1e-6)
+    per_step = int(max(1, min(total, rate * 60.0 / max(steps + warmup, 1))))
+    samples = [np.sort(rng.choice(total, per_step, replace=False)).astype(np.int64)
+               for _ in range(min(steps, 64))]
+    for i in range(warmup):
+        o.conv2d(*ops, index=samples[i % len(samples)], nthreads=cores, **kw)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        o.conv2d(*ops, index=samples[i % len(samples)], nthreads=cores, **kw)
+    secs = time.perf_counter() - t0
+    value = per_step * per_out * steps / secs / 1e12
+    return {"value": value, "secs": secs, "per_step": per_step, "cores": cores, "total": total}
+
+
+# ---- main ----------------------------------------------------------------
+def describe(L) -> str:
+    return L.description or L.name
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layer", default=HEADLINE)
+    ap.add_argument("--layers", default=None, help="'all': one line per workload layer")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="eager launches only, no e2e / CPU baseline (for profiler captures)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from workloads import LAYERS
+    rank, world, local_rank = dist_env()
+    names = sorted(LAYERS) if args.layers == "all" else [args.layer]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        for name in names:
+            L = LAYERS[name]
+            r = run_reference(L, args.steps, args.warmup)
+            line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": args.gpus,
+                    "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": r["secs"] * 1e3 / args.steps, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+                    "data": "synthetic (seeded)",
+                    "config": {"workload": describe(L), "layer": L.name,
+                               "sample_outputs_per_step": r["per_step"],
+                               "outputs_per_batch": r["total"]},
+                    "cpu_baseline": {"value": r["value"], "unit": "TFLOP/s", "cores": r["cores"],
+                                     "kind": "oracle",
+                                     "sample": f"{r['per_step']} random outputs of one batch per step"},
+                    "e2e": {"value": r["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    for name in names:
+        L = LAYERS[name]
+        r = run_ours(L, args.steps, args.warmup, world, rank, local_rank,
+                     with_cpu_baseline=(rank == 0 and world == 1 and not args.no_cpu_baseline
+                                        and not args.quick),
+                     with_e2e=not args.quick, quick=args.quick)
+        if rank != 0:
+            continue
+        line = {"metric": METRIC, "value": round(r["value"], 4), "unit": "TFLOP/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": r["secs"] * 1e3 / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": L.dtype,
+                "data": "synthetic (seeded; the layer's shapes and value distributions; random weights)",
+                "config": {"workload": describe(L), "layer": L.name, "global_batch": L.n * world,
+                           "accumulate": "f32", "variant": r["variant"],
+                           "l2": f"inputs larger than L2: {r['nsets']} rotating sets of "
+                                 f"{r['set_bytes'] / 1e6:.2f} MB",
+                           "timing": ("eager launches" if args.quick else
+                                      f"CUDA graphs of {r['chunk']} back-to-back steps"),
+                           "parallelism": f"replicas x{world}"},
+                "roofline": r["roofline"], "gpu_launches": r["launches"], "clocks": r["clocks"],
+                "e2e": r.get("e2e")}
+        if "cpu_baseline" in r:
+            line["cpu_baseline"] = r["cpu_baseline"]
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
