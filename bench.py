@@ -232,7 +232,7 @@ def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
     plan = conv.conv_plan(p, torch.cuda.get_device_properties(local_rank).multi_processor_count)
     launches_per_step = 2 if plan["split_k"] > 1 else 1
     set_bytes = layer_bytes(L)
-    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    nsets = max(1, min(256, math.ceil(2 * L2_BYTES / set_bytes)))  # tiny layers stay L2-resident
     sets = []
     for s in range(nsets):
         inp = make_inputs(L, seed_offset=s + 1000 * rank)
@@ -516,8 +516,11 @@ def main(argv=None) -> int:
                 "data": "synthetic (seeded; the layer's shapes and value distributions; random weights)",
                 "config": {"workload": describe(L), "layer": L.name, "global_batch": L.n * world,
                            "accumulate": "f32", "variant": r["variant"],
-                           "l2": f"inputs larger than L2: {r['nsets']} rotating sets of "
-                                 f"{r['set_bytes'] / 1e6:.2f} MB",
+                           "l2": (f"inputs larger than L2: {r['nsets']} rotating sets of "
+                                  f"{r['set_bytes'] / 1e6:.2f} MB"
+                                  if r["nsets"] * r["set_bytes"] > L2_BYTES else
+                                  f"L2-resident: {r['nsets']} rotating sets of "
+                                  f"{r['set_bytes'] / 1e6:.3f} MB total below L2"),
                            "timing": ("eager launches" if args.quick else
                                       f"CUDA graphs of {r['chunk']} back-to-back steps"),
                            "parallelism": f"replicas x{world}"},
