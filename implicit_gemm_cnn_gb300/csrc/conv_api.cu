@@ -15,9 +15,6 @@
 
 #include "conv_internal.h"
 
-namespace conv {
-size_t tc_smem_bytes(int bn, int k_pad, int stages, int tap_major, long long stg_bytes);
-}
 
 using namespace conv;
 
@@ -175,39 +172,33 @@ bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   return true;
 }
 
+// Geometry part of the kernel arguments (no addresses).
+void shape_args(const conv_problem* p, const Shape& s, ConvArgs* a) {
+  memset(a, 0, sizeof(*a));
+  a->n = static_cast<int>(p->n); a->c_in = static_cast<int>(p->c_in);
+  a->h = static_cast<int>(p->h); a->w = static_cast<int>(p->w);
+  a->c_out = static_cast<int>(p->c_out); a->kh = static_cast<int>(p->kh); a->kw = static_cast<int>(p->kw);
+  a->pt = static_cast<int>(p->pad_top); a->pl = static_cast<int>(p->pad_left);
+  a->sh = static_cast<int>(p->stride_h); a->sw = static_cast<int>(p->stride_w);
+  a->dh = static_cast<int>(p->dil_h); a->dw = static_cast<int>(p->dil_w);
+  a->groups = static_cast<int>(p->groups); a->cg = static_cast<int>(s.cg); a->mg = static_cast<int>(s.mg);
+  a->ho = static_cast<int>(s.ho); a->wo = static_cast<int>(s.wo);
+  a->K = static_cast<int>(s.K);
+  a->hw = p->h * p->w; a->howo = s.ho * s.wo; a->npix = s.npix;
+  a->act = p->act; a->alpha = p->act_alpha; a->beta = p->act_beta;
+}
+
 bool plan_tc(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   if (p->dtype == CONV_F32) return false;
-  static const int bns[] = {256, 128, 64, 48, 32};
-  int bn = 0;
-  long long best = -1;
-  for (int cand : bns) {  // least padded channels; ties go to the wider tile
-    const long long padded = (s.mg + cand - 1) / cand * cand;
-    if (best < 0 || padded < best) { best = padded; bn = cand; }
-  }
+  ConvArgs a;
+  shape_args(p, s, &a);
+  a.residual = p->has_residual ? reinterpret_cast<const void*>(16) : nullptr;  // presence only
   TcPlan t;
-  t.bn = bn;
-  t.k_pad = static_cast<int>((s.K + 63) / 64 * 64);
-  t.tap_major = (s.cg % 8 == 0) ? 1 : 0;
-  t.co_tiles = static_cast<int>((s.mg + bn - 1) / bn);
-  const long long pix_tiles = (s.npix + 127) / 128;
-  if (pix_tiles > kI32) return false;
-  t.pix_tiles = static_cast<int>(pix_tiles);
-  const long long stg = std::min<long long>(bn, s.mg) * s.K * 2;
-  t.stages = 0;
-  for (int st = 4; st >= 2; --st) {
-    if (tc_smem_bytes(bn, t.k_pad, st, t.tap_major, stg) <= kMaxDynSmem) { t.stages = st; break; }
-  }
-  if (!t.stages) return false;
-  t.smem = tc_smem_bytes(bn, t.k_pad, t.stages, t.tap_major, stg);
-  const long long combos = p->groups * t.co_tiles;
-  long long cpc = combos >= sm ? 1 : std::min<long long>(pix_tiles, sm / combos);
-  if (cpc < 1) cpc = 1;
-  if (combos * cpc > kI32) return false;
-  t.ctas = static_cast<int>(combos * cpc);
+  if (!tc_plan(a, sm, &t)) return false;
   out->tc = t;
   out->info.variant = CONV_VARIANT_IGEMM_TC;
   out->info.split_k = 1;
-  out->info.tile_m = bn;
+  out->info.tile_m = t.bn;
   out->info.tile_n = 128;
   out->info.ctas = t.ctas;
   out->info.scratch_bytes = 0;
@@ -351,10 +342,10 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
   if (st != CONV_OK) return st;
   const conv_plan_info& i = plan.info;
   if (i.variant == CONV_VARIANT_IGEMM_TC) {
+    static const char* orders[] = {"tap/8-channel", "channel/row/8-tap", "channel/tap"};
     snprintf(buf, len, "%s tile=128px x %dco k=%lld (padded %d, %s order) stages=%d blocks=%lld sms=%d",
              variant_name(i.variant), plan.tc.bn, static_cast<long long>(i.gemm_k), plan.tc.k_pad,
-             plan.tc.tap_major ? "tap-major" : "channel-major", plan.tc.stages,
-             static_cast<long long>(i.ctas), sm);
+             orders[plan.tc.mode], plan.tc.stages, static_cast<long long>(i.ctas), sm);
   } else if (i.variant == CONV_VARIANT_DEPTHWISE) {
     snprintf(buf, len, "%s rows/block=%d staged=%dx%d blocks=%lld sms=%d", variant_name(i.variant),
              plan.dw.th, plan.dw.in_rows, plan.dw.row, static_cast<long long>(i.ctas), sm);
@@ -397,18 +388,7 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
   }
 
   ConvArgs a;
-  memset(&a, 0, sizeof(a));
-  a.n = static_cast<int>(p->n); a.c_in = static_cast<int>(p->c_in);
-  a.h = static_cast<int>(p->h); a.w = static_cast<int>(p->w);
-  a.c_out = static_cast<int>(p->c_out); a.kh = static_cast<int>(p->kh); a.kw = static_cast<int>(p->kw);
-  a.pt = static_cast<int>(p->pad_top); a.pl = static_cast<int>(p->pad_left);
-  a.sh = static_cast<int>(p->stride_h); a.sw = static_cast<int>(p->stride_w);
-  a.dh = static_cast<int>(p->dil_h); a.dw = static_cast<int>(p->dil_w);
-  a.groups = static_cast<int>(p->groups); a.cg = static_cast<int>(s.cg); a.mg = static_cast<int>(s.mg);
-  a.ho = static_cast<int>(s.ho); a.wo = static_cast<int>(s.wo);
-  a.K = static_cast<int>(s.K);
-  a.hw = p->h * p->w; a.howo = s.ho * s.wo; a.npix = s.npix;
-  a.act = p->act; a.alpha = p->act_alpha; a.beta = p->act_beta;
+  shape_args(p, s, &a);
   a.x = x; a.wt = w; a.y = y;
   a.bias = p->has_bias ? bias : nullptr;
   a.residual = p->has_residual ? residual : nullptr;

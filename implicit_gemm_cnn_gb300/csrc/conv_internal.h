@@ -38,17 +38,23 @@ struct DwPlan {
 };
 size_t depthwise_smem_bytes(const DwPlan& d, int mg, int kh, int kw, int dtype);
 
-// tcgen05 implicit GEMM: 128 pixels x BN output channels per tile.
+// tcgen05 implicit GEMM: 128 pixels (of one image) x BN channels per tile.
+constexpr int kModeCh8 = 0;   // k = (tap, channel), units of 8 channels
+constexpr int kModeRow8 = 1;  // k = (channel, kernel row, 8 taps), 4-byte loads
+constexpr int kModeNat = 2;   // k = (channel, tap), one value at a time
+constexpr size_t kTcMaxSmem = 232448;  // 227 KB of dynamic shared memory per block
 struct TcPlan {
-  int bn;          // N tile (output channels), a multiple of 16
-  int k_pad;       // k padded to a multiple of 64
-  int tap_major;   // k ordered (tap, channel) with 8-channel chunks; else (channel, tap)
-  int stages;      // A-operand pipeline depth
-  int co_tiles;    // output-channel tiles per group
-  int pix_tiles;   // 128-pixel tiles
-  int ctas;        // persistent blocks
-  size_t smem;     // dynamic shared memory bytes
+  int bn;             // N tile (output channels), a multiple of 16
+  int mode;           // k order (kMode*)
+  int k_pad;          // k padded to a multiple of 64
+  int stages;         // A-operand pipeline depth
+  int co_tiles;       // output-channel tiles per group
+  int tiles_per_img;  // 128-pixel tiles per image
+  int pix_tiles;      // all pixel tiles (images x tiles per image)
+  int ctas;           // persistent blocks
+  size_t smem;        // dynamic shared memory bytes
 };
+bool tc_plan(const ConvArgs& a, int sm, TcPlan* t);
 
 struct Plan {
   conv_plan_info info;

@@ -10,31 +10,38 @@
 // W_g^T (K x Cout/G), K = Cin/G * kh * kw.
 //
 // Tiles and roles (one persistent block per SM, 13 warps):
-//   * a tile is 128 output pixels (flattened over the batch: MMA M = 128) x
-//     BN output channels (MMA N); its float32 accumulator lives in tensor
-//     memory, double buffered so the epilogue of one tile overlaps the next;
-//   * warps 4-11 gather the A operand: for each pixel row and each k chunk of
-//     64 terms they load 8 x 16-bit values per 16-byte unit from x, zero for
-//     taps outside the image, and store them into a 128-byte-swizzled K-major
-//     stage that tcgen05.mma reads directly.  k is ordered (tap, channel) when
-//     the channels per group are a multiple of 8 -- one window test per 8
-//     values, the channels one input plane apart, as "Convolution, pooling and
-//     resize" (Apple M2, taps innermost) orders its staging -- and (channel,
-//     tap) otherwise.  The window offsets come from a table decoded once per
-//     block;
+//   * a tile is 128 consecutive output pixels of one image (MMA M = 128) x BN
+//     output channels (MMA N); its float32 accumulator lives in tensor memory,
+//     double buffered so the epilogue of one tile overlaps the next;
+//   * warps 4-11 gather the A operand into 128-byte-swizzled K-major stages
+//     that tcgen05.mma reads directly, 16 bytes (8 k values) per store, zero
+//     for taps outside the image.  Three k orders: (tap, channel) with units
+//     of 8 channels when the channels per group are a multiple of 8 -- one
+//     window test per unit, as "Convolution, pooling and resize" (Apple M2,
+//     taps innermost) orders its staging; (channel, kernel row, 8 taps) for
+//     rows of 5..8 taps at dilation 1 -- one row test and five 4-byte loads
+//     plus byte permutes per unit, taps past the kernel width or the image
+//     masked per pixel; (channel, tap) otherwise.  Window offsets come from a
+//     table decoded once per block;
 //   * warps 0-3 first copy the block's weight rows into shared memory (one
 //     bulk copy of the OIHW rows, then a permutation into the swizzled K-major
 //     layout in the same k order -- the weight re-layout that "Convolution,
 //     pooling and resize" measured at 1.27x on 3x3 layers, done on chip), then
-//     run the epilogue: tcgen05.ld of the accumulator (thread = pixel, so each
-//     warp's stores of one channel are 32 consecutive pixels of NCHW y),
-//     bias, residual, activation in float32, one rounding to the element type;
+//     run the epilogue: tcgen05.ld of the accumulator (thread = pixel), bias,
+//     residual, activation in float32, one rounding to the element type.  The
+//     tile is staged in shared memory as one 256-byte row per channel and
+//     written with bulk copies (each row is contiguous in NCHW y); the
+//     residual tile arrives the same way ahead of its use.  Shapes or
+//     addresses that do not allow that (Ho*Wo not a multiple of 8, unaligned
+//     y) store from registers instead;
 //   * warp 12 allocates tensor memory and one lane issues the MMAs
 //     (kind::f16, M=128, N=BN, K=16 per instruction) and the commits that
 //     release stages and accumulators.
 // Every mbarrier wait is bounded: after kWaitNs the waiting thread flags the
-// block and the device error word, every role drains out, outstanding MMAs are
-// waited for (bounded again) and tensor memory is freed before exit.
+// block and the device error word, every role drains out, outstanding copies
+// and MMAs are waited for (bounded again) and tensor memory is freed before
+// exit.
+#include <algorithm>
 #include <type_traits>
 
 #include "conv_internal.h"
@@ -170,36 +177,74 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-struct TcLayout {
-  uint32_t b_off, stg_off, a_off, tab_off, bias_off, bar_off, slot_off, end;
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src_smem),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() {  // the four epilogue warps only
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiWarps * 32) : "memory");
+}
+
+// Launch-time choices that depend on the operands' addresses.
+struct TcLaunch {
+  int mode;             // kModeCh8 / kModeRow8 / kModeNat
+  int k_pad;
+  int stages;
+  int epi_bulk;         // stage the tile in shared memory, bulk-copy rows in/out
+  int nio;              // staging buffers (1 or 2)
+  int bulk_w;           // weights arrive by one bulk copy
+  long long stg_bytes;  // bytes of that copy
 };
 
-__host__ __device__ inline TcLayout tc_layout(int bn, int k_pad, int stages, int tap_major,
-                                              long long stg_bytes) {
+struct TcLayout {
+  uint32_t b_off, a_off, sio_off, tab_off, bias_off, bar_off, slot_off, end;
+};
+
+__host__ __device__ inline int tc_ntab(int mode, int k_pad) {
+  return mode == kModeNat ? k_pad : k_pad / 8;
+}
+
+__host__ __device__ inline TcLayout tc_layout(int bn, const TcLaunch& c) {
   TcLayout L;
   L.b_off = 0;
-  L.a_off = static_cast<uint32_t>(k_pad / kBK) * bn * 128;           // multiple of 1024
-  L.stg_off = L.a_off + static_cast<uint32_t>(stages) * kStageBytes;
-  L.tab_off = L.stg_off + static_cast<uint32_t>((stg_bytes + 15) / 16 * 16);
-  const int ntab = tap_major ? k_pad / 8 : k_pad;
-  L.bias_off = L.tab_off + static_cast<uint32_t>(ntab) * 16;
+  L.a_off = static_cast<uint32_t>(c.k_pad / kBK) * bn * 128;  // multiple of 1024
+  L.sio_off = L.a_off + static_cast<uint32_t>(c.stages) * kStageBytes;
+  // the weight staging copy is dead once the weights are laid out: the
+  // epilogue's tile buffers reuse its space
+  const long long stg = c.bulk_w ? (c.stg_bytes + 127) / 128 * 128 : 0;
+  const long long io = c.epi_bulk ? static_cast<long long>(c.nio) * bn * kM * 2 : 0;
+  L.tab_off = L.sio_off + static_cast<uint32_t>(stg > io ? stg : io);
+  L.bias_off = L.tab_off + static_cast<uint32_t>(tc_ntab(c.mode, c.k_pad)) * 16;
   L.bar_off = L.bias_off + static_cast<uint32_t>(bn) * 4;
-  L.slot_off = L.bar_off + static_cast<uint32_t>(2 * stages + 7) * 8;
+  L.slot_off = L.bar_off + static_cast<uint32_t>(2 * c.stages + 9) * 8;
   L.end = L.slot_off + 16;
   return L;
 }
 
 template <typename T, int BN>
-__global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const TcPlan p,
-                                                        long long stg_bytes, int bulk_ok) {
+__global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const TcPlan p, const TcLaunch c) {
   extern __shared__ uint8_t tsm_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   uint8_t* tsm = tsm_raw + ((1024 - (smem_u32(tsm_raw) & 1023)) & 1023);
-  const int S = p.stages;
-  const TcLayout L = tc_layout(BN, p.k_pad, S, p.tap_major, stg_bytes);
+  const int S = c.stages;
+  const TcLayout L = tc_layout(BN, c);
   uint8_t* sB = tsm + L.b_off;
   uint8_t* sA = tsm + L.a_off;
-  uint16_t* stg = reinterpret_cast<uint16_t*>(tsm + L.stg_off);
+  uint8_t* sio = tsm + L.sio_off;
+  const uint16_t* stg = reinterpret_cast<const uint16_t*>(sio);
   int4* tab = reinterpret_cast<int4*>(tsm + L.tab_off);
   float* sbias = reinterpret_cast<float*>(tsm + L.bias_off);
   const uint32_t bar0 = smem_u32(tsm + L.bar_off);
@@ -210,12 +255,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
   const uint32_t wready_bar = bar0 + 8u * (2 * S + 4);
   const uint32_t stg_bar = bar0 + 8u * (2 * S + 5);
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 6);
+  auto res_bar = [&](int i) { return bar0 + 8u * (2 * S + 7 + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tsm + L.slot_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tsm + L.slot_off + 4);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int kchunks = p.k_pad / kBK;
+  const int kchunks = c.k_pad / kBK;
   const int khw = a.kh * a.kw;
   constexpr uint32_t kCols = BN * 2 <= 32 ? 32 : (BN * 2 <= 64 ? 64 : (BN * 2 <= 128 ? 128 : (BN * 2 <= 256 ? 256 : 512)));
 
@@ -228,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), kEpiWarps * 32);
+      mbar_init(res_bar(b), 1);
     }
     mbar_init(wready_bar, kEpiWarps * 32);
     mbar_init(stg_bar, 1);
@@ -235,15 +282,29 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  const int ntab = p.tap_major ? p.k_pad / 8 : p.k_pad;
+  // window table: per 8-value unit (ch8: 8 channels of one tap; row8: 8 taps
+  // of one kernel row of one channel) or per value (nat)
+  const int ntab = tc_ntab(c.mode, c.k_pad);
   for (int e = tid; e < ntab; e += kThreads) {
-    const int k = p.tap_major ? e * 8 : e;
-    int tap, c;
-    if (p.tap_major) { tap = k / a.cg; c = k - tap * a.cg; }
-    else { c = k / khw; tap = k - c * khw; }
-    const int u = tap / a.kw, v = tap - (tap / a.kw) * a.kw;
-    const int dy = u * a.dh, dx = v * a.dw;
-    tab[e] = make_int4(c * static_cast<int>(a.hw) + dy * a.w + dx, dy, dx, k < a.K ? 1 : 0);
+    int coff, dy, dx, ok;
+    if (c.mode == kModeRow8) {
+      const int ch = e / a.kh, u = e - (e / a.kh) * a.kh;
+      dy = u * a.dh;
+      dx = 0;
+      coff = ch * static_cast<int>(a.hw) + dy * a.w;
+      ok = ch < a.cg;
+    } else {
+      const int k = c.mode == kModeCh8 ? e * 8 : e;
+      int tap, ch;
+      if (c.mode == kModeCh8) { tap = k / a.cg; ch = k - tap * a.cg; }
+      else { ch = k / khw; tap = k - ch * khw; }
+      const int u = tap / a.kw, v = tap - (tap / a.kw) * a.kw;
+      dy = u * a.dh;
+      dx = v * a.dw;
+      coff = ch * static_cast<int>(a.hw) + dy * a.w + dx;
+      ok = k < a.K;
+    }
+    tab[e] = make_int4(coff, dy, dx, ok);
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
@@ -257,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // ---- this block's tiles: one (group, channel tile), strided pixel tiles ---
+  // ---- this block's tiles: one (group, channel tile), strided pixel tiles.
+  // A pixel tile is 128 consecutive output pixels of one image.
   const int combos = a.groups * p.co_tiles;
   const int cpc = gridDim.x / combos;  // blocks per combination
   const int combo = blockIdx.x / cpc;
@@ -268,24 +330,23 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
   const int rows_valid = min(BN, a.mg - co0);
   const uint16_t* __restrict__ xs = static_cast<const uint16_t*>(a.x);
   const uint16_t* __restrict__ ws = static_cast<const uint16_t*>(a.wt);
+  auto tile_origin = [&](int t, int* n, int* p0) {
+    const int pt = local + t * cpc;
+    *n = pt / p.tiles_per_img;
+    *p0 = (pt - *n * p.tiles_per_img) * kM;
+  };
 
   if (warp < kEpiWarps) {
     // ======================= weights, then the epilogue ======================
     const long long wrow0 = static_cast<long long>(g) * a.mg + co0;  // first OIHW row
     bool ok = true;
-    if (bulk_ok) {
+    if (c.bulk_w) {
       if (tid == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(stg_bytes);
+        const uint32_t bytes = static_cast<uint32_t>(c.stg_bytes);
         mbar_arrive_expect_tx(stg_bar, bytes);
         const char* src = reinterpret_cast<const char*>(ws + wrow0 * a.K);
-        for (uint32_t off = 0; off < bytes; off += 32768u) {
-          const uint32_t n = min(32768u, bytes - off);
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                  smem_u32(stg) + off),
-              "l"(src + off), "r"(n), "r"(stg_bar)
-              : "memory");
-        }
+        for (uint32_t off = 0; off < bytes; off += 32768u)
+          bulk_load(smem_u32(sio) + off, src + off, min(32768u, bytes - off), stg_bar);
       }
       ok = wait_phase(stg_bar, 0, abort_flag, 1u);
     }
@@ -298,18 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
         const int kc = (q >> 3) / BN;
         const int k0 = kc * kBK + j * 8;
         uint16_t v[8];
-        int tap0 = 0, c0 = 0;
-        if (p.tap_major && k0 < a.K) { tap0 = k0 / a.cg; c0 = k0 - tap0 * a.cg; }
+        int tap0 = 0, c0 = 0, ch = 0, u = 0;
+        if (c.mode == kModeCh8 && k0 < a.K) { tap0 = k0 / a.cg; c0 = k0 - tap0 * a.cg; }
+        if (c.mode == kModeRow8) { ch = (k0 / 8) / a.kh; u = (k0 / 8) - ch * a.kh; }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int k = k0 + e;
-          uint16_t val = 0;
-          if (r < rows_valid && k < a.K) {
-            const int idx = p.tap_major ? (c0 + e) * khw + tap0 : k;  // OIHW order within the row
-            val = bulk_ok ? stg[static_cast<long long>(r) * a.K + idx]
-                          : ws[(wrow0 + r) * a.K + idx];
+          int idx = -1;  // position in the OIHW row, -1: zero padding
+          if (r < rows_valid) {
+            if (c.mode == kModeCh8) idx = (k0 + e < a.K) ? (c0 + e) * khw + tap0 : -1;
+            else if (c.mode == kModeRow8) idx = (ch < a.cg && e < a.kw) ? ch * khw + u * a.kw + e : -1;
+            else idx = (k0 + e < a.K) ? k0 + e : -1;
           }
-          v[e] = val;
+          v[e] = idx < 0 ? 0 : (c.bulk_w ? stg[static_cast<long long>(r) * a.K + idx] : ws[(wrow0 + r) * a.K + idx]);
         }
         *reinterpret_cast<uint4*>(sB + kc * (BN * 128) + swz(r, j)) =
             make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
@@ -317,62 +378,122 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       fence_proxy_async();
       mbar_arrive(wready_bar);
     }
-    // epilogue: bias of the block's channel tile staged once in shared memory
-    for (int c = tid; c < BN; c += kEpiWarps * 32)
-      sbias[c] = (a.bias && c < rows_valid) ? to_f32(static_cast<const T*>(a.bias)[g * a.mg + co0 + c]) : 0.0f;
-    asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiWarps * 32) : "memory");  // epilogue warps only
+    // bias of the block's channel tile, staged once
+    for (int cc = tid; cc < BN; cc += kEpiWarps * 32)
+      sbias[cc] = (a.bias && cc < rows_valid) ? to_f32(static_cast<const T*>(a.bias)[g * a.mg + co0 + cc]) : 0.0f;
+    epi_sync();  // the staging copy is consumed: its space becomes the tile buffers
+
     const int row = warp * 32 + lane;
     T* __restrict__ y = static_cast<T*>(a.y);
     const T* __restrict__ res = static_cast<const T*>(a.residual);
     const bool has_bias = a.bias != nullptr, has_res = res != nullptr;
+    const long long cbase = static_cast<long long>(g) * a.mg + co0;  // first output channel
+
+    // residual rows of tile t into buffer i: one bulk copy per channel row
+    auto issue_res = [&](int t, int i) {
+      int n, p0;
+      tile_origin(t, &n, &p0);
+      const int vpx = min(kM, static_cast<int>(a.howo) - p0);
+      if (tid == 0) mbar_arrive_expect_tx(res_bar(i), static_cast<uint32_t>(rows_valid * vpx * 2));
+      for (int cc = tid; cc < rows_valid; cc += kEpiWarps * 32) {
+        const T* src = res + ((static_cast<long long>(n) * a.c_out + cbase + cc) * a.howo + p0);
+        bulk_load(smem_u32(sio + (i * BN + cc) * (kM * 2)), src, static_cast<uint32_t>(vpx * 2), res_bar(i));
+      }
+    };
+    int res_pending = -1;  // tile whose residual copy is in flight and not yet waited for
+    if (c.epi_bulk && has_res && ok && ntiles > 0) { issue_res(0, 0); res_pending = 0; }
+
     for (int t = 0; ok && t < ntiles; ++t) {
       const int b = t & 1;
       const uint32_t u = static_cast<uint32_t>(t >> 1);
       // warp-uniform: the tensor-memory loads below are .sync.aligned
       if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(b), u & 1u, abort_flag, 2u))) break;
       tc_fence_after();
-      const long long pix = static_cast<long long>(local + t * cpc) * kM + row;
-      const bool valid = pix < a.npix;
-      long long obase = 0;
-      if (valid) {
-        const long long n = pix / a.howo;
-        obase = (n * a.c_out + static_cast<long long>(g) * a.mg + co0) * a.howo + (pix - n * a.howo);
-      }
+      int n, p0;
+      tile_origin(t, &n, &p0);
+      const int vpx = min(kM, static_cast<int>(a.howo) - p0);
+      const bool valid = row < vpx;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + b * BN;
-      // residual values of the next 16 channels are requested before this
-      // chunk's stores, so their latency overlaps the chunk's work
-      float rnext[16];
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj)
-        rnext[jj] = (has_res && valid && jj < rows_valid)
-                        ? to_f32(__ldg(res + obase + static_cast<long long>(jj) * a.howo)) : 0.0f;
+      if (c.epi_bulk) {
+        const int i = c.nio == 2 ? (t & 1) : 0;
+        T* io = reinterpret_cast<T*>(sio) + static_cast<long long>(i) * BN * kM;
+        if (has_res) {
+          const uint32_t rphase = static_cast<uint32_t>((c.nio == 2 ? t >> 1 : t) & 1);
+          if (!__all_sync(0xffffffffu, wait_phase(res_bar(i), rphase, abort_flag, 128u))) break;
+          res_pending = -1;
+        }
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        float rcur[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) rcur[jj] = rnext[jj];
-        if (has_res && valid && c + 16 < BN) {
+        for (int cc = 0; cc < BN; cc += 16) {
+          uint32_t r[16];
+          tmem_ld16(tbase + cc, r);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
-            const int col = c + 16 + jj;
-            rnext[jj] = col < rows_valid ? to_f32(__ldg(res + obase + static_cast<long long>(col) * a.howo)) : 0.0f;
+            const int col = cc + jj;
+            T* slot = io + col * kM + row;
+            const float rv = has_res ? to_f32(*slot) : 0.0f;
+            *slot = epilogue_vals<T>(__uint_as_float(r[jj]), sbias[col], rv, has_bias, has_res, a.act,
+                                     a.alpha, a.beta);
           }
         }
-        uint32_t r[16];
-        tmem_ld16(tbase + c, r);
-        if (valid) {
+        tc_fence_before();
+        mbar_arrive(tempty_bar(b));  // the accumulator buffer is free for the tile after next
+        fence_proxy_async();         // this thread's tile values, visible to the bulk copies
+        epi_sync();
+        for (int cc = tid; cc < rows_valid; cc += kEpiWarps * 32) {
+          T* dst = y + ((static_cast<long long>(n) * a.c_out + cbase + cc) * a.howo + p0);
+          bulk_store(dst, smem_u32(io + cc * kM), static_cast<uint32_t>(vpx * 2));
+        }
+        bulk_commit();
+        // the buffer of the next tile was last stored from a tile ago (two
+        // buffers) or just now (one): its reads must be done before reuse
+        if (c.nio == 2) bulk_wait_read<1>();
+        else bulk_wait_read<0>();
+        epi_sync();
+        if (has_res && t + 1 < ntiles) { issue_res(t + 1, c.nio == 2 ? ((t + 1) & 1) : 0); res_pending = t + 1; }
+      } else {
+        long long obase = 0;
+        if (valid) obase = (static_cast<long long>(n) * a.c_out + cbase) * a.howo + p0 + row;
+        // residual values of the next 16 channels are requested before this
+        // chunk's stores, so their latency overlaps the chunk's work
+        float rnext[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int col = c + jj;
-            if (col < rows_valid)
-              y[obase + static_cast<long long>(col) * a.howo] = epilogue_vals<T>(
-                  __uint_as_float(r[jj]), sbias[col], rcur[jj], has_bias, has_res, a.act, a.alpha, a.beta);
+        for (int jj = 0; jj < 16; ++jj)
+          rnext[jj] = (has_res && valid && jj < rows_valid)
+                          ? to_f32(__ldg(res + obase + static_cast<long long>(jj) * a.howo)) : 0.0f;
+#pragma unroll 1
+        for (int cc = 0; cc < BN; cc += 16) {
+          float rcur[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) rcur[jj] = rnext[jj];
+          if (has_res && valid && cc + 16 < BN) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = cc + 16 + jj;
+              rnext[jj] = col < rows_valid ? to_f32(__ldg(res + obase + static_cast<long long>(col) * a.howo)) : 0.0f;
+            }
+          }
+          uint32_t r[16];
+          tmem_ld16(tbase + cc, r);
+          if (valid) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = cc + jj;
+              if (col < rows_valid)
+                y[obase + static_cast<long long>(col) * a.howo] = epilogue_vals<T>(
+                    __uint_as_float(r[jj]), sbias[col], rcur[jj], has_bias, has_res, a.act, a.alpha, a.beta);
+            }
           }
         }
+        tc_fence_before();
+        mbar_arrive(tempty_bar(b));
       }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(b));
     }
+    if (res_pending >= 0) {  // aborted with a residual copy in flight: let it land first
+      const int i = c.nio == 2 ? (res_pending & 1) : 0;
+      const uint32_t rphase = static_cast<uint32_t>((c.nio == 2 ? res_pending >> 1 : res_pending) & 1);
+      wait_phase(res_bar(i), rphase, abort_flag, 128u, true);
+    }
+    if (c.epi_bulk) bulk_wait_all();  // the output rows have landed before the block retires
   } else if (warp < kEpiWarps + kProdWarps) {
     // ============================ A-operand gather ============================
     const int ptid = tid - kEpiWarps * 32;
@@ -382,23 +503,67 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
     uint32_t phase = 0;
     bool ok = true;
     for (int t = 0; ok && t < ntiles; ++t) {
-      const long long pix = static_cast<long long>(local + t * cpc) * kM + row;
-      const bool valid = pix < a.npix;
+      int n, p0;
+      tile_origin(t, &n, &p0);
+      const int pix = p0 + row;
+      const bool valid = pix < a.howo;
       int ih0 = 0, iw0 = 0;
       long long pb = 0;
       if (valid) {
-        const int n = static_cast<int>(pix / a.howo);
-        const int rem = static_cast<int>(pix - static_cast<long long>(n) * a.howo);
-        const int oh = rem / a.wo, ow = rem - (rem / a.wo) * a.wo;
+        const int oh = pix / a.wo, ow = pix - (pix / a.wo) * a.wo;
         ih0 = oh * a.sh - a.pt;
         iw0 = ow * a.sw - a.pl;
         pb = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
              static_cast<long long>(ih0) * a.w + iw0;
       }
+      // row8: which of the 8 taps of a kernel row land inside the image (per
+      // pixel), as 16-bit lane masks, and which 4-byte words are worth loading
+      // for either parity of the row segment's first element
+      uint32_t em[4] = {0, 0, 0, 0};
+      uint32_t wv[2] = {0, 0};
+      if (c.mode == kModeRow8 && valid) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const int iw = iw0 + v;
+          if (v < a.kw && iw >= 0 && iw < a.w) em[v >> 1] |= (v & 1) ? 0xFFFF0000u : 0x0000FFFFu;
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+          for (int k = 0; k < 5; ++k) {
+            const int c0 = iw0 - s + 2 * k;  // columns c0, c0 + 1 of word k
+            const bool any = (c0 >= 0 && c0 < a.w) || (c0 + 1 >= 0 && c0 + 1 < a.w);
+            if (any && c0 < iw0 + a.kw && c0 + 1 >= iw0) wv[s] |= 1u << k;
+          }
+      }
       for (int kc = 0; kc < kchunks; ++kc) {
         if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, 4u)) { ok = false; break; }
         uint8_t* As = sA + stage * kStageBytes;
-        if (p.tap_major) {
+        if (c.mode == kModeRow8) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = part * 4 + jj;
+            const int4 e = tab[kc * 8 + j];
+            const int ih = ih0 + e.y;
+            const bool in = valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (in) {
+              const long long e0 = pb + e.x;  // first tap's element
+              const int s = static_cast<int>(e0 & 1);
+              const uint32_t* wp = reinterpret_cast<const uint32_t*>(xs + (e0 - s));
+              const uint32_t m = wv[s];
+              uint32_t w5[5];
+#pragma unroll
+              for (int k = 0; k < 5; ++k) w5[k] = (m >> k & 1u) ? __ldg(wp + k) : 0u;
+              const uint32_t sel = s ? 0x5432u : 0x3210u;
+              o.x = __byte_perm(w5[0], w5[1], sel) & em[0];
+              o.y = __byte_perm(w5[1], w5[2], sel) & em[1];
+              o.z = __byte_perm(w5[2], w5[3], sel) & em[2];
+              o.w = __byte_perm(w5[3], w5[4], sel) & em[3];
+            }
+            *reinterpret_cast<uint4*>(As + swz(row, j)) = o;
+          }
+        } else if (c.mode == kModeCh8) {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int j = part * 4 + jj;
@@ -485,19 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
   }
 }
 
+// Shared-memory bytes of a launch configuration (with the 1 KB alignment slack).
+size_t tc_bytes(int bn, const TcLaunch& c) { return tc_layout(bn, c).end + 1024; }
+
 template <typename T, int BN>
-cudaError_t launch_bn(const TcPlan& p, const ConvArgs& a, cudaStream_t s) {
+cudaError_t launch_bn(const TcPlan& p, const TcLaunch& c, const ConvArgs& a, cudaStream_t s) {
   auto kern = igemm_tc<T, BN>;
-  const int rows_valid = min(BN, a.mg);  // rows copied per block (co tile 0 is the widest)
-  const long long stg_bytes = static_cast<long long>(rows_valid) * a.K * 2;
-  // the bulk copy needs 16-byte aligned source rows of every block's tile
-  const bool bulk_ok = (reinterpret_cast<uintptr_t>(a.wt) % 16 == 0) &&
-                       ((static_cast<long long>(BN) * a.K * 2) % 16 == 0) &&
-                       ((static_cast<long long>(a.mg) * a.K * 2) % 16 == 0) &&
-                       ((a.mg % BN) == 0 || a.groups * p.co_tiles == 1) && stg_bytes % 16 == 0 &&
-                       stg_bytes < (1 << 20);
-  const TcLayout L = tc_layout(BN, p.k_pad, p.stages, p.tap_major, bulk_ok ? stg_bytes : 0);
-  const size_t smem = L.end + 1024;
+  const size_t smem = tc_bytes(BN, c);
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -507,33 +666,105 @@ cudaError_t launch_bn(const TcPlan& p, const ConvArgs& a, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     configured[dev] = static_cast<int>(smem);
   }
-  kern<<<p.ctas, kThreads, smem, s>>>(a, p, bulk_ok ? stg_bytes : 0, bulk_ok ? 1 : 0);
+  kern<<<p.ctas, kThreads, smem, s>>>(a, p, c);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_typed(const TcPlan& p, const ConvArgs& a, cudaStream_t s) {
+cudaError_t launch_typed(const TcPlan& p, const TcLaunch& c, const ConvArgs& a, cudaStream_t s) {
   switch (p.bn) {
-    case 32: return launch_bn<T, 32>(p, a, s);
-    case 48: return launch_bn<T, 48>(p, a, s);
-    case 64: return launch_bn<T, 64>(p, a, s);
-    case 128: return launch_bn<T, 128>(p, a, s);
-    case 256: return launch_bn<T, 256>(p, a, s);
+    case 32: return launch_bn<T, 32>(p, c, a, s);
+    case 48: return launch_bn<T, 48>(p, c, a, s);
+    case 64: return launch_bn<T, 64>(p, c, a, s);
+    case 128: return launch_bn<T, 128>(p, c, a, s);
+    case 256: return launch_bn<T, 256>(p, c, a, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
+int kpad_of(int mode, const ConvArgs& a) {
+  const long long k = mode == kModeRow8 ? static_cast<long long>(a.cg) * a.kh * 8 : a.K;
+  return static_cast<int>((k + kBK - 1) / kBK * kBK);
+}
+
+// Fill the address-dependent part of a launch; false if nothing fits.
+bool configure(const TcPlan& p, const ConvArgs& a, bool addresses_known, TcLaunch* c) {
+  c->mode = p.mode;
+  if (c->mode == kModeRow8 && addresses_known) {
+    // 4-byte word loads: x 4-byte aligned and an even element count (so no
+    // word straddles the end of x)
+    const long long xe = static_cast<long long>(a.n) * a.c_in * a.hw;
+    if (reinterpret_cast<uintptr_t>(a.x) % 4 != 0 || (xe & 1)) c->mode = kModeNat;
+  }
+  c->k_pad = kpad_of(c->mode, a);
+  const int rows_first = min(p.bn, a.mg);  // rows of the first channel tile
+  c->stg_bytes = static_cast<long long>(rows_first) * a.K * 2;
+  c->bulk_w = (!addresses_known || reinterpret_cast<uintptr_t>(a.wt) % 16 == 0) &&
+              (static_cast<long long>(p.bn) * a.K * 2) % 16 == 0 &&
+              (static_cast<long long>(a.mg) * a.K * 2) % 16 == 0 &&
+              ((a.mg % p.bn) == 0 || a.groups * p.co_tiles == 1) && c->stg_bytes % 16 == 0 &&
+              c->stg_bytes < (1 << 20);
+  c->epi_bulk = (a.howo % 8 == 0) &&
+                (!addresses_known || (reinterpret_cast<uintptr_t>(a.y) % 16 == 0 &&
+                                      (!a.residual || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0)));
+  for (int epi = c->epi_bulk; epi >= 0; --epi) {
+    for (int nio = epi ? 2 : 1; nio >= 1; --nio) {
+      for (int st = 4; st >= 2; --st) {
+        TcLaunch t = *c;
+        t.epi_bulk = epi;
+        t.nio = nio;
+        t.stages = st;
+        if (tc_bytes(p.bn, t) <= kTcMaxSmem) {
+          *c = t;
+          return true;
+        }
+      }
+    }
+  }
+  return false;
+}
+
 }  // namespace
 
-// Shared-memory bytes of a plan (host): the planner keeps only plans that fit.
-size_t tc_smem_bytes(int bn, int k_pad, int stages, int tap_major, long long stg_bytes) {
-  return tc_layout(bn, k_pad, stages, tap_major, stg_bytes).end + 1024;
+// Planner entry (host): channel tile, k order, tiles and blocks for a shape
+// (addresses unknown: assumed aligned).  False when the weights of one
+// channel tile do not fit in shared memory.
+bool tc_plan(const ConvArgs& a, int sm, TcPlan* t) {
+  static const int bns[] = {256, 128, 64, 48, 32};
+  int bn = 0;
+  long long best = -1;
+  for (int cand : bns) {  // least padded channels; ties go to the wider tile
+    const long long padded = (a.mg + cand - 1) / cand * cand;
+    if (best < 0 || padded < best) { best = padded; bn = cand; }
+  }
+  t->bn = bn;
+  if (a.cg % 8 == 0) t->mode = kModeCh8;
+  else if (a.dw == 1 && a.kw <= 8 && a.kw >= 5) t->mode = kModeRow8;  // rows of 5..8 taps: few padded
+  else t->mode = kModeNat;
+  t->co_tiles = (a.mg + bn - 1) / bn;
+  t->tiles_per_img = static_cast<int>((a.howo + kM - 1) / kM);
+  const long long pix_tiles = static_cast<long long>(a.n) * t->tiles_per_img;
+  if (pix_tiles > 2147483647LL) return false;
+  t->pix_tiles = static_cast<int>(pix_tiles);
+  TcLaunch c;
+  if (!configure(*t, a, false, &c)) return false;
+  t->k_pad = c.k_pad;
+  t->stages = c.stages;
+  t->smem = tc_bytes(bn, c);
+  const long long combos = static_cast<long long>(a.groups) * t->co_tiles;
+  long long cpc = combos >= sm ? 1 : std::min<long long>(pix_tiles, sm / combos);
+  if (cpc < 1) cpc = 1;
+  if (combos * cpc > 2147483647LL) return false;
+  t->ctas = static_cast<int>(combos * cpc);
+  return true;
 }
 
 cudaError_t launch_tc(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s) {
+  TcLaunch c;
+  if (!configure(plan.tc, a, true, &c)) return cudaErrorInvalidConfiguration;
   switch (dtype) {
-    case CONV_F16: return launch_typed<__half>(plan.tc, a, s);
-    case CONV_BF16: return launch_typed<__nv_bfloat16>(plan.tc, a, s);
+    case CONV_F16: return launch_typed<__half>(plan.tc, c, a, s);
+    case CONV_BF16: return launch_typed<__nv_bfloat16>(plan.tc, c, a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -119,6 +119,11 @@ EDGE = [
     ("tc_grouped", (2, 32, 8, 8), (48, 16, 3, 3), dict(pads=1, groups=2, act="silu"), True, False),
     ("tc_natural_order", (1, 5, 19, 17), (20, 5, 4, 3), dict(stride=(1, 2), pads=(1, 1, 2, 0)),
      True, False),
+    ("tc_row8_stemlike", (2, 3, 30, 34), (16, 3, 7, 7), dict(stride=2, pads=3, act="relu"), True, False),
+    ("tc_row8_odd_w", (2, 5, 17, 23), (24, 5, 5, 6), dict(pads=(2, 3, 2, 2)), True, True),
+    ("tc_row8_odd_count", (1, 5, 17, 23), (24, 5, 5, 6), dict(pads=(2, 3, 2, 2)), True, False),
+    ("tc_bulk_res", (2, 16, 8, 12), (32, 16, 3, 3), dict(pads=1, act="silu"), True, True),
+    ("tc_bulk_tiles", (3, 8, 20, 16), (64, 8, 1, 1), dict(act="relu"), True, True),
     ("long_k", (1, 320, 6, 6), (16, 320, 3, 3), dict(pads=1), True, False),
     ("wide_cin_1x1", (1, 1024, 4, 4), (64, 1024, 1, 1), dict(), True, False),
 ]
