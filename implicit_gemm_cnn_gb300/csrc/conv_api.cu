@@ -138,23 +138,26 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
 }
 
 bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
-  constexpr int QW = 8;                       // outputs per thread along a row
+  constexpr int QH = 8;                       // output rows per thread (one column)
   const int es = p->dtype == CONV_F32 ? 4 : 2;
   const int al = 16 / es;                     // elements per 16 bytes
   DwPlan d;
   d.lm = static_cast<int>((p->pad_left + al - 1) / al * al);  // image column 0 on a 16-byte boundary
-  const long long strips = (s.wo + QW - 1) / QW;
-  // columns the last strip's windows reach (+1 for the paired loads)
-  const long long need = d.lm - p->pad_left + (strips * QW - 1) * p->stride_w + (p->kw - 1) * p->dil_w + 2;
+  // columns the windows of the last output column reach
+  const long long need = d.lm - p->pad_left + (s.wo - 1) * p->stride_w + (p->kw - 1) * p->dil_w + 1;
   long long row = std::max<long long>(d.lm + p->w, need);
   row = (row + al - 1) / al * al;
-  const long long wbytes = 2 * ((s.mg * p->kh * p->kw + 3) / 4 * 4) * 4;
+  const long long wbytes = 2 * ((s.mg * p->kh * p->kw + 3) / 4 * 4) * 4 + 2 * ((s.mg + 3) / 4 * 4) * 4;
   const long long per_elem = 2LL * es + (es == 4 ? 0 : 4);  // two staging buffers (+ fp32 tile)
   const long long budget = 16 * 1024 - wbytes;              // bytes: ~12 blocks per SM
   if (row > (1 << 20) || wbytes > 64 * 1024) return false;
-  auto in_rows = [&](long long t) { return (t - 1) * p->stride_h + (p->kh - 1) * p->dil_h + 1; };
+  // staged rows: a thread's 8-row strip may run past the block's last output
+  // row, so stage whole strips
+  auto in_rows = [&](long long t) {
+    return ((t + QH - 1) / QH * QH - 1) * p->stride_h + (p->kh - 1) * p->dil_h + 1;
+  };
   long long th = s.ho;
-  while (th > 1 && in_rows(th) * row * per_elem > budget) th = (th + 1) / 2;
+  while (th > QH && in_rows(th) * row * per_elem > budget) th = (th / 2 + QH - 1) / QH * QH;
   if (in_rows(th) * row * per_elem + wbytes > 200 * 1024) return false;
   d.th = static_cast<int>(th);
   d.in_rows = static_cast<int>(in_rows(th));

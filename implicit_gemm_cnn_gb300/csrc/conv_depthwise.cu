@@ -14,12 +14,16 @@
 // straight from the NCHW plane) while it computes the current one, so loads
 // and arithmetic overlap; shared-memory columns left and right of the image
 // are zeroed once and never written again, rows above / below the image are
-// zeroed per item.  16-bit tiles are converted to float32 once on chip.  Each
-// thread computes kQW adjacent outputs of a row for one of the m channels and
-// sums each window in (kernel row, kernel column) order in one float32
-// chain; for stride-1 / dilation-1 columns with a compiled kernel width the
-// row segment sits in registers and is reused across the kQW outputs.  Bias,
-// residual and activation are applied at the store.
+// zeroed per item.  16-bit tiles are converted to float32 once on chip.  The
+// next item's weights and bias travel in registers while the current item is
+// computed.
+//
+// Each thread computes kQH outputs of one output column (consecutive lanes,
+// consecutive columns: conflict-free shared-memory reads).  For stride-1 /
+// dilation-1 rows with a compiled kernel height, the kQH + kh - 1 window
+// values of one kernel column sit in registers and serve all kQH outputs;
+// each output is summed in one float32 chain in (kernel column, kernel row)
+// order.  Bias, residual and activation are applied at the store.
 #include <algorithm>
 
 #include "conv_internal.h"
@@ -28,8 +32,9 @@ namespace conv {
 namespace {
 
 constexpr int kDwThreads = 128;
-constexpr int kQW = 8;
+constexpr int kQH = 8;
 constexpr int kBlocksPerSm = 12;
+constexpr int kRegW = 4;  // weights per thread carried in registers (m*kh*kw <= 512)
 
 template <int BYTES>
 __device__ __forceinline__ void cp_async_n(void* smem, const void* gmem) {
@@ -42,35 +47,18 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Store n (1..4) consecutive outputs of one row starting at o.
-template <typename T>
-__device__ __forceinline__ void store_run(T* __restrict__ y, long long o, float v0, float v1, float v2,
-                                          float v3, int n, bool vec) {
-  if (vec && n == 4) {
-    if constexpr (sizeof(T) == 4) {
-      *reinterpret_cast<float4*>(y + o) = make_float4(v0, v1, v2, v3);
-    } else {
-      T h[4] = {from_f32<T>(v0), from_f32<T>(v1), from_f32<T>(v2), from_f32<T>(v3)};
-      *reinterpret_cast<uint2*>(y + o) = *reinterpret_cast<const uint2*>(h);
-    }
-  } else {
-    const float v[4] = {v0, v1, v2, v3};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q < n) y[o + q] = from_f32<T>(v[q]);
-  }
-}
-
-template <typename T, int KW>
+template <typename T, int KH>
 __global__ void __launch_bounds__(kDwThreads)
     depthwise(const ConvArgs a, const DwPlan d, int row_tiles, long long items) {
   extern __shared__ __align__(16) unsigned char dsm[];
   const int m = a.mg;
   const int nw = m * a.kh * a.kw;
   const int nw_pad = (nw + 3) & ~3;
+  const int mb_pad = (m + 3) & ~3;
   const int tile_elems = d.in_rows * d.row;
   float* wsm = reinterpret_cast<float*>(dsm);                  // [2][nw_pad]
-  float* ftile = wsm + 2 * nw_pad;                             // [tile] (16-bit inputs)
+  float* bsm = wsm + 2 * nw_pad;                               // [2][mb_pad]
+  float* ftile = bsm + 2 * mb_pad;                             // [tile] (16-bit inputs)
   T* raw = reinterpret_cast<T*>(ftile + (sizeof(T) == 4 ? 0 : tile_elems));  // [2][tile]
   const int tid = threadIdx.x;
   const T* __restrict__ xg = static_cast<const T*>(a.x);
@@ -78,21 +66,25 @@ __global__ void __launch_bounds__(kDwThreads)
   const T* __restrict__ bg = static_cast<const T*>(a.bias);
   const T* __restrict__ rg = static_cast<const T*>(a.residual);
   T* __restrict__ y = static_cast<T*>(a.y);
+  const bool wregs = nw <= kRegW * kDwThreads && m <= kDwThreads;
 
   for (int i = tid; i < 2 * tile_elems; i += kDwThreads) raw[i] = from_f32<T>(0.0f);
-  __syncthreads();
 
-  // Stage item `it` into buffer st: zero its out-of-image rows, copy its image
-  // rows, convert its weights.
-  auto prefetch = [&](long long it, int st) {
+  auto decode = [&](long long it, int* n, int* g, int* rt) {
     const long long plane = it / row_tiles;
-    const int rt = static_cast<int>(it - plane * row_tiles);
-    const int n = static_cast<int>(plane / a.groups);
-    const int g = static_cast<int>(plane - static_cast<long long>(n) * a.groups);
+    *rt = static_cast<int>(it - plane * row_tiles);
+    *n = static_cast<int>(plane / a.groups);
+    *g = static_cast<int>(plane - static_cast<long long>(*n) * a.groups);
+  };
+  // Stage item `it`'s input rows into buffer st (zero rows outside the image,
+  // cp.async copies of the image rows).
+  auto stage_rows = [&](long long it, int st) {
+    int n, g, rt;
+    decode(it, &n, &g, &rt);
     const int ih_start = rt * d.th * a.sh - a.pt;
     const int r_lo = max(0, ih_start), r_hi = min(a.h, ih_start + d.in_rows);
     T* buf = raw + st * tile_elems;
-    const int zr_top = min(d.in_rows, r_lo - ih_start);        // staged rows above the image
+    const int zr_top = min(d.in_rows, r_lo - ih_start);           // staged rows above the image
     const int zr_bot = d.in_rows - zr_top - max(0, r_hi - r_lo);  // staged rows below it
     const int zrows = zr_top + zr_bot;
     for (int i = tid; i < zrows * a.w; i += kDwThreads) {
@@ -122,21 +114,51 @@ __global__ void __launch_bounds__(kDwThreads)
         }
       }
     }
-    float* wd = wsm + st * nw_pad;
-    for (int i = tid; i < nw; i += kDwThreads) wd[i] = to_f32(wg[static_cast<long long>(g) * nw + i]);
+  };
+  // Weights and bias of item `it`: into registers now, into shared memory
+  // (buffer st) when the current item's compute is done.
+  float wreg[kRegW], breg = 0.0f;
+  auto load_params = [&](long long it) {
+    int n, g, rt;
+    decode(it, &n, &g, &rt);
+#pragma unroll
+    for (int k = 0; k < kRegW; ++k) {
+      const int i = tid + k * kDwThreads;
+      wreg[k] = i < nw ? to_f32(wg[static_cast<long long>(g) * nw + i]) : 0.0f;
+    }
+    breg = (bg && tid < m) ? to_f32(bg[g * m + tid]) : 0.0f;
+  };
+  auto store_params = [&](int st) {
+#pragma unroll
+    for (int k = 0; k < kRegW; ++k) {
+      const int i = tid + k * kDwThreads;
+      if (i < nw) wsm[st * nw_pad + i] = wreg[k];
+    }
+    if (tid < m) bsm[st * mb_pad + tid] = breg;
+  };
+  auto load_params_direct = [&](long long it, int st) {  // multipliers too large for registers
+    int n, g, rt;
+    decode(it, &n, &g, &rt);
+    for (int i = tid; i < nw; i += kDwThreads) wsm[st * nw_pad + i] = to_f32(wg[static_cast<long long>(g) * nw + i]);
+    for (int i = tid; i < m; i += kDwThreads) bsm[st * mb_pad + i] = bg ? to_f32(bg[g * m + i]) : 0.0f;
   };
 
-  const bool fast = (KW != 0) && a.sw == 1 && a.dw == 1 && a.kw == KW;
-  const bool pair_ok = ((d.lm - a.pl) & 1) == 0 && (d.row & 1) == 0;
-  const bool vec_out = a.vec_out && (a.wo & 3) == 0;
+  const bool fast = (KH != 0) && a.sh == 1 && a.dh == 1 && a.kh == KH;
 
   long long it = blockIdx.x;
-  if (it < items) prefetch(it, 0);
+  if (it < items) {
+    stage_rows(it, 0);
+    if (wregs) { load_params(it); store_params(0); } else { load_params_direct(it, 0); }
+  }
   cp_async_commit();
   for (int i = 0; it < items; it += gridDim.x, ++i) {
     const int st = i & 1;
     const long long nx = it + gridDim.x;
-    if (nx < items) prefetch(nx, st ^ 1);
+    if (nx < items) {
+      stage_rows(nx, st ^ 1);
+      if (wregs) load_params(nx);
+      else load_params_direct(nx, st ^ 1);
+    }
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
@@ -150,84 +172,79 @@ __global__ void __launch_bounds__(kDwThreads)
       tile = ftile;
     }
     const float* wts = wsm + st * nw_pad;
+    const float* bia = bsm + st * mb_pad;
 
-    const long long plane = it / row_tiles;
-    const int rt = static_cast<int>(it - plane * row_tiles);
-    const int n = static_cast<int>(plane / a.groups);
-    const int g = static_cast<int>(plane - static_cast<long long>(n) * a.groups);
+    int n, g, rt;
+    decode(it, &n, &g, &rt);
     const int oh0 = rt * d.th;
     const int rows_out = min(d.th, a.ho - oh0);
-    const int strips = (a.wo + kQW - 1) / kQW;
-    const int work = rows_out * strips * m;
+    const int vstrips = (rows_out + kQH - 1) / kQH;
+    const int cols32 = (a.wo + 31) / 32 * 32;
+    const int work = m * vstrips * cols32;
     for (int wi = tid; wi < work; wi += kDwThreads) {
-      const int j = wi / (rows_out * strips);
-      const int rem = wi - j * (rows_out * strips);
-      const int ohl = rem / strips;
-      const int ow0 = (rem - ohl * strips) * kQW;
+      const int ow = wi % cols32;
+      const int rest = wi / cols32;
+      const int vs = rest % vstrips;
+      const int j = rest / vstrips;
+      if (ow >= a.wo) continue;
+      const int ohl0 = vs * kQH;
+      const int nq = min(kQH, rows_out - ohl0);
+      const int co = g * m + j;
+      const long long out0 = ((static_cast<long long>(n) * a.c_out + co) * a.ho + oh0 + ohl0) * a.wo + ow;
+      float rv[kQH];
+#pragma unroll
+      for (int q = 0; q < kQH; ++q)
+        rv[q] = (rg && q < nq) ? to_f32(__ldg(rg + out0 + static_cast<long long>(q) * a.wo)) : 0.0f;
       const float* wj = wts + j * a.kh * a.kw;
-      float acc[kQW];
+      const float* scol = tile + ohl0 * a.sh * d.row + d.lm - a.pl + ow * a.sw;
+      float acc[kQH];
 #pragma unroll
-      for (int q = 0; q < kQW; ++q) acc[q] = 0.0f;
+      for (int q = 0; q < kQH; ++q) acc[q] = 0.0f;
       if (fast) {
-        constexpr int KWc = KW > 0 ? KW : 1;
-        constexpr int SEG = kQW + KWc - 1;
-        for (int u = 0; u < a.kh; ++u) {
-          const float* srow = tile + (ohl * a.sh + u * a.dh) * d.row + d.lm - a.pl + ow0;
-          float seg[SEG + 1];
-          if (pair_ok) {
+        constexpr int KHc = KH > 0 ? KH : 1;
+        for (int v = 0; v < a.kw; ++v) {
+          const float* sc = scol + v * a.dw;
+          float col[kQH + KHc - 1];
 #pragma unroll
-            for (int e = 0; e < (SEG + 1) / 2; ++e) {
-              const float2 v = *reinterpret_cast<const float2*>(srow + 2 * e);
-              seg[2 * e] = v.x;
-              seg[2 * e + 1] = v.y;
-            }
-          } else {
+          for (int r = 0; r < kQH + KHc - 1; ++r) col[r] = sc[r * d.row];
 #pragma unroll
-            for (int e = 0; e < SEG; ++e) seg[e] = srow[e];
-          }
+          for (int u = 0; u < KHc; ++u) {
+            const float wv = wj[u * a.kw + v];
 #pragma unroll
-          for (int v = 0; v < KWc; ++v) {
-            const float wv = wj[u * KWc + v];
-#pragma unroll
-            for (int q = 0; q < kQW; ++q) acc[q] = fmaf(seg[q + v], wv, acc[q]);
+            for (int q = 0; q < kQH; ++q) acc[q] = fmaf(col[q + u], wv, acc[q]);
           }
         }
       } else {
-        for (int u = 0; u < a.kh; ++u) {
-          const float* srow = tile + (ohl * a.sh + u * a.dh) * d.row + d.lm - a.pl + ow0 * a.sw;
-          for (int v = 0; v < a.kw; ++v) {
+        for (int v = 0; v < a.kw; ++v) {
+          for (int u = 0; u < a.kh; ++u) {
             const float wv = wj[u * a.kw + v];
+            const float* sc = scol + u * a.dh * d.row + v * a.dw;
 #pragma unroll
-            for (int q = 0; q < kQW; ++q) acc[q] = fmaf(srow[q * a.sw + v * a.dw], wv, acc[q]);
+            for (int q = 0; q < kQH; ++q)
+              if (q < nq) acc[q] = fmaf(sc[q * a.sh * d.row], wv, acc[q]);
           }
         }
       }
-      const int co = g * m + j;
-      const long long out = ((static_cast<long long>(n) * a.c_out + co) * a.ho + oh0 + ohl) * a.wo + ow0;
-      const float bv = bg ? to_f32(__ldg(bg + co)) : 0.0f;
-      const int nvalid = min(kQW, a.wo - ow0);
-      float rv[kQW];
+      const float bv = bia[j];
 #pragma unroll
-      for (int q = 0; q < kQW; ++q) rv[q] = (rg && q < nvalid) ? to_f32(__ldg(rg + out + q)) : 0.0f;
-      float v[kQW];
-#pragma unroll
-      for (int q = 0; q < kQW; ++q)
-        v[q] = to_f32(epilogue_vals<T>(acc[q], bv, rv[q], bg != nullptr, rg != nullptr, a.act, a.alpha, a.beta));
-      store_run<T>(y, out, v[0], v[1], v[2], v[3], min(4, nvalid), vec_out);
-      if (nvalid > 4) store_run<T>(y, out + 4, v[4], v[5], v[6], v[7], nvalid - 4, vec_out);
+      for (int q = 0; q < kQH; ++q)
+        if (q < nq)
+          y[out0 + static_cast<long long>(q) * a.wo] =
+              epilogue_vals<T>(acc[q], bv, rv[q], bg != nullptr, rg != nullptr, a.act, a.alpha, a.beta);
     }
+    if (wregs && nx < items) store_params(st ^ 1);
     __syncthreads();  // this buffer is refilled two items from now
   }
   cp_async_wait<0>();
 }
 
-template <typename T, int KW>
-cudaError_t launch_kw(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+template <typename T, int KH>
+cudaError_t launch_kh(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
   const int row_tiles = (a.ho + d.th - 1) / d.th;
   const long long items = static_cast<long long>(a.n) * a.groups * row_tiles;
   const long long blocks = std::min<long long>(items, static_cast<long long>(d.sm) * kBlocksPerSm);
   const size_t smem = depthwise_smem_bytes(d, a.mg, a.kh, a.kw, sizeof(T) == 4 ? CONV_F32 : CONV_F16);
-  auto kern = depthwise<T, KW>;
+  auto kern = depthwise<T, KH>;
   if (smem > 48 * 1024) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
@@ -239,12 +256,12 @@ cudaError_t launch_kw(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_typed(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
-  if (a.sw == 1 && a.dw == 1) {
-    if (a.kw == 3) return launch_kw<T, 3>(d, a, s);
-    if (a.kw == 5) return launch_kw<T, 5>(d, a, s);
-    if (a.kw == 7) return launch_kw<T, 7>(d, a, s);
+  if (a.sh == 1 && a.dh == 1) {
+    if (a.kh == 3) return launch_kh<T, 3>(d, a, s);
+    if (a.kh == 5) return launch_kh<T, 5>(d, a, s);
+    if (a.kh == 7) return launch_kh<T, 7>(d, a, s);
   }
-  return launch_kw<T, 0>(d, a, s);
+  return launch_kh<T, 0>(d, a, s);
 }
 
 }  // namespace
@@ -252,7 +269,8 @@ cudaError_t launch_typed(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
 size_t depthwise_smem_bytes(const DwPlan& d, int mg, int kh, int kw, int dtype) {
   const size_t tile = static_cast<size_t>(d.in_rows) * d.row;
   const size_t es = dtype == CONV_F32 ? 4 : 2;
-  return 2 * static_cast<size_t>((mg * kh * kw + 3) & ~3) * 4 + (es == 4 ? 0 : tile * 4) + 2 * tile * es;
+  return 2 * static_cast<size_t>((mg * kh * kw + 3) & ~3) * 4 + 2 * static_cast<size_t>((mg + 3) & ~3) * 4 +
+         (es == 4 ? 0 : tile * 4) + 2 * tile * es;
 }
 
 cudaError_t launch_depthwise(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s) {
