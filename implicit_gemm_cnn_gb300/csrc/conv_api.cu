@@ -96,7 +96,7 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
     const long long ctas = tm * tn * p->groups;
     if (tm * p->groups > 65535) continue;
     const long long per_sm = (ctas + sm - 1) / sm;
-    const int occ = occupancy_estimate(c, ffma_smem_bytes(i, p->dtype));
+    const int occ = occupancy_estimate(c, ffma_smem_bytes(i, static_cast<int>(s.K)));
     const double warps = static_cast<double>(std::min<long long>(per_sm, occ)) * c.threads() / 32.0;
     const double speed = ((c.tm == 8 && c.tn == 8) ? 1.0 : (c.tm * c.tn == 32 ? 0.85 : 0.6)) *
                          std::min(1.0, warps / 8.0);

@@ -60,44 +60,67 @@ __device__ __forceinline__ float sigmoid_f32(float t) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-t)));
 }
 
-__device__ __forceinline__ float activate(float t, int act, float alpha, float beta) {
-  switch (act) {
-    case ACT_RELU: return t > 0.0f ? t : 0.0f;
-    case ACT_SILU: return __fmul_rn(t, sigmoid_f32(t));
-    case ACT_SIGMOID: return sigmoid_f32(t);
-    case ACT_TANH: return tanhf(t);
-    case ACT_HARD_SWISH: {
-      float s = __fadd_rn(__fmul_rn(t, 1.0f / 6.0f), 0.5f);
-      return __fmul_rn(t, fmaxf(0.0f, fminf(1.0f, s)));
-    }
-    case ACT_HARD_SIGMOID: {
-      float s = __fadd_rn(__fmul_rn(alpha, t), beta);
-      return fmaxf(0.0f, fminf(1.0f, s));
-    }
-    case ACT_CLIP: return fminf(fmaxf(t, alpha), beta);
-    case ACT_LEAKY_RELU: return t >= 0.0f ? t : __fmul_rn(alpha, t);
-    default: return t;
+template <int ACT>
+__device__ __forceinline__ float act_fn(float t, float alpha, float beta) {
+  if constexpr (ACT == ACT_RELU) return t > 0.0f ? t : 0.0f;
+  else if constexpr (ACT == ACT_SILU) return __fmul_rn(t, sigmoid_f32(t));
+  else if constexpr (ACT == ACT_SIGMOID) return sigmoid_f32(t);
+  else if constexpr (ACT == ACT_TANH) return tanhf(t);
+  else if constexpr (ACT == ACT_HARD_SWISH) {
+    const float s = __fadd_rn(__fmul_rn(t, 1.0f / 6.0f), 0.5f);
+    return __fmul_rn(t, fmaxf(0.0f, fminf(1.0f, s)));
+  } else if constexpr (ACT == ACT_HARD_SIGMOID) {
+    const float s = __fadd_rn(__fmul_rn(alpha, t), beta);
+    return fmaxf(0.0f, fminf(1.0f, s));
+  } else if constexpr (ACT == ACT_CLIP) return fminf(fmaxf(t, alpha), beta);
+  else if constexpr (ACT == ACT_LEAKY_RELU) return t >= 0.0f ? t : __fmul_rn(alpha, t);
+  else return t;
+}
+
+// One activation, chosen at run time, applied to N register values: one
+// branch per call, each case a straight-line loop (a switch inside a per-value
+// loop would be if-converted into evaluating every activation for every value).
+template <int N>
+__device__ __forceinline__ void activate_n(float (&v)[N], int act, float alpha, float beta) {
+#define CONV_ACT_CASE(A)                                                    \
+  case A: {                                                                 \
+    _Pragma("unroll") for (int i = 0; i < N; ++i) v[i] = act_fn<A>(v[i], alpha, beta); \
+    break;                                                                  \
   }
+  switch (act) {
+    CONV_ACT_CASE(ACT_RELU)
+    CONV_ACT_CASE(ACT_SILU)
+    CONV_ACT_CASE(ACT_SIGMOID)
+    CONV_ACT_CASE(ACT_TANH)
+    CONV_ACT_CASE(ACT_HARD_SWISH)
+    CONV_ACT_CASE(ACT_HARD_SIGMOID)
+    CONV_ACT_CASE(ACT_CLIP)
+    CONV_ACT_CASE(ACT_LEAKY_RELU)
+    default: break;
+  }
+#undef CONV_ACT_CASE
 }
 
-// The epilogue on values already in registers (bias and residual converted to
-// float32 exactly): the same steps and roundings as epilogue() below.
-template <typename T>
-__device__ __forceinline__ T epilogue_vals(float acc, float bias, float res, bool has_bias,
-                                           bool has_res, int act, float alpha, float beta) {
-  float t = acc;
-  if (has_bias) t = __fadd_rn(t, bias);
-  if (has_res) t = __fadd_rn(t, res);
-  return from_f32<T>(activate(t, act, alpha, beta));
+__device__ __forceinline__ float activate(float t, int act, float alpha, float beta) {
+  float v[1] = {t};
+  activate_n<1>(v, act, alpha, beta);
+  return v[0];
 }
 
-// t = acc; t += bias[co]; t += residual[out_index]; t = act(t); round to T.
-template <typename T>
-__device__ __forceinline__ T epilogue(float acc, int co, long long out_index, const ConvArgs& a) {
-  float t = acc;
-  if (a.bias) t = __fadd_rn(t, to_f32(static_cast<const T*>(a.bias)[co]));
-  if (a.residual) t = __fadd_rn(t, to_f32(static_cast<const T*>(a.residual)[out_index]));
-  return from_f32<T>(activate(t, a.act, a.alpha, a.beta));
+// Sum, bias, residual for N values of one output channel or of N channels
+// (bias per value), then the activation: the float32 steps of the epilogue.
+template <int N>
+__device__ __forceinline__ void epilogue_n(float (&v)[N], const float (&bias)[N], const float (&res)[N],
+                                           bool has_bias, bool has_res, int act, float alpha, float beta) {
+  if (has_bias) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __fadd_rn(v[i], bias[i]);
+  }
+  if (has_res) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __fadd_rn(v[i], res[i]);
+  }
+  activate_n<N>(v, act, alpha, beta);
 }
 
 }  // namespace conv

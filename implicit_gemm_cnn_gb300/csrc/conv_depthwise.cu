@@ -225,12 +225,13 @@ __global__ void __launch_bounds__(kDwThreads)
           }
         }
       }
-      const float bv = bia[j];
+      float bv[kQH];
+#pragma unroll
+      for (int q = 0; q < kQH; ++q) bv[q] = bia[j];
+      epilogue_n<kQH>(acc, bv, rv, bg != nullptr, rg != nullptr, a.act, a.alpha, a.beta);
 #pragma unroll
       for (int q = 0; q < kQH; ++q)
-        if (q < nq)
-          y[out0 + static_cast<long long>(q) * a.wo] =
-              epilogue_vals<T>(acc[q], bv, rv[q], bg != nullptr, rg != nullptr, a.act, a.alpha, a.beta);
+        if (q < nq) y[out0 + static_cast<long long>(q) * a.wo] = from_f32<T>(acc[q]);
     }
     if (wregs && nx < items) store_params(st ^ 1);
     __syncthreads();  // this buffer is refilled two items from now

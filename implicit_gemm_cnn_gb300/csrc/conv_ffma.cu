@@ -71,7 +71,7 @@ __host__ __device__ constexpr int pow2_floor(int v) {
 
 template <typename T, int BM, int BN, int TM, int TN>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN))
-    igemm_ffma(const ConvArgs a) {
+    igemm_ffma(const ConvArgs a, const int ktab_cap) {
   constexpr int NT = (BM / TM) * (BN / TN);
   constexpr int BK = kFfmaBK;
   constexpr int S = kFfmaStages;
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
   extern __shared__ __align__(16) float smem[];
   float* As = smem;                                       // [S][BK][AS]
   float* Bs = As + S * BK * AS;                           // [S][BK][BN]
-  int2* ktab = reinterpret_cast<int2*>(Bs + S * BK * BN);  // [kFfmaKTab]
+  int2* ktab = reinterpret_cast<int2*>(Bs + S * BK * BN);  // [ktab_cap]
 
   const T* __restrict__ x = static_cast<const T*>(a.x);
   const T* __restrict__ wt = static_cast<const T*>(a.wt);
@@ -132,8 +132,8 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
   const int tx = tid % (BN / TN);
   const int ty = tid / (BN / TN);
 
-  for (int kseg = k_begin; kseg < k_end; kseg += kFfmaKTab) {
-    const int seg_end = min(k_end, kseg + kFfmaKTab);
+  for (int kseg = k_begin; kseg < k_end; kseg += ktab_cap) {
+    const int seg_end = min(k_end, kseg + ktab_cap);
     __syncthreads();  // the previous segment's table and stages are free
     for (int k = kseg + tid; k < seg_end; k += NT) {
       const int c = k / khw;
@@ -250,20 +250,32 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
           }
         }
       } else {
-        if (whole4) {
-          float v[4];
+        // the epilogue on this run of 4 pixels of one channel
+        const T* __restrict__ resp = static_cast<const T*>(a.residual);
+        const float bco = a.bias ? to_f32(static_cast<const T*>(a.bias)[co]) : 0.0f;
+        float v[4], bv[4], rv[4];
+        long long oq[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) v[q] = to_f32(epilogue<T>(acc[i][jg * 4 + q], co, out + q, a));
+        for (int q = 0; q < 4; ++q) {
+          const long long pq = p + q;
+          const bool ok = pq < a.npix;
+          if (whole4) {
+            oq[q] = out + q;
+          } else {
+            const int nq = static_cast<int>((ok ? pq : p) / a.howo);
+            oq[q] = (static_cast<long long>(nq) * a.c_out + co) * a.howo + ((ok ? pq : p) - static_cast<long long>(nq) * a.howo);
+          }
+          v[q] = acc[i][jg * 4 + q];
+          bv[q] = bco;
+          rv[q] = (resp && ok) ? to_f32(resp[oq[q]]) : 0.0f;
+        }
+        epilogue_n<4>(v, bv, rv, a.bias != nullptr, resp != nullptr, a.act, a.alpha, a.beta);
+        if (whole4) {
           store4<T>(y, out, v);
         } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const long long pq = p + q;
-            if (pq >= a.npix) break;
-            const int nq = static_cast<int>(pq / a.howo);
-            const long long oq = (static_cast<long long>(nq) * a.c_out + co) * a.howo + (pq - nq * a.howo);
-            y[oq] = epilogue<T>(acc[i][jg * 4 + q], co, oq, a);
-          }
+          for (int q = 0; q < 4; ++q)
+            if (p + q < a.npix) y[oq[q]] = from_f32<T>(v[q]);
         }
       }
     }
@@ -288,27 +300,33 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
         s.z = __fadd_rn(s.z, t.z); s.w = __fadd_rn(s.w, t.w);
       }
       const long long o = i * 4;
-      const int co = static_cast<int>((o / a.howo) % a.c_out);
-      float v[4] = {s.x, s.y, s.z, s.w};
-      if (a.vec_out && (a.howo & 3) == 0) {  // the 4 outputs share a channel
-        float r[4];
+      const T* __restrict__ bp = static_cast<const T*>(a.bias);
+      const T* __restrict__ rp = static_cast<const T*>(a.residual);
+      float v[4] = {s.x, s.y, s.z, s.w}, bv[4], rv[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) r[k] = to_f32(epilogue<T>(v[k], co, o + k, a));
-        store4<T>(y, o, r);
+      for (int k = 0; k < 4; ++k) {
+        const int ck = static_cast<int>(((o + k) / a.howo) % a.c_out);
+        bv[k] = bp ? to_f32(bp[ck]) : 0.0f;
+        rv[k] = rp ? to_f32(rp[o + k]) : 0.0f;
+      }
+      epilogue_n<4>(v, bv, rv, bp != nullptr, rp != nullptr, a.act, a.alpha, a.beta);
+      if (a.vec_out) {
+        store4<T>(y, o, v);
       } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int ck = static_cast<int>(((o + k) / a.howo) % a.c_out);
-          y[o + k] = epilogue<T>(v[k], ck, o + k, a);
-        }
+        for (int k = 0; k < 4; ++k) y[o + k] = from_f32<T>(v[k]);
       }
     }
   } else {
+    const T* __restrict__ bp = static_cast<const T*>(a.bias);
+    const T* __restrict__ rp = static_cast<const T*>(a.residual);
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total; i += stride) {
-      float s = part[i];
-      for (int z = 1; z < a.split; ++z) s = __fadd_rn(s, part[z * total + i]);
+      float v[1] = {part[i]};
+      for (int z = 1; z < a.split; ++z) v[0] = __fadd_rn(v[0], part[z * total + i]);
       const int co = static_cast<int>((i / a.howo) % a.c_out);
-      y[i] = epilogue<T>(s, co, i, a);
+      float bv[1] = {bp ? to_f32(bp[co]) : 0.0f}, rv[1] = {rp ? to_f32(rp[i]) : 0.0f};
+      epilogue_n<1>(v, bv, rv, bp != nullptr, rp != nullptr, a.act, a.alpha, a.beta);
+      y[i] = from_f32<T>(v[0]);
     }
   }
 }
@@ -317,21 +335,22 @@ template <typename T, int CFG>
 cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   constexpr FfmaCfg c = kFfmaCfgs[CFG];
   auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn>;
-  const size_t smem = ffma_smem_bytes(CFG, sizeof(T) == 4 ? CONV_F32 : CONV_F16);
+  const int ktab_cap = ffma_ktab_entries(a.k_per_split);
+  const size_t smem = ffma_smem_bytes(CFG, a.k_per_split);
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && !configured[dev]) {
+  if (dev < 64 && configured[dev] < static_cast<int>(smem)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    configured[dev] = 1;
+    configured[dev] = static_cast<int>(smem);
   }
   const long long gx = (a.npix + c.bn - 1) / c.bn;
   const int co_tiles = (a.mg + c.bm - 1) / c.bm;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(co_tiles * a.groups),
             static_cast<unsigned>(a.split));
-  kern<<<grid, c.threads(), smem, s>>>(a);
+  kern<<<grid, c.threads(), smem, s>>>(a, ktab_cap);
   (void)plan;
   return cudaGetLastError();
 }
@@ -364,11 +383,14 @@ cudaError_t launch_reduce_typed(const ConvArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-size_t ffma_smem_bytes(int cfg, int dtype) {
-  (void)dtype;
+int ffma_ktab_entries(int k_per_block) {
+  return k_per_block < kFfmaKTab ? (k_per_block + 7) / 8 * 8 : kFfmaKTab;
+}
+
+size_t ffma_smem_bytes(int cfg, int k_per_block) {
   const FfmaCfg c = kFfmaCfgs[cfg];
   return static_cast<size_t>(kFfmaStages) * kFfmaBK * (c.bm + 4 + c.bn) * sizeof(float) +
-         static_cast<size_t>(kFfmaKTab) * sizeof(int2);
+         static_cast<size_t>(ffma_ktab_entries(k_per_block)) * sizeof(int2);
 }
 
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s) {

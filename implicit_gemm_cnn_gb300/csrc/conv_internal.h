@@ -25,7 +25,8 @@ constexpr FfmaCfg kFfmaCfgs[kNumFfmaCfgs] = {
     {128, 128, 8, 8}, {64, 128, 8, 8}, {128, 64, 8, 8}, {64, 64, 4, 4}, {32, 256, 4, 8},
     {16, 256, 4, 8},  {40, 128, 8, 4}, {16, 64, 4, 4},  {40, 64, 8, 4}};
 
-size_t ffma_smem_bytes(int cfg, int dtype);
+size_t ffma_smem_bytes(int cfg, int k_per_block);  // k_per_block: terms one block sums
+int ffma_ktab_entries(int k_per_block);
 
 // Depthwise (one input channel per group) halo-tiled direct kernel.
 struct DwPlan {

@@ -252,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
-  const uint32_t wready_bar = bar0 + 8u * (2 * S + 4);
   const uint32_t stg_bar = bar0 + 8u * (2 * S + 5);
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 6);
   auto res_bar = [&](int i) { return bar0 + 8u * (2 * S + 7 + i); };
@@ -276,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       mbar_init(tempty_bar(b), kEpiWarps * 32);
       mbar_init(res_bar(b), 1);
     }
-    mbar_init(wready_bar, kEpiWarps * 32);
     mbar_init(stg_bar, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -336,10 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
     *p0 = (pt - *n * p.tiles_per_img) * kM;
   };
 
-  if (warp < kEpiWarps) {
-    // ======================= weights, then the epilogue ======================
+  // ---- the block's weight rows: one bulk copy of the OIHW rows, then every
+  // thread lays them out as swizzled K-major tiles in the block's k order,
+  // four 16-byte units at a time with their loads issued first
+  {
     const long long wrow0 = static_cast<long long>(g) * a.mg + co0;  // first OIHW row
-    bool ok = true;
+    bool okw = true;
     if (c.bulk_w) {
       if (tid == 0) {
         const uint32_t bytes = static_cast<uint32_t>(c.stg_bytes);
@@ -348,41 +348,54 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
         for (uint32_t off = 0; off < bytes; off += 32768u)
           bulk_load(smem_u32(sio) + off, src + off, min(32768u, bytes - off), stg_bar);
       }
-      ok = wait_phase(stg_bar, 0, abort_flag, 1u);
+      okw = wait_phase(stg_bar, 0, abort_flag, 1u);
     }
-    ok = __all_sync(0xffffffffu, ok);  // warp-uniform before the loop below
-    if (ok) {
+    if (okw) {
       const int units = BN * kchunks * 8;
-      for (int q = tid; q < units; q += kEpiWarps * 32) {
-        const int j = q & 7;
-        const int r = (q >> 3) % BN;
-        const int kc = (q >> 3) / BN;
-        const int k0 = kc * kBK + j * 8;
-        uint16_t v[8];
-        int tap0 = 0, c0 = 0, ch = 0, u = 0;
-        if (c.mode == kModeCh8 && k0 < a.K) { tap0 = k0 / a.cg; c0 = k0 - tap0 * a.cg; }
-        if (c.mode == kModeRow8) { ch = (k0 / 8) / a.kh; u = (k0 / 8) - ch * a.kh; }
+      for (int base = tid; base < units; base += 4 * kThreads) {
+        uint16_t v[4][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          int idx = -1;  // position in the OIHW row, -1: zero padding
-          if (r < rows_valid) {
-            if (c.mode == kModeCh8) idx = (k0 + e < a.K) ? (c0 + e) * khw + tap0 : -1;
-            else if (c.mode == kModeRow8) idx = (ch < a.cg && e < a.kw) ? ch * khw + u * a.kw + e : -1;
-            else idx = (k0 + e < a.K) ? k0 + e : -1;
+        for (int b = 0; b < 4; ++b) {
+          const int q = base + b * kThreads;
+          const int j = q & 7;
+          const int r = (q >> 3) % BN;
+          const int kc = (q >> 3) / BN;
+          const int k0 = kc * kBK + j * 8;
+          int tap0 = 0, c0 = 0, ch = 0, u = 0;
+          if (c.mode == kModeCh8 && k0 < a.K) { tap0 = k0 / a.cg; c0 = k0 - tap0 * a.cg; }
+          if (c.mode == kModeRow8) { ch = (k0 / 8) / a.kh; u = (k0 / 8) - ch * a.kh; }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            int idx = -1;  // position in the OIHW row, -1: zero padding
+            if (q < units && r < rows_valid) {
+              if (c.mode == kModeCh8) idx = (k0 + e < a.K) ? (c0 + e) * khw + tap0 : -1;
+              else if (c.mode == kModeRow8) idx = (ch < a.cg && e < a.kw) ? ch * khw + u * a.kw + e : -1;
+              else idx = (k0 + e < a.K) ? k0 + e : -1;
+            }
+            v[b][e] = idx < 0 ? 0 : (c.bulk_w ? stg[static_cast<long long>(r) * a.K + idx] : ws[(wrow0 + r) * a.K + idx]);
           }
-          v[e] = idx < 0 ? 0 : (c.bulk_w ? stg[static_cast<long long>(r) * a.K + idx] : ws[(wrow0 + r) * a.K + idx]);
         }
-        *reinterpret_cast<uint4*>(sB + kc * (BN * 128) + swz(r, j)) =
-            make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int q = base + b * kThreads;
+          if (q < units) {
+            const int j = q & 7, r = (q >> 3) % BN, kc = (q >> 3) / BN;
+            *reinterpret_cast<uint4*>(sB + kc * (BN * 128) + swz(r, j)) =
+                make_uint4(pack2(v[b][0], v[b][1]), pack2(v[b][2], v[b][3]), pack2(v[b][4], v[b][5]),
+                           pack2(v[b][6], v[b][7]));
+          }
+        }
       }
-      fence_proxy_async();
-      mbar_arrive(wready_bar);
+      for (int cc = tid; cc < BN; cc += kThreads)
+        sbias[cc] = (a.bias && cc < rows_valid) ? to_f32(static_cast<const T*>(a.bias)[g * a.mg + co0 + cc]) : 0.0f;
     }
-    // bias of the block's channel tile, staged once
-    for (int cc = tid; cc < BN; cc += kEpiWarps * 32)
-      sbias[cc] = (a.bias && cc < rows_valid) ? to_f32(static_cast<const T*>(a.bias)[g * a.mg + co0 + cc]) : 0.0f;
-    epi_sync();  // the staging copy is consumed: its space becomes the tile buffers
+    fence_proxy_async();  // the generic-proxy stores above, visible to tcgen05.mma
+  }
+  __syncthreads();  // weights laid out; the staging space becomes the tile buffers
 
+  if (warp < kEpiWarps) {
+    // ================================ epilogue ================================
+    bool ok = !*abort_flag;
     const int row = warp * 32 + lane;
     T* __restrict__ y = static_cast<T*>(a.y);
     const T* __restrict__ res = static_cast<const T*>(a.residual);
@@ -426,14 +439,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
         for (int cc = 0; cc < BN; cc += 16) {
           uint32_t r[16];
           tmem_ld16(tbase + cc, r);
+          float v[16], bv[16], rv[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
-            const int col = cc + jj;
-            T* slot = io + col * kM + row;
-            const float rv = has_res ? to_f32(*slot) : 0.0f;
-            *slot = epilogue_vals<T>(__uint_as_float(r[jj]), sbias[col], rv, has_bias, has_res, a.act,
-                                     a.alpha, a.beta);
+            v[jj] = __uint_as_float(r[jj]);
+            bv[jj] = sbias[cc + jj];
+            rv[jj] = has_res ? to_f32(io[(cc + jj) * kM + row]) : 0.0f;
           }
+          epilogue_n<16>(v, bv, rv, has_bias, has_res, a.act, a.alpha, a.beta);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) io[(cc + jj) * kM + row] = from_f32<T>(v[jj]);
         }
         tc_fence_before();
         mbar_arrive(tempty_bar(b));  // the accumulator buffer is free for the tile after next
@@ -474,14 +489,17 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
           }
           uint32_t r[16];
           tmem_ld16(tbase + cc, r);
+          float v[16], bv[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            v[jj] = __uint_as_float(r[jj]);
+            bv[jj] = sbias[cc + jj];
+          }
+          epilogue_n<16>(v, bv, rcur, has_bias, has_res, a.act, a.alpha, a.beta);
           if (valid) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int col = cc + jj;
-              if (col < rows_valid)
-                y[obase + static_cast<long long>(col) * a.howo] = epilogue_vals<T>(
-                    __uint_as_float(r[jj]), sbias[col], rcur[jj], has_bias, has_res, a.act, a.alpha, a.beta);
-            }
+            for (int jj = 0; jj < 16; ++jj)
+              if (cc + jj < rows_valid) y[obase + static_cast<long long>(cc + jj) * a.howo] = from_f32<T>(v[jj]);
           }
         }
         tc_fence_before();
@@ -496,108 +514,143 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
     if (c.epi_bulk) bulk_wait_all();  // the output rows have landed before the block retires
   } else if (warp < kEpiWarps + kProdWarps) {
     // ============================ A-operand gather ============================
+    // Stage jobs (tile, k chunk) run as a software pipeline: the loads of the
+    // next job are issued into registers before the current job's values are
+    // packed into its stage, so two jobs' loads are in flight per thread.
     const int ptid = tid - kEpiWarps * 32;
     const int row = ptid & (kM - 1);
     const int part = ptid >> 7;  // 0 or 1: 16-byte units 4*part .. 4*part+3 of each row
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    for (int t = 0; ok && t < ntiles; ++t) {
+    bool ok = !*abort_flag;
+    struct Pix {
+      bool valid;
+      int ih0, iw0;
+      long long pb;
+      uint32_t em[4];  // row8: valid taps of a kernel row as 16-bit lane masks
+      uint32_t wv0, wv1;  // row8: 4-byte words worth loading, for an even / odd first tap
+    };
+    auto pix_of = [&](int t) {
+      Pix ps;
       int n, p0;
       tile_origin(t, &n, &p0);
       const int pix = p0 + row;
-      const bool valid = pix < a.howo;
-      int ih0 = 0, iw0 = 0;
-      long long pb = 0;
-      if (valid) {
+      ps.valid = pix < a.howo;
+      ps.ih0 = 0; ps.iw0 = 0; ps.pb = 0;
+      ps.em[0] = ps.em[1] = ps.em[2] = ps.em[3] = 0;
+      ps.wv0 = ps.wv1 = 0;
+      if (ps.valid) {
         const int oh = pix / a.wo, ow = pix - (pix / a.wo) * a.wo;
-        ih0 = oh * a.sh - a.pt;
-        iw0 = ow * a.sw - a.pl;
-        pb = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
-             static_cast<long long>(ih0) * a.w + iw0;
-      }
-      // row8: which of the 8 taps of a kernel row land inside the image (per
-      // pixel), as 16-bit lane masks, and which 4-byte words are worth loading
-      // for either parity of the row segment's first element
-      uint32_t em[4] = {0, 0, 0, 0};
-      uint32_t wv[2] = {0, 0};
-      if (c.mode == kModeRow8 && valid) {
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const int iw = iw0 + v;
-          if (v < a.kw && iw >= 0 && iw < a.w) em[v >> 1] |= (v & 1) ? 0xFFFF0000u : 0x0000FFFFu;
-        }
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-#pragma unroll
-          for (int k = 0; k < 5; ++k) {
-            const int c0 = iw0 - s + 2 * k;  // columns c0, c0 + 1 of word k
-            const bool any = (c0 >= 0 && c0 < a.w) || (c0 + 1 >= 0 && c0 + 1 < a.w);
-            if (any && c0 < iw0 + a.kw && c0 + 1 >= iw0) wv[s] |= 1u << k;
-          }
-      }
-      for (int kc = 0; kc < kchunks; ++kc) {
-        if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, 4u)) { ok = false; break; }
-        uint8_t* As = sA + stage * kStageBytes;
+        ps.ih0 = oh * a.sh - a.pt;
+        ps.iw0 = ow * a.sw - a.pl;
+        ps.pb = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
+                static_cast<long long>(ps.ih0) * a.w + ps.iw0;
         if (c.mode == kModeRow8) {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = part * 4 + jj;
-            const int4 e = tab[kc * 8 + j];
-            const int ih = ih0 + e.y;
-            const bool in = valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (in) {
-              const long long e0 = pb + e.x;  // first tap's element
-              const int s = static_cast<int>(e0 & 1);
-              const uint32_t* wp = reinterpret_cast<const uint32_t*>(xs + (e0 - s));
-              const uint32_t m = wv[s];
-              uint32_t w5[5];
+          for (int v = 0; v < 8; ++v) {
+            const int iw = ps.iw0 + v;
+            if (v < a.kw && iw >= 0 && iw < a.w) ps.em[v >> 1] |= (v & 1) ? 0xFFFF0000u : 0x0000FFFFu;
+          }
 #pragma unroll
-              for (int k = 0; k < 5; ++k) w5[k] = (m >> k & 1u) ? __ldg(wp + k) : 0u;
-              const uint32_t sel = s ? 0x5432u : 0x3210u;
-              o.x = __byte_perm(w5[0], w5[1], sel) & em[0];
-              o.y = __byte_perm(w5[1], w5[2], sel) & em[1];
-              o.z = __byte_perm(w5[2], w5[3], sel) & em[2];
-              o.w = __byte_perm(w5[3], w5[4], sel) & em[3];
+          for (int sp = 0; sp < 2; ++sp)
+#pragma unroll
+            for (int k = 0; k < 5; ++k) {
+              const int c0 = ps.iw0 - sp + 2 * k;  // columns c0, c0 + 1 of word k
+              const bool any = (c0 >= 0 && c0 < a.w) || (c0 + 1 >= 0 && c0 + 1 < a.w);
+              if (any && c0 < ps.iw0 + a.kw && c0 + 1 >= ps.iw0) {
+                if (sp) ps.wv1 |= 1u << k;
+                else ps.wv0 |= 1u << k;
+              }
             }
-            *reinterpret_cast<uint4*>(As + swz(row, j)) = o;
-          }
+        }
+      }
+      return ps;
+    };
+    // raw values of one job's 4 units: row8 keeps 5 words + selector + flag,
+    // the others 8 zero-extended 16-bit values
+    auto load_job = [&](const Pix& ps, int kc, uint32_t (&raw)[4][8]) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = part * 4 + jj;
+        if (c.mode == kModeRow8) {
+          const int4 e = tab[kc * 8 + j];
+          const int ih = ps.ih0 + e.y;
+          const bool in = ps.valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
+          const long long e0 = ps.pb + e.x;  // first tap's element
+          const int sp = static_cast<int>(e0 & 1);
+          const uint32_t* wp = reinterpret_cast<const uint32_t*>(xs + (in ? e0 - sp : 0));
+          const uint32_t m = in ? (sp ? ps.wv1 : ps.wv0) : 0u;
+#pragma unroll
+          for (int k = 0; k < 5; ++k) raw[jj][k] = (m >> k & 1u) ? __ldg(wp + k) : 0u;
+          raw[jj][5] = sp ? 0x5432u : 0x3210u;
+          raw[jj][6] = in ? 1u : 0u;
+          raw[jj][7] = 0u;
         } else if (c.mode == kModeCh8) {
+          const int4 e = tab[kc * 8 + j];
+          const int ih = ps.ih0 + e.y, iw = ps.iw0 + e.z;
+          const bool in = ps.valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
+                          static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
+          const uint16_t* src = xs + (in ? ps.pb + e.x : 0);
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = part * 4 + jj;
-            const int4 e = tab[kc * 8 + j];
-            const int ih = ih0 + e.y, iw = iw0 + e.z;
-            const bool in = valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
-                            static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
-            uint16_t v[8];
-            const uint16_t* src = xs + (in ? pb + e.x : 0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = in ? src[static_cast<long long>(q) * a.hw] : 0;
-            *reinterpret_cast<uint4*>(As + swz(row, j)) =
-                make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
-          }
+          for (int q = 0; q < 8; ++q) raw[jj][q] = in ? src[static_cast<long long>(q) * a.hw] : 0u;
         } else {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = part * 4 + jj;
-            uint16_t v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int4 e = tab[kc * kBK + j * 8 + q];
-              const int ih = ih0 + e.y, iw = iw0 + e.z;
-              const bool in = valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
-                              static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
-              v[q] = in ? xs[pb + e.x] : 0;
-            }
-            *reinterpret_cast<uint4*>(As + swz(row, j)) =
-                make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+          for (int q = 0; q < 8; ++q) {
+            const int4 e = tab[kc * kBK + j * 8 + q];
+            const int ih = ps.ih0 + e.y, iw = ps.iw0 + e.z;
+            const bool in = ps.valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
+                            static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
+            raw[jj][q] = in ? xs[ps.pb + e.x] : 0u;
           }
         }
-        fence_proxy_async();
-        mbar_arrive(full_bar(stage));
-        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    };
+    auto emit_job = [&](const Pix& ps, const uint32_t (&raw)[4][8], uint8_t* As) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = part * 4 + jj;
+        uint4 o;
+        if (c.mode == kModeRow8) {
+          const uint32_t sel = raw[jj][5];
+          const uint32_t keep = raw[jj][6] ? 0xFFFFFFFFu : 0u;
+          o.x = __byte_perm(raw[jj][0], raw[jj][1], sel) & ps.em[0] & keep;
+          o.y = __byte_perm(raw[jj][1], raw[jj][2], sel) & ps.em[1] & keep;
+          o.z = __byte_perm(raw[jj][2], raw[jj][3], sel) & ps.em[2] & keep;
+          o.w = __byte_perm(raw[jj][3], raw[jj][4], sel) & ps.em[3] & keep;
+        } else {
+          o = make_uint4(raw[jj][0] | (raw[jj][1] << 16), raw[jj][2] | (raw[jj][3] << 16),
+                         raw[jj][4] | (raw[jj][5] << 16), raw[jj][6] | (raw[jj][7] << 16));
+        }
+        *reinterpret_cast<uint4*>(As + swz(row, j)) = o;
+      }
+    };
+    const int njobs = ntiles * kchunks;
+    uint32_t cur[4][8], nxt[4][8];
+    Pix pc = pix_of(0);
+    if (ok && njobs > 0) load_job(pc, 0, cur);
+    int t = 0, kc = 0;
+    for (int jb = 0; ok && jb < njobs; ++jb) {
+      int tn = t, kcn = kc + 1;
+      if (kcn == kchunks) { kcn = 0; tn = t + 1; }
+      const bool has_next = jb + 1 < njobs;
+      Pix pn = pc;
+      if (has_next) {
+        if (tn != t) pn = pix_of(tn);
+        load_job(pn, kcn, nxt);
+      }
+      if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, 4u)) { ok = false; break; }
+      emit_job(pc, cur, sA + stage * kStageBytes);
+      fence_proxy_async();
+      mbar_arrive(full_bar(stage));
+      if (++stage == S) { stage = 0; phase ^= 1u; }
+      if (has_next) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) cur[jj][q] = nxt[jj][q];
+        pc = pn;
+        t = tn;
+        kc = kcn;
       }
     }
   } else {
@@ -606,8 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       constexpr uint32_t idesc = make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value, BN);
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = wait_phase(wready_bar, 0, abort_flag, 8u);
-      if (ok) tc_fence_after();
+      bool ok = !*abort_flag;
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
       for (int t = 0; ok && t < ntiles; ++t) {
         const int b = t & 1;
