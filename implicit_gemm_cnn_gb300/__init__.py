@@ -23,7 +23,8 @@ __all__ = [
     "ConvError", "ConvLibraryError", "ConvProblem", "ConvPlanInfo", "ACTIVATIONS", "DTYPES",
     "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
-    "conv_forward", "conv_device_error", "make_problem", "conv2d", "library_path", "load",
+    "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
+    "make_problem", "conv2d", "library_path", "load",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +35,7 @@ ACTIVATIONS = {"identity": 0, "relu": 1, "silu": 2, "sigmoid": 3, "tanh": 4, "ha
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 VARIANTS = {0: "igemm_ffma", 1: "igemm_ffma_split_k", 2: "depthwise_halo", 3: "igemm_tcgen05",
             4: "igemm_tcgen05_1x1"}
+FIXED_SCRATCH_BYTES = 8 << 20  # CONV_FIXED_SCRATCH_BYTES
 FLAG_FORCE_FFMA = 0x1
 FLAG_NO_SPLIT_K = 0x2
 SPLIT_K_SHIFT = 8
@@ -112,8 +114,9 @@ def load() -> ctypes.CDLL:
         lib.conv_describe_variant.argtypes = [P(ConvProblem), ctypes.c_char_p, ctypes.c_size_t]
         lib.conv_forward.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_device_error.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
+        lib.conv_forward_fixed_scratch.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp]
         for f in ("conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
-                  "conv_forward", "conv_device_error"):
+                  "conv_forward", "conv_device_error", "conv_forward_fixed_scratch"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -182,6 +185,24 @@ def conv_forward(p: ConvProblem, x, w, bias, residual, y, scratch=None, scratch_
     _check(load().conv_forward(ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias), _ptr(residual),
                                _ptr(y), _ptr(scratch), scratch_bytes, stream or None),
            "conv_forward")
+
+
+def conv_forward_fixed_scratch(p: ConvProblem, x, w, bias, residual, y, stream=None) -> None:
+    """conv_forward with the split-k scratch in the library's own fixed device
+    array (FIXED_SCRATCH_BYTES) instead of caller memory: for callers that
+    cannot allocate device memory.  The first call on a device sets the array
+    up (before any stream capture); calls that overlap on the GPU race on it."""
+    if stream is None:
+        try:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream
+        except Exception:  # noqa: BLE001 - no torch / no CUDA: the legacy default stream
+            stream = 0
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    _check(load().conv_forward_fixed_scratch(ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias),
+                                             _ptr(residual), _ptr(y), stream or None),
+           "conv_forward_fixed_scratch")
 
 
 def conv_device_error(reset: bool = True) -> int:

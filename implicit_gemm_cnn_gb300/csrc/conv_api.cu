@@ -439,3 +439,49 @@ conv_status conv_device_error(uint32_t* word, int32_t reset) {
 }
 
 }  // extern "C"
+
+// ---- a forward call for callers that cannot allocate device memory ---------
+//
+// Some callers cannot call cudaMalloc: code running where allocation is not
+// permitted (a plug-in of a host framework that owns every allocation, a
+// real-time path that must not touch the allocator, a caller with no CUDA
+// runtime of its own beyond this library).  For them the split-k planes live
+// in one fixed device array that the library owns.  It is reserved on every
+// GPU that loads this library and kept until the process exits.
+static __device__ __align__(256) unsigned char g_fixed_scratch[CONV_FIXED_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_fixed_mu;
+void* g_fixed_addr[kMaxDevices];  // device address of g_fixed_scratch, per device
+}  // namespace
+
+extern "C" conv_status conv_forward_fixed_scratch(const conv_problem* p, const void* x, const void* w,
+                                                  const void* bias, const void* residual, void* y,
+                                                  void* stream) {
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  int dev, sm;
+  st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  Plan plan;
+  st = make_plan(p, sm, &plan, nullptr);
+  if (st != CONV_OK) return st;
+  if (plan.info.scratch_bytes > CONV_FIXED_SCRATCH_BYTES) return CONV_ERR_SCRATCH;
+  void* addr = nullptr;
+  {
+    // set-up, once per device, with that device current: the array's name is
+    // a host-side stand-in, the kernels need its device address
+    std::lock_guard<std::mutex> lock(g_fixed_mu);
+    if (!g_fixed_addr[dev]) {
+      void* a = nullptr;
+      if (cudaGetSymbolAddress(&a, g_fixed_scratch) != cudaSuccess || !a) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+      }
+      g_fixed_addr[dev] = a;
+    }
+    addr = g_fixed_addr[dev];
+  }
+  return conv_forward(p, x, w, bias, residual, y, addr, CONV_FIXED_SCRATCH_BYTES, stream);
+}

@@ -200,6 +200,36 @@ CONV_API conv_status conv_forward(const conv_problem* p, const void* x, const vo
  * incomplete).  Synchronises the device; for tests and diagnostics. */
 CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
 
+/* Bytes of the library-owned scratch array of conv_forward_fixed_scratch. */
+#define CONV_FIXED_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+
+/* conv_forward without caller-provided scratch, for callers that cannot
+ * allocate device memory (no counterpart on the pages this library follows).
+ *
+ * Who needs it: code that may not call cudaMalloc -- a plug-in inside a host
+ * framework that owns every device allocation, a latency-critical path that
+ * must not enter the allocator, or a caller whose only CUDA code is this
+ * library.  Such a caller still passes x, w, bias, residual and y (device
+ * memory it was given), exactly as for conv_forward; the split-k planes, the
+ * only scratch any variant needs, live instead in one fixed array of
+ * CONV_FIXED_SCRATCH_BYTES that the library declares in device memory.  Every
+ * GPU that loads the library holds that array until the process exits.
+ *
+ * Nothing is allocated by this call.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture on the device.
+ * Every call shares the one array and leaves its last contents there (each
+ * call overwrites every scratch byte it reads before reading it, so nothing
+ * needs clearing); two calls whose kernels overlap on the GPU -- on different
+ * streams, say -- race on it and must be serialised by the caller.
+ *
+ * Errors: those of conv_forward; CONV_ERR_SCRATCH when the problem's scratch
+ * (conv_scratch_bytes) exceeds CONV_FIXED_SCRATCH_BYTES, before anything is
+ * enqueued; CONV_ERR_CUDA when the array's address cannot be obtained. */
+CONV_API conv_status conv_forward_fixed_scratch(const conv_problem* p, const void* x, const void* w,
+                                                const void* bias, const void* residual, void* y,
+                                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif
