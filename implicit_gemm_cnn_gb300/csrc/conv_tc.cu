@@ -207,10 +207,13 @@ struct TcLaunch {
   int nio;              // staging buffers (1 or 2)
   int bulk_w;           // weights arrive by one bulk copy
   long long stg_bytes;  // bytes of that copy
+  int halo_bufs;        // input halo buffers in shared memory (0: gather from global)
+  int halo_slot;        // elements per input channel in a halo buffer (a multiple of 8)
+  int halo_cg;          // input channels per group (channels per halo buffer)
 };
 
 struct TcLayout {
-  uint32_t b_off, a_off, sio_off, tab_off, bias_off, bar_off, slot_off, end;
+  uint32_t b_off, a_off, sio_off, halo_off, tab_off, bias_off, bar_off, slot_off, end;
 };
 
 __host__ __device__ inline int tc_ntab(int mode, int k_pad) {
@@ -226,16 +229,19 @@ __host__ __device__ inline TcLayout tc_layout(int bn, const TcLaunch& c) {
   // epilogue's tile buffers reuse its space
   const long long stg = c.bulk_w ? (c.stg_bytes + 127) / 128 * 128 : 0;
   const long long io = c.epi_bulk ? static_cast<long long>(c.nio) * bn * kM * 2 : 0;
-  L.tab_off = L.sio_off + static_cast<uint32_t>(stg > io ? stg : io);
+  const long long halo = static_cast<long long>(c.halo_bufs) * c.halo_cg * c.halo_slot * 2;
+  L.halo_off = L.sio_off + static_cast<uint32_t>((io + 127) / 128 * 128);  // after the tile buffers
+  const long long r1 = (io + 127) / 128 * 128 + halo;
+  L.tab_off = L.sio_off + static_cast<uint32_t>(stg > r1 ? stg : r1);
   L.bias_off = L.tab_off + static_cast<uint32_t>(tc_ntab(c.mode, c.k_pad)) * 16;
   L.bar_off = L.bias_off + static_cast<uint32_t>(bn) * 4;
-  L.slot_off = L.bar_off + static_cast<uint32_t>(2 * c.stages + 9) * 8;
+  L.slot_off = L.bar_off + static_cast<uint32_t>(2 * c.stages + 13) * 8;
   L.end = L.slot_off + 16;
   return L;
 }
 
 template <typename T, int BN>
-__global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const TcPlan p, const TcLaunch c) {
+__global__ void __maxnreg__(152) igemm_tc(const ConvArgs a, const TcPlan p, const TcLaunch c) {
   extern __shared__ uint8_t tsm_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   uint8_t* tsm = tsm_raw + ((1024 - (smem_u32(tsm_raw) & 1023)) & 1023);
@@ -255,6 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
   const uint32_t stg_bar = bar0 + 8u * (2 * S + 5);
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 6);
   auto res_bar = [&](int i) { return bar0 + 8u * (2 * S + 7 + i); };
+  auto hfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 9 + i); };   // halo buffer filled
+  auto hempty_bar = [&](int i) { return bar0 + 8u * (2 * S + 11 + i); };  // halo buffer consumed
+  volatile int* halo_a0 = reinterpret_cast<volatile int*>(tsm + L.slot_off + 8);  // [2] first element copied
+  uint16_t* halo = reinterpret_cast<uint16_t*>(tsm + L.halo_off);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tsm + L.slot_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tsm + L.slot_off + 4);
 
@@ -274,6 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), kEpiWarps * 32);
       mbar_init(res_bar(b), 1);
+      mbar_init(hfull_bar(b), 1);
+      mbar_init(hempty_bar(b), kProd);
     }
     mbar_init(stg_bar, 1);
     mbar_init(drain_bar, 1);
@@ -289,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       const int ch = e / a.kh, u = e - (e / a.kh) * a.kh;
       dy = u * a.dh;
       dx = 0;
-      coff = ch * static_cast<int>(a.hw) + dy * a.w;
+      coff = ch * (c.halo_bufs ? c.halo_slot : static_cast<int>(a.hw)) + dy * a.w;
       ok = ch < a.cg;
     } else {
       const int k = c.mode == kModeCh8 ? e * 8 : e;
@@ -299,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       const int u = tap / a.kw, v = tap - (tap / a.kw) * a.kw;
       dy = u * a.dh;
       dx = v * a.dw;
-      coff = ch * static_cast<int>(a.hw) + dy * a.w + dx;
+      coff = ch * (c.halo_bufs ? c.halo_slot : static_cast<int>(a.hw)) + dy * a.w + dx;
       ok = k < a.K;
     }
     tab[e] = make_int4(coff, dy, dx, ok);
@@ -364,15 +376,25 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
           int tap0 = 0, c0 = 0, ch = 0, u = 0;
           if (c.mode == kModeCh8 && k0 < a.K) { tap0 = k0 / a.cg; c0 = k0 - tap0 * a.cg; }
           if (c.mode == kModeRow8) { ch = (k0 / 8) / a.kh; u = (k0 / 8) - ch * a.kh; }
+          int idx[8];  // positions in the OIHW row, -1: zero padding
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            int idx = -1;  // position in the OIHW row, -1: zero padding
+            idx[e] = -1;
             if (q < units && r < rows_valid) {
-              if (c.mode == kModeCh8) idx = (k0 + e < a.K) ? (c0 + e) * khw + tap0 : -1;
-              else if (c.mode == kModeRow8) idx = (ch < a.cg && e < a.kw) ? ch * khw + u * a.kw + e : -1;
-              else idx = (k0 + e < a.K) ? k0 + e : -1;
+              if (c.mode == kModeCh8) idx[e] = (k0 + e < a.K) ? (c0 + e) * khw + tap0 : -1;
+              else if (c.mode == kModeRow8) idx[e] = (ch < a.cg && e < a.kw) ? ch * khw + u * a.kw + e : -1;
+              else idx[e] = (k0 + e < a.K) ? k0 + e : -1;
             }
-            v[b][e] = idx < 0 ? 0 : (c.bulk_w ? stg[static_cast<long long>(r) * a.K + idx] : ws[(wrow0 + r) * a.K + idx]);
+          }
+          // one source per launch (a uniform branch, not a select of two loads)
+          if (c.bulk_w) {
+            const uint16_t* src = stg + static_cast<long long>(min(r, rows_valid - 1)) * a.K;  // a real row
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[b][e] = idx[e] < 0 ? 0 : src[idx[e] < 0 ? 0 : idx[e]];
+          } else {
+            const uint16_t* src = ws + (wrow0 + min(r, rows_valid - 1)) * a.K;  // a real row
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[b][e] = idx[e] < 0 ? 0 : src[idx[e] < 0 ? 0 : idx[e]];
           }
         }
 #pragma unroll
@@ -523,10 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
     int stage = 0;
     uint32_t phase = 0;
     bool ok = !*abort_flag;
+    const int HB = c.halo_bufs;
     struct Pix {
       bool valid;
       int ih0, iw0;
-      long long pb;
+      long long pb;          // element of tap (0,0), channel 0, in src
+      const uint16_t* src;   // x, or the tile's halo buffer in shared memory
+      long long cs;          // elements from one input channel to the next in src
       uint32_t em[4];  // row8: valid taps of a kernel row as 16-bit lane masks
       uint32_t wv0, wv1;  // row8: 4-byte words worth loading, for an even / odd first tap
     };
@@ -537,14 +562,20 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       const int pix = p0 + row;
       ps.valid = pix < a.howo;
       ps.ih0 = 0; ps.iw0 = 0; ps.pb = 0;
+      ps.src = HB ? halo + static_cast<long long>(t % HB) * c.halo_cg * c.halo_slot : xs;
+      ps.cs = HB ? c.halo_slot : a.hw;
       ps.em[0] = ps.em[1] = ps.em[2] = ps.em[3] = 0;
       ps.wv0 = ps.wv1 = 0;
       if (ps.valid) {
         const int oh = pix / a.wo, ow = pix - (pix / a.wo) * a.wo;
         ps.ih0 = oh * a.sh - a.pt;
         ps.iw0 = ow * a.sw - a.pl;
-        ps.pb = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
-                static_cast<long long>(ps.ih0) * a.w + ps.iw0;
+        if (HB) {  // the halo slot holds the plane from element halo_a0 on, 8 elements in
+          ps.pb = 8 + static_cast<long long>(ps.ih0) * a.w + ps.iw0 - halo_a0[t % HB];
+        } else {
+          ps.pb = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
+                  static_cast<long long>(ps.ih0) * a.w + ps.iw0;
+        }
         if (c.mode == kModeRow8) {
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
@@ -562,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
                 else ps.wv0 |= 1u << k;
               }
             }
+          if (HB) ps.wv0 = ps.wv1 = 0x1Fu;  // shared memory around the slot: every word is readable
         }
       }
       return ps;
@@ -578,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
           const bool in = ps.valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
           const long long e0 = ps.pb + e.x;  // first tap's element
           const int sp = static_cast<int>(e0 & 1);
-          const uint32_t* wp = reinterpret_cast<const uint32_t*>(xs + (in ? e0 - sp : 0));
+          const uint32_t* wp = reinterpret_cast<const uint32_t*>(ps.src + (in ? e0 - sp : 0));
           const uint32_t m = in ? (sp ? ps.wv1 : ps.wv0) : 0u;
 #pragma unroll
           for (int k = 0; k < 5; ++k) raw[jj][k] = (m >> k & 1u) ? __ldg(wp + k) : 0u;
@@ -590,9 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
           const int ih = ps.ih0 + e.y, iw = ps.iw0 + e.z;
           const bool in = ps.valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
                           static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
-          const uint16_t* src = xs + (in ? ps.pb + e.x : 0);
+          const uint16_t* src = ps.src + (in ? ps.pb + e.x : 0);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) raw[jj][q] = in ? src[static_cast<long long>(q) * a.hw] : 0u;
+          for (int q = 0; q < 8; ++q) raw[jj][q] = in ? src[static_cast<long long>(q) * ps.cs] : 0u;
         } else {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -600,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
             const int ih = ps.ih0 + e.y, iw = ps.iw0 + e.z;
             const bool in = ps.valid && e.w && static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
                             static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
-            raw[jj][q] = in ? xs[ps.pb + e.x] : 0u;
+            raw[jj][q] = in ? ps.src[in ? ps.pb + e.x : 0] : 0u;
           }
         }
       }
@@ -625,36 +657,96 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
       }
     };
     const int njobs = ntiles * kchunks;
-    uint32_t cur[4][8], nxt[4][8];
-    Pix pc = pix_of(0);
-    if (ok && njobs > 0) load_job(pc, 0, cur);
+    // two raw buffers used in turn (no copy between them, so nothing waits on
+    // the loads just issued until their job is emitted)
+    uint32_t ra[4][8], rb[4][8];
+    // the halo of tile tt is in its buffer / this thread is done reading it
+    auto halo_in = [&](int tt) -> bool {
+      return !HB || wait_phase(hfull_bar(tt % HB), static_cast<uint32_t>((tt / HB) & 1), abort_flag, 512u);
+    };
+    auto halo_out = [&](int tt) {
+      if (HB) mbar_arrive(hempty_bar(tt % HB));
+    };
+    Pix pa, pb;
+    if (ok && njobs > 0) {
+      ok = halo_in(0);
+      if (ok) {
+        pa = pix_of(0);
+        load_job(pa, 0, ra);
+        if (kchunks == 1) halo_out(0);
+      }
+    }
     int t = 0, kc = 0;
-    for (int jb = 0; ok && jb < njobs; ++jb) {
+    // one pipeline step: issue the next job's loads into `nxt`, then emit `cur`
+    auto step = [&](int jb, const Pix& pc, uint32_t (&cur)[4][8], Pix& pn, uint32_t (&nxt)[4][8]) {
       int tn = t, kcn = kc + 1;
       if (kcn == kchunks) { kcn = 0; tn = t + 1; }
-      const bool has_next = jb + 1 < njobs;
-      Pix pn = pc;
-      if (has_next) {
-        if (tn != t) pn = pix_of(tn);
+      if (jb + 1 < njobs) {
+        if (tn != t) {
+          if (!halo_in(tn)) return false;
+          pn = pix_of(tn);
+        } else {
+          pn = pc;
+        }
         load_job(pn, kcn, nxt);
+        if (kcn == kchunks - 1) halo_out(tn);
       }
-      if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, 4u)) { ok = false; break; }
+      if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, 4u)) return false;
       emit_job(pc, cur, sA + stage * kStageBytes);
       fence_proxy_async();
       mbar_arrive(full_bar(stage));
       if (++stage == S) { stage = 0; phase ^= 1u; }
-      if (has_next) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-          for (int q = 0; q < 8; ++q) cur[jj][q] = nxt[jj][q];
-        pc = pn;
-        t = tn;
-        kc = kcn;
-      }
+      t = tn;
+      kc = kcn;
+      return true;
+    };
+    for (int jb = 0; ok && jb < njobs; jb += 2) {
+      ok = step(jb, pa, ra, pb, rb);
+      if (ok && jb + 1 < njobs) ok = step(jb + 1, pb, rb, pa, ra);
     }
   } else {
-    // ============================ MMA issue (one lane) ========================
+    // ============ halo copies (lanes 1-31) and MMA issue (lane 0) ==============
+    const int HB = c.halo_bufs;
+    if (lane != 0 && HB > 0) {
+      // per tile: the input rows its windows reach, one contiguous span of each
+      // input channel's plane, rounded out to 16 bytes, into the tile's buffer
+      bool okl = !*abort_flag;
+      int issued = 0;
+      for (int t = 0; okl && t < ntiles; ++t) {
+        const int hb = t % HB;
+        okl = __all_sync(0xFFFFFFFEu, wait_phase(hempty_bar(hb), static_cast<uint32_t>(((t / HB) & 1) ^ 1),
+                                                 abort_flag, 256u));
+        if (!okl) break;
+        int n, p0;
+        tile_origin(t, &n, &p0);
+        const int vpx = min(kM, static_cast<int>(a.howo) - p0);
+        const int oh_f = p0 / a.wo, oh_l = (p0 + vpx - 1) / a.wo;
+        const int r_lo = max(0, oh_f * a.sh - a.pt);
+        const int r_hi = min(a.h, oh_l * a.sh - a.pt + (a.kh - 1) * a.dh + 1);
+        long long a0 = 0, a1 = 0;
+        if (r_hi > r_lo) {
+          a0 = (static_cast<long long>(r_lo) * a.w) & ~7LL;
+          a1 = (static_cast<long long>(r_hi) * a.w + 7) & ~7LL;
+        }
+        const uint32_t bytes = static_cast<uint32_t>((a1 - a0) * 2);
+        if (lane == 1) {
+          halo_a0[hb] = static_cast<int>(a0);
+          mbar_arrive_expect_tx(hfull_bar(hb), bytes * static_cast<uint32_t>(a.cg));
+        }
+        __syncwarp(0xFFFFFFFEu);
+        if (bytes) {
+          const uint16_t* plane0 = xs + (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw;
+          for (int ch = lane - 1; ch < a.cg; ch += 31)
+            bulk_load(smem_u32(halo + (static_cast<long long>(hb) * a.cg + ch) * c.halo_slot + 8),
+                      plane0 + static_cast<long long>(ch) * a.hw + a0, bytes, hfull_bar(hb));
+        }
+        issued = t + 1;
+      }
+      if (!okl) {  // aborted: copies still in flight must land before the block retires
+        for (int t = max(0, issued - HB); t < issued; ++t)
+          wait_phase(hfull_bar(t % HB), static_cast<uint32_t>((t / HB) & 1), abort_flag, 512u, true);
+      }
+    }
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc = make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value, BN);
       int stage = 0;
@@ -759,16 +851,28 @@ bool configure(const TcPlan& p, const ConvArgs& a, bool addresses_known, TcLaunc
   c->epi_bulk = (a.howo % 8 == 0) &&
                 (!addresses_known || (reinterpret_cast<uintptr_t>(a.y) % 16 == 0 &&
                                       (!a.residual || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0)));
-  for (int epi = c->epi_bulk; epi >= 0; --epi) {
-    for (int nio = epi ? 2 : 1; nio >= 1; --nio) {
-      for (int st = 4; st >= 2; --st) {
-        TcLaunch t = *c;
-        t.epi_bulk = epi;
-        t.nio = nio;
-        t.stages = st;
-        if (tc_bytes(p.bn, t) <= kTcMaxSmem) {
-          *c = t;
-          return true;
+  // input halo: the rows a tile's windows reach, per input channel of the
+  // group, copied whole into shared memory (planes must start on 16 bytes)
+  const int r_out = min(a.ho, (a.wo - 1 + kM - 1) / a.wo + 1);  // output rows a tile can touch
+  const long long r_in = static_cast<long long>(r_out - 1) * a.sh + static_cast<long long>(a.kh - 1) * a.dh + 1;
+  const long long slot = (r_in * a.w + 7) / 8 * 8 + 24;       // 8 elements of slack on each side
+  const bool halo_ok = (a.hw % 8 == 0) && slot * a.cg * 2 < (1 << 20) &&
+                       (!addresses_known || reinterpret_cast<uintptr_t>(a.x) % 16 == 0);
+  c->halo_cg = a.cg;
+  c->halo_slot = static_cast<int>(halo_ok ? slot : 0);
+  for (int hb = halo_ok ? 2 : 0; hb >= 0; --hb) {
+    for (int epi = c->epi_bulk; epi >= 0; --epi) {
+      for (int nio = epi ? 2 : 1; nio >= 1; --nio) {
+        for (int st = 4; st >= 2; --st) {
+          TcLaunch t = *c;
+          t.halo_bufs = hb;
+          t.epi_bulk = epi;
+          t.nio = nio;
+          t.stages = st;
+          if (tc_bytes(p.bn, t) <= kTcMaxSmem) {
+            *c = t;
+            return true;
+          }
         }
       }
     }

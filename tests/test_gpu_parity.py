@@ -124,6 +124,9 @@ EDGE = [
     ("tc_row8_odd_count", (1, 5, 17, 23), (24, 5, 5, 6), dict(pads=(2, 3, 2, 2)), True, False),
     ("tc_bulk_res", (2, 16, 8, 12), (32, 16, 3, 3), dict(pads=1, act="silu"), True, True),
     ("tc_bulk_tiles", (3, 8, 20, 16), (64, 8, 1, 1), dict(act="relu"), True, True),
+    ("tc_halo_row8", (2, 3, 32, 40), (16, 3, 7, 7), dict(stride=2, pads=3, act="relu"), True, False),
+    ("tc_halo_s2_d2", (2, 16, 24, 16), (32, 16, 3, 3), dict(stride=2, pads=2, dilation=2), True, True),
+    ("tc_halo_narrow", (1, 8, 40, 8), (16, 8, 3, 3), dict(pads=1, act="tanh"), True, False),
     ("long_k", (1, 320, 6, 6), (16, 320, 3, 3), dict(pads=1), True, False),
     ("wide_cin_1x1", (1, 1024, 4, 4), (64, 1024, 1, 1), dict(), True, False),
 ]
