@@ -241,7 +241,7 @@ __host__ __device__ inline TcLayout tc_layout(int bn, const TcLaunch& c) {
 }
 
 template <typename T, int BN>
-__global__ void __maxnreg__(152) igemm_tc(const ConvArgs a, const TcPlan p, const TcLaunch c) {
+__global__ void __maxnreg__(144) igemm_tc(const ConvArgs a, const TcPlan p, const TcLaunch c) {
   extern __shared__ uint8_t tsm_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   uint8_t* tsm = tsm_raw + ((1024 - (smem_u32(tsm_raw) & 1023)) & 1023);
