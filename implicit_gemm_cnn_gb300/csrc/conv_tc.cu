@@ -241,7 +241,7 @@ __host__ __device__ inline TcLayout tc_layout(int bn, const TcLaunch& c) {
 }
 
 template <typename T, int BN>
-__global__ void __maxnreg__(144) igemm_tc(const ConvArgs a, const TcPlan p, const TcLaunch c) {
+__global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const TcPlan p, const TcLaunch c) {
   extern __shared__ uint8_t tsm_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   uint8_t* tsm = tsm_raw + ((1024 - (smem_u32(tsm_raw) & 1023)) & 1023);
@@ -700,9 +700,32 @@ __global__ void __maxnreg__(144) igemm_tc(const ConvArgs a, const TcPlan p, cons
       kc = kcn;
       return true;
     };
-    for (int jb = 0; ok && jb < njobs; jb += 2) {
-      ok = step(jb, pa, ra, pb, rb);
-      if (ok && jb + 1 < njobs) ok = step(jb + 1, pb, rb, pa, ra);
+    if (HB) {
+      // gathering from shared memory: short latency, no register pipeline
+      for (int jb = 0; ok && jb < njobs; ++jb) {
+        if (jb > 0) {
+          int tn = t, kcn = kc + 1;
+          if (kcn == kchunks) { kcn = 0; tn = t + 1; }
+          if (tn != t) {
+            if (!halo_in(tn)) { ok = false; break; }
+            pa = pix_of(tn);
+          }
+          load_job(pa, kcn, ra);
+          if (kcn == kchunks - 1) halo_out(tn);
+          t = tn;
+          kc = kcn;
+        }
+        if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, 4u)) { ok = false; break; }
+        emit_job(pa, ra, sA + stage * kStageBytes);
+        fence_proxy_async();
+        mbar_arrive(full_bar(stage));
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    } else {
+      for (int jb = 0; ok && jb < njobs; jb += 2) {
+        ok = step(jb, pa, ra, pb, rb);
+        if (ok && jb + 1 < njobs) ok = step(jb + 1, pb, rb, pa, ra);
+      }
     }
   } else {
     // ============ halo copies (lanes 1-31) and MMA issue (lane 0) ==============
