@@ -612,8 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tc(const ConvArgs a, const 
           const int sp = static_cast<int>(e0 & 1);
           const uint32_t* wp = reinterpret_cast<const uint32_t*>(ps.src + (in ? e0 - sp : 0));
           const uint32_t m = in ? (sp ? ps.wv1 : ps.wv0) : 0u;
+          if (HB) {  // shared memory: generic loads (ld.global.nc is for global addresses only)
 #pragma unroll
-          for (int k = 0; k < 5; ++k) raw[jj][k] = (m >> k & 1u) ? __ldg(wp + k) : 0u;
+            for (int k = 0; k < 5; ++k) raw[jj][k] = (m >> k & 1u) ? wp[k] : 0u;
+          } else {
+#pragma unroll
+            for (int k = 0; k < 5; ++k) raw[jj][k] = (m >> k & 1u) ? __ldg(wp + k) : 0u;
+          }
           raw[jj][5] = sp ? 0x5432u : 0x3210u;
           raw[jj][6] = in ? 1u : 0u;
           raw[jj][7] = 0u;
