@@ -21,7 +21,7 @@ import threading
 
 __all__ = [
     "ConvError", "ConvLibraryError", "ConvProblem", "ConvPlanInfo", "ACTIVATIONS", "DTYPES",
-    "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "VARIANTS", "conv_abi_version", "conv_status_string",
+    "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
     "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
     "make_problem", "conv2d", "library_path", "load",
@@ -34,10 +34,11 @@ ACTIVATIONS = {"identity": 0, "relu": 1, "silu": 2, "sigmoid": 3, "tanh": 4, "ha
                "hard_sigmoid": 6, "clip": 7, "leaky_relu": 8}
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 VARIANTS = {0: "igemm_ffma", 1: "igemm_ffma_split_k", 2: "depthwise_halo", 3: "igemm_tcgen05",
-            4: "igemm_tcgen05_1x1"}
+            4: "igemm_tcgen05_window"}
 FIXED_SCRATCH_BYTES = 8 << 20  # CONV_FIXED_SCRATCH_BYTES
 FLAG_FORCE_FFMA = 0x1
 FLAG_NO_SPLIT_K = 0x2
+FLAG_NO_WINDOW = 0x4
 SPLIT_K_SHIFT = 8
 STATUS = {0: "CONV_OK", 1: "CONV_ERR_SHAPE", 2: "CONV_ERR_OVERFLOW", 3: "CONV_ERR_DTYPE",
           4: "CONV_ERR_ACT", 5: "CONV_ERR_NULL", 6: "CONV_ERR_SCRATCH", 7: "CONV_ERR_ALIAS",
@@ -254,8 +255,9 @@ def _dtype_name(t) -> str:
 def conv2d(x, w, bias=None, residual=None, *, stride=1, pads=0, dilation=1, groups=1,
            act="identity", alpha=0.0, beta=0.0, out=None, scratch=None, flags=0, stream=None):
     """y = act(conv(x, w) + bias + residual) on CUDA tensors (NCHW / OIHW,
-    contiguous, one element type).  Allocates y (and split-k scratch, when the
-    plan needs it) with torch unless ``out`` / ``scratch`` are given."""
+    contiguous, one element type).  Allocates y (and the scratch the plan needs:
+    split-k planes or repacked weights) with torch unless ``out`` / ``scratch``
+    are given."""
     import torch
     dt = _dtype_name(x)
     for t in (w, bias, residual, out):

@@ -205,6 +205,18 @@ bool plan_tc(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   out->info.tile_n = 128;
   out->info.ctas = t.ctas;
   out->info.scratch_bytes = 0;
+  // the shifted-window kernel where it takes the shape (the gather kernel
+  // above stays planned: the launch falls back to it when x is not 16-byte
+  // aligned)
+  WinPlan w;
+  if (!(p->flags & CONV_FLAG_NO_WINDOW) && tcw_plan(a, sm, &w)) {
+    out->tcw = w;
+    out->tcw_ok = 1;
+    out->info.variant = CONV_VARIANT_IGEMM_TC_WINDOW;
+    out->info.tile_m = w.nt;
+    out->info.ctas = w.ctas;
+    out->info.scratch_bytes = w.w_bytes;
+  }
   return true;
 }
 
@@ -272,7 +284,7 @@ const char* variant_name(int v) {
     case CONV_VARIANT_IGEMM_FFMA_SPLIT: return "igemm_ffma_split_k";
     case CONV_VARIANT_DEPTHWISE: return "depthwise_halo";
     case CONV_VARIANT_IGEMM_TC: return "igemm_tcgen05";
-    case CONV_VARIANT_IGEMM_TC_1X1: return "igemm_tcgen05_1x1";
+    case CONV_VARIANT_IGEMM_TC_WINDOW: return "igemm_tcgen05_window";
     default: return "unknown";
   }
 }
@@ -349,6 +361,14 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
     snprintf(buf, len, "%s tile=128px x %dco k=%lld (padded %d, %s order) stages=%d blocks=%lld sms=%d",
              variant_name(i.variant), plan.tc.bn, static_cast<long long>(i.gemm_k), plan.tc.k_pad,
              orders[plan.tc.mode], plan.tc.stages, static_cast<long long>(i.ctas), sm);
+  } else if (i.variant == CONV_VARIANT_IGEMM_TC_WINDOW) {
+    const WinPlan& w = plan.tcw;
+    snprintf(buf, len,
+             "%s tile=128pos x %dco phases=%dx%d taps=%dx%d k=%lld (padded %d) padded plane=%dx%d "
+             "ring=%d+%d bands of %d rows, %d in flight, lookahead=%d blocks=%lld sms=%d",
+             variant_name(i.variant), w.nt, w.ph, w.ph, w.khp, w.kwp, static_cast<long long>(i.gemm_k),
+             w.kblocks * 8, w.hp, w.wp, w.ring, w.mirror, w.band, w.stages, w.lookahead,
+             static_cast<long long>(i.ctas), sm);
   } else if (i.variant == CONV_VARIANT_DEPTHWISE) {
     snprintf(buf, len, "%s rows/block=%d staged=%dx%d blocks=%lld sms=%d", variant_name(i.variant),
              plan.dw.th, plan.dw.in_rows, plan.dw.row, static_cast<long long>(i.ctas), sm);
@@ -411,6 +431,11 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
       err = launch_depthwise(plan, a, p->dtype, cs);
       break;
     }
+    case CONV_VARIANT_IGEMM_TC_WINDOW:
+      // bulk copies of x rows need a 16-byte-aligned x; otherwise the gather kernel
+      if (reinterpret_cast<uintptr_t>(x) % 16 == 0) err = launch_tcw(plan, a, p->dtype, scratch, cs);
+      else err = launch_tc(plan, a, p->dtype, cs);
+      break;
     case CONV_VARIANT_IGEMM_TC:
       err = launch_tc(plan, a, p->dtype, cs);
       break;
@@ -435,7 +460,10 @@ conv_status conv_device_error(uint32_t* word, int32_t reset) {
   int dev, sm;
   conv_status st = device_info(&dev, &sm);
   if (st != CONV_OK) return st;
-  return tc_error_word(word, reset) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+  uint32_t w1 = 0, w2 = 0;
+  if (tc_error_word(&w1, reset) != cudaSuccess || tcw_error_word(&w2, reset) != cudaSuccess) return CONV_ERR_CUDA;
+  *word = w1 | (w2 << 16);
+  return CONV_OK;
 }
 
 }  // extern "C"

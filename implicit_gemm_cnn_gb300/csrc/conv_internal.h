@@ -57,18 +57,53 @@ struct TcPlan {
 };
 bool tc_plan(const ConvArgs& a, int sm, TcPlan* t);
 
+// tcgen05 implicit GEMM over shifted windows of a padded input band: 128
+// positions of the padded plane x nt channels per tile.
+struct WinPlan {
+  int ph;          // phase split: 1 (stride 1) or 2 (stride 2 as 2x2 phases)
+  int vh, vw;      // input rows and columns as read (a 1x1 layer's planes cut into rows of vw)
+  int ho, wo;      // output rows and columns in the same view
+  int khp, kwp;    // taps per axis after the phase split
+  int hp, wp;      // padded positions per image: ho + (khp-1)*dh rows of wo + (kwp-1)*dw
+  int c16;         // phase channels (cg * ph * ph) rounded up to 16
+  int kblocks;     // k blocks of 8: khp * kwp * c16 / 8
+  int hq;          // largest tap shift, in positions
+  int nt;          // output channels per tile (MMA N): a multiple of 16, at most 256
+  int co_tiles;    // channel tiles
+  int ring;        // ring depth R in positions
+  int mirror;      // slots written twice past the ring end (128, or 0 when no window straddles it)
+  int lookahead;   // tiles the producers may run ahead of the MMAs (1 or 2)
+  int band;        // padded rows per TMA band (one box: vw x ph*band rows x cg channels)
+  int stages;      // bands in flight
+  int band_bytes;  // bytes of one band
+  int rt;          // padded rows per tile (128 / wp): a tile is rt whole rows of one image
+  int tpi;         // tiles per image: ceil(ho / rt)
+  int out_bytes;   // one output staging buffer: nt x rt x wo elements
+  int ostages;     // output staging buffers (1 or 2)
+  int tiles;       // tiles over all images
+  int parts;       // position ranges (blocks per channel tile)
+  int ctas;        // blocks
+  size_t smem;     // dynamic shared memory bytes
+  size_t w_bytes;  // repacked weights in scratch
+};
+bool tcw_plan(const ConvArgs& a, int sm, WinPlan* w);
+
 struct Plan {
   conv_plan_info info;
   int ffma_cfg;
   int k_per_split;  // terms per k range of the split variant
   DwPlan dw;
   TcPlan tc;
+  WinPlan tcw;
+  int tcw_ok;       // tcw holds a plan (the variant may still fall back to tc at launch)
 };
 
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_split_reduce(const ConvArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_depthwise(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_tc(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_tcw(const Plan& plan, const ConvArgs& a, int dtype, void* scratch, cudaStream_t s);
 cudaError_t tc_error_word(uint32_t* word, int reset);
+cudaError_t tcw_error_word(uint32_t* word, int reset);
 
 }  // namespace conv

@@ -1,0 +1,744 @@
+// conv_tcw.cu -- implicit-GEMM convolution on the tcgen05 tensor cores over
+// shifted windows of a zero-padded input band held in shared memory
+// (half / bfloat16 operands, float32 accumulation in tensor memory).
+//
+// The GEMM is the one of "Convolutions en compute" (implicit im2col: Y^T =
+// cols^T . W^T per image, K = Cin * kh * kw) with the column matrix never
+// formed, not even per tile.  Positions are counted in the zero-padded input
+// plane of each image, hp x wp with hp = Ho + (kh-1)*dh and wp = Wo + (kw-1)*dw,
+// images one after another: output (n, oh, ow) is position
+// q = (n*hp + oh)*wp + ow, and the input it reads through tap (u, v) is
+// position q + u*dh*wp + v*dw.  Every tap is therefore a shift of one
+// position sequence: if shared memory holds the padded input with the
+// channels of a position side by side (16 bytes = 8 channels per position
+// and channel block), the A operand of tap (u, v) for the tile of positions
+// q0 .. q0+127 is the same buffer read from position q0 + u*dh*wp + v*dw, and
+// the MMA descriptor's start address does the im2col.  Positions with
+// ow >= Wo or oh >= Ho are computed and dropped (a few percent of the tile).
+//
+// Stride 2 (dilation 1) becomes stride 1 by splitting the input into its
+// 2 x 2 phases: channel (c, a, b) of phase position (i, j) is input pixel
+// (2i + a - pad_top, 2j + b - pad_left), and the kernel becomes
+// ceil(kh/2) x ceil(kw/2) taps over Cin*4 channels (taps past kh or kw get
+// zero weights).  The ResNet-50 stem (7x7 / 2, 3 channels) becomes a 4x4 /1
+// convolution over 12 (padded to 16) channels.
+//
+// Roles (one persistent block per SM, 13 warps):
+//   * warps 8-11 (producers) stream the block's band of padded input rows:
+//     the rows of x each padded row needs arrive in shared memory by bulk
+//     copies, several rows in flight; the producers then interleave each row's
+//     channels into the ring (16 bytes per position and 8-channel block; zero
+//     for padding, phantom channels and rows outside the image).  The ring is
+//     R positions deep; positions at ring slots below 128 are also written
+//     R slots further on, so that every 128-position window is contiguous;
+//   * warp 12 loads the repacked weights of its channel tile once (one bulk
+//     copy), allocates tensor memory and one lane issues, per tile, kh*kw*C/16
+//     MMAs (kind::f16, M = 128 positions, N = the channel tile, K = 16) whose
+//     A descriptors point at the shifted windows; a commit releases the ring
+//     for the producers and another hands the accumulator to the epilogue;
+//   * warps 0-7 (epilogue): tcgen05.ld of the float32 accumulator (thread =
+//     position; two warps per 32-lane quarter, alternating 8-column chunks),
+//     bias, residual, activation in float32, one rounding, and a store of each
+//     valid position's value to NCHW y -- the output is written once.
+// Accumulators are double buffered in tensor memory, so the epilogue of one
+// tile overlaps the MMAs of the next; the producers run up to two tiles ahead.
+// Every wait is bounded: after the limit the waiting thread flags the block
+// and the device error word, every role drains out, outstanding copies and
+// MMAs are waited for (bounded) and tensor memory is freed before exit.
+//
+// The weights are repacked by a small kernel into the layout the MMA reads
+// ([channel tile][k block of 8][output channel][8 k values]), in the k order
+// (tap, phase channel): the weight re-layout "Convolution, pooling and
+// resize" measured at 1.27x on 3x3 layers, done once per call into scratch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "conv_internal.h"
+#include "tc_ptx.cuh"
+
+namespace conv {
+
+__device__ uint32_t g_tcw_error;  // nonzero once a bounded wait gave up
+
+namespace {
+
+using namespace tcx;
+
+constexpr int kEpiWarps = 8;   // warps 0-7: tensor-memory lanes 32*(w%4) .., column half w/4
+constexpr int kProdWarps = 4;  // warps 8-11
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 13 * 32;
+constexpr int kEpi = kEpiWarps * 32;
+constexpr int kProd = kProdWarps * 32;
+constexpr uint32_t kProdBar = 2;  // named barrier of the producer warps
+constexpr size_t kOneBlockPerSm = 116 * 1024;  // shared memory that keeps a second block off the SM
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t code,
+                                           bool ignore_abort = false, uint32_t sleep_ns = 0) {
+  return tcx::wait_phase(&g_tcw_error, bar, parity, abort_flag, code, ignore_abort, sleep_ns);
+}
+
+// True on every thread of named barrier `id` (`count` threads) iff `pred`
+// holds on all of them; a barrier for those threads.
+__device__ __forceinline__ bool group_all(uint32_t id, uint32_t count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " barrier.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ bool producers_all(bool pred) { return group_all(kProdBar, kProd, pred); }
+constexpr uint32_t kEpiBar = 1;  // named barrier of the epilogue warps
+
+struct WinLayout {
+  uint32_t w_off, ring_off, stg_off, out_off, bias_off, tab_off, bar_off, slot_off, end;
+};
+
+__host__ __device__ inline uint32_t align128(uint32_t v) { return (v + 127u) / 128u * 128u; }
+
+// Barriers (8 bytes each, from bar_off): weights, full[2], rel[2], tfull[2],
+// tempty[2], drain, res[2], then one per band stage.
+constexpr int kBarFixed = 12;
+
+__host__ __device__ inline WinLayout win_layout(const WinPlan& p) {
+  WinLayout L;
+  L.w_off = 0;
+  L.ring_off = align128(static_cast<uint32_t>(p.kblocks) * p.nt * 16u);
+  L.stg_off = L.ring_off + align128(static_cast<uint32_t>(p.c16 / 8) * (p.ring + p.mirror) * 16u);
+  L.out_off = L.stg_off + align128(static_cast<uint32_t>(p.stages) * p.band_bytes);
+  L.bias_off = L.out_off + align128(static_cast<uint32_t>(p.ostages) * p.out_bytes);
+  L.tab_off = L.bias_off + align128(static_cast<uint32_t>(p.nt) * 4u);
+  L.bar_off = L.tab_off + align128(static_cast<uint32_t>(p.kblocks / 2) * 16u);  // one int4 per MMA
+  L.slot_off = L.bar_off + static_cast<uint32_t>(kBarFixed + p.stages) * 8u;
+  L.end = L.slot_off + 16u;
+  return L;
+}
+
+// What the epilogue warps need besides the element type and the activation
+// (copied from the launch arguments and the plan into registers).
+struct EpiCtx {
+  uint32_t tmem_base, bar0, out_s, bias_s;  // tensor memory; barriers, output staging, bias (shared addresses)
+  int t0, ntiles, co0;
+  int tpi, rt, wp, wo, ho, nt, out_bytes, ostages;
+  bool has_b, has_r;
+  float alpha, beta;
+  volatile int* abort_flag;
+  const CUtensorMap* ymap;
+  const CUtensorMap* rmap;
+};
+
+// The epilogue warps' loop over the block's tiles, for activation ACT.  Warp
+// w reads tensor-memory lanes 32*(w%4) .. +31 (thread = position of the tile)
+// and the 8-column chunks w/4, w/4+2, ..., up to four chunks per
+// tensor-memory wait; bias, residual and activation in float32, one rounding
+// into the tile's staging buffer [channel][row][column]; then one TMA store
+// of the box (wo x rows x channels) to y -- rows past Ho and channels past
+// Cout fall outside y and are not written.  The residual tile arrives in the
+// same buffer by TMA ahead of its tile.  Dropped positions (columns past Wo)
+// are computed and not staged.
+template <typename T, int ACT>
+__device__ __forceinline__ void epilogue_role(const EpiCtx e) {
+  const int tid = threadIdx.x;  // 0 .. kEpi-1
+  const int warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, hf = warp >> 2;
+  const int nchunks = e.nt / 8;
+  const uint32_t plane2 = static_cast<uint32_t>(e.rt * e.wo) * 2u;  // bytes per channel in a staging buffer
+  const int OS = e.ostages;
+  auto res_bar = [&](int k) { return e.bar0 + 8u * (10 + k); };
+  auto issue_res = [&](int i) {  // thread 0: the residual box of tile t0+i into buffer i % OS
+    const int t = e.t0 + i, n = t / e.tpi, j = t - (t / e.tpi) * e.tpi;
+    const int ob = i % OS;
+    mbar_arrive_expect_tx(res_bar(ob), static_cast<uint32_t>(e.out_bytes));
+    tma_load_4d(e.out_s + static_cast<uint32_t>(ob * e.out_bytes), e.rmap, 0, j * e.rt, e.co0, n, res_bar(ob));
+  };
+  if (e.has_r && tid == 0 && e.ntiles > 0) issue_res(0);
+  // the thread's position in every tile
+  const int qq = qd * 32 + lane;
+  const int rr = qq / e.wp, c = qq - (qq / e.wp) * e.wp;
+  const uint32_t soff2 = static_cast<uint32_t>(rr * e.wo + c) * 2u;
+  for (int i = 0; i < e.ntiles; ++i) {
+    const int t = e.t0 + i, n = t / e.tpi, j = t - (t / e.tpi) * e.tpi;
+    const int b = i & 1, ob = i % OS;
+    const uint32_t tfull = e.bar0 + 8u * (5 + b), tempty = e.bar0 + 8u * (7 + b);
+    // accumulator ready, residual landed; the barrier also orders the staging
+    // writes after thread 0's wait for the store that last read the buffer
+    bool okw = wait_phase(tfull, static_cast<uint32_t>(i >> 1) & 1u, e.abort_flag, 2u, false, 64u);
+    if (okw && e.has_r) okw = wait_phase(res_bar(ob), static_cast<uint32_t>(i / OS) & 1u, e.abort_flag, 128u);
+    if (!group_all(kEpiBar, kEpi, okw)) break;
+    tc_fence_after();
+    const int rows_here = min(e.rt, e.ho - j * e.rt);
+    const bool valid = rr < rows_here && c < e.wo;
+    const uint32_t st = e.out_s + static_cast<uint32_t>(ob * e.out_bytes) + soff2;
+    const uint32_t tb = e.tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + static_cast<uint32_t>(b * e.nt);
+    for (int k0 = hf; k0 < nchunks; k0 += 8) {
+      uint32_t v[4][8];
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        if (k0 + 2 * g < nchunks) tmem_ld8_nowait(tb + (k0 + 2 * g) * 8, v[g]);
+      tmem_wait_ld();
+      if (valid) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int k = k0 + 2 * g;
+          if (k >= nchunks) break;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint32_t ch = static_cast<uint32_t>(k * 8 + jj);
+            const uint32_t addr = st + ch * plane2;
+            float x = __uint_as_float(v[g][jj]);
+            if (e.has_b) x = __fadd_rn(x, lds_f32(e.bias_s + ch * 4u));
+            if (e.has_r) {
+              const uint16_t rb = lds_u16(addr);
+              x = __fadd_rn(x, to_f32<T>(*reinterpret_cast<const T*>(&rb)));
+            }
+            x = act_fn<ACT>(x, e.alpha, e.beta);
+            const T o = from_f32<T>(x);
+            sts_u16(addr, *reinterpret_cast<const uint16_t*>(&o));
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(tempty);
+    fence_proxy_async();  // the staged tile is visible to the TMA store
+    named_sync(kEpiBar, kEpi);
+    if (tid == 0) {
+      tma_store_4d(e.ymap, e.out_s + static_cast<uint32_t>(ob * e.out_bytes), 0, j * e.rt, e.co0, n);
+      bulk_commit();
+      if (OS == 2) bulk_wait_read<1>();  // the store of the previous tile has read its buffer
+      else bulk_wait_read<0>();
+      if (e.has_r && i + 1 < e.ntiles) issue_res(i + 1);
+    }
+  }
+  if (tid == 0) bulk_wait_all();  // the stores have landed before the block retires
+}
+
+template <typename T, int PH>
+__global__ void __launch_bounds__(kThreads, 1)
+    igemm_tcw(const ConvArgs a, const WinPlan p, const uint8_t* __restrict__ wpack,
+              const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+              const __grid_constant__ CUtensorMap rmap) {
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((128u - (smem_u32(sm_raw) & 127u)) & 127u);  // the launch adds 128 bytes of slack
+  const WinLayout L = win_layout(p);
+  const uint32_t bar0 = smem_u32(sm + L.bar_off);
+  const uint32_t wbar = bar0;
+  auto full_bar = [&](int i) { return bar0 + 8u * (1 + i); };    // tile's input rows are in the ring
+  auto rel_bar = [&](int i) { return bar0 + 8u * (3 + i); };     // tile's MMAs done: ring reusable
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (5 + b); };   // accumulator b ready
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (7 + b); };  // accumulator b read out
+  const uint32_t drain_bar = bar0 + 8u * 9;
+  auto res_bar = [&](int k) { return bar0 + 8u * (10 + k); };    // residual tile k landed
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (kBarFixed + s); };  // staged band s landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L.slot_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.slot_off + 4);
+  float* sbias = reinterpret_cast<float*>(sm + L.bias_off);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int ct = static_cast<int>(blockIdx.x) % p.co_tiles;
+  const int part = static_cast<int>(blockIdx.x) / p.co_tiles;
+  const int t0 = static_cast<int>(static_cast<long long>(p.tiles) * part / p.parts);
+  const int t1 = static_cast<int>(static_cast<long long>(p.tiles) * (part + 1) / p.parts);
+  const int ntiles = t1 - t0;
+  const int co0 = ct * p.nt;
+  uint32_t cols = 32;
+  while (cols < 2u * p.nt) cols <<= 1;
+  // tile t: rows j*rt .. of image n (t = n*tpi + j); its first position
+  auto tile_q0 = [&](int t) {
+    const int n = t / p.tpi, j = t - (t / p.tpi) * p.tpi;
+    return (n * p.hp + j * p.rt) * p.wp;
+  };
+
+  // ---- set-up: barriers, bias, MMA table, tensor memory --------------------
+  if (tid == 0) {
+    mbar_init(wbar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(full_bar(i), kProd);
+      mbar_init(rel_bar(i), 1);
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), kEpi);
+      mbar_init(res_bar(i), 1);
+    }
+    mbar_init(drain_bar, 1);
+    for (int s = 0; s < p.stages; ++s) mbar_init(sfull_bar(s), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (tid < kEpi) {
+    const T* bias = static_cast<const T*>(a.bias);
+    for (int j = tid; j < p.nt; j += kEpi)
+      sbias[j] = (bias && co0 + j < a.c_out) ? to_f32<T>(bias[co0 + j]) : 0.0f;
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), cols);
+    // per MMA of a tile: the window shift of its tap, the k-block offset of
+    // its channel pair in the ring, and its weights' offset (16-byte units)
+    int4* tab = reinterpret_cast<int4*>(sm + L.tab_off);
+    const int pairs = p.c16 / 16, nmma = p.kblocks / 2;
+    for (int e = lane; e < nmma; e += 32) {
+      const int tap = e / pairs, m = e - (e / pairs) * pairs;
+      const int u = tap / p.kwp, v = tap - (tap / p.kwp) * p.kwp;
+      tab[e] = make_int4(u * a.dh * p.wp + v * a.dw, 2 * m * (p.ring + p.mirror), (2 * e) * p.nt, 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < kEpiWarps) {
+    // ---- epilogue: the activation is chosen once; each case is its own loop
+    EpiCtx e;
+    e.tmem_base = tmem_base;
+    e.bar0 = bar0;
+    e.out_s = smem_u32(sm + L.out_off);
+    e.bias_s = smem_u32(sbias);
+    e.t0 = t0;
+    e.ntiles = ntiles;
+    e.co0 = co0;
+    e.tpi = p.tpi;
+    e.rt = p.rt;
+    e.wp = p.wp;
+    e.wo = p.wo;
+    e.ho = p.ho;
+    e.nt = p.nt;
+    e.out_bytes = p.out_bytes;
+    e.ostages = p.ostages;
+    e.has_b = a.bias != nullptr;
+    e.has_r = a.residual != nullptr;
+    e.alpha = a.alpha;
+    e.beta = a.beta;
+    e.abort_flag = abort_flag;
+    e.ymap = &ymap;
+    e.rmap = &rmap;
+    switch (a.act) {
+#define CONV_EPI_CASE(A)          \
+  case A:                         \
+    epilogue_role<T, A>(e);       \
+    break;
+      CONV_EPI_CASE(ACT_RELU)
+      CONV_EPI_CASE(ACT_SILU)
+      CONV_EPI_CASE(ACT_SIGMOID)
+      CONV_EPI_CASE(ACT_TANH)
+      CONV_EPI_CASE(ACT_HARD_SWISH)
+      CONV_EPI_CASE(ACT_HARD_SIGMOID)
+      CONV_EPI_CASE(ACT_CLIP)
+      CONV_EPI_CASE(ACT_LEAKY_RELU)
+#undef CONV_EPI_CASE
+      default:
+        epilogue_role<T, ACT_IDENTITY>(e);
+    }
+  } else if (warp < kEpiWarps + kProdWarps) {
+    // ---- producers: bands of input rows by TMA, channels interleaved into the ring
+    const int ptid = tid - kEpi;
+    const int pw = ptid >> 5;
+    const int nb = p.c16 / 8;
+    const int R = p.ring, RM = p.ring + p.mirror;
+    const int DS = p.stages, SB = p.band;
+    auto row_end = [&](int i) {  // padded rows (exclusive) the valid outputs of tile t0+i read
+      const int t = t0 + i, n = t / p.tpi, j = t - (t / p.tpi) * p.tpi;
+      return n * p.hp + min((j + 1) * p.rt, p.ho) + (p.khp - 1) * a.dh;
+    };
+    const int rho0 = tile_q0(t0) / p.wp;
+    const int rho_end = ntiles > 0 ? row_end(ntiles - 1) : rho0;
+    const uint32_t stg_s = smem_u32(sm + L.stg_off);
+    uint8_t* ring = sm + L.ring_off;
+    // bands: rows [b*SB, min((b+1)*SB, hp)) of one image; the next band to
+    // load is (ni, bi), the band being consumed is (nf, bf)
+    int ni = rho0 / p.hp, bi = (rho0 - (rho0 / p.hp) * p.hp) / SB;
+    int nf = ni, bf = bi;
+    int k_issue = 0, k_fill = 0;
+    auto band_row0 = [&](int n, int b) { return n * p.hp + b * SB; };
+    // one TMA box per band: vw columns x PH*SB input rows x cg channels of image n
+    auto issue = [&]() {
+      const int s = k_issue % DS;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(sfull_bar(s), static_cast<uint32_t>(p.band_bytes));
+        tma_load_4d(stg_s + static_cast<uint32_t>(s) * p.band_bytes, &xmap, 0, PH * bi * SB - a.pt, 0, ni,
+                    sfull_bar(s));
+      }
+      __syncwarp();
+      if (++bi * SB >= p.hp) { bi = 0; ++ni; }
+      ++k_issue;
+    };
+    if (pw == 0)
+      for (int k = 0; k < DS && band_row0(ni, bi) < rho_end; ++k) issue();
+    int filled = rho0;  // rows below this are in the ring
+    // the thread's next unit is kProd units on: step_br rows, step_cb blocks, step_c columns
+    const int step_br = kProd / (p.wp * nb);
+    const int step_cb = (kProd % (p.wp * nb)) / p.wp, step_c = kProd % p.wp;
+    bool ok = true;
+    for (int i = 0; ok && i < ntiles; ++i) {
+      if (i >= p.lookahead) {
+        const int j = i - p.lookahead;
+        ok = producers_all(wait_phase(rel_bar(j & 1), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, 4u));
+        if (!ok) break;
+      }
+      const int re = row_end(i);
+      while (filled < re) {
+        // the whole band (nf, bf) from row `filled` on
+        const int s = k_fill % DS;
+        ok = producers_all(wait_phase(sfull_bar(s), static_cast<uint32_t>(k_fill / DS) & 1u, abort_flag, 8u));
+        if (!ok) break;
+        const int brow0 = band_row0(nf, bf);
+        const int blen = min(SB, p.hp - bf * SB);
+        const int first = filled - brow0;  // rows of the band already in the ring (first band only)
+        const uint16_t* sg = reinterpret_cast<const uint16_t*>(sm + L.stg_off + static_cast<uint32_t>(s) * p.band_bytes);
+        const int rows = blen - first;
+        const int units = rows * p.wp * nb;  // (row, channel block, column)
+        const int per_row = p.wp * nb;
+        const int base_slot = static_cast<int>((static_cast<long long>(brow0) * p.wp) % R);
+        int br = first + ptid / per_row, cb = (ptid % per_row) / p.wp, c = ptid % p.wp;
+        for (int e = ptid; e < units; e += kProd) {
+          uint16_t v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            int ch, ph, wc;
+            if constexpr (PH == 1) {
+              ch = cb * 8 + j;
+              ph = 0;
+              wc = c - a.pl;
+            } else {
+              ch = cb * 2 + (j >> 2);
+              ph = (j >> 1) & 1;
+              wc = 2 * c + (j & 1) - a.pl;
+            }
+            const bool okv = wc >= 0 && wc < p.vw && ch < a.cg;
+            v[j] = okv ? sg[(ch * (PH * SB) + PH * br + ph) * p.vw + wc] : static_cast<uint16_t>(0);
+          }
+          int slot = base_slot + br * p.wp + c;  // < 2R: R exceeds a band's positions
+          if (slot >= R) slot -= R;
+          const uint4 u4 = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+          uint8_t* dst = ring + (static_cast<size_t>(cb) * RM + slot) * 16u;
+          *reinterpret_cast<uint4*>(dst) = u4;
+          if (slot < p.mirror) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(R) * 16u) = u4;
+          c += step_c;
+          cb += step_cb;
+          br += step_br;
+          if (c >= p.wp) { c -= p.wp; ++cb; }
+          if (cb >= nb) { cb -= nb; ++br; }
+        }
+        named_sync(kProdBar, kProd);  // the staged band is consumed: its slot may be refilled
+        if (pw == 0 && band_row0(ni, bi) < rho_end) {
+          fence_proxy_async();
+          issue();
+        }
+        filled = brow0 + blen;
+        if (++bf * SB >= p.hp) { bf = 0; ++nf; }
+        ++k_fill;
+      }
+      if (!ok) break;
+      fence_proxy_async();  // ring writes visible to the tensor cores
+      mbar_arrive(full_bar(i & 1));
+    }
+    if (pw == 0) {  // copies still in flight land before the block retires
+      for (int k = k_fill; k < k_issue; ++k)
+        wait_phase(sfull_bar(k % DS), static_cast<uint32_t>(k / DS) & 1u, abort_flag, 8u, true);
+    }
+  } else if (ntiles > 0) {
+    // ---- MMA issuer: the whole warp runs the loop, one elected lane issues ----
+    const uint32_t wbytes = static_cast<uint32_t>(p.kblocks) * p.nt * 16u;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(wbar, wbytes);
+      bulk_load(smem_u32(sm + L.w_off), wpack + static_cast<size_t>(ct) * wbytes, wbytes, wbar);
+    }
+    __syncwarp();
+    bool ok = __all_sync(0xffffffffu, wait_phase(wbar, 0, abort_flag, 1u));
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t idesc = make_idesc(kBf16, p.nt);
+    const int R = p.ring, RM = p.ring + p.mirror;
+    // descriptors of the ring's and the weights' first core matrices; every
+    // operand is one of them advanced by a whole number of 16-byte units
+    // (the start-address field holds addr >> 4 and never carries out)
+    const uint64_t ad0 = kmajor_desc(smem_u32(sm + L.ring_off), static_cast<uint32_t>(RM) * 16u, 128u);
+    const uint64_t bd0 = kmajor_desc(smem_u32(sm + L.w_off), static_cast<uint32_t>(p.nt) * 16u, 128u);
+    const int4* tab = reinterpret_cast<const int4*>(sm + L.tab_off);
+    const int nmma = p.kblocks / 2;
+    for (int i = 0; ok && i < ntiles; ++i) {
+      const int b = i & 1;
+      ok = __all_sync(0xffffffffu, wait_phase(tempty_bar(b), (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, abort_flag, 16u));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, wait_phase(full_bar(i & 1), static_cast<uint32_t>(i >> 1) & 1u, abort_flag, 32u));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tmem_base + static_cast<uint32_t>(b * p.nt);
+      const int pbase = tile_q0(t0 + i) % R;
+#pragma unroll 4
+      for (int e = 0; e < nmma; ++e) {
+        const int4 tv = tab[e];
+        int pos = pbase + tv.x;
+        if (pos >= R) pos -= R;
+        mma_f16_elect(d, ad0 + static_cast<uint64_t>(pos + tv.y), bd0 + static_cast<uint64_t>(tv.z), idesc,
+                      e > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(rel_bar(i & 1));
+      mma_commit_elect(tfull_bar(b));
+    }
+  }
+
+  // ---- teardown ----------------------------------------------------------
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    if (*abort_flag) {
+      mma_commit_elect(drain_bar);  // outstanding MMAs finish before their tensor memory is freed
+      wait_phase(drain_bar, 0, abort_flag, 64u, true);
+      if (ntiles > 0) wait_phase(wbar, 0, abort_flag, 1u, true);  // the weight copy has landed
+    }
+    __syncwarp();
+    tmem_dealloc(tmem_base, cols);
+  }
+}
+
+// Weights OIHW -> [channel tile][k block][output channel][8 k values], k in
+// (tap, phase channel) order, zero for phantom channels, taps past the kernel
+// and output channels past c_out.
+template <int PH>
+__global__ void tcw_repack(const ConvArgs a, const WinPlan p, uint4* __restrict__ out) {
+  const uint16_t* w = static_cast<const uint16_t*>(a.wt);
+  const int nb = p.c16 / 8;
+  const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
+  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < units;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int col = static_cast<int>(e % p.nt);
+    const long long rest = e / p.nt;
+    const int kb = static_cast<int>(rest % p.kblocks);
+    const int ct = static_cast<int>(rest / p.kblocks);
+    const int co = ct * p.nt + col;
+    const int tap = kb / nb, cb = kb - (kb / nb) * nb;
+    const int u0 = tap / p.kwp, v0 = tap - (tap / p.kwp) * p.kwp;
+    uint16_t v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = cb * 8 + j;
+      const int ch = k / (PH * PH), ph = (k / PH) % PH, pb = k % PH;
+      const int u = u0 * PH + ph, vv = v0 * PH + pb;
+      const bool ok = co < a.c_out && ch < a.cg && u < a.kh && vv < a.kw;
+      v[j] = ok ? w[((static_cast<long long>(co) * a.cg + ch) * a.kh + u) * a.kw + vv] : static_cast<uint16_t>(0);
+    }
+    out[e] = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+  }
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// A 4-d tensor map over an NCHW array viewed as (cols, rows, channels, n),
+// boxes of (box_cols, box_rows, box_ch, 1), zeros outside.
+template <typename T>
+bool encode_nchw(CUtensorMap* map, const void* base, int cols, int rows, int ch, int n, int box_cols, int box_rows,
+                 int box_ch) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (!encode) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(ch), static_cast<cuuint64_t>(n)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(cols) * rows * 2,
+                                 static_cast<cuuint64_t>(cols) * rows * ch * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(box_ch), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return encode(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int PH>
+cudaError_t launch_win(const WinPlan& p, const ConvArgs& a, void* scratch, cudaStream_t s) {
+  // x: one box = a band of every channel; y and the residual: one box = a tile
+  CUtensorMap xmap, ymap, rmap;
+  if (!encode_nchw<T>(&xmap, a.x, p.vw, p.vh, a.c_in, a.n, p.vw, PH * p.band, a.cg) ||
+      !encode_nchw<T>(&ymap, a.y, p.wo, p.ho, a.c_out, a.n, p.wo, p.rt, p.nt))
+    return cudaErrorInvalidValue;
+  rmap = ymap;
+  if (a.residual && !encode_nchw<T>(&rmap, a.residual, p.wo, p.ho, a.c_out, a.n, p.wo, p.rt, p.nt))
+    return cudaErrorInvalidValue;
+
+  const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
+  const int rblocks = static_cast<int>(std::min<long long>((units + 255) / 256, 1024));
+  tcw_repack<PH><<<rblocks, 256, 0, s>>>(a, p, static_cast<uint4*>(scratch));
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  auto kern = igemm_tcw<T, PH>;
+  static int configured[64] = {0};
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && configured[dev] < static_cast<int>(p.smem)) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
+    if (err != cudaSuccess) return err;
+    configured[dev] = static_cast<int>(p.smem);
+  }
+  kern<<<p.ctas, kThreads, p.smem, s>>>(a, p, static_cast<const uint8_t*>(scratch), xmap, ymap, rmap);
+  return cudaGetLastError();
+}
+
+// Channel tile, lookahead, output buffers, band height and band stages that
+// fit shared memory for the geometry already in `p` (widest tile, deepest
+// lookahead, two output buffers, bands of about 8 KB, most bands in flight
+// first), with the ring depth each choice needs.  False if none fits.
+bool fit_smem(const ConvArgs& a, WinPlan* p) {
+  const long long row_bytes = static_cast<long long>(p->vw) * p->ph * a.cg * 2;  // one padded row's box
+  const int sb_max = static_cast<int>(std::min<long long>({8, p->hp, 256 / p->ph}));
+  int sb_pref = 1;
+  while (sb_pref < sb_max && row_bytes * sb_pref < 8192) ++sb_pref;
+  const int nt0 = static_cast<int>(std::min<long long>((a.c_out + 15) / 16 * 16, 256));
+  for (int nt = nt0; nt >= 16; nt = nt > 16 ? std::max(16, (nt / 2 + 15) / 16 * 16) : 0) {
+    p->nt = nt;
+    p->co_tiles = (a.c_out + nt - 1) / nt;
+    p->out_bytes = nt * p->rt * p->wo * 2;
+    for (int la = 2; la >= 1; --la) {
+      for (int os = 2; os >= 1; --os) {
+        for (int sb = sb_pref; sb >= 1; --sb) {
+          if (row_bytes * sb >= (1 << 20)) continue;  // transaction count of one mbarrier phase
+          for (int ds = 4; ds >= 2; --ds) {
+            // rows the producers may write beyond the oldest window still in
+            // use: la tiles of rt rows (one of them across an image's dropped
+            // rows), the kernel's reach and a band
+            const long long rows = static_cast<long long>(la - 1) * (p->rt + p->hp - p->ho) + p->rt +
+                                   static_cast<long long>(p->khp - 1) * a.dh + sb;
+            const long long ring = (rows * p->wp + 7) / 8 * 8;
+            if (ring + 128 > 16000) continue;  // the descriptors' 14-bit offsets
+            p->ring = static_cast<int>(ring);
+            p->mirror = 128;  // windows start anywhere: 128 slots written twice
+            p->lookahead = la;
+            p->ostages = os;
+            p->band = sb;
+            p->band_bytes = static_cast<int>(row_bytes * sb);
+            p->stages = ds;
+            if (win_layout(*p).end + 128 <= kTcMaxSmem) return true;
+          }
+        }
+      }
+    }
+  }
+  return false;
+}
+
+// Everything of the plan that follows from the view (vh, vw, ho, wo) and the
+// phase split: padded plane, rows per tile, channels, shifts, tiles.  False
+// if a size is past the kernel's limits or nothing fits shared memory.
+bool plan_view(const ConvArgs& a, WinPlan* p) {
+  if (p->vw > 256 || a.cg > 256 || p->wo % 8 != 0) return false;  // TMA boxes: rows of 16-byte multiples
+  p->khp = (a.kh + p->ph - 1) / p->ph;
+  p->kwp = (a.kw + p->ph - 1) / p->ph;
+  const long long hp = p->ho + static_cast<long long>(p->khp - 1) * a.dh;
+  const long long wp = p->wo + static_cast<long long>(p->kwp - 1) * a.dw;
+  if (wp > 128 || hp > 65535) return false;  // a tile holds whole padded rows
+  p->hp = static_cast<int>(hp);
+  p->wp = static_cast<int>(wp);
+  p->rt = 128 / p->wp;
+  if (p->rt > 256) p->rt = 256;
+  p->tpi = (p->ho + p->rt - 1) / p->rt;
+  const long long cgp = static_cast<long long>(a.cg) * p->ph * p->ph;
+  if (cgp > 512) return false;
+  p->c16 = static_cast<int>((cgp + 15) / 16 * 16);
+  p->hq = static_cast<int>(static_cast<long long>(p->khp - 1) * a.dh * wp + static_cast<long long>(p->kwp - 1) * a.dw);
+  const long long npos = static_cast<long long>(a.n) * hp * wp;
+  if (npos + 1024 + p->hq + 16 * wp > (1LL << 30)) return false;
+  const long long tiles = static_cast<long long>(a.n) * p->tpi;
+  if (tiles > (1LL << 30)) return false;
+  p->tiles = static_cast<int>(tiles);
+  p->kblocks = p->khp * p->kwp * p->c16 / 8;
+  return fit_smem(a, p);
+}
+
+}  // namespace
+
+// Planner (host): whether the shifted-window kernel takes the shape, and its
+// geometry, channel tile, ring and staging depth.  Addresses are not known
+// here; the launch checks them.
+bool tcw_plan(const ConvArgs& a, int sm, WinPlan* out) {
+  if (a.groups != 1) return false;
+  WinPlan p;
+  memset(&p, 0, sizeof(p));
+  if (a.sh == 1 && a.sw == 1) p.ph = 1;
+  else if (a.sh == 2 && a.sw == 2 && a.dh == 1 && a.dw == 1) p.ph = 2;
+  else return false;
+  const bool pointwise = a.kh == 1 && a.kw == 1 && p.ph == 1 && a.pt == 0 && a.pl == 0 && a.ho == a.h &&
+                         a.wo == a.w;
+  bool ok = false;
+  if (pointwise) {
+    // a 1x1 layer reads each plane as it lies: view it as rows of vw
+    // positions (a multiple of 8 dividing h*w, for 16-byte rows), the view
+    // whose tiles use most of the 128 MMA rows, longer rows first
+    int best = 0;
+    double best_eff = 0.0;
+    for (long long l = std::min<long long>(128, a.hw) / 8 * 8; l >= 8; l -= 8) {
+      if (a.hw % l) continue;
+      const double eff = static_cast<double>((128 / l) * l) / 128.0;
+      if (eff > best_eff + 1e-9) { best_eff = eff; best = static_cast<int>(l); }
+    }
+    for (int pass = 0; pass < 2 && !ok && best; ++pass) {
+      for (long long l = best; l >= 8 && !ok; l -= 8) {
+        if (a.hw % l) continue;
+        if (pass == 0 && l != best) continue;
+        p.vw = static_cast<int>(l);
+        p.vh = static_cast<int>(a.hw / l);
+        p.ho = p.vh;
+        p.wo = p.vw;
+        ok = plan_view(a, &p);
+      }
+    }
+  } else if (a.w % 8 == 0) {  // x rows start on 16 bytes
+    p.vh = a.h;
+    p.vw = a.w;
+    p.ho = a.ho;
+    p.wo = a.wo;
+    ok = plan_view(a, &p);
+  }
+  if (!ok) return false;
+  p.parts = static_cast<int>(std::min<long long>(p.tiles, std::max(1, sm / p.co_tiles)));
+  p.ctas = p.parts * p.co_tiles;
+  p.smem = std::max<size_t>(win_layout(p).end + 128, kOneBlockPerSm);
+  p.w_bytes = static_cast<size_t>(p.co_tiles) * p.kblocks * p.nt * 16;
+  *out = p;
+  return true;
+}
+
+cudaError_t launch_tcw(const Plan& plan, const ConvArgs& a, int dtype, void* scratch, cudaStream_t s) {
+  const WinPlan& p = plan.tcw;
+  if (dtype == CONV_F16)
+    return p.ph == 2 ? launch_win<__half, 2>(p, a, scratch, s) : launch_win<__half, 1>(p, a, scratch, s);
+  if (dtype == CONV_BF16)
+    return p.ph == 2 ? launch_win<__nv_bfloat16, 2>(p, a, scratch, s)
+                     : launch_win<__nv_bfloat16, 1>(p, a, scratch, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t tcw_error_word(uint32_t* word, int reset) {
+  cudaError_t err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) return err;
+  err = cudaMemcpyFromSymbol(word, g_tcw_error, sizeof(uint32_t));
+  if (err != cudaSuccess || !reset) return err;
+  const uint32_t zero = 0;
+  return cudaMemcpyToSymbol(g_tcw_error, &zero, sizeof(uint32_t));
+}
+
+}  // namespace conv

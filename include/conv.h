@@ -80,6 +80,7 @@ typedef enum conv_act {
 /* conv_problem.flags: testing and measurement switches.  0 = automatic. */
 #define CONV_FLAG_FORCE_FFMA 0x1u   /* the CUDA-core implicit GEMM for every shape   */
 #define CONV_FLAG_NO_SPLIT_K 0x2u   /* never split k                                 */
+#define CONV_FLAG_NO_WINDOW 0x4u    /* never the shifted-window tcgen05 variant       */
 #define CONV_FLAG_SPLIT_K_SHIFT 8   /* bits 8..13: force this many ranges of k (1-63) */
 #define CONV_FLAG_SPLIT_K_MASK 0x3f00u
 
@@ -131,8 +132,11 @@ typedef enum conv_variant {
                                       per group, any channel multiplier)     */
   CONV_VARIANT_IGEMM_TC = 3,       /* implicit GEMM on tcgen05 tensor cores,
                                       input window gathered into shared memory */
-  CONV_VARIANT_IGEMM_TC_1X1 = 4    /* tcgen05 implicit GEMM for 1x1 / stride 1 /
-                                      no pad: input tiles read as they lie, by TMA */
+  CONV_VARIANT_IGEMM_TC_WINDOW = 4 /* tcgen05 implicit GEMM over shifted windows of
+                                      a zero-padded input band in shared memory
+                                      (stride 1, or stride 2 split into 2x2
+                                      phases; one group); weights repacked into
+                                      scratch first                          */
 } conv_variant;
 
 /* The host-side plan of a problem for a device with `sm_count` SMs. */
@@ -172,7 +176,8 @@ CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_pla
 /* Scratch bytes conv_forward needs for `p` on the current CUDA device
  * ("Convolution, pooling and resize", Layout and operands: the scratch
  * query): the float32 partial planes of split k (ranges x output elements),
- * 0 for every variant that keeps its sums on chip.
+ * the repacked weights of the shifted-window variant (channel tiles x k
+ * blocks x tile channels x 16 bytes), 0 for the other variants.
  * Errors: as conv_plan, and CONV_ERR_DEVICE without a usable device. */
 CONV_API conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes);
 
@@ -197,7 +202,9 @@ CONV_API conv_status conv_forward(const conv_problem* p, const void* x, const vo
 
 /* Reads (and, if `reset`, clears) the current device's error word: nonzero
  * when a tensor-core kernel gave up a bounded wait (its output is then
- * incomplete).  Synchronises the device; for tests and diagnostics. */
+ * incomplete); bits 0-15 come from the gather variant, bits 16-31 from the
+ * shifted-window variant.  Synchronises the device; for tests and
+ * diagnostics. */
 CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
 
 /* Bytes of the library-owned scratch array of conv_forward_fixed_scratch. */

@@ -129,10 +129,10 @@ def _layer_problem(L, flags=0):
 
 
 EXPECTED_VARIANT = {
-    "small_3x3_f32": "igemm_ffma", "resnet50_stem_f16": "igemm_tcgen05",
-    "resnet50_3x3_f16": "igemm_tcgen05", "resnet50_1x1_res_f16": "igemm_tcgen05",
+    "small_3x3_f32": "igemm_ffma", "resnet50_stem_f16": "igemm_tcgen05_window",
+    "resnet50_3x3_f16": "igemm_tcgen05_window", "resnet50_1x1_res_f16": "igemm_tcgen05_window",
     "mbv3_dw5x5_f32": "depthwise_halo", "mbv3_dw5x5_f16": "depthwise_halo",
-    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05",
+    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05_window",
     "grouped_dil2_f32": "igemm_ffma", "late_1x1_splitk_f32": "igemm_ffma_split_k",
     "strided_3x3_s2_f32": "igemm_ffma",
 }
@@ -151,6 +151,16 @@ def test_plans_of_the_workloads(lib, name):
     if plan["split_k"] > 1:
         assert plan["scratch_bytes"] == plan["split_k"] * y_elems * 4
         assert plan["ctas"] <= 2 * 152
+    elif plan["variant_name"] == "igemm_tcgen05_window":
+        # repacked weights: channel tiles x k blocks of 8 x tile channels x 16 bytes
+        tile = plan["tile_m"]
+        assert tile % 16 == 0 and tile <= 256
+        assert plan["scratch_bytes"] % (16 * tile) == 0
+        assert plan["scratch_bytes"] >= L.c_out * (L.c_in // L.groups) * L.kh * L.kw * 2
+        assert plan["ctas"] <= 152
+        p2 = _layer_problem(L, flags=conv.FLAG_NO_WINDOW)
+        assert conv.conv_plan(p2, 152)["variant_name"] == "igemm_tcgen05"
+        assert conv.conv_plan(p2, 152)["scratch_bytes"] == 0
     else:
         assert plan["scratch_bytes"] == 0
     assert conv.conv_plan(p, 152) == plan      # a pure function of (problem, SMs)

@@ -40,9 +40,9 @@ def _problem(L, flags=0):
 # reduced sizes: (n, h, w); the residual shape follows
 REDUCED = {
     "small_3x3_f32": (1, 32, 32),
-    "resnet50_stem_f16": (1, 62, 62),
-    "resnet50_3x3_f16": (2, 23, 23),
-    "resnet50_1x1_res_f16": (2, 23, 23),
+    "resnet50_stem_f16": (2, 61, 64),
+    "resnet50_3x3_f16": (2, 23, 24),
+    "resnet50_1x1_res_f16": (2, 23, 24),
     "mbv3_dw5x5_f32": (2, 28, 28),
     "mbv3_dw5x5_f16": (2, 28, 28),
     "mbv3_pw1x1_f32": (2, 28, 28),
@@ -53,10 +53,10 @@ REDUCED = {
 }
 
 EXPECTED = {
-    "small_3x3_f32": "igemm_ffma", "resnet50_stem_f16": "igemm_tcgen05",
-    "resnet50_3x3_f16": "igemm_tcgen05", "resnet50_1x1_res_f16": "igemm_tcgen05",
+    "small_3x3_f32": "igemm_ffma", "resnet50_stem_f16": "igemm_tcgen05_window",
+    "resnet50_3x3_f16": "igemm_tcgen05_window", "resnet50_1x1_res_f16": "igemm_tcgen05_window",
     "mbv3_dw5x5_f32": "depthwise_halo", "mbv3_dw5x5_f16": "depthwise_halo",
-    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05",
+    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05_window",
     "grouped_dil2_f32": "igemm_ffma", "late_1x1_splitk_f32": "igemm_ffma_split_k",
     "strided_3x3_s2_f32": "igemm_ffma",
 }
@@ -128,23 +128,40 @@ EDGE = [
     ("tc_halo_s2_d2", (2, 16, 24, 16), (32, 16, 3, 3), dict(stride=2, pads=2, dilation=2), True, True),
     ("tc_halo_narrow", (1, 8, 40, 8), (16, 8, 3, 3), dict(pads=1, act="tanh"), True, False),
     ("long_k", (1, 320, 6, 6), (16, 320, 3, 3), dict(pads=1), True, False),
+    # shifted-window tcgen05 variant (x rows a multiple of 8 elements)
+    ("win_stem_phases", (2, 3, 40, 48), (16, 3, 7, 7), dict(stride=2, pads=3, act="relu"), True, False),
+    ("win_3x3_res", (2, 16, 12, 16), (40, 16, 3, 3), dict(pads=1, act="silu"), True, True),
+    ("win_asym_dil", (2, 8, 19, 16), (24, 8, 3, 2), dict(pads=(2, 0, 1, 3), dilation=(2, 3)), True, False),
+    ("win_1x1_co_tiles", (3, 32, 20, 16), (300, 32, 1, 1), dict(act="relu"), True, True),
+    ("win_s2_even_k", (2, 5, 32, 32), (20, 5, 4, 4), dict(stride=2, pads=(1, 2, 1, 0), act="tanh"),
+     True, False),
+    ("win_1x1_240", (2, 240, 28, 28), (40, 240, 1, 1), dict(), True, False),
+    ("win_cin_20", (1, 20, 9, 16), (24, 20, 3, 3), dict(pads=1, act="hard_swish"), False, True),
+    ("win_many_tiles", (8, 8, 64, 64), (16, 8, 3, 3), dict(pads=1, act="leaky_relu", alpha=0.1),
+     True, False),
+    ("win_s2_3x3_c64", (2, 64, 16, 16), (32, 64, 3, 3), dict(stride=2, pads=1), True, True),
     ("wide_cin_1x1", (1, 1024, 4, 4), (64, 1024, 1, 1), dict(), True, False),
 ]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("case", EDGE, ids=[c[0] for c in EDGE])
-@pytest.mark.parametrize("path", ["auto", "ffma"])
+@pytest.mark.parametrize("path", ["auto", "ffma", "gather"])
 def test_edge_cases(case, dtype, path):
     name, xs, ws, g, bias, res = case
     if path == "ffma" and dtype == "f32" and not name.startswith("depthwise"):
+        pytest.skip("same as auto")
+    if path == "gather" and (dtype == "f32" or not name.startswith("win_")):
         pytest.skip("same as auto")
     p = conv.make_problem(xs, ws, dtype=dtype, **{k: v for k, v in g.items()},
                           has_bias=bias, has_residual=res)
     ho, wo = conv.conv_output_shape(p)
     rs = (xs[0], ws[0], ho, wo) if res else None
     inp = random_layer_inputs(xs, ws, dtype, seed=zlib.crc32(name.encode()) % 10000, bias=bias, residual_shape=rs)
-    flags = conv.FLAG_FORCE_FFMA if path == "ffma" else 0
+    flags = {"auto": 0, "ffma": conv.FLAG_FORCE_FFMA, "gather": conv.FLAG_NO_WINDOW}[path]
+    if name.startswith("win_") and dtype != "f32" and path == "auto":
+        desc = conv.conv_describe_variant(p)
+        assert desc.startswith("igemm_tcgen05_window"), desc
     y = run_gpu(inp, flags=flags, **g)
     assert tuple(y.shape) == (xs[0], ws[0], ho, wo)
     out = check_full(inp, dtype, y, **g)
