@@ -46,10 +46,13 @@
 // and the device error word, every role drains out, outstanding copies and
 // MMAs are waited for (bounded) and tensor memory is freed before exit.
 //
-// The weights are repacked by a small kernel into the layout the MMA reads
-// ([channel tile][k block of 8][output channel][8 k values]), in the k order
-// (tap, phase channel): the weight re-layout "Convolution, pooling and
-// resize" measured at 1.27x on 3x3 layers, done once per call into scratch.
+// The weights reach shared memory in the layout the MMA reads ([k block of
+// 8][output channel][8 k values], k in (tap, phase channel) order): the
+// weight re-layout "Convolution, pooling and resize" measured at 1.27x on 3x3
+// layers.  With several taps it is a transpose, done once per call by a small
+// kernel into scratch (the conv kernel is launched as its programmatic
+// dependent: everything up to the first MMA overlaps it); a 1x1 layer's rows
+// are already in k order, and each block copies them in whole 16-byte units.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -125,11 +128,16 @@ __host__ __device__ inline WinLayout win_layout(const WinPlan& p) {
 // What the epilogue warps need besides the element type and the activation
 // (copied from the launch arguments and the plan into registers).
 struct EpiCtx {
-  uint32_t tmem_base, bar0, out_s, bias_s;  // tensor memory; barriers, output staging, bias (shared addresses)
+  uint32_t tmem_base, bar0, out_s;  // tensor memory; barriers and output staging (shared addresses)
+  uint8_t* out;                     // output staging and bias (shared memory)
+  const float* sbias;
   int t0, ntiles, co0;
   int tpi, rt, wp, wo, ho, nt, out_bytes, ostages;
   bool has_b, has_r;
   float alpha, beta;
+  const void* bias;  // the layer's bias (has_b), staged into sbias first
+  float* sbias_w;
+  int c_out;
   volatile int* abort_flag;
   const CUtensorMap* ymap;
   const CUtensorMap* rmap;
@@ -150,7 +158,7 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
   const int warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2;
   const int nchunks = e.nt / 8;
-  const uint32_t plane2 = static_cast<uint32_t>(e.rt * e.wo) * 2u;  // bytes per channel in a staging buffer
+  const int plane = e.rt * e.wo;  // elements per channel in a staging buffer
   const int OS = e.ostages;
   auto res_bar = [&](int k) { return e.bar0 + 8u * (10 + k); };
   auto issue_res = [&](int i) {  // thread 0: the residual box of tile t0+i into buffer i % OS
@@ -160,10 +168,14 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
     tma_load_4d(e.out_s + static_cast<uint32_t>(ob * e.out_bytes), e.rmap, 0, j * e.rt, e.co0, n, res_bar(ob));
   };
   if (e.has_r && tid == 0 && e.ntiles > 0) issue_res(0);
+  if (e.has_b) {  // ordered before its first use by the first tile's barrier
+    const T* bias = static_cast<const T*>(e.bias);
+    for (int j = tid; j < e.nt; j += kEpi) e.sbias_w[j] = e.co0 + j < e.c_out ? to_f32<T>(bias[e.co0 + j]) : 0.0f;
+  }
   // the thread's position in every tile
   const int qq = qd * 32 + lane;
   const int rr = qq / e.wp, c = qq - (qq / e.wp) * e.wp;
-  const uint32_t soff2 = static_cast<uint32_t>(rr * e.wo + c) * 2u;
+  const int soff2 = (rr * e.wo + c) * 2;
   for (int i = 0; i < e.ntiles; ++i) {
     const int t = e.t0 + i, n = t / e.tpi, j = t - (t / e.tpi) * e.tpi;
     const int b = i & 1, ob = i % OS;
@@ -176,7 +188,7 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
     tc_fence_after();
     const int rows_here = min(e.rt, e.ho - j * e.rt);
     const bool valid = rr < rows_here && c < e.wo;
-    const uint32_t st = e.out_s + static_cast<uint32_t>(ob * e.out_bytes) + soff2;
+    T* st = reinterpret_cast<T*>(e.out + ob * e.out_bytes + soff2);
     const uint32_t tb = e.tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + static_cast<uint32_t>(b * e.nt);
     for (int k0 = hf; k0 < nchunks; k0 += 8) {
       uint32_t v[4][8];
@@ -191,17 +203,12 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
           if (k >= nchunks) break;
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const uint32_t ch = static_cast<uint32_t>(k * 8 + jj);
-            const uint32_t addr = st + ch * plane2;
+            const int ch = k * 8 + jj;
+            T* dst = st + ch * plane;
             float x = __uint_as_float(v[g][jj]);
-            if (e.has_b) x = __fadd_rn(x, lds_f32(e.bias_s + ch * 4u));
-            if (e.has_r) {
-              const uint16_t rb = lds_u16(addr);
-              x = __fadd_rn(x, to_f32<T>(*reinterpret_cast<const T*>(&rb)));
-            }
-            x = act_fn<ACT>(x, e.alpha, e.beta);
-            const T o = from_f32<T>(x);
-            sts_u16(addr, *reinterpret_cast<const uint16_t*>(&o));
+            if (e.has_b) x = __fadd_rn(x, e.sbias[ch]);
+            if (e.has_r) x = __fadd_rn(x, to_f32<T>(*dst));
+            *dst = from_f32<T>(act_fn<ACT>(x, e.alpha, e.beta));
           }
         }
       }
@@ -230,11 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = sm_raw + ((128u - (smem_u32(sm_raw) & 127u)) & 127u);  // the launch adds 128 bytes of slack
   const WinLayout L = win_layout(p);
   const uint32_t bar0 = smem_u32(sm + L.bar_off);
-  const uint32_t wbar = bar0;
   auto full_bar = [&](int i) { return bar0 + 8u * (1 + i); };    // tile's input rows are in the ring
   auto rel_bar = [&](int i) { return bar0 + 8u * (3 + i); };     // tile's MMAs done: ring reusable
   auto tfull_bar = [&](int b) { return bar0 + 8u * (5 + b); };   // accumulator b ready
   auto tempty_bar = [&](int b) { return bar0 + 8u * (7 + b); };  // accumulator b read out
+  const uint32_t wbar = bar0;  // the raw weight copy landed
   const uint32_t drain_bar = bar0 + 8u * 9;
   auto res_bar = [&](int k) { return bar0 + 8u * (10 + k); };    // residual tile k landed
   auto sfull_bar = [&](int s) { return bar0 + 8u * (kBarFixed + s); };  // staged band s landed
@@ -260,7 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, bias, MMA table, tensor memory --------------------
   if (tid == 0) {
-    mbar_init(wbar, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(full_bar(i), kProd);
       mbar_init(rel_bar(i), 1);
@@ -270,13 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     for (int s = 0; s < p.stages; ++s) mbar_init(sfull_bar(s), 1);
+    mbar_init(wbar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  if (tid < kEpi) {
-    const T* bias = static_cast<const T*>(a.bias);
-    for (int j = tid; j < p.nt; j += kEpi)
-      sbias[j] = (bias && co0 + j < a.c_out) ? to_f32<T>(bias[co0 + j]) : 0.0f;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), cols);
@@ -295,13 +297,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // ---- producers' band state; their first bands are requested before the
+  // weights are laid out, so the two overlap
+  const int ptid = tid - kEpi;
+  const int pw = ptid >> 5;
+  const int DS = p.stages, SB = p.band;
+  auto row_end = [&](int i) {  // padded rows (exclusive) the valid outputs of tile t0+i read
+    const int t = t0 + i, n = t / p.tpi, j = t - (t / p.tpi) * p.tpi;
+    return n * p.hp + min((j + 1) * p.rt, p.ho) + (p.khp - 1) * a.dh;
+  };
+  const int rho0 = tile_q0(t0) / p.wp;
+  const int rho_end = ntiles > 0 ? row_end(ntiles - 1) : rho0;
+  const uint32_t stg_s = smem_u32(sm + L.stg_off);
+  // bands: rows [b*SB, min((b+1)*SB, hp)) of one image; the next band to
+  // load is (ni, bi), the band being consumed is (nf, bf)
+  int ni = rho0 / p.hp, bi = (rho0 - (rho0 / p.hp) * p.hp) / SB;
+  int nf = ni, bf = bi;
+  int k_issue = 0, k_fill = 0;
+  auto band_row0 = [&](int n, int b) { return n * p.hp + b * SB; };
+  // one TMA box per band: vw columns x PH*SB input rows x cg channels of image n
+  auto issue = [&]() {
+    const int s = k_issue % DS;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sfull_bar(s), static_cast<uint32_t>(p.band_bytes));
+      tma_load_4d(stg_s + static_cast<uint32_t>(s) * p.band_bytes, &xmap, 0, PH * bi * SB - a.pt, 0, ni,
+                  sfull_bar(s));
+    }
+    __syncwarp();
+    if (++bi * SB >= p.hp) { bi = 0; ++ni; }
+    ++k_issue;
+  };
+  if (warp == kEpiWarps)
+    for (int k = 0; k < DS && band_row0(ni, bi) < rho_end; ++k) issue();
+
+  // ---- 1x1: the weights of the channel tile into shared memory -------------
+  // The tile's rows arrive by one bulk copy each in the ring's space (unused
+  // until this block passes the barrier below) at a pitch of an odd number of
+  // 16-byte units, so that the unit copies below hit distinct banks; unit
+  // (channel block cb, channel co) is row co's channels 8cb .. 8cb+7.
+  if (p.wmode == 1) {
+    const int rows = min(p.nt, a.c_out - co0);
+    const int K = a.cg;
+    const int pitch = ((K * 2 / 16) | 1) * 16;  // bytes between staged rows
+    if (warp == kMmaWarp) {
+      const uint32_t dst = smem_u32(sm + L.ring_off);
+      const uint16_t* wg = static_cast<const uint16_t*>(a.wt) + static_cast<long long>(co0) * K;
+      if (lane == 0) mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(rows * K * 2));
+      __syncwarp();
+      for (int r = lane; r < rows; r += 32)
+        bulk_load(dst + static_cast<uint32_t>(r * pitch), wg + static_cast<long long>(r) * K,
+                  static_cast<uint32_t>(K * 2), wbar);
+    }
+    wait_phase(wbar, 0, abort_flag, 1u);
+    const uint8_t* raw = sm + L.ring_off;
+    uint4* wsm = reinterpret_cast<uint4*>(sm + L.w_off);
+    const int nb = p.c16 / 8;
+    for (int e = tid; e < nb * p.nt; e += kThreads) {
+      const int cb = e / p.nt, co_l = e - (e / p.nt) * p.nt;
+      wsm[e] = co_l < rows ? *reinterpret_cast<const uint4*>(raw + co_l * pitch + cb * 16) : make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async();  // the weights are visible to the tensor cores
+  }
+  __syncthreads();  // the ring's space is free again; the weights are in place
+  if (p.wmode == 1 && *abort_flag) {
+    wait_phase(wbar, 0, abort_flag, 1u, true);  // a copy still in flight lands before anything else
+    __syncthreads();
+  }
+
   if (warp < kEpiWarps) {
     // ---- epilogue: the activation is chosen once; each case is its own loop
     EpiCtx e;
     e.tmem_base = tmem_base;
     e.bar0 = bar0;
     e.out_s = smem_u32(sm + L.out_off);
-    e.bias_s = smem_u32(sbias);
+    e.out = sm + L.out_off;
+    e.sbias = sbias;
     e.t0 = t0;
     e.ntiles = ntiles;
     e.co0 = co0;
@@ -317,6 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     e.has_r = a.residual != nullptr;
     e.alpha = a.alpha;
     e.beta = a.beta;
+    e.bias = a.bias;
+    e.sbias_w = sbias;
+    e.c_out = a.c_out;
     e.abort_flag = abort_flag;
     e.ymap = &ymap;
     e.rmap = &rmap;
@@ -339,39 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kEpiWarps + kProdWarps) {
     // ---- producers: bands of input rows by TMA, channels interleaved into the ring
-    const int ptid = tid - kEpi;
-    const int pw = ptid >> 5;
     const int nb = p.c16 / 8;
     const int R = p.ring, RM = p.ring + p.mirror;
-    const int DS = p.stages, SB = p.band;
-    auto row_end = [&](int i) {  // padded rows (exclusive) the valid outputs of tile t0+i read
-      const int t = t0 + i, n = t / p.tpi, j = t - (t / p.tpi) * p.tpi;
-      return n * p.hp + min((j + 1) * p.rt, p.ho) + (p.khp - 1) * a.dh;
-    };
-    const int rho0 = tile_q0(t0) / p.wp;
-    const int rho_end = ntiles > 0 ? row_end(ntiles - 1) : rho0;
-    const uint32_t stg_s = smem_u32(sm + L.stg_off);
     uint8_t* ring = sm + L.ring_off;
-    // bands: rows [b*SB, min((b+1)*SB, hp)) of one image; the next band to
-    // load is (ni, bi), the band being consumed is (nf, bf)
-    int ni = rho0 / p.hp, bi = (rho0 - (rho0 / p.hp) * p.hp) / SB;
-    int nf = ni, bf = bi;
-    int k_issue = 0, k_fill = 0;
-    auto band_row0 = [&](int n, int b) { return n * p.hp + b * SB; };
-    // one TMA box per band: vw columns x PH*SB input rows x cg channels of image n
-    auto issue = [&]() {
-      const int s = k_issue % DS;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(sfull_bar(s), static_cast<uint32_t>(p.band_bytes));
-        tma_load_4d(stg_s + static_cast<uint32_t>(s) * p.band_bytes, &xmap, 0, PH * bi * SB - a.pt, 0, ni,
-                    sfull_bar(s));
-      }
-      __syncwarp();
-      if (++bi * SB >= p.hp) { bi = 0; ++ni; }
-      ++k_issue;
-    };
-    if (pw == 0)
-      for (int k = 0; k < DS && band_row0(ni, bi) < rho_end; ++k) issue();
     int filled = rho0;  // rows below this are in the ring
     // the thread's next unit is kProd units on: step_br rows, step_cb blocks, step_c columns
     const int step_br = kProd / (p.wp * nb);
@@ -446,13 +489,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (ntiles > 0) {
     // ---- MMA issuer: the whole warp runs the loop, one elected lane issues ----
-    const uint32_t wbytes = static_cast<uint32_t>(p.kblocks) * p.nt * 16u;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(wbar, wbytes);
-      bulk_load(smem_u32(sm + L.w_off), wpack + static_cast<size_t>(ct) * wbytes, wbytes, wbar);
+    bool ok = true;
+    if (p.wmode == 0) {
+      // the packed weights come from the repack kernel launched just before
+      // this one (programmatic dependent launch: everything above overlapped it)
+      asm volatile("griddepcontrol.wait;\n" ::: "memory");
+      const uint32_t wbytes = static_cast<uint32_t>(p.kblocks) * p.nt * 16u;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(wbar, wbytes);
+        bulk_load(smem_u32(sm + L.w_off), wpack + static_cast<size_t>(ct) * wbytes, wbytes, wbar);
+      }
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, wait_phase(wbar, 0, abort_flag, 1u));
     }
-    __syncwarp();
-    bool ok = __all_sync(0xffffffffu, wait_phase(wbar, 0, abort_flag, 1u));
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t idesc = make_idesc(kBf16, p.nt);
     const int R = p.ring, RM = p.ring + p.mirror;
@@ -494,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag) {
       mma_commit_elect(drain_bar);  // outstanding MMAs finish before their tensor memory is freed
       wait_phase(drain_bar, 0, abort_flag, 64u, true);
-      if (ntiles > 0) wait_phase(wbar, 0, abort_flag, 1u, true);  // the weight copy has landed
+      if (p.wmode == 0 && ntiles > 0) wait_phase(wbar, 0, abort_flag, 1u, true);  // the weight copy has landed
     }
     __syncwarp();
     tmem_dealloc(tmem_base, cols);
@@ -506,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and output channels past c_out.
 template <int PH>
 __global__ void tcw_repack(const ConvArgs a, const WinPlan p, uint4* __restrict__ out) {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");  // the conv kernel may start now
   const uint16_t* w = static_cast<const uint16_t*>(a.wt);
   const int nb = p.c16 / 8;
   const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
@@ -579,24 +629,39 @@ cudaError_t launch_win(const WinPlan& p, const ConvArgs& a, void* scratch, cudaS
   rmap = ymap;
   if (a.residual && !encode_nchw<T>(&rmap, a.residual, p.wo, p.ho, a.c_out, a.n, p.wo, p.rt, p.nt))
     return cudaErrorInvalidValue;
-
-  const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
-  const int rblocks = static_cast<int>(std::min<long long>((units + 255) / 256, 1024));
-  tcw_repack<PH><<<rblocks, 256, 0, s>>>(a, p, static_cast<uint4*>(scratch));
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
   auto kern = igemm_tcw<T, PH>;
+  auto repack = tcw_repack<PH>;
   static int configured[64] = {0};
   int dev = 0;
-  err = cudaGetDevice(&dev);
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && configured[dev] < static_cast<int>(p.smem)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
     if (err != cudaSuccess) return err;
     configured[dev] = static_cast<int>(p.smem);
   }
-  kern<<<p.ctas, kThreads, p.smem, s>>>(a, p, static_cast<const uint8_t*>(scratch), xmap, ymap, rmap);
-  return cudaGetLastError();
+  if (p.wmode == 1) {  // 1x1: the blocks copy their weights themselves
+    kern<<<p.ctas, kThreads, p.smem, s>>>(a, p, nullptr, xmap, ymap, rmap);
+    return cudaGetLastError();
+  }
+  const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
+  const int rblocks = static_cast<int>(std::min<long long>((units + 255) / 256, 1024));
+  repack<<<rblocks, 256, 0, s>>>(a, p, static_cast<uint4*>(scratch));
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  // programmatic dependent launch: the conv kernel's set-up and input staging
+  // overlap the repack; its MMA warp waits for the repack's completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.ctas));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, p, static_cast<const uint8_t*>(scratch), xmap, ymap, rmap);
 }
 
 // Channel tile, lookahead, output buffers, band height and band stages that
@@ -716,8 +781,13 @@ bool tcw_plan(const ConvArgs& a, int sm, WinPlan* out) {
   if (!ok) return false;
   p.parts = static_cast<int>(std::min<long long>(p.tiles, std::max(1, sm / p.co_tiles)));
   p.ctas = p.parts * p.co_tiles;
+  // 1x1 with whole 16-byte channel blocks and rows that fit the ring: the
+  // blocks copy their weights; otherwise a repack into scratch
+  const long long ring_bytes = static_cast<long long>(p.c16 / 8) * (p.ring + p.mirror) * 16;
+  const long long rows_max = std::min<long long>(p.nt, a.c_out);
+  p.wmode = (a.kh == 1 && a.kw == 1 && a.cg % 8 == 0 && rows_max * ((a.cg * 2 / 16) | 1) * 16 <= ring_bytes) ? 1 : 0;
+  p.w_bytes = p.wmode == 0 ? static_cast<size_t>(p.co_tiles) * p.kblocks * p.nt * 16 : 0;
   p.smem = std::max<size_t>(win_layout(p).end + 128, kOneBlockPerSm);
-  p.w_bytes = static_cast<size_t>(p.co_tiles) * p.kblocks * p.nt * 16;
   *out = p;
   return true;
 }

@@ -135,8 +135,8 @@ typedef enum conv_variant {
   CONV_VARIANT_IGEMM_TC_WINDOW = 4 /* tcgen05 implicit GEMM over shifted windows of
                                       a zero-padded input band in shared memory
                                       (stride 1, or stride 2 split into 2x2
-                                      phases; one group); weights repacked into
-                                      scratch first                          */
+                                      phases; one group; the output's rows a
+                                      multiple of 8 elements)                */
 } conv_variant;
 
 /* The host-side plan of a problem for a device with `sm_count` SMs. */
@@ -176,8 +176,8 @@ CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_pla
 /* Scratch bytes conv_forward needs for `p` on the current CUDA device
  * ("Convolution, pooling and resize", Layout and operands: the scratch
  * query): the float32 partial planes of split k (ranges x output elements),
- * the repacked weights of the shifted-window variant (channel tiles x k
- * blocks x tile channels x 16 bytes), 0 for the other variants.
+ * the repacked weights of the shifted-window variant with several taps
+ * (channel tiles x k blocks x tile channels x 16 bytes), 0 otherwise.
  * Errors: as conv_plan, and CONV_ERR_DEVICE without a usable device. */
 CONV_API conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes);
 
