@@ -87,8 +87,11 @@ def roofline_bound(L, variant: str, pk: dict) -> tuple[str, float, str]:
     arithmetic intensity is below the ridge of its compute path."""
     intensity = layer_flops(L) / layer_bytes(L)
     if variant.startswith("depthwise"):
-        compute, kind = FFMA_PEAK_TFLOPS, "alu"
-    elif variant.startswith("igemm_tcgen05"):
+        # a direct stencil doing k*k multiply-adds per value it reads: its
+        # roofline is HBM ("Convolutions", 2.3: the depthwise layer's low
+        # arithmetic intensity)
+        return "hbm", pk["hbm_gbs"], "GB/s"
+    if variant.startswith("igemm_tcgen05"):
         compute, kind = pk["bf16_tflops"], "tensor"  # fp16 and bf16 share the dense rate
     else:
         compute, kind = FFMA_PEAK_TFLOPS, "alu"
@@ -99,8 +102,8 @@ def roofline_bound(L, variant: str, pk: dict) -> tuple[str, float, str]:
 
 
 def kernel_source(variant: str) -> str:
-    name = {"igemm_tcgen05": "conv_tc.cu", "depthwise_halo": "conv_depthwise.cu"}.get(
-        variant.split()[0], "conv_ffma.cu")
+    name = {"igemm_tcgen05": "conv_tc.cu", "igemm_tcgen05_window": "conv_tcw.cu",
+            "depthwise_halo": "conv_depthwise.cu"}.get(variant.split()[0], "conv_ffma.cu")
     return os.path.join(ROOT, "implicit_gemm_cnn_gb300", "csrc", name)
 
 
