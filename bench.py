@@ -12,9 +12,9 @@ operands from HBM.  The K timed steps are replayed from CUDA graphs of
 back-to-back launches; the region is bracketed by a barrier and device
 synchronisation, timed with CUDA events, and the max over ranks is taken.
 
-The JSON line also carries: the roofline of the main kernel (algorithmic bytes
-or FLOPs of one launch over the launch's duration measured with CUDA events
-captured in the same graphs, against the measured peaks), the end-to-end rate
+The JSON line also carries: the roofline of one call (algorithmic bytes or
+FLOPs of one call over its average duration in the timed region, measured with
+the CUDA events around that region, against the measured peaks), the end-to-end rate
 through the public API with pinned host buffers, the CPU oracle's rate on a
 bounded sample (test infrastructure, timed only here), the kernel launch
 count and the SM clocks seen.
@@ -253,35 +253,19 @@ def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
         step(i)
     torch.cuda.synchronize()
 
-    # graphs of back-to-back launches, with external events around each launch
+    # graphs of back-to-back calls (no event nodes between the steps: they
+    # would add their own gaps to the timed region)
     chunk = max(1, min(steps, max(nsets, 500)))
 
-    def capture(n, with_events=True):
-        evs = None
-        if with_events:
-            try:
-                evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                        torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
-            except TypeError:  # a torch without external events
-                evs = None
+    def capture(n):
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device=dev)
         s.wait_stream(torch.cuda.current_stream())
-        try:
-            with torch.cuda.graph(g, stream=s):
-                for i in range(n):
-                    if evs:
-                        evs[i][0].record()
-                    step(i)
-                    if evs:
-                        evs[i][1].record()
-        except RuntimeError:
-            if not evs:
-                raise
-            torch.cuda.synchronize()
-            return capture(n, with_events=False)
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                step(i)
         torch.cuda.synchronize()
-        return g, evs
+        return g
 
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -297,11 +281,10 @@ def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
         torch.cuda.synchronize()
         barrier(world)
         clocks = sampler.stop()
-        ev_full, full_reps = None, 0
     else:
-        g_full, ev_full = capture(chunk)
+        g_full = capture(chunk)
         full_reps, rem = divmod(steps, chunk)
-        g_rem = capture(rem)[0] if rem else None
+        g_rem = capture(rem) if rem else None
         # settle clocks under load (untimed); clocks are sampled through the timed region
         sampler = ClockSampler(local_rank).start()
         t_end = time.time() + 1.0
@@ -322,17 +305,9 @@ def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
     secs = e0.elapsed_time(e1) / 1e3
     secs_max = max_over_ranks(secs, world)
 
-    # per-launch durations: the events captured in the full-chunk graph, as
-    # recorded by its last replay inside the timed region
-    launch_ms = None
-    if ev_full and full_reps > 0:
-        try:
-            d = [a.elapsed_time(b) for a, b in ev_full]
-            launch_ms = statistics.mean(d)
-        except RuntimeError:
-            launch_ms = None
-    if launch_ms is None:
-        launch_ms = secs * 1e3 / steps
+    # average duration of one call (all its kernels, back to back in the
+    # graphs), from the CUDA events around the timed region
+    launch_ms = secs * 1e3 / steps
 
     flops = layer_flops(L)
     value = aggregate(flops * steps, world, secs_max) / 1e12

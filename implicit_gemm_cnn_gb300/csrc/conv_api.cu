@@ -433,11 +433,10 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
     }
     case CONV_VARIANT_IGEMM_TC_WINDOW:
       // bulk copies of x rows need a 16-byte-aligned x; otherwise the gather kernel
-      // TMA boxes of x, y (and the residual) and the 1x1 weight copies want
-      // 16-byte-aligned arrays; otherwise the gather kernel
+      // TMA boxes of x, y (and the residual) want 16-byte-aligned arrays;
+      // otherwise the gather kernel
       if (reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
-          (!residual || reinterpret_cast<uintptr_t>(residual) % 16 == 0) &&
-          (plan.tcw.wmode != 1 || reinterpret_cast<uintptr_t>(w) % 16 == 0))
+          (!residual || reinterpret_cast<uintptr_t>(residual) % 16 == 0))
         err = launch_tcw(plan, a, p->dtype, scratch, cs);
       else err = launch_tc(plan, a, p->dtype, cs);
       break;

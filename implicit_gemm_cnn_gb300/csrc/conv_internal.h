@@ -83,9 +83,8 @@ struct WinPlan {
   int tiles;       // tiles over all images
   int parts;       // position ranges (blocks per channel tile)
   int ctas;        // blocks
-  int wmode;       // weights: 0 repacked into scratch by a kernel, 1 copied by each block (1x1)
   size_t smem;     // dynamic shared memory bytes
-  size_t w_bytes;  // scratch: the repacked weights (wmode 0)
+  size_t w_bytes;  // scratch: the repacked weights
 };
 bool tcw_plan(const ConvArgs& a, int sm, WinPlan* w);
 

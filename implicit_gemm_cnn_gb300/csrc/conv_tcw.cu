@@ -49,10 +49,9 @@
 // The weights reach shared memory in the layout the MMA reads ([k block of
 // 8][output channel][8 k values], k in (tap, phase channel) order): the
 // weight re-layout "Convolution, pooling and resize" measured at 1.27x on 3x3
-// layers.  With several taps it is a transpose, done once per call by a small
-// kernel into scratch (the conv kernel is launched as its programmatic
-// dependent: everything up to the first MMA overlaps it); a 1x1 layer's rows
-// are already in k order, and each block copies them in whole 16-byte units.
+// layers, done once per call by a small kernel into scratch; the conv kernel
+// is launched as its programmatic dependent, so everything up to the first
+// MMA overlaps it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -330,40 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kEpiWarps)
     for (int k = 0; k < DS && band_row0(ni, bi) < rho_end; ++k) issue();
 
-  // ---- 1x1: the weights of the channel tile into shared memory -------------
-  // The tile's rows arrive by one bulk copy each in the ring's space (unused
-  // until this block passes the barrier below) at a pitch of an odd number of
-  // 16-byte units, so that the unit copies below hit distinct banks; unit
-  // (channel block cb, channel co) is row co's channels 8cb .. 8cb+7.
-  if (p.wmode == 1) {
-    const int rows = min(p.nt, a.c_out - co0);
-    const int K = a.cg;
-    const int pitch = ((K * 2 / 16) | 1) * 16;  // bytes between staged rows
-    if (warp == kMmaWarp) {
-      const uint32_t dst = smem_u32(sm + L.ring_off);
-      const uint16_t* wg = static_cast<const uint16_t*>(a.wt) + static_cast<long long>(co0) * K;
-      if (lane == 0) mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(rows * K * 2));
-      __syncwarp();
-      for (int r = lane; r < rows; r += 32)
-        bulk_load(dst + static_cast<uint32_t>(r * pitch), wg + static_cast<long long>(r) * K,
-                  static_cast<uint32_t>(K * 2), wbar);
-    }
-    wait_phase(wbar, 0, abort_flag, 1u);
-    const uint8_t* raw = sm + L.ring_off;
-    uint4* wsm = reinterpret_cast<uint4*>(sm + L.w_off);
-    const int nb = p.c16 / 8;
-    for (int e = tid; e < nb * p.nt; e += kThreads) {
-      const int cb = e / p.nt, co_l = e - (e / p.nt) * p.nt;
-      wsm[e] = co_l < rows ? *reinterpret_cast<const uint4*>(raw + co_l * pitch + cb * 16) : make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async();  // the weights are visible to the tensor cores
-  }
-  __syncthreads();  // the ring's space is free again; the weights are in place
-  if (p.wmode == 1 && *abort_flag) {
-    wait_phase(wbar, 0, abort_flag, 1u, true);  // a copy still in flight lands before anything else
-    __syncthreads();
-  }
-
   if (warp < kEpiWarps) {
     // ---- epilogue: the activation is chosen once; each case is its own loop
     EpiCtx e;
@@ -489,19 +454,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (ntiles > 0) {
     // ---- MMA issuer: the whole warp runs the loop, one elected lane issues ----
-    bool ok = true;
-    if (p.wmode == 0) {
-      // the packed weights come from the repack kernel launched just before
-      // this one (programmatic dependent launch: everything above overlapped it)
-      asm volatile("griddepcontrol.wait;\n" ::: "memory");
-      const uint32_t wbytes = static_cast<uint32_t>(p.kblocks) * p.nt * 16u;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(wbar, wbytes);
-        bulk_load(smem_u32(sm + L.w_off), wpack + static_cast<size_t>(ct) * wbytes, wbytes, wbar);
-      }
-      __syncwarp();
-      ok = __all_sync(0xffffffffu, wait_phase(wbar, 0, abort_flag, 1u));
+    // the packed weights come from the repack kernel launched just before
+    // this one (programmatic dependent launch: everything above overlapped it)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    const uint32_t wbytes = static_cast<uint32_t>(p.kblocks) * p.nt * 16u;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(wbar, wbytes);
+      bulk_load(smem_u32(sm + L.w_off), wpack + static_cast<size_t>(ct) * wbytes, wbytes, wbar);
     }
+    __syncwarp();
+    bool ok = __all_sync(0xffffffffu, wait_phase(wbar, 0, abort_flag, 1u));
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t idesc = make_idesc(kBf16, p.nt);
     const int R = p.ring, RM = p.ring + p.mirror;
@@ -543,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag) {
       mma_commit_elect(drain_bar);  // outstanding MMAs finish before their tensor memory is freed
       wait_phase(drain_bar, 0, abort_flag, 64u, true);
-      if (p.wmode == 0 && ntiles > 0) wait_phase(wbar, 0, abort_flag, 1u, true);  // the weight copy has landed
+      if (ntiles > 0) wait_phase(wbar, 0, abort_flag, 1u, true);  // the weight copy has landed
     }
     __syncwarp();
     tmem_dealloc(tmem_base, cols);
@@ -639,10 +601,6 @@ cudaError_t launch_win(const WinPlan& p, const ConvArgs& a, void* scratch, cudaS
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
     if (err != cudaSuccess) return err;
     configured[dev] = static_cast<int>(p.smem);
-  }
-  if (p.wmode == 1) {  // 1x1: the blocks copy their weights themselves
-    kern<<<p.ctas, kThreads, p.smem, s>>>(a, p, nullptr, xmap, ymap, rmap);
-    return cudaGetLastError();
   }
   const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
   const int rblocks = static_cast<int>(std::min<long long>((units + 255) / 256, 1024));
@@ -781,12 +739,7 @@ bool tcw_plan(const ConvArgs& a, int sm, WinPlan* out) {
   if (!ok) return false;
   p.parts = static_cast<int>(std::min<long long>(p.tiles, std::max(1, sm / p.co_tiles)));
   p.ctas = p.parts * p.co_tiles;
-  // 1x1 with whole 16-byte channel blocks and rows that fit the ring: the
-  // blocks copy their weights; otherwise a repack into scratch
-  const long long ring_bytes = static_cast<long long>(p.c16 / 8) * (p.ring + p.mirror) * 16;
-  const long long rows_max = std::min<long long>(p.nt, a.c_out);
-  p.wmode = (a.kh == 1 && a.kw == 1 && a.cg % 8 == 0 && rows_max * ((a.cg * 2 / 16) | 1) * 16 <= ring_bytes) ? 1 : 0;
-  p.w_bytes = p.wmode == 0 ? static_cast<size_t>(p.co_tiles) * p.kblocks * p.nt * 16 : 0;
+  p.w_bytes = static_cast<size_t>(p.co_tiles) * p.kblocks * p.nt * 16;
   p.smem = std::max<size_t>(win_layout(p).end + 128, kOneBlockPerSm);
   *out = p;
   return true;

@@ -176,8 +176,8 @@ CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_pla
 /* Scratch bytes conv_forward needs for `p` on the current CUDA device
  * ("Convolution, pooling and resize", Layout and operands: the scratch
  * query): the float32 partial planes of split k (ranges x output elements),
- * the repacked weights of the shifted-window variant with several taps
- * (channel tiles x k blocks x tile channels x 16 bytes), 0 otherwise.
+ * the repacked weights of the shifted-window variant (channel tiles x k
+ * blocks x tile channels x 16 bytes), 0 for the other variants.
  * Errors: as conv_plan, and CONV_ERR_DEVICE without a usable device. */
 CONV_API conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes);
 

@@ -154,11 +154,9 @@ def test_plans_of_the_workloads(lib, name):
     elif plan["variant_name"] == "igemm_tcgen05_window":
         tile = plan["tile_m"]
         assert tile % 16 == 0 and tile <= 256
-        if L.kh * L.kw == 1:   # 1x1: each block copies its weights
-            assert plan["scratch_bytes"] == 0
-        else:                  # repacked weights: channel tiles x k blocks x tile channels x 16 bytes
-            assert plan["scratch_bytes"] % (16 * tile) == 0
-            assert plan["scratch_bytes"] >= L.c_out * (L.c_in // L.groups) * L.kh * L.kw * 2
+        # repacked weights: channel tiles x k blocks x tile channels x 16 bytes
+        assert plan["scratch_bytes"] % (16 * tile) == 0
+        assert plan["scratch_bytes"] >= L.c_out * (L.c_in // L.groups) * L.kh * L.kw * 2
         assert plan["ctas"] <= 152
         p2 = _layer_problem(L, flags=conv.FLAG_NO_WINDOW)
         assert conv.conv_plan(p2, 152)["variant_name"] == "igemm_tcgen05"
