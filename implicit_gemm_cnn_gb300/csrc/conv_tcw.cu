@@ -23,21 +23,21 @@
 // zero weights).  The ResNet-50 stem (7x7 / 2, 3 channels) becomes a 4x4 /1
 // convolution over 12 (padded to 16) channels.
 //
-// Roles (one persistent block per SM, 13 warps):
-//   * warps 8-11 (producers) stream the block's band of padded input rows:
+// Roles (one persistent block per SM, 21 warps):
+//   * warps 16-19 (producers) stream the block's band of padded input rows:
 //     the rows of x each padded row needs arrive in shared memory by bulk
 //     copies, several rows in flight; the producers then interleave each row's
 //     channels into the ring (16 bytes per position and 8-channel block; zero
 //     for padding, phantom channels and rows outside the image).  The ring is
 //     R positions deep; positions at ring slots below 128 are also written
 //     R slots further on, so that every 128-position window is contiguous;
-//   * warp 12 loads the repacked weights of its channel tile once (one bulk
+//   * warp 20 loads the repacked weights of its channel tile once (one bulk
 //     copy), allocates tensor memory and one lane issues, per tile, kh*kw*C/16
 //     MMAs (kind::f16, M = 128 positions, N = the channel tile, K = 16) whose
 //     A descriptors point at the shifted windows; a commit releases the ring
 //     for the producers and another hands the accumulator to the epilogue;
-//   * warps 0-7 (epilogue): tcgen05.ld of the float32 accumulator (thread =
-//     position; two warps per 32-lane quarter, alternating 8-column chunks),
+//   * warps 0-15 (epilogue): tcgen05.ld of the float32 accumulator (thread =
+//     position; four warps per 32-lane quarter, every fourth 8-column chunk),
 //     bias, residual, activation in float32, one rounding, and a store of each
 //     valid position's value to NCHW y -- the output is written once.
 // Accumulators are double buffered in tensor memory, so the epilogue of one
@@ -71,10 +71,11 @@ namespace {
 
 using namespace tcx;
 
-constexpr int kEpiWarps = 8;   // warps 0-7: tensor-memory lanes 32*(w%4) .., column half w/4
-constexpr int kProdWarps = 4;  // warps 8-11
-constexpr int kMmaWarp = 12;
-constexpr int kThreads = 13 * 32;
+constexpr int kEpiWarps = 16;  // warps 0-15: tensor-memory lanes 32*(w%4) .., column group w/4
+constexpr int kEpiGroups = kEpiWarps / 4;  // warps per lane quarter: chunks g, g+kEpiGroups, ...
+constexpr int kProdWarps = 4;  // warps 16-19
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kEpi = kEpiWarps * 32;
 constexpr int kProd = kProdWarps * 32;
 constexpr uint32_t kProdBar = 2;  // named barrier of the producer warps
@@ -144,7 +145,7 @@ struct EpiCtx {
 
 // The epilogue warps' loop over the block's tiles, for activation ACT.  Warp
 // w reads tensor-memory lanes 32*(w%4) .. +31 (thread = position of the tile)
-// and the 8-column chunks w/4, w/4+2, ..., up to four chunks per
+// and the 8-column chunks w/4, w/4+4, ..., up to four chunks per
 // tensor-memory wait; bias, residual and activation in float32, one rounding
 // into the tile's staging buffer [channel][row][column]; then one TMA store
 // of the box (wo x rows x channels) to y -- rows past Ho and channels past
@@ -155,7 +156,7 @@ template <typename T, int ACT>
 __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
   const int tid = threadIdx.x;  // 0 .. kEpi-1
   const int warp = tid >> 5, lane = tid & 31;
-  const int qd = warp & 3, hf = warp >> 2;
+  const int qd = warp & 3, hf = warp >> 2;  // lane quarter, column group
   const int nchunks = e.nt / 8;
   const int plane = e.rt * e.wo;  // elements per channel in a staging buffer
   const int OS = e.ostages;
@@ -189,16 +190,16 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
     const bool valid = rr < rows_here && c < e.wo;
     T* st = reinterpret_cast<T*>(e.out + ob * e.out_bytes + soff2);
     const uint32_t tb = e.tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + static_cast<uint32_t>(b * e.nt);
-    for (int k0 = hf; k0 < nchunks; k0 += 8) {
+    for (int k0 = hf; k0 < nchunks; k0 += 4 * kEpiGroups) {
       uint32_t v[4][8];
 #pragma unroll
       for (int g = 0; g < 4; ++g)
-        if (k0 + 2 * g < nchunks) tmem_ld8_nowait(tb + (k0 + 2 * g) * 8, v[g]);
+        if (k0 + kEpiGroups * g < nchunks) tmem_ld8_nowait(tb + (k0 + kEpiGroups * g) * 8, v[g]);
       tmem_wait_ld();
       if (valid) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const int k = k0 + 2 * g;
+          const int k = k0 + kEpiGroups * g;
           if (k >= nchunks) break;
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
