@@ -164,6 +164,11 @@ bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   d.row = static_cast<int>(row);
   d.vec = 0;
   d.sm = sm;
+  // narrow planes: one warp per plane, two (Ho + k - 1)-row buffers of the
+  // plane in shared memory per warp (8 warps per block)
+  const long long nw_bytes = 8LL * 2 * (s.ho + p->kh - 1) * (s.wo + p->kw + 2) * es;
+  d.narrow = p->stride_h == 1 && p->stride_w == 1 && p->dil_h == 1 && p->dil_w == 1 && p->kh == p->kw &&
+             (p->kh == 3 || p->kh == 5 || p->kh == 7) && s.wo <= 32 && nw_bytes <= 96 * 1024;
   out->dw = d;
   out->info.variant = CONV_VARIANT_DEPTHWISE;
   out->info.split_k = 1;
@@ -369,6 +374,9 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
              variant_name(i.variant), w.nt, w.ph, w.ph, w.khp, w.kwp, static_cast<long long>(i.gemm_k),
              w.kblocks * 8, w.hp, w.wp, w.ring, w.mirror, w.band, w.stages, w.lookahead,
              static_cast<long long>(i.ctas), sm);
+  } else if (i.variant == CONV_VARIANT_DEPTHWISE && plan.dw.narrow) {
+    snprintf(buf, len, "%s one warp per plane, window in registers, double-buffered planes sms=%d",
+             variant_name(i.variant), sm);
   } else if (i.variant == CONV_VARIANT_DEPTHWISE) {
     snprintf(buf, len, "%s rows/block=%d staged=%dx%d blocks=%lld sms=%d", variant_name(i.variant),
              plan.dw.th, plan.dw.in_rows, plan.dw.row, static_cast<long long>(i.ctas), sm);

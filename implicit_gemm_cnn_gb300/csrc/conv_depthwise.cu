@@ -24,6 +24,10 @@
 // values of one kernel column sit in registers and serve all kQH outputs;
 // each output is summed in one float32 chain in (kernel column, kernel row)
 // order.  Bias, residual and activation are applied at the store.
+//
+// Planes at most 32 output columns wide at stride 1 take a leaner path (one
+// warp per plane, below): no work-item arithmetic per output, the window in
+// registers, the next plane copied while the current one is computed.
 #include <algorithm>
 
 #include "conv_internal.h"
@@ -239,6 +243,163 @@ __global__ void __launch_bounds__(kDwThreads)
   cp_async_wait<0>();
 }
 
+// ---- narrow planes: one warp per (image, output channel) plane -------------
+// For stride 1, dilation 1, square 3/5/7 kernels and planes at most 32 output
+// columns wide (the late layers of MobileNet-style networks): lane = output
+// column.  Each warp owns two shared-memory buffers of (Ho + K - 1) rows of
+// `pitch` elements holding a zero-bordered input plane (the border is written
+// once); while it computes one plane, cp.async copies of the next plane's rows
+// fill the other buffer.  Each lane walks down its column with the K x K input
+// window in registers, loading one new row segment (K values) per output row,
+// and sums each output in one float32 chain in (kernel row, kernel column)
+// order.  The activation is a template parameter, so the value loop holds no
+// switch.
+constexpr int kNwWarps = 8;  // warps per block (one plane each at a time)
+
+struct NarrowGeo {
+  int pitch;  // elements per staged row (even)
+  int rows;   // staged rows: Ho + K - 1
+  int cofs;   // buffer column of image column 0 (even for 16-bit elements)
+  int async;  // rows copied with 4-byte cp.async (else element loads)
+};
+
+template <typename T, int K, int ACT>
+__device__ __forceinline__ void narrow_planes(const ConvArgs& a, const NarrowGeo& g, T* buf0, long long planes,
+                                              long long first, long long stride) {
+  const int lane = threadIdx.x & 31;
+  const T* __restrict__ xg = static_cast<const T*>(a.x);
+  const T* __restrict__ wg = static_cast<const T*>(a.wt);
+  const T* __restrict__ bg = static_cast<const T*>(a.bias);
+  const T* __restrict__ rg = static_cast<const T*>(a.residual);
+  T* __restrict__ y = static_cast<T*>(a.y);
+  const int m = a.mg;  // output channels per input channel
+  const int bufsz = g.pitch * g.rows;
+  // image rows / columns land at (pt + r, cofs + c); clip what no window reads
+  const int r_hi = min(a.h, g.rows - a.pt), c_hi = min(a.w, g.pitch - g.cofs);
+  constexpr int kPer = 4 / sizeof(T);  // elements per 4-byte copy
+  auto stage = [&](long long pl, T* buf) {
+    const int n = static_cast<int>(pl / a.c_out);
+    const int co = static_cast<int>(pl - static_cast<long long>(n) * a.c_out);
+    const T* src = xg + (static_cast<long long>(n) * a.c_in + co / m) * a.hw;
+    if (g.async) {
+      const int units = (c_hi + kPer - 1) / kPer;  // 4-byte units per row
+      for (int r = 0; r < r_hi; ++r) {
+        T* drow = buf + (a.pt + r) * g.pitch + g.cofs;
+        const T* srow = src + static_cast<long long>(r) * a.w;
+        for (int q = lane; q < units; q += 32) cp_async_n<4>(drow + q * kPer, srow + q * kPer);
+      }
+    } else {
+      for (int r = 0; r < r_hi; ++r) {
+        T* drow = buf + (a.pt + r) * g.pitch + g.cofs;
+        const T* srow = src + static_cast<long long>(r) * a.w;
+        for (int c = lane; c < c_hi; c += 32) drow[c] = srow[c];
+      }
+    }
+  };
+  int k = 0;
+  if (first < planes) stage(first, buf0);
+  cp_async_commit();
+  for (long long pl = first; pl < planes; pl += stride, ++k) {
+    T* buf = buf0 + (k & 1) * bufsz;
+    if (pl + stride < planes) stage(pl + stride, buf0 + ((k + 1) & 1) * bufsz);
+    cp_async_commit();
+    const int n = static_cast<int>(pl / a.c_out);
+    const int co = static_cast<int>(pl - static_cast<long long>(n) * a.c_out);
+    float wv[K][K];
+#pragma unroll
+    for (int u = 0; u < K; ++u)
+#pragma unroll
+      for (int v = 0; v < K; ++v) wv[u][v] = to_f32(wg[static_cast<long long>(co) * K * K + u * K + v]);
+    const float bv = bg ? to_f32(bg[co]) : 0.0f;
+    cp_async_wait<1>();  // this plane's copies (the next plane's may still fly)
+    __syncwarp();
+    if (lane < a.wo) {
+      const T* col = buf + g.cofs - a.pl + lane;
+      float win[K][K];  // slot (row % K) holds an input row of the window
+#pragma unroll
+      for (int i = 0; i < K - 1; ++i)
+#pragma unroll
+        for (int v = 0; v < K; ++v) win[i][v] = to_f32(col[i * g.pitch + v]);
+      T* yo = y + (static_cast<long long>(n) * a.c_out + co) * a.howo + lane;
+      const T* ro = rg ? rg + (static_cast<long long>(n) * a.c_out + co) * a.howo + lane : nullptr;
+      for (int oh0 = 0; oh0 < a.ho; oh0 += K) {
+#pragma unroll
+        for (int s = 0; s < K; ++s) {
+          const int oh = oh0 + s;
+          if (oh >= a.ho) break;
+          // the window's newest row: input row oh + K - 1 into slot (s + K - 1) % K
+#pragma unroll
+          for (int v = 0; v < K; ++v) win[(s + K - 1) % K][v] = to_f32(col[(oh + K - 1) * g.pitch + v]);
+          float acc = 0.0f;
+#pragma unroll
+          for (int u = 0; u < K; ++u)
+#pragma unroll
+            for (int v = 0; v < K; ++v) acc = fmaf(win[(s + u) % K][v], wv[u][v], acc);
+          float t = acc;
+          if (bg) t = __fadd_rn(t, bv);
+          if (ro) t = __fadd_rn(t, to_f32(ro[oh * a.wo]));
+          yo[oh * a.wo] = from_f32<T>(act_fn<ACT>(t, a.alpha, a.beta));
+        }
+      }
+    }
+    __syncwarp();  // this buffer's reads are done before it is refilled
+  }
+  cp_async_wait<0>();
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kNwWarps * 32, K == 7 ? 2 : 3) depthwise_narrow(const ConvArgs a, const NarrowGeo g) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  T* buf = reinterpret_cast<T*>(dsm) + static_cast<size_t>(warp) * 2 * g.pitch * g.rows;
+  for (int i = lane; i < 2 * g.pitch * g.rows; i += 32) buf[i] = from_f32<T>(0.0f);  // the border stays zero
+  __syncwarp();
+  const long long planes = static_cast<long long>(a.n) * a.c_out;
+  const long long first = static_cast<long long>(blockIdx.x) * kNwWarps + warp;
+  const long long stride = static_cast<long long>(gridDim.x) * kNwWarps;
+  switch (a.act) {
+#define CONV_NW_CASE(A) \
+  case A: narrow_planes<T, K, A>(a, g, buf, planes, first, stride); break;
+    CONV_NW_CASE(ACT_RELU)
+    CONV_NW_CASE(ACT_SILU)
+    CONV_NW_CASE(ACT_SIGMOID)
+    CONV_NW_CASE(ACT_TANH)
+    CONV_NW_CASE(ACT_HARD_SWISH)
+    CONV_NW_CASE(ACT_HARD_SIGMOID)
+    CONV_NW_CASE(ACT_CLIP)
+    CONV_NW_CASE(ACT_LEAKY_RELU)
+#undef CONV_NW_CASE
+    default: narrow_planes<T, K, ACT_IDENTITY>(a, g, buf, planes, first, stride);
+  }
+}
+
+template <typename T, int K>
+cudaError_t launch_narrow(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  NarrowGeo g;
+  constexpr int es = static_cast<int>(sizeof(T));
+  g.cofs = es == 4 ? a.pl : (a.pl + 1) / 2 * 2;
+  g.pitch = (g.cofs - a.pl + a.wo + K - 1 + 1) / 2 * 2;
+  g.rows = a.ho + K - 1;
+  // 4-byte copies: x 4-byte aligned, every image row starting on 4 bytes
+  g.async = reinterpret_cast<uintptr_t>(a.x) % 4 == 0 && (static_cast<long long>(a.w) * es) % 4 == 0 &&
+            (a.hw * es) % 4 == 0;
+  const size_t smem = static_cast<size_t>(kNwWarps) * 2 * g.pitch * g.rows * es;
+  auto kern = depthwise_narrow<T, K>;
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+  }
+  const long long planes = static_cast<long long>(a.n) * a.c_out;
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNwWarps * 32, smem);
+  if (err != cudaSuccess) return err;
+  const long long blocks = std::min<long long>((planes + kNwWarps - 1) / kNwWarps,
+                                               static_cast<long long>(d.sm) * std::max(per_sm, 1));
+  kern<<<static_cast<unsigned>(blocks), kNwWarps * 32, smem, s>>>(a, g);
+  return cudaGetLastError();
+}
+
 template <typename T, int KH>
 cudaError_t launch_kh(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
   const int row_tiles = (a.ho + d.th - 1) / d.th;
@@ -257,6 +418,11 @@ cudaError_t launch_kh(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_typed(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  if (d.narrow) {
+    if (a.kh == 3) return launch_narrow<T, 3>(d, a, s);
+    if (a.kh == 5) return launch_narrow<T, 5>(d, a, s);
+    if (a.kh == 7) return launch_narrow<T, 7>(d, a, s);
+  }
   if (a.sh == 1 && a.dh == 1) {
     if (a.kh == 3) return launch_kh<T, 3>(d, a, s);
     if (a.kh == 5) return launch_kh<T, 5>(d, a, s);

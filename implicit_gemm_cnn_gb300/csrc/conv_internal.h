@@ -36,6 +36,7 @@ struct DwPlan {
   int row;       // staged row length in elements (>= lm + needed columns)
   int vec;       // bytes per cp.async copy of input rows (16/8/4; 0: element copies)
   int sm;        // SMs of the device (blocks loop over the work items)
+  int narrow;    // one warp per plane (stride 1, dilation 1, square 3/5/7, Wo <= 32)
 };
 size_t depthwise_smem_bytes(const DwPlan& d, int mg, int kh, int kw, int dtype);
 

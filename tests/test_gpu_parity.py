@@ -107,6 +107,13 @@ EDGE = [
     ("depthwise_dil", (1, 16, 15, 15), (16, 1, 5, 5),
      dict(pads=4, dilation=2, groups=16, act="clip", alpha=-0.5, beta=0.5), True, True),
     ("depthwise_7x7", (2, 8, 20, 24), (8, 1, 7, 7), dict(pads=3, groups=8, act="relu"), False, False),
+    # one warp per narrow plane (stride 1, dilation 1, square 3/5/7, Wo <= 32)
+    ("depthwise_narrow_mult2", (2, 6, 14, 14), (12, 1, 3, 3), dict(pads=1, groups=6, act="silu"), True, True),
+    ("depthwise_narrow_w32", (1, 4, 9, 34), (4, 1, 3, 3), dict(groups=4), True, False),
+    ("depthwise_narrow_asym", (2, 5, 11, 13), (5, 1, 5, 5),
+     dict(pads=(2, 1, 0, 3), groups=5, act="hard_sigmoid", alpha=0.2, beta=0.5), True, True),
+    ("depthwise_narrow_tall", (1, 3, 60, 7), (3, 1, 7, 7), dict(pads=3, groups=3, act="leaky_relu", alpha=0.1),
+     True, False),
     ("one_d", (3, 4, 1, 37), (6, 4, 1, 5), dict(pads=(0, 2, 0, 2), act="leaky_relu", alpha=0.1),
      True, False),
     ("single_output", (2, 3, 5, 5), (4, 3, 5, 5), dict(act="sigmoid"), True, False),
