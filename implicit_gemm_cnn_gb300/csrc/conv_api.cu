@@ -128,6 +128,12 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   }
   if (split <= 1) { split = 1; len = s.K; }
   out->ffma_cfg = bi;
+  // pointwise fp32 (1x1, stride 1, no pad, dilation 1) whose planes hold whole
+  // groups of 4 pixels: 16-byte B copies (x's alignment is checked at launch)
+  const long long hw = p->h * p->w;
+  out->ffma_vec = p->dtype == CONV_F32 && p->kh == 1 && p->kw == 1 && p->stride_h == 1 && p->stride_w == 1 &&
+                  p->pad_top == 0 && p->pad_left == 0 && p->pad_bottom == 0 && p->pad_right == 0 &&
+                  hw % 4 == 0 && kFfmaCfgs[bi].bn % 4 == 0;
   out->info.variant = split > 1 ? CONV_VARIANT_IGEMM_FFMA_SPLIT : CONV_VARIANT_IGEMM_FFMA;
   out->info.split_k = split;
   out->info.tile_m = c.bm;

@@ -35,6 +35,11 @@ __device__ __forceinline__ void cp_async4(float* smem, const void* gmem, bool pr
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
                : "memory");
 }
+__device__ __forceinline__ void cp_async16(float* smem, const void* gmem, bool pred) {
+  unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  int n = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -69,7 +74,11 @@ __host__ __device__ constexpr int pow2_floor(int v) {
   return p;
 }
 
-template <typename T, int BM, int BN, int TM, int TN>
+// VB: a pointwise layer (1x1, stride 1, no pad, plane length a multiple of 4,
+// x 16-byte aligned) whose k rows of 4 consecutive pixels are 16 contiguous
+// bytes of one channel plane: the B tile arrives by 16-byte cp.async copies,
+// each thread's pixel offsets computed once, no window table.
+template <typename T, int BM, int BN, int TM, int TN, bool VB>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN))
     igemm_ffma(const ConvArgs a, const int ktab_cap) {
   constexpr int NT = (BM / TM) * (BN / TN);
@@ -123,6 +132,24 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
                static_cast<long long>(ih0[j]) * a.w + iw0[j];
   }
 
+  // VB: the thread's 16-byte copies of a stage: q = tid + i*NT -> k row q / (BN/4),
+  // pixels pix0 + 4*(q % (BN/4)) .. +3 (all in one image: the plane length is a
+  // multiple of 4)
+  constexpr int QV = VB ? (BK * BN / 4 + NT - 1) / NT : 1;
+  long long vbase[QV];
+  bool vok[QV];
+  if constexpr (VB) {
+#pragma unroll
+    for (int i = 0; i < QV; ++i) {
+      const int q = tid + i * NT;
+      const long long p = pix0 + 4 * (q % (BN / 4));
+      vok[i] = q < BK * BN / 4 && p < a.npix;
+      const long long pp = vok[i] ? p : 0;
+      const long long n = pp / a.howo;
+      vbase[i] = (n * a.c_in + static_cast<long long>(g) * a.cg) * a.hw + (pp - n * a.howo);
+    }
+  }
+
   float acc[TM][TN];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
@@ -135,7 +162,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
   for (int kseg = k_begin; kseg < k_end; kseg += ktab_cap) {
     const int seg_end = min(k_end, kseg + ktab_cap);
     __syncthreads();  // the previous segment's table and stages are free
-    for (int k = kseg + tid; k < seg_end; k += NT) {
+    for (int k = kseg + tid; !VB && k < seg_end; k += NT) {
       const int c = k / khw;
       const int tap = k - c * khw;
       const int u = tap / a.kw, v = tap - (tap / a.kw) * a.kw;
@@ -159,7 +186,18 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
           stage_elem<T>(as + kk * AS + m, src, ok);
         }
       }
-      if (bloader) {
+      if constexpr (VB) {
+#pragma unroll
+        for (int i = 0; i < QV; ++i) {
+          const int q = tid + i * NT;
+          const int kk = q / (BN / 4), c4 = q % (BN / 4);
+          const int k = k0 + kk;
+          const bool ok = vok[i] && k < seg_end;
+          const float* src = ok ? reinterpret_cast<const float*>(x) + vbase[i] + static_cast<long long>(k) * a.hw
+                                : reinterpret_cast<const float*>(x);
+          if (q < BK * BN / 4) cp_async16(bs + kk * BN + 4 * c4, src, ok);
+        }
+      } else if (bloader) {
 #pragma unroll
         for (int i = 0; i < BROWS; ++i) {
           const int kk = r0 + i * RSTEP;
@@ -331,10 +369,10 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
   }
 }
 
-template <typename T, int CFG>
-cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
+template <typename T, int CFG, bool VB>
+cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   constexpr FfmaCfg c = kFfmaCfgs[CFG];
-  auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn>;
+  auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn, VB>;
   const int ktab_cap = ffma_ktab_entries(a.k_per_split);
   const size_t smem = ffma_smem_bytes(CFG, a.k_per_split);
   static int configured[64] = {0};
@@ -353,6 +391,14 @@ cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   kern<<<grid, c.threads(), smem, s>>>(a, ktab_cap);
   (void)plan;
   return cudaGetLastError();
+}
+
+template <typename T, int CFG>
+cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
+  if constexpr (sizeof(T) == 4) {
+    if (plan.ffma_vec && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) return launch_cfg_vb<T, CFG, true>(plan, a, s);
+  }
+  return launch_cfg_vb<T, CFG, false>(plan, a, s);
 }
 
 template <typename T>

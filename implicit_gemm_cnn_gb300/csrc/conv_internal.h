@@ -92,6 +92,7 @@ bool tcw_plan(const ConvArgs& a, int sm, WinPlan* w);
 struct Plan {
   conv_plan_info info;
   int ffma_cfg;
+  int ffma_vec;     // pointwise fp32 with whole 16-byte pixel groups: vector B loads
   int k_per_split;  // terms per k range of the split variant
   DwPlan dw;
   TcPlan tc;
