@@ -23,7 +23,7 @@
 // zero weights).  The ResNet-50 stem (7x7 / 2, 3 channels) becomes a 4x4 /1
 // convolution over 12 (padded to 16) channels.
 //
-// Roles (one persistent block per SM, 21 warps):
+// Roles (one persistent block per SM, 22 warps):
 //   * warps 16-19 (producers) stream the block's band of padded input rows:
 //     the rows of x each padded row needs arrive in shared memory by bulk
 //     copies, several rows in flight; the producers then interleave each row's
@@ -31,17 +31,23 @@
 //     for padding, phantom channels and rows outside the image).  The ring is
 //     R positions deep; positions at ring slots below 128 are also written
 //     R slots further on, so that every 128-position window is contiguous;
-//   * warp 20 loads the repacked weights of its channel tile once (one bulk
-//     copy), allocates tensor memory and one lane issues, per tile, kh*kw*C/16
-//     MMAs (kind::f16, M = 128 positions, N = the channel tile, K = 16) whose
-//     A descriptors point at the shifted windows; a commit releases the ring
-//     for the producers and another hands the accumulator to the epilogue;
+//   * warps 20 and 21 issue the MMAs, warp 20 of the even tiles and warp 21 of
+//     the odd ones (one warp issues an MMA every 80-140 cycles, slower than
+//     the tensor pipe runs a 128 x 64 x 16 MMA, so two warps keep it busy):
+//     per tile kh*kw*C/16 MMAs (kind::f16, M = 128 positions, N = the channel
+//     tile, K = 16) whose A descriptors point at the shifted windows; a commit
+//     releases the ring for the producers and another hands the accumulator
+//     to the epilogue.  Warp 20 also loads the repacked weights of its
+//     channel tile once (one bulk copy) and owns the tensor memory;
 //   * warps 0-15 (epilogue): tcgen05.ld of the float32 accumulator (thread =
-//     position; four warps per 32-lane quarter, every fourth 8-column chunk),
+//     position; warps split over the 32-lane quarters and 8-column chunks),
 //     bias, residual, activation in float32, one rounding, and a store of each
-//     valid position's value to NCHW y -- the output is written once.
-// Accumulators are double buffered in tensor memory, so the epilogue of one
-// tile overlaps the MMAs of the next; the producers run up to two tiles ahead.
+//     valid position's value to NCHW y -- the output is written once.  With
+//     two output staging buffers the epilogue works as two groups of eight
+//     warps, one per accumulator, so two tiles are read out at once.
+// Accumulators are double buffered in tensor memory (tile i in buffer i % 2),
+// so a tile's epilogue overlaps the MMAs of the next; the producers run up to
+// two tiles ahead.
 // Every wait is bounded: after the limit the waiting thread flags the block
 // and the device error word, every role drains out, outstanding copies and
 // MMAs are waited for (bounded) and tensor memory is freed before exit.
@@ -71,11 +77,11 @@ namespace {
 
 using namespace tcx;
 
-constexpr int kEpiWarps = 16;  // warps 0-15: tensor-memory lanes 32*(w%4) .., column group w/4
-constexpr int kEpiGroups = kEpiWarps / 4;  // warps per lane quarter: chunks g, g+kEpiGroups, ...
+constexpr int kEpiWarps = 16;  // warps 0-15: one or two groups, see epilogue_role
 constexpr int kProdWarps = 4;  // warps 16-19
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;  // warps 20, 21 issue the MMAs of even, odd tiles
+constexpr int kMmaWarps = 2;
+constexpr int kThreads = (kMmaWarp + kMmaWarps) * 32;
 constexpr int kEpi = kEpiWarps * 32;
 constexpr int kProd = kProdWarps * 32;
 constexpr uint32_t kProdBar = 2;  // named barrier of the producer warps
@@ -99,7 +105,8 @@ __device__ __forceinline__ bool group_all(uint32_t id, uint32_t count, bool pred
   return out != 0;
 }
 __device__ __forceinline__ bool producers_all(bool pred) { return group_all(kProdBar, kProd, pred); }
-constexpr uint32_t kEpiBar = 1;  // named barrier of the epilogue warps
+// named barriers of the epilogue groups: 1 and 3 (0 is __syncthreads, 2 the producers')
+__device__ __forceinline__ uint32_t epi_bar(int g) { return g ? 3u : 1u; }
 
 struct WinLayout {
   uint32_t w_off, ring_off, stg_off, out_off, bias_off, tab_off, bar_off, slot_off, end;
@@ -118,7 +125,7 @@ __host__ __device__ inline WinLayout win_layout(const WinPlan& p) {
   L.stg_off = L.ring_off + align128(static_cast<uint32_t>(p.c16 / 8) * (p.ring + p.mirror) * 16u);
   L.out_off = L.stg_off + align128(static_cast<uint32_t>(p.stages) * p.band_bytes);
   L.bias_off = L.out_off + align128(static_cast<uint32_t>(p.ostages) * p.out_bytes);
-  L.tab_off = L.bias_off + align128(static_cast<uint32_t>(p.nt) * 4u);
+  L.tab_off = L.bias_off + align128(static_cast<uint32_t>(p.nt) * 8u);  // bias: one copy per epilogue group
   L.bar_off = L.tab_off + align128(static_cast<uint32_t>(p.kblocks / 2) * 16u);  // one int4 per MMA
   L.slot_off = L.bar_off + static_cast<uint32_t>(kBarFixed + p.stages) * 8u;
   L.end = L.slot_off + 16u;
@@ -130,9 +137,9 @@ __host__ __device__ inline WinLayout win_layout(const WinPlan& p) {
 struct EpiCtx {
   uint32_t tmem_base, bar0, out_s;  // tensor memory; barriers and output staging (shared addresses)
   uint8_t* out;                     // output staging and bias (shared memory)
-  const float* sbias;
   int t0, ntiles, co0;
   int tpi, rt, wp, wo, ho, nt, out_bytes, ostages;
+  int groups;  // epilogue groups: 2 (group g reads out tiles g, g+2, ... into staging buffer g) or 1
   bool has_b, has_r;
   float alpha, beta;
   const void* bias;  // the layer's bias (has_b), staged into sbias first
@@ -143,70 +150,78 @@ struct EpiCtx {
   const CUtensorMap* rmap;
 };
 
-// The epilogue warps' loop over the block's tiles, for activation ACT.  Warp
-// w reads tensor-memory lanes 32*(w%4) .. +31 (thread = position of the tile)
-// and the 8-column chunks w/4, w/4+4, ..., up to four chunks per
-// tensor-memory wait; bias, residual and activation in float32, one rounding
-// into the tile's staging buffer [channel][row][column]; then one TMA store
-// of the box (wo x rows x channels) to y -- rows past Ho and channels past
-// Cout fall outside y and are not written.  The residual tile arrives in the
-// same buffer by TMA ahead of its tile.  Dropped positions (columns past Wo)
-// are computed and not staged.
+// The epilogue warps' loop over the block's tiles, for activation ACT.  The
+// sixteen warps form e.groups groups; group g reads out tiles g, g + groups,
+// ... (with two groups, group g always meets accumulator g and staging buffer
+// g).  Within a group, warp w reads tensor-memory lanes 32*(w%4) .. +31
+// (thread = position of the tile) and every (warps per quarter)-th 8-column
+// chunk, up to four chunks per tensor-memory wait; bias, residual and
+// activation in float32, one rounding into the tile's staging buffer
+// [channel][row][column]; then one TMA store of the box (wo x rows x channels)
+// to y -- rows past Ho and channels past Cout fall outside y and are not
+// written.  The residual tile arrives in the same buffer by TMA ahead of its
+// tile.  Dropped positions (columns past Wo) are computed and not staged.
 template <typename T, int ACT>
 __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
-  const int tid = threadIdx.x;  // 0 .. kEpi-1
+  const int gw = kEpiWarps / e.groups;  // warps per group
+  const int gthreads = gw * 32;
+  const int g = static_cast<int>(threadIdx.x) / gthreads;
+  const int tid = static_cast<int>(threadIdx.x) - g * gthreads;  // thread within the group
   const int warp = tid >> 5, lane = tid & 31;
+  const int nq = gw / 4;                    // warps per lane quarter
   const int qd = warp & 3, hf = warp >> 2;  // lane quarter, column group
+  const uint32_t gbar = epi_bar(g);
   const int nchunks = e.nt / 8;
   const int plane = e.rt * e.wo;  // elements per channel in a staging buffer
   const int OS = e.ostages;
+  float* sbias = e.sbias_w + g * e.nt;  // the group's copy of the bias
   auto res_bar = [&](int k) { return e.bar0 + 8u * (10 + k); };
-  auto issue_res = [&](int i) {  // thread 0: the residual box of tile t0+i into buffer i % OS
+  auto issue_res = [&](int i) {  // group leader: the residual box of tile t0+i into buffer i % OS
     const int t = e.t0 + i, n = t / e.tpi, j = t - (t / e.tpi) * e.tpi;
     const int ob = i % OS;
     mbar_arrive_expect_tx(res_bar(ob), static_cast<uint32_t>(e.out_bytes));
     tma_load_4d(e.out_s + static_cast<uint32_t>(ob * e.out_bytes), e.rmap, 0, j * e.rt, e.co0, n, res_bar(ob));
   };
-  if (e.has_r && tid == 0 && e.ntiles > 0) issue_res(0);
-  if (e.has_b) {  // ordered before its first use by the first tile's barrier
+  if (e.has_r && tid == 0 && g < e.ntiles) issue_res(g);
+  if (e.has_b) {  // ordered before its first use by the group's first tile barrier
     const T* bias = static_cast<const T*>(e.bias);
-    for (int j = tid; j < e.nt; j += kEpi) e.sbias_w[j] = e.co0 + j < e.c_out ? to_f32<T>(bias[e.co0 + j]) : 0.0f;
+    for (int j = tid; j < e.nt; j += gthreads) sbias[j] = e.co0 + j < e.c_out ? to_f32<T>(bias[e.co0 + j]) : 0.0f;
   }
   // the thread's position in every tile
   const int qq = qd * 32 + lane;
   const int rr = qq / e.wp, c = qq - (qq / e.wp) * e.wp;
   const int soff2 = (rr * e.wo + c) * 2;
-  for (int i = 0; i < e.ntiles; ++i) {
+  for (int i = g; i < e.ntiles; i += e.groups) {
     const int t = e.t0 + i, n = t / e.tpi, j = t - (t / e.tpi) * e.tpi;
     const int b = i & 1, ob = i % OS;
     const uint32_t tfull = e.bar0 + 8u * (5 + b), tempty = e.bar0 + 8u * (7 + b);
     // accumulator ready, residual landed; the barrier also orders the staging
-    // writes after thread 0's wait for the store that last read the buffer
+    // writes after the leader's wait for the store that last read the buffer
     bool okw = wait_phase(tfull, static_cast<uint32_t>(i >> 1) & 1u, e.abort_flag, 2u, false, 64u);
     if (okw && e.has_r) okw = wait_phase(res_bar(ob), static_cast<uint32_t>(i / OS) & 1u, e.abort_flag, 128u);
-    if (!group_all(kEpiBar, kEpi, okw)) break;
+    if (!group_all(gbar, gthreads, okw)) break;
     tc_fence_after();
     const int rows_here = min(e.rt, e.ho - j * e.rt);
     const bool valid = rr < rows_here && c < e.wo;
     T* st = reinterpret_cast<T*>(e.out + ob * e.out_bytes + soff2);
     const uint32_t tb = e.tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + static_cast<uint32_t>(b * e.nt);
-    for (int k0 = hf; k0 < nchunks; k0 += 4 * kEpiGroups) {
+    for (int k0 = hf; k0 < nchunks; k0 += 4 * nq) {
       uint32_t v[4][8];
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
-        if (k0 + kEpiGroups * g < nchunks) tmem_ld8_nowait(tb + (k0 + kEpiGroups * g) * 8, v[g]);
+      for (int q = 0; q < 4; ++q)
+        if (k0 + nq * q < nchunks) tmem_ld8_nowait(tb + (k0 + nq * q) * 8, v[q]);
       tmem_wait_ld();
       if (valid) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int k = k0 + kEpiGroups * g;
+        for (int q = 0; q < 4; ++q) {
+          const int k = k0 + nq * q;
           if (k >= nchunks) break;
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
             const int ch = k * 8 + jj;
             T* dst = st + ch * plane;
-            float x = __uint_as_float(v[g][jj]);
-            if (e.has_b) x = __fadd_rn(x, e.sbias[ch]);
+            float x = __uint_as_float(v[q][jj]);
+            if (e.has_b) x = __fadd_rn(x, sbias[ch]);
             if (e.has_r) x = __fadd_rn(x, to_f32<T>(*dst));
             *dst = from_f32<T>(act_fn<ACT>(x, e.alpha, e.beta));
           }
@@ -216,13 +231,13 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
     tc_fence_before();
     mbar_arrive(tempty);
     fence_proxy_async();  // the staged tile is visible to the TMA store
-    named_sync(kEpiBar, kEpi);
+    named_sync(gbar, gthreads);
     if (tid == 0) {
       tma_store_4d(e.ymap, e.out_s + static_cast<uint32_t>(ob * e.out_bytes), 0, j * e.rt, e.co0, n);
       bulk_commit();
-      if (OS == 2) bulk_wait_read<1>();  // the store of the previous tile has read its buffer
-      else bulk_wait_read<0>();
-      if (e.has_r && i + 1 < e.ntiles) issue_res(i + 1);
+      if (OS > e.groups) bulk_wait_read<1>();  // one group, two buffers: the previous tile's store has read its buffer
+      else bulk_wait_read<0>();                // the group's one buffer has been read
+      if (e.has_r && i + e.groups < e.ntiles) issue_res(i + e.groups);
     }
   }
   if (tid == 0) bulk_wait_all();  // the stores have landed before the block retires
@@ -266,15 +281,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ---- set-up: barriers, bias, MMA table, tensor memory --------------------
+  const int epi_groups = p.ostages == 2 ? 2 : 1;
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(full_bar(i), kProd);
       mbar_init(rel_bar(i), 1);
       mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), kEpi);
+      mbar_init(tempty_bar(i), kEpi / epi_groups);
       mbar_init(res_bar(i), 1);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, kMmaWarps);
     for (int s = 0; s < p.stages; ++s) mbar_init(sfull_bar(s), 1);
     mbar_init(wbar, 1);
     *abort_flag = 0;
@@ -337,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     e.bar0 = bar0;
     e.out_s = smem_u32(sm + L.out_off);
     e.out = sm + L.out_off;
-    e.sbias = sbias;
     e.t0 = t0;
     e.ntiles = ntiles;
     e.co0 = co0;
@@ -349,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     e.nt = p.nt;
     e.out_bytes = p.out_bytes;
     e.ostages = p.ostages;
+    e.groups = epi_groups;
     e.has_b = a.bias != nullptr;
     e.has_r = a.residual != nullptr;
     e.alpha = a.alpha;
@@ -454,16 +470,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_phase(sfull_bar(k % DS), static_cast<uint32_t>(k / DS) & 1u, abort_flag, 8u, true);
     }
   } else if (ntiles > 0) {
-    // ---- MMA issuer: the whole warp runs the loop, one elected lane issues ----
-    // the packed weights come from the repack kernel launched just before
-    // this one (programmatic dependent launch: everything above overlapped it)
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    const uint32_t wbytes = static_cast<uint32_t>(p.kblocks) * p.nt * 16u;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(wbar, wbytes);
-      bulk_load(smem_u32(sm + L.w_off), wpack + static_cast<size_t>(ct) * wbytes, wbytes, wbar);
+    // ---- MMA issuers: warp 20 + mw takes tiles mw, mw + 2, ...; the whole
+    // warp runs the loop, one elected lane issues
+    const int mw = warp - kMmaWarp;
+    if (mw == 0) {
+      // the packed weights come from the repack kernel launched just before
+      // this one (programmatic dependent launch: everything above overlapped it)
+      asm volatile("griddepcontrol.wait;\n" ::: "memory");
+      const uint32_t wbytes = static_cast<uint32_t>(p.kblocks) * p.nt * 16u;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(wbar, wbytes);
+        bulk_load(smem_u32(sm + L.w_off), wpack + static_cast<size_t>(ct) * wbytes, wbytes, wbar);
+      }
+      __syncwarp();
     }
-    __syncwarp();
     bool ok = __all_sync(0xffffffffu, wait_phase(wbar, 0, abort_flag, 1u));
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t idesc = make_idesc(kBf16, p.nt);
@@ -475,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t bd0 = kmajor_desc(smem_u32(sm + L.w_off), static_cast<uint32_t>(p.nt) * 16u, 128u);
     const int4* tab = reinterpret_cast<const int4*>(sm + L.tab_off);
     const int nmma = p.kblocks / 2;
-    for (int i = 0; ok && i < ntiles; ++i) {
+    for (int i = mw; ok && i < ntiles; i += kMmaWarps) {
       const int b = i & 1;
       ok = __all_sync(0xffffffffu, wait_phase(tempty_bar(b), (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, abort_flag, 16u));
       if (!ok) break;
@@ -502,14 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) {
+  if (warp >= kMmaWarp) {
     if (*abort_flag) {
-      mma_commit_elect(drain_bar);  // outstanding MMAs finish before their tensor memory is freed
-      wait_phase(drain_bar, 0, abort_flag, 64u, true);
-      if (ntiles > 0) wait_phase(wbar, 0, abort_flag, 1u, true);  // the weight copy has landed
+      // outstanding MMAs of both issuing warps finish before their tensor
+      // memory is freed
+      mma_commit_elect(drain_bar);
+      if (warp == kMmaWarp) {
+        wait_phase(drain_bar, 0, abort_flag, 64u, true);
+        if (ntiles > 0) wait_phase(wbar, 0, abort_flag, 1u, true);  // the weight copy has landed
+      }
     }
     __syncwarp();
-    tmem_dealloc(tmem_base, cols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem_base, cols);
   }
 }
 
