@@ -114,9 +114,17 @@ struct WinLayout {
 
 __host__ __device__ inline uint32_t align128(uint32_t v) { return (v + 127u) / 128u * 128u; }
 
-// Barriers (8 bytes each, from bar_off): weights, full[2], rel[2], tfull[2],
-// tempty[2], drain, res[2], then one per band stage.
-constexpr int kBarFixed = 12;
+// Barriers (8 bytes each, from bar_off): weights, full[4], rel[4], tfull[4],
+// tempty[4], drain, res[2], then one per band stage.  Tile i uses full and
+// rel i % max(lookahead, 2) (lookahead 1, 2 or 4) and accumulator, tfull and
+// tempty i % (2 or 4): the tiles of one barrier belong to one MMA warp and
+// one epilogue group, in order.
+constexpr int kMaxLookahead = 4;
+constexpr int kMaxAcc = 4;  // accumulators in tensor memory: four when 4 x N columns fit, else two
+constexpr int kBarFull = 1, kBarRel = kBarFull + kMaxLookahead, kBarTfull = kBarRel + kMaxLookahead;
+constexpr int kBarTempty = kBarTfull + kMaxAcc, kBarDrain = kBarTempty + kMaxAcc, kBarRes = kBarDrain + 1;
+__host__ __device__ inline int tmem_accs(int nt) { return kMaxAcc * nt <= 512 ? kMaxAcc : 2; }
+constexpr int kBarFixed = kBarRes + 2;
 
 __host__ __device__ inline WinLayout win_layout(const WinPlan& p) {
   WinLayout L;
@@ -140,6 +148,7 @@ struct EpiCtx {
   int t0, ntiles, co0;
   int tpi, rt, wp, wo, ho, nt, out_bytes, ostages;
   int groups;  // epilogue groups: 2 (group g reads out tiles g, g+2, ... into staging buffer g) or 1
+  int accs;    // accumulators in tensor memory (tile i in accumulator i % accs)
   bool has_b, has_r;
   float alpha, beta;
   const void* bias;  // the layer's bias (has_b), staged into sbias first
@@ -175,7 +184,7 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
   const int plane = e.rt * e.wo;  // elements per channel in a staging buffer
   const int OS = e.ostages;
   float* sbias = e.sbias_w + g * e.nt;  // the group's copy of the bias
-  auto res_bar = [&](int k) { return e.bar0 + 8u * (10 + k); };
+  auto res_bar = [&](int k) { return e.bar0 + 8u * (kBarRes + k); };
   auto issue_res = [&](int i) {  // group leader: the residual box of tile t0+i into buffer i % OS
     const int t = e.t0 + i, n = t / e.tpi, j = t - (t / e.tpi) * e.tpi;
     const int ob = i % OS;
@@ -193,11 +202,17 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
   const int soff2 = (rr * e.wo + c) * 2;
   for (int i = g; i < e.ntiles; i += e.groups) {
     const int t = e.t0 + i, n = t / e.tpi, j = t - (t / e.tpi) * e.tpi;
-    const int b = i & 1, ob = i % OS;
-    const uint32_t tfull = e.bar0 + 8u * (5 + b), tempty = e.bar0 + 8u * (7 + b);
+    const int b = i % e.accs, ob = i % OS;
+    const uint32_t tfull = e.bar0 + 8u * (kBarTfull + b), tempty = e.bar0 + 8u * (kBarTempty + b);
     // accumulator ready, residual landed; the barrier also orders the staging
     // writes after the leader's wait for the store that last read the buffer
-    bool okw = wait_phase(tfull, static_cast<uint32_t>(i >> 1) & 1u, e.abort_flag, 2u, false, 64u);
+    // (without a residual that wait comes here, in the shadow of the MMAs,
+    // rather than straight after the store)
+    if (!e.has_r && tid == 0) {
+      if (OS > e.groups) bulk_wait_read<1>();  // one group, two buffers: the store of tile i-2
+      else bulk_wait_read<0>();                // the group's one buffer
+    }
+    bool okw = wait_phase(tfull, static_cast<uint32_t>(i / e.accs) & 1u, e.abort_flag, 2u, false, 64u);
     if (okw && e.has_r) okw = wait_phase(res_bar(ob), static_cast<uint32_t>(i / OS) & 1u, e.abort_flag, 128u);
     if (!group_all(gbar, gthreads, okw)) break;
     tc_fence_after();
@@ -216,14 +231,24 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
         for (int q = 0; q < 4; ++q) {
           const int k = k0 + nq * q;
           if (k >= nchunks) break;
+          // the chunk's bias values are loaded before any of its stores: the
+          // compiler cannot tell the staging stores from the bias copy
+          T* dst = st + k * 8 * plane;
+          float add[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) add[jj] = 0.0f;
+          if (e.has_b) {
+            const float4 b0 = *reinterpret_cast<const float4*>(sbias + k * 8);
+            const float4 b1 = *reinterpret_cast<const float4*>(sbias + k * 8 + 4);
+            add[0] = b0.x, add[1] = b0.y, add[2] = b0.z, add[3] = b0.w;
+            add[4] = b1.x, add[5] = b1.y, add[6] = b1.z, add[7] = b1.w;
+          }
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const int ch = k * 8 + jj;
-            T* dst = st + ch * plane;
             float x = __uint_as_float(v[q][jj]);
-            if (e.has_b) x = __fadd_rn(x, sbias[ch]);
-            if (e.has_r) x = __fadd_rn(x, to_f32<T>(*dst));
-            *dst = from_f32<T>(act_fn<ACT>(x, e.alpha, e.beta));
+            if (e.has_b) x = __fadd_rn(x, add[jj]);
+            if (e.has_r) x = __fadd_rn(x, to_f32<T>(dst[jj * plane]));
+            dst[jj * plane] = from_f32<T>(act_fn<ACT>(x, e.alpha, e.beta));
           }
         }
       }
@@ -235,9 +260,11 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
     if (tid == 0) {
       tma_store_4d(e.ymap, e.out_s + static_cast<uint32_t>(ob * e.out_bytes), 0, j * e.rt, e.co0, n);
       bulk_commit();
-      if (OS > e.groups) bulk_wait_read<1>();  // one group, two buffers: the previous tile's store has read its buffer
-      else bulk_wait_read<0>();                // the group's one buffer has been read
-      if (e.has_r && i + e.groups < e.ntiles) issue_res(i + e.groups);
+      if (e.has_r) {  // the next residual tile of this buffer goes in as soon as the store has read it
+        if (OS > e.groups) bulk_wait_read<1>();
+        else bulk_wait_read<0>();
+        if (i + e.groups < e.ntiles) issue_res(i + e.groups);
+      }
     }
   }
   if (tid == 0) bulk_wait_all();  // the stores have landed before the block retires
@@ -252,13 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = sm_raw + ((128u - (smem_u32(sm_raw) & 127u)) & 127u);  // the launch adds 128 bytes of slack
   const WinLayout L = win_layout(p);
   const uint32_t bar0 = smem_u32(sm + L.bar_off);
-  auto full_bar = [&](int i) { return bar0 + 8u * (1 + i); };    // tile's input rows are in the ring
-  auto rel_bar = [&](int i) { return bar0 + 8u * (3 + i); };     // tile's MMAs done: ring reusable
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (5 + b); };   // accumulator b ready
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (7 + b); };  // accumulator b read out
+  auto full_bar = [&](int k) { return bar0 + 8u * (kBarFull + k); };     // tile's input rows are in the ring
+  auto rel_bar = [&](int k) { return bar0 + 8u * (kBarRel + k); };       // tile's MMAs done: ring reusable
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (kBarTfull + b); };   // accumulator b ready
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (kBarTempty + b); }; // accumulator b read out
   const uint32_t wbar = bar0;  // the raw weight copy landed
-  const uint32_t drain_bar = bar0 + 8u * 9;
-  auto res_bar = [&](int k) { return bar0 + 8u * (10 + k); };    // residual tile k landed
+  const uint32_t drain_bar = bar0 + 8u * kBarDrain;
+  auto res_bar = [&](int k) { return bar0 + 8u * (kBarRes + k); };       // residual tile k landed
   auto sfull_bar = [&](int s) { return bar0 + 8u * (kBarFixed + s); };  // staged band s landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L.slot_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.slot_off + 4);
@@ -272,8 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t1 = static_cast<int>(static_cast<long long>(p.tiles) * (part + 1) / p.parts);
   const int ntiles = t1 - t0;
   const int co0 = ct * p.nt;
+  const int TA = tmem_accs(p.nt);
   uint32_t cols = 32;
-  while (cols < 2u * p.nt) cols <<= 1;
+  while (cols < static_cast<uint32_t>(TA * p.nt)) cols <<= 1;
   // tile t: rows j*rt .. of image n (t = n*tpi + j); its first position
   auto tile_q0 = [&](int t) {
     const int n = t / p.tpi, j = t - (t / p.tpi) * p.tpi;
@@ -283,11 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, bias, MMA table, tensor memory --------------------
   const int epi_groups = p.ostages == 2 ? 2 : 1;
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(full_bar(i), kProd);
-      mbar_init(rel_bar(i), 1);
+    for (int k = 0; k < kMaxLookahead; ++k) {
+      mbar_init(full_bar(k), kProd);
+      mbar_init(rel_bar(k), 1);
+    }
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(tfull_bar(i), 1);
       mbar_init(tempty_bar(i), kEpi / epi_groups);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(res_bar(i), 1);
     }
     mbar_init(drain_bar, kMmaWarps);
@@ -317,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // weights are laid out, so the two overlap
   const int ptid = tid - kEpi;
   const int pw = ptid >> 5;
-  const int DS = p.stages, SB = p.band;
+  const int DS = p.stages, SB = p.band, LA = p.lookahead, NB = LA < 2 ? 2 : LA;
   auto row_end = [&](int i) {  // padded rows (exclusive) the valid outputs of tile t0+i read
     const int t = t0 + i, n = t / p.tpi, j = t - (t / p.tpi) * p.tpi;
     return n * p.hp + min((j + 1) * p.rt, p.ho) + (p.khp - 1) * a.dh;
@@ -365,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     e.out_bytes = p.out_bytes;
     e.ostages = p.ostages;
     e.groups = epi_groups;
+    e.accs = TA;
     e.has_b = a.bias != nullptr;
     e.has_r = a.residual != nullptr;
     e.alpha = a.alpha;
@@ -403,9 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int step_cb = (kProd % (p.wp * nb)) / p.wp, step_c = kProd % p.wp;
     bool ok = true;
     for (int i = 0; ok && i < ntiles; ++i) {
-      if (i >= p.lookahead) {
-        const int j = i - p.lookahead;
-        ok = producers_all(wait_phase(rel_bar(j & 1), static_cast<uint32_t>(j >> 1) & 1u, abort_flag, 4u));
+      if (i >= LA) {
+        const int j = i - LA;
+        ok = producers_all(wait_phase(rel_bar(j % NB), static_cast<uint32_t>(j / NB) & 1u, abort_flag, 4u));
         if (!ok) break;
       }
       const int re = row_end(i);
@@ -463,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       fence_proxy_async();  // ring writes visible to the tensor cores
-      mbar_arrive(full_bar(i & 1));
+      mbar_arrive(full_bar(i % NB));
     }
     if (pw == 0) {  // copies still in flight land before the block retires
       for (int k = k_fill; k < k_issue; ++k)
@@ -496,10 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int4* tab = reinterpret_cast<const int4*>(sm + L.tab_off);
     const int nmma = p.kblocks / 2;
     for (int i = mw; ok && i < ntiles; i += kMmaWarps) {
-      const int b = i & 1;
-      ok = __all_sync(0xffffffffu, wait_phase(tempty_bar(b), (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, abort_flag, 16u));
+      const int b = i % TA;
+      ok = __all_sync(0xffffffffu, wait_phase(tempty_bar(b), (static_cast<uint32_t>(i / TA) & 1u) ^ 1u, abort_flag, 16u));
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, wait_phase(full_bar(i & 1), static_cast<uint32_t>(i >> 1) & 1u, abort_flag, 32u));
+      ok = __all_sync(0xffffffffu, wait_phase(full_bar(i % NB), static_cast<uint32_t>(i / NB) & 1u, abort_flag, 32u));
       if (!ok) break;
       tc_fence_after();
       const uint32_t d = tmem_base + static_cast<uint32_t>(b * p.nt);
@@ -512,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_f16_elect(d, ad0 + static_cast<uint64_t>(pos + tv.y), bd0 + static_cast<uint64_t>(tv.z), idesc,
                       e > 0 ? 1u : 0u);
       }
-      mma_commit_elect(rel_bar(i & 1));
+      mma_commit_elect(rel_bar(i % NB));
       mma_commit_elect(tfull_bar(b));
     }
   }
@@ -661,27 +694,31 @@ bool fit_smem(const ConvArgs& a, WinPlan* p) {
     p->nt = nt;
     p->co_tiles = (a.c_out + nt - 1) / nt;
     p->out_bytes = nt * p->rt * p->wo * 2;
-    for (int la = 2; la >= 1; --la) {
-      for (int os = 2; os >= 1; --os) {
-        for (int sb = sb_pref; sb >= 1; --sb) {
-          if (row_bytes * sb >= (1 << 20)) continue;  // transaction count of one mbarrier phase
-          for (int ds = 4; ds >= 2; --ds) {
-            // rows the producers may write beyond the oldest window still in
-            // use: la tiles of rt rows (one of them across an image's dropped
-            // rows), the kernel's reach and a band
-            const long long rows = static_cast<long long>(la - 1) * (p->rt + p->hp - p->ho) + p->rt +
-                                   static_cast<long long>(p->khp - 1) * a.dh + sb;
-            const long long ring = (rows * p->wp + 7) / 8 * 8;
-            if (ring + 128 > 16000) continue;  // the descriptors' 14-bit offsets
-            p->ring = static_cast<int>(ring);
-            p->mirror = 128;  // windows start anywhere: 128 slots written twice
-            p->lookahead = la;
-            p->ostages = os;
-            p->band = sb;
-            p->band_bytes = static_cast<int>(row_bytes * sb);
-            p->stages = ds;
-            if (win_layout(*p).end + 128 <= kTcMaxSmem) return true;
-          }
+    // (lookahead, output buffers): deeper lookahead first, but two output
+    // buffers (two epilogue groups) before a lookahead past two, and a
+    // lookahead past two only with full bands and stages
+    static const int kChoice[][2] = {{4, 2}, {2, 2}, {2, 1}, {1, 2}, {1, 1}};
+    for (const auto& choice : kChoice) {
+      const int la = choice[0], os = choice[1];
+      for (int sb = sb_pref; sb >= 1; --sb) {
+        if (row_bytes * sb >= (1 << 20)) continue;  // transaction count of one mbarrier phase
+        for (int ds = 4; ds >= 2; --ds) {
+          if (la > 2 && (sb != sb_pref || ds != 4)) continue;
+          // rows the producers may write beyond the oldest window still in
+          // use: la tiles of rt rows (one of them across an image's dropped
+          // rows), the kernel's reach and a band
+          const long long rows = static_cast<long long>(la - 1) * (p->rt + p->hp - p->ho) + p->rt +
+                                 static_cast<long long>(p->khp - 1) * a.dh + sb;
+          const long long ring = (rows * p->wp + 7) / 8 * 8;
+          if (ring + 128 > 16000) continue;  // the descriptors' 14-bit offsets
+          p->ring = static_cast<int>(ring);
+          p->mirror = 128;  // windows start anywhere: 128 slots written twice
+          p->lookahead = la;
+          p->ostages = os;
+          p->band = sb;
+          p->band_bytes = static_cast<int>(row_bytes * sb);
+          p->stages = ds;
+          if (win_layout(*p).end + 128 <= kTcMaxSmem) return true;
         }
       }
     }
