@@ -236,7 +236,7 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
           T* dst = st + k * 8 * plane;
           float add[8];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) add[jj] = 0.0f;
+          for (int jj = 0; jj < 8; ++jj) add[jj] = -0.0f;  // x + -0 == x for every x
           if (e.has_b) {
             const float4 b0 = *reinterpret_cast<const float4*>(sbias + k * 8);
             const float4 b1 = *reinterpret_cast<const float4*>(sbias + k * 8 + 4);
@@ -246,7 +246,7 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
             float x = __uint_as_float(v[q][jj]);
-            if (e.has_b) x = __fadd_rn(x, add[jj]);
+            x = __fadd_rn(x, add[jj]);
             if (e.has_r) x = __fadd_rn(x, to_f32<T>(dst[jj * plane]));
             dst[jj * plane] = from_f32<T>(act_fn<ACT>(x, e.alpha, e.beta));
           }
@@ -270,7 +270,9 @@ __device__ __forceinline__ void epilogue_role(const EpiCtx e) {
   if (tid == 0) bulk_wait_all();  // the stores have landed before the block retires
 }
 
-template <typename T, int PH>
+// One kernel per (element type, phase split, activation): each carries only
+// its own epilogue, which keeps the code the warps run close together.
+template <typename T, int PH, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_tcw(const ConvArgs a, const WinPlan p, const uint8_t* __restrict__ wpack,
               const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
@@ -408,23 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     e.abort_flag = abort_flag;
     e.ymap = &ymap;
     e.rmap = &rmap;
-    switch (a.act) {
-#define CONV_EPI_CASE(A)          \
-  case A:                         \
-    epilogue_role<T, A>(e);       \
-    break;
-      CONV_EPI_CASE(ACT_RELU)
-      CONV_EPI_CASE(ACT_SILU)
-      CONV_EPI_CASE(ACT_SIGMOID)
-      CONV_EPI_CASE(ACT_TANH)
-      CONV_EPI_CASE(ACT_HARD_SWISH)
-      CONV_EPI_CASE(ACT_HARD_SIGMOID)
-      CONV_EPI_CASE(ACT_CLIP)
-      CONV_EPI_CASE(ACT_LEAKY_RELU)
-#undef CONV_EPI_CASE
-      default:
-        epilogue_role<T, ACT_IDENTITY>(e);
-    }
+    epilogue_role<T, ACT>(e);
   } else if (warp < kEpiWarps + kProdWarps) {
     // ---- producers: bands of input rows by TMA, channels interleaved into the ring
     const int nb = p.c16 / 8;
@@ -649,16 +635,34 @@ cudaError_t launch_win(const WinPlan& p, const ConvArgs& a, void* scratch, cudaS
   rmap = ymap;
   if (a.residual && !encode_nchw<T>(&rmap, a.residual, p.wo, p.ho, a.c_out, a.n, p.wo, p.rt, p.nt))
     return cudaErrorInvalidValue;
-  auto kern = igemm_tcw<T, PH>;
+  auto kern = igemm_tcw<T, PH, ACT_IDENTITY>;
+  switch (a.act) {
+#define CONV_TCW_CASE(A)           \
+  case A:                          \
+    kern = igemm_tcw<T, PH, A>;    \
+    break;
+    CONV_TCW_CASE(ACT_RELU)
+    CONV_TCW_CASE(ACT_SILU)
+    CONV_TCW_CASE(ACT_SIGMOID)
+    CONV_TCW_CASE(ACT_TANH)
+    CONV_TCW_CASE(ACT_HARD_SWISH)
+    CONV_TCW_CASE(ACT_HARD_SIGMOID)
+    CONV_TCW_CASE(ACT_CLIP)
+    CONV_TCW_CASE(ACT_LEAKY_RELU)
+#undef CONV_TCW_CASE
+    default:
+      break;
+  }
   auto repack = tcw_repack<PH>;
-  static int configured[64] = {0};
+  static int configured[9][64] = {{0}};  // per activation and device: shared memory opted in
+  const int act = a.act >= 0 && a.act < 9 ? a.act : 0;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && configured[dev] < static_cast<int>(p.smem)) {
+  if (dev < 64 && configured[act][dev] < static_cast<int>(p.smem)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
     if (err != cudaSuccess) return err;
-    configured[dev] = static_cast<int>(p.smem);
+    configured[act][dev] = static_cast<int>(p.smem);
   }
   const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
   const int rblocks = static_cast<int>(std::min<long long>((units + 255) / 256, 1024));
