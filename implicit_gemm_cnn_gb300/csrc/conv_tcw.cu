@@ -310,45 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return (n * p.hp + j * p.rt) * p.wp;
   };
 
-  // ---- set-up: barriers, bias, MMA table, tensor memory --------------------
-  const int epi_groups = p.ostages == 2 ? 2 : 1;
-  if (tid == 0) {
-    for (int k = 0; k < kMaxLookahead; ++k) {
-      mbar_init(full_bar(k), kProd);
-      mbar_init(rel_bar(k), 1);
-    }
-    for (int i = 0; i < kMaxAcc; ++i) {
-      mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), kEpi / epi_groups);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(res_bar(i), 1);
-    }
-    mbar_init(drain_bar, kMmaWarps);
-    for (int s = 0; s < p.stages; ++s) mbar_init(sfull_bar(s), 1);
-    mbar_init(wbar, 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), cols);
-    // per MMA of a tile: the window shift of its tap, the k-block offset of
-    // its channel pair in the ring, and its weights' offset (16-byte units)
-    int4* tab = reinterpret_cast<int4*>(sm + L.tab_off);
-    const int pairs = p.c16 / 16, nmma = p.kblocks / 2;
-    for (int e = lane; e < nmma; e += 32) {
-      const int tap = e / pairs, m = e - (e / pairs) * pairs;
-      const int u = tap / p.kwp, v = tap - (tap / p.kwp) * p.kwp;
-      tab[e] = make_int4(u * a.dh * p.wp + v * a.dw, 2 * m * (p.ring + p.mirror), (2 * e) * p.nt, 0);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  // ---- producers' band state; their first bands are requested before the
-  // weights are laid out, so the two overlap
+  // ---- producers' band state.  Their first bands are requested first thing,
+  // before the rest of the set-up and the weights, so the input's trip from
+  // memory overlaps all of it: lane 0 of the first producer warp sets up the
+  // band barriers itself and issues the copies.
   const int ptid = tid - kEpi;
   const int pw = ptid >> 5;
   const int DS = p.stages, SB = p.band, LA = p.lookahead, NB = LA < 2 ? 2 : LA;
@@ -377,11 +342,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (++bi * SB >= p.hp) { bi = 0; ++ni; }
     ++k_issue;
   };
-  if (warp == kEpiWarps)
+  if (warp == kEpiWarps) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+      for (int st = 0; st < DS; ++st) mbar_init(sfull_bar(st), 1);
+      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncwarp();
     for (int k = 0; k < DS && band_row0(ni, bi) < rho_end; ++k) issue();
+  }
+
+  // ---- set-up: barriers, bias, MMA table, tensor memory --------------------
+  const int epi_groups = p.ostages == 2 ? 2 : 1;
+  if (tid == 0) {
+    for (int k = 0; k < kMaxLookahead; ++k) {
+      mbar_init(full_bar(k), kProd);
+      mbar_init(rel_bar(k), 1);
+    }
+    for (int i = 0; i < kMaxAcc; ++i) {
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), kEpi / epi_groups);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(res_bar(i), 1);
+    }
+    mbar_init(drain_bar, kMmaWarps);
+    mbar_init(wbar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), cols);
+    // per MMA of a tile: the window shift of its tap, the k-block offset of
+    // its channel pair in the ring, and its weights' offset (16-byte units)
+    int4* tab = reinterpret_cast<int4*>(sm + L.tab_off);
+    const int pairs = p.c16 / 16, nmma = p.kblocks / 2;
+    for (int e = lane; e < nmma; e += 32) {
+      const int tap = e / pairs, m = e - (e / pairs) * pairs;
+      const int u = tap / p.kwp, v = tap - (tap / p.kwp) * p.kwp;
+      tab[e] = make_int4(u * a.dh * p.wp + v * a.dw, 2 * m * (p.ring + p.mirror), (2 * e) * p.nt, 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
 
   if (warp < kEpiWarps) {
-    // ---- epilogue: the activation is chosen once; each case is its own loop
+    // ---- epilogue
     EpiCtx e;
     e.tmem_base = tmem_base;
     e.bar0 = bar0;
