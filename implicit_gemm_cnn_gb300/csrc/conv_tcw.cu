@@ -23,21 +23,21 @@
 // zero weights).  The ResNet-50 stem (7x7 / 2, 3 channels) becomes a 4x4 /1
 // convolution over 12 (padded to 16) channels.
 //
-// Roles (one persistent block per SM, 22 warps):
-//   * warps 16-19 (producers) stream the block's band of padded input rows:
+// Roles (one persistent block per SM, 24 warps):
+//   * warps 16-21 (producers) stream the block's band of padded input rows:
 //     the rows of x each padded row needs arrive in shared memory by bulk
 //     copies, several rows in flight; the producers then interleave each row's
 //     channels into the ring (16 bytes per position and 8-channel block; zero
 //     for padding, phantom channels and rows outside the image).  The ring is
 //     R positions deep; positions at ring slots below 128 are also written
 //     R slots further on, so that every 128-position window is contiguous;
-//   * warps 20 and 21 issue the MMAs, warp 20 of the even tiles and warp 21 of
+//   * warps 22 and 23 issue the MMAs, warp 22 of the even tiles and warp 23 of
 //     the odd ones (one warp issues an MMA every 80-140 cycles, slower than
 //     the tensor pipe runs a 128 x 64 x 16 MMA, so two warps keep it busy):
 //     per tile kh*kw*C/16 MMAs (kind::f16, M = 128 positions, N = the channel
 //     tile, K = 16) whose A descriptors point at the shifted windows; a commit
 //     releases the ring for the producers and another hands the accumulator
-//     to the epilogue.  Warp 20 also loads the repacked weights of its
+//     to the epilogue.  Warp 22 also loads the repacked weights of its
 //     channel tile once (one bulk copy) and owns the tensor memory;
 //   * warps 0-15 (epilogue): tcgen05.ld of the float32 accumulator (thread =
 //     position; warps split over the 32-lane quarters and 8-column chunks),
@@ -78,8 +78,8 @@ namespace {
 using namespace tcx;
 
 constexpr int kEpiWarps = 16;  // warps 0-15: one or two groups, see epilogue_role
-constexpr int kProdWarps = 4;  // warps 16-19
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;  // warps 20, 21 issue the MMAs of even, odd tiles
+constexpr int kProdWarps = 6;  // warps 16-21
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;  // warps 22, 23 issue the MMAs of even, odd tiles
 constexpr int kMmaWarps = 2;
 constexpr int kThreads = (kMmaWarp + kMmaWarps) * 32;
 constexpr int kEpi = kEpiWarps * 32;
@@ -426,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = sm + L.ring_off;
     int filled = rho0;  // rows below this are in the ring
     // the thread's next unit is kProd units on: step_br rows, step_cb blocks, step_c columns
+    const int cstride = PH * SB * p.vw;  // one staged channel
     const int step_br = kProd / (p.wp * nb);
     const int step_cb = (kProd % (p.wp * nb)) / p.wp, step_c = kProd % p.wp;
     bool ok = true;
@@ -451,21 +452,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int base_slot = static_cast<int>((static_cast<long long>(brow0) * p.wp) % R);
         int br = first + ptid / per_row, cb = (ptid % per_row) / p.wp, c = ptid % p.wp;
         for (int e = ptid; e < units; e += kProd) {
+          // value j of the unit: channel cb*8 + j (PH 1), or channel
+          // cb*2 + j/4, phase row (j/2)%2, phase column j%2 (PH 2); staged at
+          // [channel][PH*SB rows][vw columns]
           uint16_t v[8];
+          if constexpr (PH == 1) {
+            const int wc = c - a.pl;
+            const uint16_t* src = sg + (cb * 8 * SB + br) * p.vw + wc;
+            const int nv = static_cast<unsigned>(wc) < static_cast<unsigned>(p.vw) ? min(8, a.cg - cb * 8) : 0;
+            if (nv == 8) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            int ch, ph, wc;
-            if constexpr (PH == 1) {
-              ch = cb * 8 + j;
-              ph = 0;
-              wc = c - a.pl;
+              for (int j = 0; j < 8; ++j) v[j] = src[j * cstride];
             } else {
-              ch = cb * 2 + (j >> 2);
-              ph = (j >> 1) & 1;
-              wc = 2 * c + (j & 1) - a.pl;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = j < nv ? src[j * cstride] : static_cast<uint16_t>(0);
             }
-            const bool okv = wc >= 0 && wc < p.vw && ch < a.cg;
-            v[j] = okv ? sg[(ch * (PH * SB) + PH * br + ph) * p.vw + wc] : static_cast<uint16_t>(0);
+          } else {
+            const int wc = 2 * c - a.pl;
+            const uint16_t* src = sg + (cb * 2 * 2 * SB + 2 * br) * p.vw + wc;
+            const bool ok0 = static_cast<unsigned>(wc) < static_cast<unsigned>(p.vw);
+            const bool ok1 = static_cast<unsigned>(wc + 1) < static_cast<unsigned>(p.vw);
+            const int nch = min(2, a.cg - cb * 2);  // real channels of the unit
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const bool okv = ((j & 1) ? ok1 : ok0) && (j >> 2) < nch;
+              v[j] = okv ? src[(j >> 2) * cstride + ((j >> 1) & 1) * p.vw + (j & 1)] : static_cast<uint16_t>(0);
+            }
           }
           int slot = base_slot + br * p.wp + c;  // < 2R: R exceeds a band's positions
           if (slot >= R) slot -= R;
@@ -497,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_phase(sfull_bar(k % DS), static_cast<uint32_t>(k / DS) & 1u, abort_flag, 8u, true);
     }
   } else if (ntiles > 0) {
-    // ---- MMA issuers: warp 20 + mw takes tiles mw, mw + 2, ...; the whole
+    // ---- MMA issuers: warp kMmaWarp + mw takes tiles mw, mw + 2, ...; the whole
     // warp runs the loop, one elected lane issues
     const int mw = warp - kMmaWarp;
     if (mw == 0) {
