@@ -127,6 +127,9 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
     split = static_cast<int>((s.K + len - 1) / len);
   }
   if (split <= 1) { split = 1; len = s.K; }
+  // grouped layers with few channels per group: input rows staged once per
+  // item instead of a per-k gather (no split k there)
+  if (split == 1) gd_plan(p, s.ho, s.wo, &out->gd);
   out->ffma_cfg = bi;
   // pointwise fp32 (1x1, stride 1, no pad, dilation 1) whose planes hold whole
   // groups of 4 pixels: 16-byte B copies (x's alignment is checked at launch)
@@ -141,6 +144,11 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   out->info.ctas = ctas * split;
   out->info.scratch_bytes = split > 1 ? static_cast<uint64_t>(split) * s.y_elems * sizeof(float) : 0;
   out->k_per_split = static_cast<int>(len);
+  if (out->gd.ok) {
+    out->info.tile_m = static_cast<int>(s.mg);
+    out->info.tile_n = static_cast<int>(kGdRows * s.wo);
+    out->info.ctas = std::min<long long>(out->gd.items, 3LL * sm);
+  }
 }
 
 bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
@@ -380,6 +388,11 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
              variant_name(i.variant), w.nt, w.ph, w.ph, w.khp, w.kwp, static_cast<long long>(i.gemm_k),
              w.kblocks * 8, w.hp, w.wp, w.ring, w.mirror, w.band, w.stages, w.lookahead,
              static_cast<long long>(i.ctas), sm);
+  } else if (i.variant == CONV_VARIANT_IGEMM_FFMA && plan.gd.ok) {
+    snprintf(buf, len,
+             "%s grouped: input rows staged once per (group, image, %d output rows), %d staged rows of %d, "
+             "8co x 4px per thread, items=%lld sms=%d",
+             variant_name(i.variant), kGdRows, plan.gd.rows_in, plan.gd.pitch, static_cast<long long>(plan.gd.items), sm);
   } else if (i.variant == CONV_VARIANT_DEPTHWISE && plan.dw.narrow) {
     snprintf(buf, len, "%s one warp per plane, window in registers, double-buffered planes sms=%d",
              variant_name(i.variant), sm);

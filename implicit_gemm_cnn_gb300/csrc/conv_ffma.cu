@@ -24,6 +24,10 @@
 // tensor-core kernel does not take) are converted to fp32 as they are staged.
 // The window offsets of the block's k range are decoded once into a table in
 // shared memory (offset in the input plane set, row and column displacement).
+#include <string.h>
+
+#include <algorithm>
+
 #include "conv_internal.h"
 
 namespace conv {
@@ -369,6 +373,175 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
   }
 }
 
+// ---- grouped layers, input rows staged once per item ------------------------
+// The implicit GEMM of one group (M = Cout/groups, K = (Cin/groups)*k*k,
+// N = pixels) with its B operand read in place: item = (group, image, kGdRows
+// output rows); the group's input rows (zero rows above and below the image,
+// zero columns left and right, written once) and its weights, transposed to
+// [channel][tap][output channel], arrive in shared memory by cp.async, the
+// next item's while this one is computed.  A thread holds 8 output channels
+// x 4 consecutive pixels of one row; each k term (channel c, tap u, v) is 4
+// staged inputs at the tap's offset, two broadcast float4 weight loads and 32
+// FMAs, k in (c, u, v) order into one float32 chain per output, then the fused
+// epilogue and one 16-byte store per output channel.
+template <int K, int ACT>
+__global__ void __launch_bounds__(kGdThreads, 3) grouped_direct(const ConvArgs a, const GdPlan g) {
+  extern __shared__ __align__(16) float gsm[];
+  const int tid = threadIdx.x;
+  const int xs_floats = a.cg * g.rows_in * g.pitch;
+  const int buf_floats = xs_floats + a.cg * K * K * a.mg;
+  for (int i = tid; i < 2 * buf_floats; i += kGdThreads) gsm[i] = 0.0f;  // borders stay zero
+  __syncthreads();
+  const float* __restrict__ x = static_cast<const float*>(a.x);
+  const float* __restrict__ wt = static_cast<const float*>(a.wt);
+  const float* __restrict__ bias = static_cast<const float*>(a.bias);
+  const float* __restrict__ res = static_cast<const float*>(a.residual);
+  float* __restrict__ y = static_cast<float*>(a.y);
+  const bool vec16 = (a.w & 3) == 0 && (a.hw & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  const int q_per_row = vec16 ? a.w / 4 : a.w;  // copies per staged row
+  const int taps = K * K;
+  auto decode = [&](long long item, int* n, int* gi, int* oh0) {
+    const int rt = static_cast<int>(item % g.row_tiles);
+    const long long rest = item / g.row_tiles;
+    *n = static_cast<int>(rest % a.n);
+    *gi = static_cast<int>(rest / a.n);
+    *oh0 = rt * kGdRows;
+  };
+  auto stage = [&](long long item, float* buf) {
+    int n, gi, oh0;
+    decode(item, &n, &gi, &oh0);
+    const float* xg = x + (static_cast<long long>(n) * a.c_in + static_cast<long long>(gi) * a.cg) * a.hw;
+    const int copies = a.cg * g.rows_in * q_per_row;
+    for (int e = tid; e < copies; e += kGdThreads) {
+      const int c = e / (g.rows_in * q_per_row);
+      const int rem = e - c * (g.rows_in * q_per_row);
+      const int rr = rem / q_per_row, qq = rem - (rem / q_per_row) * q_per_row;
+      const int ih = oh0 - a.pt + rr;
+      const bool ok = static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);  // else zeros
+      float* dst = buf + (c * g.rows_in + rr) * g.pitch + g.cofs + (vec16 ? 4 * qq : qq);
+      const float* src = ok ? xg + static_cast<long long>(c) * a.hw + static_cast<long long>(ih) * a.w +
+                                  (vec16 ? 4 * qq : qq)
+                            : x;
+      if (vec16) cp_async16(dst, src, ok);
+      else cp_async4(dst, src, ok);
+    }
+    // weights of the group: OIHW rows (contiguous over channel and tap) into
+    // [channel * taps + tap][output channel]
+    float* ws = buf + xs_floats;
+    const int ck = a.cg * taps;
+    const float* wg = wt + static_cast<long long>(gi) * a.mg * ck;
+    for (int e = tid; e < a.mg * ck; e += kGdThreads) {
+      const int m = e / ck, r = e - (e / ck) * ck;
+      cp_async4(ws + r * a.mg + m, wg + e, true);
+    }
+  };
+  const long long first = blockIdx.x, step = gridDim.x;
+  if (first < g.items) stage(first, gsm);
+  cp_async_commit();
+  const int groups4 = a.wo / 4, halves = a.mg / 8;
+  const int units = kGdRows * groups4 * halves;
+  int k = 0;
+  for (long long item = first; item < g.items; item += step, ++k) {
+    float* buf = gsm + (k & 1) * buf_floats;
+    if (item + step < g.items) stage(item + step, gsm + ((k + 1) & 1) * buf_floats);
+    cp_async_commit();
+    cp_async_wait<1>();  // this item's copies (the next item's may still fly)
+    __syncthreads();
+    int n, gi, oh0;
+    decode(item, &n, &gi, &oh0);
+    const float* xs = buf;
+    const float* ws = buf + xs_floats;
+    for (int u_ = tid; u_ < units; u_ += kGdThreads) {
+      const int h8 = u_ % halves, pg = u_ / halves;
+      const int r = pg / groups4, col0 = 4 * (pg - (pg / groups4) * groups4);
+      if (oh0 + r >= a.ho) continue;
+      float acc[8][4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
+      const float* xb = xs + r * g.pitch + g.cofs - a.pl + col0;
+      const float* wb = ws + 8 * h8;
+      for (int c = 0; c < a.cg; ++c) {
+        const float* xc = xb + c * g.rows_in * g.pitch;
+        const float* wc = wb + c * taps * a.mg;
+#pragma unroll
+        for (int u = 0; u < K; ++u)
+#pragma unroll
+          for (int v = 0; v < K; ++v) {
+            const float* xp = xc + u * a.dh * g.pitch + v * a.dw;
+            const float xv[4] = {xp[0], xp[1], xp[2], xp[3]};
+            const float4 w0 = *reinterpret_cast<const float4*>(wc + (u * K + v) * a.mg);
+            const float4 w1 = *reinterpret_cast<const float4*>(wc + (u * K + v) * a.mg + 4);
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[j][q] = fmaf(wv[j], xv[q], acc[j][q]);
+          }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int co = gi * a.mg + 8 * h8 + j;
+        const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo +
+                              static_cast<long long>(oh0 + r) * a.wo + col0;
+        const float b = bias ? bias[co] : 0.0f;
+        float rv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (res) {
+          const float4 t = *reinterpret_cast<const float4*>(res + out);
+          rv[0] = t.x, rv[1] = t.y, rv[2] = t.z, rv[3] = t.w;
+        }
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float t = acc[j][q];
+          if (bias) t = __fadd_rn(t, b);
+          if (res) t = __fadd_rn(t, rv[q]);
+          v[q] = act_fn<ACT>(t, a.alpha, a.beta);
+        }
+        *reinterpret_cast<float4*>(y + out) = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+    __syncthreads();  // this buffer is refilled two items from now
+  }
+  cp_async_wait<0>();
+}
+
+template <int K>
+cudaError_t launch_gd_k(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
+  auto kern = grouped_direct<K, ACT_IDENTITY>;
+  switch (a.act) {
+#define CONV_GD_CASE(A)             \
+  case A:                           \
+    kern = grouped_direct<K, A>;    \
+    break;
+    CONV_GD_CASE(ACT_RELU)
+    CONV_GD_CASE(ACT_SILU)
+    CONV_GD_CASE(ACT_SIGMOID)
+    CONV_GD_CASE(ACT_TANH)
+    CONV_GD_CASE(ACT_HARD_SWISH)
+    CONV_GD_CASE(ACT_HARD_SIGMOID)
+    CONV_GD_CASE(ACT_CLIP)
+    CONV_GD_CASE(ACT_LEAKY_RELU)
+#undef CONV_GD_CASE
+    default:
+      break;
+  }
+  const GdPlan& g = plan.gd;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(g.smem));
+  if (err != cudaSuccess) return err;
+  int per_sm = 0, dev = 0, sms = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGdThreads, g.smem);
+  if (err != cudaSuccess) return err;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const long long blocks = std::min<long long>(g.items, static_cast<long long>(sms) * std::max(per_sm, 1));
+  kern<<<static_cast<unsigned>(blocks), kGdThreads, g.smem, s>>>(a, g);
+  return cudaGetLastError();
+}
+
 template <typename T, int CFG, bool VB>
 cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   constexpr FfmaCfg c = kFfmaCfgs[CFG];
@@ -439,7 +612,32 @@ size_t ffma_smem_bytes(int cfg, int k_per_block) {
          static_cast<size_t>(ffma_ktab_entries(k_per_block)) * sizeof(int2);
 }
 
+bool gd_plan(const conv_problem* p, long long ho, long long wo, GdPlan* g) {
+  memset(g, 0, sizeof(*g));
+  if (p->dtype != CONV_F32 || p->groups < 2 || p->stride_h != 1 || p->stride_w != 1) return false;
+  if (p->kh != p->kw || (p->kh != 3 && p->kh != 5) || wo % 4 != 0) return false;
+  const long long cg = p->c_in / p->groups, mg = p->c_out / p->groups;
+  if (mg % 8 != 0 || mg > 64 || cg > 64) return false;
+  g->k = static_cast<int>(p->kh);
+  g->rows_in = static_cast<int>(kGdRows + (p->kh - 1) * p->dil_h);
+  g->cofs = static_cast<int>((p->pad_left + 3) / 4 * 4);
+  const long long reach = g->cofs - p->pad_left + wo + (p->kw - 1) * p->dil_w;  // columns a tap reads
+  const long long pitch = std::max<long long>(reach, g->cofs + p->w);
+  g->pitch = static_cast<int>((pitch + 3) / 4 * 4);
+  g->row_tiles = static_cast<int>((ho + kGdRows - 1) / kGdRows);
+  g->items = p->n * p->groups * g->row_tiles;
+  const long long buf = cg * g->rows_in * g->pitch + cg * p->kh * p->kw * mg;
+  g->smem = static_cast<size_t>(2 * buf * 4);
+  if (g->smem > 100 * 1024) return false;  // at least two blocks per SM
+  g->ok = 1;
+  return true;
+}
+
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s) {
+  // the grouped path stores (and reads the residual) 16 bytes at a time
+  if (plan.gd.ok && dtype == CONV_F32 && reinterpret_cast<uintptr_t>(a.y) % 16 == 0 &&
+      (a.residual == nullptr || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0))
+    return plan.gd.k == 3 ? launch_gd_k<3>(plan, a, s) : launch_gd_k<5>(plan, a, s);
   switch (dtype) {
     case CONV_F32: return launch_typed<float>(plan, a, s);
     case CONV_F16: return launch_typed<__half>(plan, a, s);

@@ -89,8 +89,28 @@ struct WinPlan {
 };
 bool tcw_plan(const ConvArgs& a, int sm, WinPlan* w);
 
+// Grouped layers with few channels per group on CUDA cores (float32, stride
+// 1, square 3x3 or 5x5 kernel, output rows a multiple of 4, Cout/groups a
+// multiple of 8): per work item (image, group, kGdRows output rows) the
+// group's input rows and weights are staged once and every k term (channel,
+// tap) reads its B values from the staged rows at the tap's offset.
+constexpr int kGdThreads = 128;
+constexpr int kGdRows = 8;
+struct GdPlan {
+  int ok;           // the path applies
+  int k;            // kernel size (3 or 5)
+  int rows_in;      // staged input rows per item: kGdRows + (k - 1) * dh
+  int pitch;        // floats per staged row (a multiple of 4)
+  int cofs;         // staged column of input column 0 (a multiple of 4, >= the left pad)
+  int row_tiles;    // ceil(Ho / kGdRows)
+  long long items;  // n * groups * row_tiles
+  size_t smem;      // two buffers of (input rows + weights)
+};
+bool gd_plan(const conv_problem* p, long long ho, long long wo, GdPlan* g);
+
 struct Plan {
   conv_plan_info info;
+  GdPlan gd;
   int ffma_cfg;
   int ffma_vec;     // pointwise fp32 with whole 16-byte pixel groups: vector B loads
   int k_per_split;  // terms per k range of the split variant

@@ -148,6 +148,12 @@ EDGE = [
      True, False),
     ("win_s2_3x3_c64", (2, 64, 16, 16), (32, 64, 3, 3), dict(stride=2, pads=1), True, True),
     ("wide_cin_1x1", (1, 1024, 4, 4), (64, 1024, 1, 1), dict(), True, False),
+    # grouped fp32 with input rows staged once per item (Cout/groups a multiple of 8, Wo of 4)
+    ("gd_dil2_res", (2, 32, 13, 12), (32, 16, 3, 3), dict(pads=2, dilation=2, groups=2, act="silu"), True, True),
+    ("gd_5x5_asym", (1, 24, 10, 16), (24, 8, 5, 5), dict(pads=(2, 1, 2, 3), groups=3, act="hard_swish"),
+     True, False),
+    ("gd_wide_nobias", (1, 64, 6, 40), (64, 8, 3, 3), dict(pads=1, groups=8), False, False),
+    ("gd_pad_left2", (2, 16, 9, 16), (16, 8, 3, 3), dict(pads=(1, 2, 1, 0), groups=2, act="relu"), True, True),
 ]
 
 
@@ -169,6 +175,9 @@ def test_edge_cases(case, dtype, path):
     if name.startswith("win_") and dtype != "f32" and path == "auto":
         desc = conv.conv_describe_variant(p)
         assert desc.startswith("igemm_tcgen05_window"), desc
+    if name.startswith("gd_") and dtype == "f32":
+        desc = conv.conv_describe_variant(p)
+        assert desc.startswith("igemm_ffma grouped"), desc
     y = run_gpu(inp, flags=flags, **g)
     assert tuple(y.shape) == (xs[0], ws[0], ho, wo)
     out = check_full(inp, dtype, y, **g)
