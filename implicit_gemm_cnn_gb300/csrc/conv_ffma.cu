@@ -24,6 +24,12 @@
 // tensor-core kernel does not take) are converted to fp32 as they are staged.
 // The window offsets of the block's k range are decoded once into a table in
 // shared memory (offset in the input plane set, row and column displacement).
+//
+// Two special cases skip the per-k gather: a pointwise layer whose planes
+// hold whole 4-pixel groups copies its B tile with 16-byte cp.async, and a
+// grouped layer with few channels per group (grouped_direct) stages each
+// group's input rows once per work item and reads every k term from them at
+// the tap's offset.
 #include <string.h>
 
 #include <algorithm>

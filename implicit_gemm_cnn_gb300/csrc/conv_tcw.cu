@@ -45,9 +45,10 @@
 //     valid position's value to NCHW y -- the output is written once.  With
 //     two output staging buffers the epilogue works as two groups of eight
 //     warps, one per accumulator, so two tiles are read out at once.
-// Accumulators are double buffered in tensor memory (tile i in buffer i % 2),
-// so a tile's epilogue overlaps the MMAs of the next; the producers run up to
-// two tiles ahead.
+// Accumulators live in tensor memory, four of them when four channel tiles fit
+// the 512 columns, else two (tile i in accumulator i % that), so a tile's
+// epilogue overlaps the MMAs of the next ones; the producers run up to four
+// tiles ahead (as deep as shared memory holds the ring).
 // Every wait is bounded: after the limit the waiting thread flags the block
 // and the device error word, every role drains out, outstanding copies and
 // MMAs are waited for (bounded) and tensor memory is freed before exit.
