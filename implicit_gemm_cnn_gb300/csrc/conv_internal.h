@@ -83,6 +83,7 @@ struct WinPlan {
   int ostages;     // output staging buffers (1 or 2)
   int tiles;       // tiles over all images
   int parts;       // position ranges (blocks per channel tile)
+  int tq, tr;      // tiles per range: tq, and one more for the first tr ranges
   int ctas;        // blocks
   size_t smem;     // dynamic shared memory bytes
   size_t w_bytes;  // scratch: the repacked weights

@@ -298,9 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int ct = static_cast<int>(blockIdx.x) % p.co_tiles;
   const int part = static_cast<int>(blockIdx.x) / p.co_tiles;
-  const int t0 = static_cast<int>(static_cast<long long>(p.tiles) * part / p.parts);
-  const int t1 = static_cast<int>(static_cast<long long>(p.tiles) * (part + 1) / p.parts);
-  const int ntiles = t1 - t0;
+  // the block's tiles: tq each, one more for the first tr blocks (no division
+  // here: every warp runs this before its role)
+  const int t0 = part * p.tq + min(part, p.tr);
+  const int ntiles = p.tq + (part < p.tr ? 1 : 0);
   const int co0 = ct * p.nt;
   const int TA = tmem_accs(p.nt);
   uint32_t cols = 32;
@@ -322,12 +323,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = t0 + i, n = t / p.tpi, j = t - (t / p.tpi) * p.tpi;
     return n * p.hp + min((j + 1) * p.rt, p.ho) + (p.khp - 1) * a.dh;
   };
-  const int rho0 = tile_q0(t0) / p.wp;
-  const int rho_end = ntiles > 0 ? row_end(ntiles - 1) : rho0;
+  // (the divisions below run on the producer warps only)
+  const bool producer = warp >= kEpiWarps && warp < kMmaWarp;
+  int rho0 = 0, rho_end = 0;
   const uint32_t stg_s = smem_u32(sm + L.stg_off);
   // bands: rows [b*SB, min((b+1)*SB, hp)) of one image; the next band to
   // load is (ni, bi), the band being consumed is (nf, bf)
-  int ni = rho0 / p.hp, bi = (rho0 - (rho0 / p.hp) * p.hp) / SB;
+  int ni = 0, bi = 0;
+  if (producer) {
+    rho0 = tile_q0(t0) / p.wp;
+    rho_end = ntiles > 0 ? row_end(ntiles - 1) : rho0;
+    ni = rho0 / p.hp;
+    bi = (rho0 - ni * p.hp) / SB;
+  }
   int nf = ni, bf = bi;
   int k_issue = 0, k_fill = 0;
   auto band_row0 = [&](int n, int b) { return n * p.hp + b * SB; };
@@ -825,6 +833,8 @@ bool tcw_plan(const ConvArgs& a, int sm, WinPlan* out) {
   }
   if (!ok) return false;
   p.parts = static_cast<int>(std::min<long long>(p.tiles, std::max(1, sm / p.co_tiles)));
+  p.tq = p.tiles / p.parts;
+  p.tr = p.tiles % p.parts;
   p.ctas = p.parts * p.co_tiles;
   p.w_bytes = static_cast<size_t>(p.co_tiles) * p.kblocks * p.nt * 16;
   p.smem = std::max<size_t>(win_layout(p).end + 128, kOneBlockPerSm);
