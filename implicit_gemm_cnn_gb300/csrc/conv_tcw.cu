@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
               const __grid_constant__ CUtensorMap rmap) {
   extern __shared__ uint8_t sm_raw[];
+  if (threadIdx.x == kEpi)  // the input's tensor map is fetched while every warp runs its prologue
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
   uint8_t* sm = sm_raw + ((128u - (smem_u32(sm_raw) & 127u)) & 127u);  // the launch adds 128 bytes of slack
   const WinLayout L = win_layout(p);
   const uint32_t bar0 = smem_u32(sm + L.bar_off);
@@ -331,10 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // load is (ni, bi), the band being consumed is (nf, bf)
   int ni = 0, bi = 0;
   if (producer) {
-    rho0 = tile_q0(t0) / p.wp;
+    const int n0 = t0 / p.tpi, j0 = t0 - n0 * p.tpi;  // first tile: image n0, rows j0*rt ..
+    rho0 = n0 * p.hp + j0 * p.rt;
     rho_end = ntiles > 0 ? row_end(ntiles - 1) : rho0;
-    ni = rho0 / p.hp;
-    bi = (rho0 - ni * p.hp) / SB;
+    ni = n0;
+    bi = j0 * p.rt / SB;
   }
   int nf = ni, bf = bi;
   int k_issue = 0, k_fill = 0;
@@ -353,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (warp == kEpiWarps) {
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
       for (int st = 0; st < DS; ++st) mbar_init(sfull_bar(st), 1);
       asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
