@@ -195,3 +195,21 @@ def test_force_ffma_flag(lib):
 def test_plan_rejects_bad_sm_count(lib):
     p = _layer_problem(LAYERS["small_3x3_f32"])
     assert _status(conv.conv_plan, p, 0) == "CONV_ERR_ARG"
+
+
+def test_grouped_layers_take_the_staged_rows_path(lib):
+    """fp32 grouped layers with Cout/groups a multiple of 8 (at most 64), stride
+    1, a square 3x3 or 5x5 kernel and Wo a multiple of 4 run the grouped path:
+    tile = the group's output channels x 8 output rows, no scratch, no split."""
+    p = conv.make_problem((16, 512, 28, 28), (512, 16, 3, 3), dtype="f32", pads=2, dilation=2, groups=32,
+                          act="silu", has_bias=True)
+    plan = conv.conv_plan(p, 152)
+    assert plan["variant_name"] == "igemm_ffma" and plan["split_k"] == 1 and plan["scratch_bytes"] == 0
+    assert (plan["tile_m"], plan["tile_n"]) == (16, 8 * 28)
+    # outside the path: Cout/groups of 4, stride 2, Wo of 15, fp16
+    for xs, ws, g, dt in [((2, 16, 12, 12), (8, 8, 3, 3), dict(pads=1, groups=2), "f32"),
+                          ((2, 16, 12, 12), (16, 8, 3, 3), dict(pads=1, groups=2, stride=2), "f32"),
+                          ((2, 16, 12, 15), (16, 8, 3, 3), dict(pads=1, groups=2), "f32")]:
+        q = conv.conv_plan(conv.make_problem(xs, ws, dtype=dt, **g), 152)
+        assert q["tile_n"] != 8 * conv.conv_output_shape(conv.make_problem(xs, ws, dtype=dt, **g))[1], q
+
