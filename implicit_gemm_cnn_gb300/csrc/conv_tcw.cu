@@ -716,44 +716,51 @@ cudaError_t launch_win(const WinPlan& p, const ConvArgs& a, void* scratch, cudaS
 }
 
 // Channel tile, lookahead, output buffers, band height and band stages that
-// fit shared memory for the geometry already in `p` (widest tile, deepest
-// lookahead, two output buffers, bands of about 8 KB, most bands in flight
-// first), with the ring depth each choice needs.  False if none fits.
+// fit shared memory for the geometry already in `p` (two output buffers
+// first -- the epilogue's two groups are worth more than lookahead or the
+// widest tile -- then the widest tile, deepest lookahead, bands of about
+// 8 KB, most bands in flight), with the ring depth each choice needs.  False
+// if none fits.
 bool fit_smem(const ConvArgs& a, WinPlan* p) {
   const long long row_bytes = static_cast<long long>(p->vw) * p->ph * a.cg * 2;  // one padded row's box
   const int sb_max = static_cast<int>(std::min<long long>({8, p->hp, 256 / p->ph}));
   int sb_pref = 1;
   while (sb_pref < sb_max && row_bytes * sb_pref < 8192) ++sb_pref;
   const int nt0 = static_cast<int>(std::min<long long>((a.c_out + 15) / 16 * 16, 256));
-  for (int nt = nt0; nt >= 16; nt = nt > 16 ? std::max(16, (nt / 2 + 15) / 16 * 16) : 0) {
-    p->nt = nt;
-    p->co_tiles = (a.c_out + nt - 1) / nt;
-    p->out_bytes = nt * p->rt * p->wo * 2;
-    // (lookahead, output buffers): deeper lookahead first, but two output
-    // buffers (two epilogue groups) before a lookahead past two, and a
-    // lookahead past two only with full bands and stages
-    static const int kChoice[][2] = {{4, 2}, {2, 2}, {2, 1}, {1, 2}, {1, 1}};
-    for (const auto& choice : kChoice) {
-      const int la = choice[0], os = choice[1];
-      for (int sb = sb_pref; sb >= 1; --sb) {
-        if (row_bytes * sb >= (1 << 20)) continue;  // transaction count of one mbarrier phase
-        for (int ds = 4; ds >= 2; --ds) {
-          if (la > 2 && (sb != sb_pref || ds != 4)) continue;
-          // rows the producers may write beyond the oldest window still in
-          // use: la tiles of rt rows (one of them across an image's dropped
-          // rows), the kernel's reach and a band
-          const long long rows = static_cast<long long>(la - 1) * (p->rt + p->hp - p->ho) + p->rt +
-                                 static_cast<long long>(p->khp - 1) * a.dh + sb;
-          const long long ring = (rows * p->wp + 7) / 8 * 8;
-          if (ring + 128 > 16000) continue;  // the descriptors' 14-bit offsets
-          p->ring = static_cast<int>(ring);
-          p->mirror = 128;  // windows start anywhere: 128 slots written twice
-          p->lookahead = la;
-          p->ostages = os;
-          p->band = sb;
-          p->band_bytes = static_cast<int>(row_bytes * sb);
-          p->stages = ds;
-          if (win_layout(*p).end + 128 <= kTcMaxSmem) return true;
+  // first pass: two output buffers (two epilogue groups) with a channel tile
+  // of 64 or more, at any lookahead; then anything that fits
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int nt = nt0; nt >= 16; nt = nt > 16 ? std::max(16, (nt / 2 + 15) / 16 * 16) : 0) {
+      p->nt = nt;
+      p->co_tiles = (a.c_out + nt - 1) / nt;
+      p->out_bytes = nt * p->rt * p->wo * 2;
+      // (lookahead, output buffers): deeper lookahead first, but two output
+      // buffers (two epilogue groups) before a lookahead past two, and a
+      // lookahead past two only with full bands and stages
+      static const int kChoice[][2] = {{4, 2}, {2, 2}, {2, 1}, {1, 2}, {1, 1}};
+      for (const auto& choice : kChoice) {
+        const int la = choice[0], os = choice[1];
+        if (pass == 0 && (os != 2 || nt < 64)) continue;
+        for (int sb = sb_pref; sb >= 1; --sb) {
+          if (row_bytes * sb >= (1 << 20)) continue;  // transaction count of one mbarrier phase
+          for (int ds = 4; ds >= 2; --ds) {
+            if (la > 2 && (sb != sb_pref || ds != 4)) continue;
+            // rows the producers may write beyond the oldest window still in
+            // use: la tiles of rt rows (one of them across an image's dropped
+            // rows), the kernel's reach and a band
+            const long long rows = static_cast<long long>(la - 1) * (p->rt + p->hp - p->ho) + p->rt +
+                                   static_cast<long long>(p->khp - 1) * a.dh + sb;
+            const long long ring = (rows * p->wp + 7) / 8 * 8;
+            if (ring + 128 > 16000) continue;  // the descriptors' 14-bit offsets
+            p->ring = static_cast<int>(ring);
+            p->mirror = 128;  // windows start anywhere: 128 slots written twice
+            p->lookahead = la;
+            p->ostages = os;
+            p->band = sb;
+            p->band_bytes = static_cast<int>(row_bytes * sb);
+            p->stages = ds;
+            if (win_layout(*p).end + 128 <= kTcMaxSmem) return true;
+          }
         }
       }
     }
