@@ -213,3 +213,55 @@ def test_grouped_layers_take_the_staged_rows_path(lib):
         q = conv.conv_plan(conv.make_problem(xs, ws, dtype=dt, **g), 152)
         assert q["tile_n"] != 8 * conv.conv_output_shape(conv.make_problem(xs, ws, dtype=dt, **g))[1], q
 
+
+
+def test_planner_rules_on_random_shapes(lib):
+    """Seeded random problems: every valid one plans, deterministically, and
+    the variant respects what each kernel takes -- depthwise for one input
+    channel per group, the shifted-window kernel only for 16-bit, one group,
+    stride 1 or 2 (dilation 1) and rows of 8-element multiples,
+    tensor-core variants never for fp32, split k only with its planes in
+    scratch."""
+    import random
+    rng = random.Random(20260101)
+    seen = set()
+    for _ in range(300):
+        dt = rng.choice(["f32", "f16", "bf16"])
+        groups = rng.choice([1, 1, 1, 2, 4, 8])
+        cg = rng.choice([1, 3, 4, 8, 16, 24, 64])
+        mg = rng.choice([1, 2, 8, 16, 40])
+        k = rng.choice([1, 3, 5, 7])
+        kh, kw = (k, k) if rng.random() < 0.8 else (k, rng.choice([1, 3]))
+        s = rng.choice([1, 1, 2, 3])
+        d = rng.choice([1, 1, 2])
+        n, h, w = rng.choice([1, 2, 4]), rng.randint(kh, 40), rng.randint(kw, 48)
+        pads = tuple(rng.randint(0, 3) for _ in range(4))
+        p = conv.make_problem((n, cg * groups, h, w), (mg * groups, cg, kh, kw), dtype=dt, stride=s, pads=pads,
+                              dilation=d, groups=groups, has_bias=rng.random() < 0.5,
+                              has_residual=rng.random() < 0.3)
+        try:
+            ho, wo = conv.conv_output_shape(p)
+        except conv.ConvError:
+            continue  # the kernel does not fit the padded input
+        plan = conv.conv_plan(p, 152)
+        assert conv.conv_plan(p, 152) == plan
+        v = plan["variant_name"]
+        seen.add(v)
+        assert (plan["ho"], plan["wo"]) == (ho, wo)
+        if cg == 1:
+            assert v == "depthwise_halo", (p, plan)
+        if dt == "f32":
+            assert v in ("igemm_ffma", "igemm_ffma_split_k", "depthwise_halo"), (p, plan)
+        if v == "igemm_tcgen05_window":
+            # rows of 8-element multiples: the output's, or for a 1x1 layer
+            # read as it lies, a row length dividing the plane
+            pointwise = kh == kw == 1 and s == 1 and not any(pads)
+            assert dt != "f32" and groups == 1, (p, plan)
+            assert wo % 8 == 0 or (pointwise and (ho * wo) % 8 == 0), (p, plan)
+            assert s == 1 or (s == 2 and d == 1), (p, plan)
+            assert plan["scratch_bytes"] > 0 and plan["scratch_bytes"] % 16 == 0
+        if v == "igemm_ffma_split_k":
+            assert plan["split_k"] > 1 and plan["scratch_bytes"] == plan["split_k"] * n * mg * groups * ho * wo * 4
+        else:
+            assert plan["split_k"] == 1
+    assert {"igemm_ffma", "depthwise_halo", "igemm_tcgen05_window"} <= seen, seen
