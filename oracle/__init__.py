@@ -194,7 +194,8 @@ def ulp(y: np.ndarray, dtype: str) -> np.ndarray:
     representable values there; the subnormal spacing below the normal range)."""
     mant_bits, min_exp = {"f32": (23, -126), "f16": (10, -14), "bf16": (7, -126)}[dtype]
     a = np.abs(np.asarray(y, dtype=np.float64))
+    # zero and the subnormals share the spacing of the smallest normal binade
     with np.errstate(divide="ignore"):
-        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+        e = np.floor(np.log2(np.where(a > 0, a, 2.0 ** min_exp)))
     e = np.maximum(e, min_exp)
     return np.ldexp(1.0, (e - mant_bits).astype(np.int64))

@@ -1,57 +1,79 @@
 """Second, independent brute force of the convolution sum: unfold then multiply.
 
-TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  This is a numpy
-restatement of "Convolutions", section 2.4 (convolution as a matrix multiply:
-cols = im2col(X) with one column of C*kh*kw taps per output position, then
-Y = W cols per group) and the im2col description of its section 3 (a tap
-index table over the zero-padded input, gathered in one step).  It is written
-separately from the C nested loop so that the two can check each other:
-padding here is a zero-padded copy, taps are gathered by index arrays, the
-sum is a float64 matrix product.  Pads are per side (top, left, bottom,
-right) and stride / dilation per axis.
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  "Convolutions",
+section 2.4, writes the convolution as one matrix product per group:
+``Y_g = W_g . cols_g``, where ``W_g`` is the group's weights flattened to
+(Cout/G) x (Cin/G * kh * kw) and ``cols_g`` has one column per output position
+and one row per tap (channel c, kernel row u, kernel column v).  This module
+builds that column matrix from its definition, one element at a time,
+
+    cols[(c*kh + u)*kw + v, oh*Wo + ow] = x[c, oh*sh - pt + u*dh, ow*sw - pl + v*dw]
+                                          (0 where that position is outside x),
+
+and then multiplies in float64 with a library matrix product.  It shares
+nothing with the C nested loop: here the taps become a matrix and the sum
+is numpy's; there the sum runs over (c, u, v) in a fixed order.  Pads are per
+side (top, left, bottom, right), stride and dilation per axis.
 """
 from __future__ import annotations
 
 import numpy as np
 
 
-def _extent(size, k, pad_begin, pad_end, stride, dil):
-    return (size + pad_begin + pad_end - dil * (k - 1) - 1) // stride + 1
+def output_extent(size: int, k: int, pad_begin: int, pad_end: int, stride: int, dil: int) -> int:
+    """Window starts 0, s, 2s, ... of a padded axis whose span d(k-1)+1 still
+    fits ("Convolutions", section 2.1)."""
+    span = dil * (k - 1) + 1
+    padded = size + pad_begin + pad_end
+    count = 0
+    start = 0
+    while start + span <= padded:
+        count += 1
+        start += stride
+    return count
 
 
-def unfold(x: np.ndarray, kh: int, kw: int, stride, pads, dilation) -> np.ndarray:
-    """(B, C, H, W) float64 -> (B, C*kh*kw, Ho*Wo) columns, rows ordered (c, u, v)."""
-    b, c, h, w = x.shape
+def column_matrix(x: np.ndarray, kh: int, kw: int, stride, pads, dilation):
+    """One image's channels (C, H, W) -> the (C*kh*kw, Ho*Wo) column matrix."""
+    c_n, h, w = x.shape
     pt, pl, pb, pr = pads
     sh, sw = stride
     dh, dw = dilation
-    ho = _extent(h, kh, pt, pb, sh, dh)
-    wo = _extent(w, kw, pl, pr, sw, dw)
-    xp = np.zeros((b, c, h + pt + pb, w + pl + pr), dtype=np.float64)
-    xp[:, :, pt:pt + h, pl:pl + w] = x
-    u, v = np.meshgrid(np.arange(kh), np.arange(kw), indexing="ij")
-    i, j = np.meshgrid(np.arange(ho), np.arange(wo), indexing="ij")
-    rows = i.reshape(1, -1) * sh + u.reshape(-1, 1) * dh   # (kh*kw, P)
-    cols = j.reshape(1, -1) * sw + v.reshape(-1, 1) * dw   # (kh*kw, P)
-    gathered = xp[:, :, rows, cols]                          # (B, C, kh*kw, P)
-    return gathered.reshape(b, c * kh * kw, ho * wo), ho, wo
+    ho = output_extent(h, kh, pt, pb, sh, dh)
+    wo = output_extent(w, kw, pl, pr, sw, dw)
+    cols = np.zeros((c_n * kh * kw, ho * wo), dtype=np.float64)
+    for c in range(c_n):
+        for u in range(kh):
+            for v in range(kw):
+                row = (c * kh + u) * kw + v
+                for oh in range(ho):
+                    ih = oh * sh - pt + u * dh
+                    if ih < 0 or ih >= h:
+                        continue  # the whole output row reads padding for this tap
+                    for ow in range(wo):
+                        iw = ow * sw - pl + v * dw
+                        if 0 <= iw < w:
+                            cols[row, oh * wo + ow] = x[c, ih, iw]
+    return cols, ho, wo
 
 
 def conv2d_sum(x: np.ndarray, w: np.ndarray, stride=(1, 1), pads=(0, 0, 0, 0),
                dilation=(1, 1), groups=1) -> np.ndarray:
-    """The raw convolution sum (no bias, residual or activation) in float64,
-    one matrix product per group."""
+    """The raw convolution sum (no bias, residual or activation) in float64:
+    for every image and group, the weight matrix times the column matrix."""
     x = np.asarray(x, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)
     b, cin, h, wd = x.shape
     cout, cin_g, kh, kw = w.shape
     assert cin_g * groups == cin and cout % groups == 0
     mg = cout // groups
-    out = None
-    for g in range(groups):
-        cols, ho, wo = unfold(x[:, g * cin_g:(g + 1) * cin_g], kh, kw, stride, pads, dilation)
-        wmat = w[g * mg:(g + 1) * mg].reshape(mg, -1)       # (Cout/g, Cin/g*kh*kw)
-        if out is None:
-            out = np.empty((b, cout, ho * wo), dtype=np.float64)
-        out[:, g * mg:(g + 1) * mg] = np.einsum("ok,bkp->bop", wmat, cols)
+    ho = output_extent(h, kh, pads[0], pads[2], stride[0], dilation[0])
+    wo = output_extent(wd, kw, pads[1], pads[3], stride[1], dilation[1])
+    out = np.zeros((b, cout, ho * wo), dtype=np.float64)
+    for img in range(b):
+        for g in range(groups):
+            cols, _, _ = column_matrix(x[img, g * cin_g:(g + 1) * cin_g], kh, kw, stride, pads,
+                                       dilation)
+            wmat = w[g * mg:(g + 1) * mg].reshape(mg, cin_g * kh * kw)
+            out[img, g * mg:(g + 1) * mg] = wmat @ cols
     return out.reshape(b, cout, ho, wo)

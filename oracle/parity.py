@@ -50,6 +50,12 @@ def bound(ref: dict, dtype: str, act: str, alpha=0.0, beta=0.0, bias_abs=None, r
             + ulp(y_ref, dtype))
 
 
+def _max_not_nan(a) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    a = a[~np.isnan(a)]
+    return float(a.max()) if a.size else 0.0
+
+
 def compare(y, ref: dict, dtype: str, act: str, alpha=0.0, beta=0.0, bias=None,
             residual=None, co_index=None) -> dict:
     """Check ``y`` (numpy, same layout as ``ref['y']``: float32 or uint16 bits)
@@ -81,8 +87,8 @@ def compare(y, ref: dict, dtype: str, act: str, alpha=0.0, beta=0.0, bias=None,
     out = {
         "ok": not bool(bad.any()),
         "n_bad": int(bad.sum()),
-        "max_scaled_err": float(np.nanmax(scaled)) if scaled.size else 0.0,
-        "worst": float(np.nanmax(err / lim)) if err.size else 0.0,
+        "max_scaled_err": _max_not_nan(scaled),
+        "worst": _max_not_nan(err / lim),
     }
     if bad.any():
         i = np.unravel_index(int(np.argmax(bad)), bad.shape)
