@@ -11,7 +11,9 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "conv_internal.h"
 
@@ -308,7 +310,23 @@ const char* variant_name(int v) {
   }
 }
 
+std::mutex g_smem_mu;
+std::map<std::pair<const void*, int>, size_t> g_smem_optin;  // (kernel, device) -> bytes
+
 }  // namespace
+
+cudaError_t conv::opt_in_smem(const void* func, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;  // no opt-in needed
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  size_t& cur = g_smem_optin[std::make_pair(func, dev)];
+  if (cur >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (err == cudaSuccess) cur = bytes;
+  return err;
+}
 
 extern "C" {
 
@@ -504,7 +522,8 @@ conv_status conv_device_error(uint32_t* word, int32_t reset) {
 // Some callers cannot call cudaMalloc: code running where allocation is not
 // permitted (a plug-in of a host framework that owns every allocation, a
 // real-time path that must not touch the allocator, a caller with no CUDA
-// runtime of its own beyond this library).  For them the split-k planes live
+// runtime of its own beyond this library).  For them the scratch -- the
+// split-k planes, or the shifted-window variant's repacked weights -- lives
 // in one fixed device array that the library owns.  It is reserved on every
 // GPU that loads this library and kept until the process exits.
 static __device__ __align__(256) unsigned char g_fixed_scratch[CONV_FIXED_SCRATCH_BYTES];
@@ -526,6 +545,21 @@ extern "C" conv_status conv_forward_fixed_scratch(const conv_problem* p, const v
   Plan plan;
   st = make_plan(p, sm, &plan, nullptr);
   if (st != CONV_OK) return st;
+  // When the plan's scratch does not fit the array, a variant that needs none
+  // may still run the problem: the gather tensor-core kernel instead of the
+  // shifted-window one (no repacked weights), or k unsplit (no partial
+  // planes), unless the caller forced the split.
+  conv_problem q = *p;
+  const int forced_split = static_cast<int>((p->flags & CONV_FLAG_SPLIT_K_MASK) >> CONV_FLAG_SPLIT_K_SHIFT);
+  if (plan.info.scratch_bytes > CONV_FIXED_SCRATCH_BYTES && plan.info.variant == CONV_VARIANT_IGEMM_TC_WINDOW)
+    q.flags |= CONV_FLAG_NO_WINDOW;
+  else if (plan.info.scratch_bytes > CONV_FIXED_SCRATCH_BYTES &&
+           plan.info.variant == CONV_VARIANT_IGEMM_FFMA_SPLIT && forced_split == 0)
+    q.flags |= CONV_FLAG_NO_SPLIT_K;
+  if (q.flags != p->flags) {
+    st = make_plan(&q, sm, &plan, nullptr);
+    if (st != CONV_OK) return st;
+  }
   if (plan.info.scratch_bytes > CONV_FIXED_SCRATCH_BYTES) return CONV_ERR_SCRATCH;
   void* addr = nullptr;
   {
@@ -542,5 +576,5 @@ extern "C" conv_status conv_forward_fixed_scratch(const conv_problem* p, const v
     }
     addr = g_fixed_addr[dev];
   }
-  return conv_forward(p, x, w, bias, residual, y, addr, CONV_FIXED_SCRATCH_BYTES, stream);
+  return conv_forward(&q, x, w, bias, residual, y, addr, CONV_FIXED_SCRATCH_BYTES, stream);
 }

@@ -385,14 +385,11 @@ cudaError_t launch_narrow(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
             (a.hw * es) % 4 == 0;
   const size_t smem = static_cast<size_t>(kNwWarps) * 2 * g.pitch * g.rows * es;
   auto kern = depthwise_narrow<T, K>;
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
+  if (err != cudaSuccess) return err;
   const long long planes = static_cast<long long>(a.n) * a.c_out;
   int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNwWarps * 32, smem);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNwWarps * 32, smem);
   if (err != cudaSuccess) return err;
   const long long blocks = std::min<long long>((planes + kNwWarps - 1) / kNwWarps,
                                                static_cast<long long>(d.sm) * std::max(per_sm, 1));
@@ -407,11 +404,8 @@ cudaError_t launch_kh(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
   const long long blocks = std::min<long long>(items, static_cast<long long>(d.sm) * kBlocksPerSm);
   const size_t smem = depthwise_smem_bytes(d, a.mg, a.kh, a.kw, sizeof(T) == 4 ? CONV_F32 : CONV_F16);
   auto kern = depthwise<T, KH>;
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
+  if (err != cudaSuccess) return err;
   kern<<<static_cast<unsigned>(blocks), kDwThreads, smem, s>>>(a, d, row_tiles, items);
   return cudaGetLastError();
 }

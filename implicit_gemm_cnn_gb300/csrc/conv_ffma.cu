@@ -534,7 +534,7 @@ cudaError_t launch_gd_k(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
       break;
   }
   const GdPlan& g = plan.gd;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(g.smem));
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), g.smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0, dev = 0, sms = 0;
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGdThreads, g.smem);
@@ -554,15 +554,8 @@ cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn, VB>;
   const int ktab_cap = ffma_ktab_entries(a.k_per_split);
   const size_t smem = ffma_smem_bytes(CFG, a.k_per_split);
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && configured[dev] < static_cast<int>(smem)) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    configured[dev] = static_cast<int>(smem);
-  }
   const long long gx = (a.npix + c.bn - 1) / c.bn;
   const int co_tiles = (a.mg + c.bm - 1) / c.bm;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(co_tiles * a.groups),

@@ -121,6 +121,12 @@ struct Plan {
   int tcw_ok;       // tcw holds a plan (the variant may still fall back to tc at launch)
 };
 
+// Opt `func` in to `bytes` of dynamic shared memory on the current device.
+// The opted-in size only grows and is remembered per (kernel, device); the
+// check and the update hold one lock, so concurrent host threads never lower
+// it under another thread's launch.
+cudaError_t opt_in_smem(const void* func, size_t bytes);
+
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_split_reduce(const ConvArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_depthwise(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);

@@ -711,15 +711,8 @@ template <typename T, int BN>
 cudaError_t launch_bn(const TcPlan& p, const TcLaunch& c, const ConvArgs& a, cudaStream_t s) {
   auto kern = igemm_tc<T, BN>;
   const size_t smem = tc_bytes(BN, c);
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && configured[dev] < static_cast<int>(smem)) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    configured[dev] = static_cast<int>(smem);
-  }
   kern<<<p.ctas, kThreads, smem, s>>>(a, p, c);
   return cudaGetLastError();
 }
@@ -793,27 +786,32 @@ bool configure(const TcPlan& p, const ConvArgs& a, bool addresses_known, TcLaunc
 }  // namespace
 
 // Planner entry (host): channel tile, k order, tiles and blocks for a shape
-// (addresses unknown: assumed aligned).  False when the weights of one
-// channel tile do not fit in shared memory.
+// (addresses unknown: assumed aligned).  The channel tile is the one with
+// the fewest padded channels (ties: the wider) whose weights fit in shared
+// memory; false when not even the narrowest fits.
 bool tc_plan(const ConvArgs& a, int sm, TcPlan* t) {
   static const int bns[] = {256, 128, 64, 48, 32};
-  int bn = 0;
-  long long best = -1;
-  for (int cand : bns) {  // least padded channels; ties go to the wider tile
-    const long long padded = (a.mg + cand - 1) / cand * cand;
-    if (best < 0 || padded < best) { best = padded; bn = cand; }
-  }
-  t->bn = bn;
+  constexpr int kNb = sizeof(bns) / sizeof(bns[0]);
+  int order[kNb];
+  for (int i = 0; i < kNb; ++i) order[i] = i;
+  auto padded = [&](int i) { return (static_cast<long long>(a.mg) + bns[i] - 1) / bns[i] * bns[i]; };
+  std::stable_sort(order, order + kNb, [&](int x, int y) { return padded(x) < padded(y); });
   if (a.cg % 8 == 0) t->mode = kModeCh8;
   else if (a.dw == 1 && a.kw <= 8 && a.kw >= 5) t->mode = kModeRow8;  // rows of 5..8 taps: few padded
   else t->mode = kModeNat;
-  t->co_tiles = (a.mg + bn - 1) / bn;
   t->tiles_per_img = static_cast<int>((a.howo + kM - 1) / kM);
   const long long pix_tiles = static_cast<long long>(a.n) * t->tiles_per_img;
   if (pix_tiles > 2147483647LL) return false;
   t->pix_tiles = static_cast<int>(pix_tiles);
   TcLaunch c;
-  if (!configure(*t, a, false, &c)) return false;
+  bool fits = false;
+  for (int i = 0; i < kNb && !fits; ++i) {
+    t->bn = bns[order[i]];
+    t->co_tiles = (a.mg + t->bn - 1) / t->bn;
+    fits = configure(*t, a, false, &c);
+  }
+  if (!fits) return false;
+  const int bn = t->bn;
   t->k_pad = c.k_pad;
   t->stages = c.stages;
   t->smem = tc_bytes(bn, c);

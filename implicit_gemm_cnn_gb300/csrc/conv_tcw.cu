@@ -685,16 +685,8 @@ cudaError_t launch_win(const WinPlan& p, const ConvArgs& a, void* scratch, cudaS
       break;
   }
   auto repack = tcw_repack<PH>;
-  static int configured[9][64] = {{0}};  // per activation and device: shared memory opted in
-  const int act = a.act >= 0 && a.act < 9 ? a.act : 0;
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), p.smem);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && configured[act][dev] < static_cast<int>(p.smem)) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
-    if (err != cudaSuccess) return err;
-    configured[act][dev] = static_cast<int>(p.smem);
-  }
   const long long units = static_cast<long long>(p.co_tiles) * p.kblocks * p.nt;
   const int rblocks = static_cast<int>(std::min<long long>((units + 255) / 256, 1024));
   repack<<<rblocks, 256, 0, s>>>(a, p, static_cast<uint4*>(scratch));

@@ -217,10 +217,18 @@ CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
  * framework that owns every device allocation, a latency-critical path that
  * must not enter the allocator, or a caller whose only CUDA code is this
  * library.  Such a caller still passes x, w, bias, residual and y (device
- * memory it was given), exactly as for conv_forward; the split-k planes, the
- * only scratch any variant needs, live instead in one fixed array of
- * CONV_FIXED_SCRATCH_BYTES that the library declares in device memory.  Every
- * GPU that loads the library holds that array until the process exits.
+ * memory it was given), exactly as for conv_forward; the scratch conv_forward
+ * would take from the caller -- the float32 planes of split k, or the repacked
+ * weights of the shifted-window tensor-core variant -- lives instead in one
+ * fixed array of CONV_FIXED_SCRATCH_BYTES that the library declares in device
+ * memory.  Every GPU that loads the library holds that array until the
+ * process exits.
+ *
+ * When that scratch would exceed the array, the call runs the problem on a
+ * variant that needs none, if there is one: the gather tensor-core kernel in
+ * place of the shifted-window one, or k summed in one range in place of an
+ * automatic split.  Such a call gives results within the same error bound as
+ * conv_forward's, but not necessarily the same bits (another summation order).
  *
  * Nothing is allocated by this call.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, with that device
@@ -231,8 +239,9 @@ CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
  * streams, say -- race on it and must be serialised by the caller.
  *
  * Errors: those of conv_forward; CONV_ERR_SCRATCH when the problem's scratch
- * (conv_scratch_bytes) exceeds CONV_FIXED_SCRATCH_BYTES, before anything is
- * enqueued; CONV_ERR_CUDA when the array's address cannot be obtained. */
+ * exceeds CONV_FIXED_SCRATCH_BYTES and no variant without scratch applies (a
+ * split forced by the flags), before anything is enqueued; CONV_ERR_CUDA when
+ * the array's address cannot be obtained. */
 CONV_API conv_status conv_forward_fixed_scratch(const conv_problem* p, const void* x, const void* w,
                                                 const void* bias, const void* residual, void* y,
                                                 void* stream);
