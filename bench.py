@@ -3,9 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--layer NAME | --layers all]
 
-One step is one conv_forward over one batch of the workload layer: the
-ResNet-50 stem (N=8, 3->64, 7x7, stride 2, pad 3, 224->112, bias + ReLU,
-fp16) by default.  Inputs are seeded synthetic tensors of the layer's shapes
+One step is one conv_forward over one batch of the workload layer: by
+default the largest configuration by arithmetic, N=16 256->512 3x3 stride 2
+pad 1 on 56x56 with leaky-relu 0.1 in fp32 (14.8 G multiply-adds).  Inputs are seeded synthetic tensors of the layer's shapes
 and distributions, resident in HBM; the step rotates over enough independent
 input sets that their total exceeds twice the L2, so every step reads its
 operands from HBM.  The K timed steps are replayed from CUDA graphs of
@@ -19,8 +19,13 @@ through the public API with pinned host buffers, the CPU oracle's rate on a
 bounded sample (test infrastructure, timed only here), the kernel launch
 count and the SM clocks seen.
 
+The default run also times every other workload layer (fewer steps, no
+end-to-end or CPU legs) and nests their rates -- TFLOP/s for every layer and
+GB/s for the depthwise ones -- under "layers" in the same single JSON line.
+
 --impl reference times the CPU oracle itself on the same workload and metric,
-one bounded sample per step.  --layers all prints one line per workload layer.
+one bounded sample per step.  --layers all prints one full line per workload
+layer.
 """
 from __future__ import annotations
 
@@ -41,7 +46,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "conv TFLOP/s (2·N·Ho·Wo·Co·Ci·k²/g) and depthwise GB/s, % of roofline"
-HEADLINE = "resnet50_stem_f16"
+HEADLINE = "strided_3x3_s2_f32"
 L2_BYTES = 129 * 1024 * 1024
 # float32 FFMA peak: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
 FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
@@ -233,7 +238,9 @@ def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
     variant = conv.conv_describe_variant(p)
     need = conv.conv_scratch_bytes(p)
     plan = conv.conv_plan(p, torch.cuda.get_device_properties(local_rank).multi_processor_count)
-    launches_per_step = 2 if plan["split_k"] > 1 else 1
+    # kernels one call launches: split k adds the ordered-sum pass, the
+    # shifted-window variant its weight repack
+    launches_per_step = 2 if (plan["split_k"] > 1 or variant.startswith("igemm_tcgen05_window")) else 1
     set_bytes = layer_bytes(L)
     nsets = max(1, min(256, math.ceil(2 * L2_BYTES / set_bytes)))  # tiny layers stay L2-resident
     sets = []
@@ -428,6 +435,31 @@ def run_reference(L, steps: int, warmup: int) -> dict:
     return {"value": value, "secs": secs, "per_step": per_step, "cores": cores, "total": total}
 
 
+def nested_layers(headline: str, args, world: int, rank: int, local_rank: int) -> list:
+    """Every other workload layer, timed like the headline (graphs of
+    back-to-back calls, inputs rotated past L2, events on the launching
+    stream) with --layer-steps steps: one compact record each."""
+    from workloads import LAYERS
+    out = []
+    for name in sorted(LAYERS):
+        if name == headline:
+            continue
+        L = LAYERS[name]
+        r = run_ours(L, args.layer_steps, args.warmup, world, rank, local_rank,
+                     with_cpu_baseline=False, with_e2e=False)
+        roof = r["roofline"]
+        rec = {"layer": name, "workload": describe(L), "dtype": L.dtype, "variant": r["variant"],
+               "steps": args.layer_steps, "us_per_call": roof["launch_us"],
+               "tflops": round(r["value"], 3),
+               "gbs": round(aggregate(layer_bytes(L) * args.layer_steps, world, r["secs"]) / 1e9, 1),
+               "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic",
+                                                 "tensor_or_alu_frac")},
+               "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
+               "clock_reasons": r["clocks"].get("reasons")}
+        out.append(rec)
+    return out
+
+
 # ---- main ----------------------------------------------------------------
 def describe(L) -> str:
     return L.description or L.name
@@ -436,8 +468,12 @@ def describe(L) -> str:
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--layer-steps", type=int, default=300,
+                    help="steps per nested layer of the default run")
+    ap.add_argument("--no-layers", action="store_true",
+                    help="the headline layer only (no nested per-layer rates)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layer", default=HEADLINE)
     ap.add_argument("--layers", default=None, help="'all': one line per workload layer")
@@ -479,6 +515,7 @@ def main(argv=None) -> int:
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    nested = args.layers != "all" and not args.quick and not args.no_layers
     for name in names:
         L = LAYERS[name]
         r = run_ours(L, args.steps, args.warmup, world, rank, local_rank,
@@ -506,6 +543,8 @@ def main(argv=None) -> int:
                 "e2e": r.get("e2e")}
         if "cpu_baseline" in r:
             line["cpu_baseline"] = r["cpu_baseline"]
+        if nested:
+            line["layers"] = nested_layers(name, args, world, rank, local_rank)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
