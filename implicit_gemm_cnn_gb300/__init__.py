@@ -21,7 +21,7 @@ import threading
 
 __all__ = [
     "ConvError", "ConvLibraryError", "ConvProblem", "ConvPlanInfo", "ACTIVATIONS", "DTYPES",
-    "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "VARIANTS", "conv_abi_version", "conv_status_string",
+    "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "FLAG_NO_UNFOLD", "FLAG_FORCE_UNFOLD", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
     "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
     "make_problem", "conv2d", "library_path", "load",
@@ -39,6 +39,8 @@ FIXED_SCRATCH_BYTES = 8 << 20  # CONV_FIXED_SCRATCH_BYTES
 FLAG_FORCE_FFMA = 0x1
 FLAG_NO_SPLIT_K = 0x2
 FLAG_NO_WINDOW = 0x4
+FLAG_NO_UNFOLD = 0x8
+FLAG_FORCE_UNFOLD = 0x10
 SPLIT_K_SHIFT = 8
 STATUS = {0: "CONV_OK", 1: "CONV_ERR_SHAPE", 2: "CONV_ERR_OVERFLOW", 3: "CONV_ERR_DTYPE",
           4: "CONV_ERR_ACT", 5: "CONV_ERR_NULL", 6: "CONV_ERR_SCRATCH", 7: "CONV_ERR_ALIAS",

@@ -85,24 +85,59 @@ int occupancy_estimate(const FfmaCfg& c, size_t smem) {
   return std::max(occ, 1);
 }
 
+// Whether the unfolded-B pre-pass pays for a CUDA-core layer: it moves x once
+// and writes and reads the unfolded copy once, so it is taken when the
+// layer's arithmetic is at least 64 FLOP per byte of that traffic (the
+// multiply-adds then take several times the pre-pass) and k is long enough
+// for 16-byte staging to matter.
+bool unf_worth(const conv_problem* p, const Shape& s, const UnfPlan& u) {
+  const double es = p->dtype == CONV_F32 ? 4.0 : 2.0;
+  const double traffic = static_cast<double>(s.x_elems) * es + 2.0 * 4.0 * static_cast<double>(u.xw_elems);
+  const double flops = 2.0 * static_cast<double>(s.y_elems) * static_cast<double>(s.K);
+  return s.K >= 64 && flops >= 64.0 * traffic;
+}
+
 void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
+  // the B operand: 16-byte copies from an unfolded copy of x where that
+  // applies and pays (or is forced), else the per-k gather
+  const bool pointwise = p->kh == 1 && p->kw == 1 && p->stride_h == 1 && p->stride_w == 1 &&
+                         p->pad_top == 0 && p->pad_left == 0 && p->pad_bottom == 0 && p->pad_right == 0;
+  UnfPlan u;
+  const bool unf_ok = !(p->flags & CONV_FLAG_NO_UNFOLD) && !(pointwise && p->dtype == CONV_F32) &&
+                      unf_plan(p, s.ho, s.wo, &u);
+  const bool unf = unf_ok && ((p->flags & CONV_FLAG_FORCE_UNFOLD) || unf_worth(p, s, u));
   // Per-SM time model: an SM runs ceil(blocks / SMs) tiles of bm x bn outputs
   // (padding included) at a rate set by the register tile, slowed when fewer
   // than 8 warps are resident to hide latency.  Lowest time wins; ties go to
-  // the earlier (larger) tile.
+  // the earlier (larger) tile.  With unfolded B the model follows the waves:
+  // the resident blocks of an SM run in rounds of `occupancy`, the last
+  // round perhaps partly filled, each round at a speed set by its warps
+  // (12 resident warps to hide the pipeline's latency).
   double best = 0.0;
   int bi = -1;
   for (int i = 0; i < kNumFfmaCfgs; ++i) {
     const FfmaCfg& c = kFfmaCfgs[i];
+    if (!unf && i >= kFfmaFirstWide) continue;
     const long long tm = (s.mg + c.bm - 1) / c.bm, tn = (s.npix + c.bn - 1) / c.bn;
     const long long ctas = tm * tn * p->groups;
     if (tm * p->groups > 65535) continue;
     const long long per_sm = (ctas + sm - 1) / sm;
     const int occ = occupancy_estimate(c, ffma_smem_bytes(i, static_cast<int>(s.K)));
-    const double warps = static_cast<double>(std::min<long long>(per_sm, occ)) * c.threads() / 32.0;
-    const double speed = ((c.tm == 8 && c.tn == 8) ? 1.0 : (c.tm * c.tn == 32 ? 0.85 : 0.6)) *
-                         std::min(1.0, warps / 8.0);
-    const double t = static_cast<double>(per_sm) * c.bm * c.bn / speed;
+    const double base = c.tm * c.tn >= 64 ? (c.tn == 12 ? 1.05 : 1.0) : (c.tm * c.tn == 32 ? 0.85 : 0.6);
+    double t;
+    if (!unf) {
+      const double warps = static_cast<double>(std::min<long long>(per_sm, occ)) * c.threads() / 32.0;
+      const double speed = base * std::min(1.0, warps / 8.0);
+      t = static_cast<double>(per_sm) * c.bm * c.bn / speed;
+    } else {
+      const long long rounds = (per_sm + occ - 1) / occ;
+      const long long last = per_sm - (rounds - 1) * occ;
+      auto speed = [&](long long blocks) {
+        return base * std::min(1.0, static_cast<double>(blocks) * c.threads() / 32.0 / 12.0);
+      };
+      const double work = static_cast<double>(c.bm) * c.bn;
+      t = static_cast<double>(rounds - 1) * occ * work / speed(occ) + static_cast<double>(last) * work / speed(last);
+    }
     if (bi < 0 || t < best * (1.0 - 1e-9)) { best = t; bi = i; }
   }
   if (bi < 0) bi = 0;
@@ -131,8 +166,9 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   if (split <= 1) { split = 1; len = s.K; }
   // grouped layers with few channels per group: input rows staged once per
   // item instead of a per-k gather (no split k there)
-  if (split == 1) gd_plan(p, s.ho, s.wo, &out->gd);
+  if (split == 1 && !unf) gd_plan(p, s.ho, s.wo, &out->gd);
   out->ffma_cfg = bi;
+  out->ffma_unf = unf ? 1 : 0;
   // pointwise fp32 (1x1, stride 1, no pad, dilation 1) whose planes hold whole
   // groups of 4 pixels: 16-byte B copies (x's alignment is checked at launch)
   const long long hw = p->h * p->w;
@@ -144,7 +180,15 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   out->info.tile_m = c.bm;
   out->info.tile_n = c.bn;
   out->info.ctas = ctas * split;
-  out->info.scratch_bytes = split > 1 ? static_cast<uint64_t>(split) * s.y_elems * sizeof(float) : 0;
+  uint64_t scratch = split > 1 ? static_cast<uint64_t>(split) * s.y_elems * sizeof(float) : 0;
+  if (unf) {
+    // after the split planes: the unfolded x, then the transposed weights
+    u.xw_off = (scratch + 255) / 256 * 256;
+    u.wt_off = (u.xw_off + static_cast<uint64_t>(u.xw_elems) * sizeof(float) + 255) / 256 * 256;
+    scratch = u.wt_off + static_cast<uint64_t>(u.wt_elems) * sizeof(float);
+    out->unf = u;
+  }
+  out->info.scratch_bytes = scratch;
   out->k_per_split = static_cast<int>(len);
   if (out->gd.ok) {
     out->info.tile_m = static_cast<int>(s.mg);
@@ -418,9 +462,11 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
     snprintf(buf, len, "%s rows/block=%d staged=%dx%d blocks=%lld sms=%d", variant_name(i.variant),
              plan.dw.th, plan.dw.in_rows, plan.dw.row, static_cast<long long>(i.ctas), sm);
   } else {
-    snprintf(buf, len, "%s tile=%dco x %dpx split_k=%d blocks=%lld scratch=%llu sms=%d",
-             variant_name(i.variant), i.tile_m, i.tile_n, i.split_k, static_cast<long long>(i.ctas),
-             static_cast<unsigned long long>(i.scratch_bytes), sm);
+    const FfmaCfg& c = kFfmaCfgs[plan.ffma_cfg];
+    snprintf(buf, len, "%s tile=%dco x %dpx (%dx%d per thread) B=%s split_k=%d blocks=%lld scratch=%llu sms=%d",
+             variant_name(i.variant), i.tile_m, i.tile_n, c.tm, c.tn,
+             plan.ffma_unf ? "unfolded" : (plan.ffma_vec ? "pointwise" : "gathered"), i.split_k,
+             static_cast<long long>(i.ctas), static_cast<unsigned long long>(i.scratch_bytes), sm);
   }
   return CONV_OK;
 }
@@ -492,6 +538,12 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
       a.split = plan.info.split_k;
       a.k_per_split = plan.k_per_split;
       a.partial = static_cast<float*>(scratch);
+      if (plan.ffma_unf) {
+        a.xw = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan.unf.xw_off);
+        a.wtt = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan.unf.wt_off);
+        a.hu = plan.unf.hu;
+        a.mg4 = plan.unf.mg4;
+      }
       err = launch_ffma(plan, a, p->dtype, cs);
       if (err == cudaSuccess && a.split > 1) err = launch_split_reduce(a, p->dtype, cs);
       break;
@@ -551,12 +603,12 @@ extern "C" conv_status conv_forward_fixed_scratch(const conv_problem* p, const v
   // planes), unless the caller forced the split.
   conv_problem q = *p;
   const int forced_split = static_cast<int>((p->flags & CONV_FLAG_SPLIT_K_MASK) >> CONV_FLAG_SPLIT_K_SHIFT);
-  if (plan.info.scratch_bytes > CONV_FIXED_SCRATCH_BYTES && plan.info.variant == CONV_VARIANT_IGEMM_TC_WINDOW)
-    q.flags |= CONV_FLAG_NO_WINDOW;
-  else if (plan.info.scratch_bytes > CONV_FIXED_SCRATCH_BYTES &&
-           plan.info.variant == CONV_VARIANT_IGEMM_FFMA_SPLIT && forced_split == 0)
-    q.flags |= CONV_FLAG_NO_SPLIT_K;
-  if (q.flags != p->flags) {
+  const uint32_t fallbacks[] = {CONV_FLAG_NO_WINDOW, CONV_FLAG_NO_UNFOLD, forced_split ? 0u : CONV_FLAG_NO_SPLIT_K};
+  for (uint32_t f : fallbacks) {
+    if (plan.info.scratch_bytes <= CONV_FIXED_SCRATCH_BYTES) break;
+    if (!f || (q.flags & f)) continue;
+    if (f == CONV_FLAG_NO_UNFOLD && (q.flags & CONV_FLAG_FORCE_UNFOLD)) continue;
+    q.flags |= f;
     st = make_plan(&q, sm, &plan, nullptr);
     if (st != CONV_OK) return st;
   }

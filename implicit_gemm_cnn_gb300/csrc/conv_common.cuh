@@ -35,6 +35,9 @@ struct ConvArgs {
   int split;               // ranges of k (1 = whole)
   int k_per_split;         // terms per range (a multiple of the k chunk)
   int vec_out;             // y (and scratch) 16-byte aligned: vector stores allowed
+  float* xw;               // unfolded B: the column-unfolded x (float32), or nullptr
+  float* wtt;              // unfolded B: the transposed weights [g][k][mg4]
+  int hu, mg4;             // unfolded B: padded input rows, channels per group rounded to 4
 };
 
 enum Act {

@@ -84,19 +84,36 @@ __host__ __device__ constexpr int pow2_floor(int v) {
   return p;
 }
 
-// VB: a pointwise layer (1x1, stride 1, no pad, plane length a multiple of 4,
-// x 16-byte aligned) whose k rows of 4 consecutive pixels are 16 contiguous
-// bytes of one channel plane: the B tile arrives by 16-byte cp.async copies,
-// each thread's pixel offsets computed once, no window table.
-template <typename T, int BM, int BN, int TM, int TN, bool VB>
-__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+// The B operand (BMODE):
+//  * kBGather: each k row of a pixel tile is gathered from x with 4-byte
+//    copies, a window-table lookup and bounds tests per element;
+//  * kBPointwise: a pointwise layer (1x1, stride 1, no pad, plane length a
+//    multiple of 4, x 16-byte aligned) whose k rows of 4 consecutive pixels are
+//    16 contiguous bytes of one channel plane: 16-byte copies, each thread's
+//    pixel offsets computed once, the table holding k * plane length;
+//  * kBUnfolded: 16-byte copies from the column-unfolded copy xw of x (see
+//    UnfPlan): a thread's pixel offsets are computed once, the table holds
+//    each term's offset, no bounds tests; the weights come transposed (wtt), so
+//    the A tile arrives by 16-byte copies too.
+// TN = 12 (three 4-pixel groups per thread) is used with unfolded B only.
+// Registers per thread for a block of nt threads: two blocks per SM from 192
+// threads on, three from 128 (multiples of 8, the allocation unit).
+__host__ __device__ constexpr int ffma_maxreg(int nt) {
+  return nt >= 192 ? (65536 / (2 * nt)) / 8 * 8 : (nt >= 128 ? (65536 / (3 * nt)) / 8 * 8 : 255);
+}
+
+template <typename T, int BM, int BN, int TM, int TN, int BMODE>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg((BM / TM) * (BN / TN)))
     igemm_ffma(const ConvArgs a, const int ktab_cap) {
   constexpr int NT = (BM / TM) * (BN / TN);
   constexpr int BK = kFfmaBK;
   constexpr int S = kFfmaStages;
   constexpr int AS = BM + 4;  // padded weight-tile row: conflict-free transposed stores
+  constexpr bool VEC = BMODE != kBGather;
+  constexpr int GN = BN * 4 / TN;  // distance between a thread's 4-pixel groups
   static_assert(TM == 4 || TM == 8, "TM");
-  static_assert(TN == 4 || TN == 8, "TN");
+  static_assert(TN == 4 || TN == 8 || TN == 12, "TN");
+  static_assert(BN % TN == 0 && (BN / TN) * 4 * (TN / 4) == BN, "pixel groups");
   extern __shared__ __align__(16) float smem[];
   float* As = smem;                                       // [S][BK][AS]
   float* Bs = As + S * BK * AS;                           // [S][BK][BN]
@@ -113,42 +130,45 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
   const int k_end = min(a.K, k_begin + a.k_per_split);
   const int khw = a.kh * a.kw;
 
-  // ---- the pixel columns this thread stages --------------------------------
+  // ---- the pixel columns this thread stages (gathered B) -------------------
   // LB threads gather the input tile: RSTEP rows at a time of BN pixels each
   // (LB >= BN), or PCOLS pixel columns each over all BK rows (LB < BN).
   constexpr int LB = NT >= BN ? pow2_floor(NT / BN < BK ? NT / BN : BK) * BN : pow2_floor(NT);
-  constexpr int PCOLS = LB >= BN ? 1 : BN / LB;
+  constexpr int PCOLS = VEC ? 1 : (LB >= BN ? 1 : BN / LB);
   constexpr int RSTEP = LB >= BN ? LB / BN : 1;
   constexpr int BROWS = BK / RSTEP;
-  static_assert(BK % RSTEP == 0 && (LB >= BN ? LB % BN == 0 : BN % LB == 0), "loader mapping");
+  static_assert(VEC || (BK % RSTEP == 0 && (LB >= BN ? LB % BN == 0 : BN % LB == 0)), "loader mapping");
   const bool bloader = tid < LB;
   const int r0 = LB >= BN ? tid / BN : 0;
   const int cbase = LB >= BN ? tid % BN : tid;
   long long pbase[PCOLS];
   int ih0[PCOLS], iw0[PCOLS];
   bool pval[PCOLS];
+  if constexpr (!VEC) {
 #pragma unroll
-  for (int j = 0; j < PCOLS; ++j) {
-    const int col = cbase + j * LB;
-    const long long p = pix0 + col;
-    pval[j] = bloader && p < a.npix;
-    const long long pp = pval[j] ? p : 0;
-    const int n = static_cast<int>(pp / a.howo);
-    const int rem = static_cast<int>(pp - static_cast<long long>(n) * a.howo);
-    const int oh = rem / a.wo, ow = rem - (rem / a.wo) * a.wo;
-    ih0[j] = oh * a.sh - a.pt;
-    iw0[j] = ow * a.sw - a.pl;
-    pbase[j] = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
-               static_cast<long long>(ih0[j]) * a.w + iw0[j];
+    for (int j = 0; j < PCOLS; ++j) {
+      const int col = cbase + j * LB;
+      const long long p = pix0 + col;
+      pval[j] = bloader && p < a.npix;
+      const long long pp = pval[j] ? p : 0;
+      const int n = static_cast<int>(pp / a.howo);
+      const int rem = static_cast<int>(pp - static_cast<long long>(n) * a.howo);
+      const int oh = rem / a.wo, ow = rem - (rem / a.wo) * a.wo;
+      ih0[j] = oh * a.sh - a.pt;
+      iw0[j] = ow * a.sw - a.pl;
+      pbase[j] = (static_cast<long long>(n) * a.c_in + static_cast<long long>(g) * a.cg) * a.hw +
+                 static_cast<long long>(ih0[j]) * a.w + iw0[j];
+    }
   }
 
-  // VB: the thread's 16-byte copies of a stage: q = tid + i*NT -> k row q / (BN/4),
-  // pixels pix0 + 4*(q % (BN/4)) .. +3 (all in one image: the plane length is a
-  // multiple of 4)
-  constexpr int QV = VB ? (BK * BN / 4 + NT - 1) / NT : 1;
+  // vector B: the thread's 16-byte copies of a stage: q = tid + i*NT -> k row
+  // q / (BN/4), pixels pix0 + 4*(q % (BN/4)) .. +3, all in one image row (the
+  // plane length, or the output row, is a multiple of 4)
+  constexpr int QV = VEC ? (BK * BN / 4 + NT - 1) / NT : 1;
   long long vbase[QV];
   bool vok[QV];
-  if constexpr (VB) {
+  if constexpr (VEC) {
+    const long long unf_img = static_cast<long long>(a.c_in) * a.kw * a.hu * a.wo;  // xw per image
 #pragma unroll
     for (int i = 0; i < QV; ++i) {
       const int q = tid + i * NT;
@@ -156,9 +176,17 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
       vok[i] = q < BK * BN / 4 && p < a.npix;
       const long long pp = vok[i] ? p : 0;
       const long long n = pp / a.howo;
-      vbase[i] = (n * a.c_in + static_cast<long long>(g) * a.cg) * a.hw + (pp - n * a.howo);
+      const long long rem = pp - n * a.howo;
+      if constexpr (BMODE == kBPointwise) {
+        vbase[i] = (n * a.c_in + static_cast<long long>(g) * a.cg) * a.hw + rem;
+      } else {
+        const long long oh = rem / a.wo, ow = rem - oh * a.wo;
+        vbase[i] = n * unf_img + static_cast<long long>(g) * a.cg * a.kw * a.hu * a.wo + oh * a.sh * a.wo + ow;
+      }
     }
   }
+  // unfolded A: 16-byte copies of the transposed weights
+  constexpr int QA = BMODE == kBUnfolded ? (BK * BM / 4 + NT - 1) / NT : 1;
 
   float acc[TM][TN];
 #pragma unroll
@@ -172,39 +200,56 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
   for (int kseg = k_begin; kseg < k_end; kseg += ktab_cap) {
     const int seg_end = min(k_end, kseg + ktab_cap);
     __syncthreads();  // the previous segment's table and stages are free
-    for (int k = kseg + tid; !VB && k < seg_end; k += NT) {
+    for (int k = kseg + tid; k < seg_end; k += NT) {
       const int c = k / khw;
       const int tap = k - c * khw;
       const int u = tap / a.kw, v = tap - (tap / a.kw) * a.kw;
       const int dy = u * a.dh, dx = v * a.dw;
-      ktab[k - kseg] = make_int2(c * static_cast<int>(a.hw) + dy * a.w + dx, (dy << 16) | dx);
+      if constexpr (BMODE == kBGather)
+        ktab[k - kseg] = make_int2(c * static_cast<int>(a.hw) + dy * a.w + dx, (dy << 16) | dx);
+      else if constexpr (BMODE == kBPointwise)
+        ktab[k - kseg] = make_int2(k * static_cast<int>(a.hw), 0);
+      else
+        ktab[k - kseg] = make_int2(((c * a.kw + v) * a.hu + dy) * a.wo, 0);
     }
     __syncthreads();
 
     auto load_stage = [&](int st, int k0) {
       float* as = As + st * BK * AS;
       float* bs = Bs + st * BK * BN;
-      constexpr int AE = (BM * BK + NT - 1) / NT;
+      if constexpr (BMODE == kBUnfolded) {
 #pragma unroll
-      for (int i = 0; i < AE; ++i) {
-        const int e = tid + i * NT;
-        if (e < BM * BK) {
-          const int kk = e % BK, m = e / BK;
+        for (int i = 0; i < QA; ++i) {
+          const int q = tid + i * NT;
+          const int kk = q / (BM / 4), m4 = q - (q / (BM / 4)) * (BM / 4);
           const int k = k0 + kk;
-          const bool ok = (m0 + m < a.mg) && (k < seg_end);
-          const T* src = ok ? wt + static_cast<long long>(g * a.mg + m0 + m) * a.K + k : wt;
-          stage_elem<T>(as + kk * AS + m, src, ok);
+          const bool ok = q < BK * BM / 4 && k < seg_end && m0 + 4 * m4 < a.mg4;
+          const float* src = ok ? a.wtt + (static_cast<long long>(g) * a.K + k) * a.mg4 + m0 + 4 * m4 : a.wtt;
+          if (q < BK * BM / 4) cp_async16(as + kk * AS + 4 * m4, src, ok);
+        }
+      } else {
+        constexpr int AE = (BM * BK + NT - 1) / NT;
+#pragma unroll
+        for (int i = 0; i < AE; ++i) {
+          const int e = tid + i * NT;
+          if (e < BM * BK) {
+            const int kk = e % BK, m = e / BK;
+            const int k = k0 + kk;
+            const bool ok = (m0 + m < a.mg) && (k < seg_end);
+            const T* src = ok ? wt + static_cast<long long>(g * a.mg + m0 + m) * a.K + k : wt;
+            stage_elem<T>(as + kk * AS + m, src, ok);
+          }
         }
       }
-      if constexpr (VB) {
+      if constexpr (VEC) {
+        const float* xb = BMODE == kBPointwise ? reinterpret_cast<const float*>(x) : a.xw;
 #pragma unroll
         for (int i = 0; i < QV; ++i) {
           const int q = tid + i * NT;
           const int kk = q / (BN / 4), c4 = q % (BN / 4);
           const int k = k0 + kk;
           const bool ok = vok[i] && k < seg_end;
-          const float* src = ok ? reinterpret_cast<const float*>(x) + vbase[i] + static_cast<long long>(k) * a.hw
-                                : reinterpret_cast<const float*>(x);
+          const float* src = ok ? xb + vbase[i] + ktab[k - kseg].x : xb;
           if (q < BK * BN / 4) cp_async16(bs + kk * BN + 4 * c4, src, ok);
         }
       } else if (bloader) {
@@ -251,11 +296,10 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
           const float4 a1 = *reinterpret_cast<const float4*>(as + kk * AS + BM / 2 + ty * 4);
           ra[4] = a1.x; ra[5] = a1.y; ra[6] = a1.z; ra[7] = a1.w;
         }
-        const float4 b0 = *reinterpret_cast<const float4*>(bs + kk * BN + tx * 4);
-        rb[0] = b0.x; rb[1] = b0.y; rb[2] = b0.z; rb[3] = b0.w;
-        if constexpr (TN == 8) {
-          const float4 b1 = *reinterpret_cast<const float4*>(bs + kk * BN + BN / 2 + tx * 4);
-          rb[4] = b1.x; rb[5] = b1.y; rb[6] = b1.z; rb[7] = b1.w;
+#pragma unroll
+        for (int jg = 0; jg < TN / 4; ++jg) {
+          const float4 b = *reinterpret_cast<const float4*>(bs + kk * BN + jg * GN + tx * 4);
+          rb[jg * 4] = b.x; rb[jg * 4 + 1] = b.y; rb[jg * 4 + 2] = b.z; rb[jg * 4 + 3] = b.w;
         }
 #pragma unroll
         for (int i = 0; i < TM; ++i)
@@ -271,7 +315,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
   T* y = static_cast<T*>(a.y);
 #pragma unroll
   for (int jg = 0; jg < TN / 4; ++jg) {
-    const long long p = pix0 + jg * (BN / 2) + tx * 4;
+    const long long p = pix0 + jg * GN + tx * 4;
     if (p >= a.npix) continue;
     const int n = static_cast<int>(p / a.howo);
     const long long rem = p - static_cast<long long>(n) * a.howo;
@@ -327,6 +371,58 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
         }
       }
     }
+  }
+}
+
+// The unfolded-B pre-pass.  Blocks [0, planes) unfold one input plane (n, c)
+// each into xw[n][c][v][r][ow] (float32, 16-byte stores, zeros outside x);
+// the blocks after them transpose the weights into wtt[g][k][m] (float32,
+// channels padded to mg4 with zeros) through 32 x 32 shared-memory tiles.
+template <typename T>
+__global__ void __launch_bounds__(256) ffma_unfold(const ConvArgs a, long long planes, int wt_tiles_k,
+                                                   int wt_tiles_m) {
+  __shared__ float tile[32][33];
+  const T* __restrict__ x = static_cast<const T*>(a.x);
+  const T* __restrict__ w = static_cast<const T*>(a.wt);
+  const int tid = threadIdx.x;
+  if (blockIdx.x < planes) {
+    const long long nc = blockIdx.x;
+    const T* __restrict__ plane = x + nc * a.hw;
+    const int wq = a.wo / 4;
+    const int units = a.kw * a.hu * wq;
+    float* out = a.xw + nc * static_cast<long long>(a.kw) * a.hu * a.wo;
+    for (int e = tid; e < units; e += 256) {
+      const int ow4 = e % wq;
+      const int t = e / wq;
+      const int r = t % a.hu, v = t / a.hu;
+      const int ih = r - a.pt;
+      const bool rok = static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
+      const T* __restrict__ row = plane + static_cast<long long>(rok ? ih : 0) * a.w;
+      float o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int iw = (ow4 * 4 + j) * a.sw - a.pl + v * a.dw;
+        o[j] = rok && static_cast<unsigned>(iw) < static_cast<unsigned>(a.w) ? to_f32(row[iw]) : 0.0f;
+      }
+      *reinterpret_cast<float4*>(out + static_cast<long long>(t) * a.wo + 4 * ow4) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+    return;
+  }
+  // weights: tile (g, k block, m block) of 32 x 32
+  const long long b = blockIdx.x - planes;
+  const int mb = static_cast<int>(b % wt_tiles_m);
+  const long long rest = b / wt_tiles_m;
+  const int kb = static_cast<int>(rest % wt_tiles_k);
+  const int g = static_cast<int>(rest / wt_tiles_k);
+  const int tx = tid % 32, ty = tid / 32;  // 8 rows of 32
+  for (int i = ty; i < 32; i += 8) {       // read along k (OIHW rows are contiguous in k)
+    const int m = mb * 32 + i, k = kb * 32 + tx;
+    tile[i][tx] = (m < a.mg && k < a.K) ? to_f32(w[(static_cast<long long>(g) * a.mg + m) * a.K + k]) : 0.0f;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {       // write along m
+    const int k = kb * 32 + i, m = mb * 32 + tx;
+    if (k < a.K && m < a.mg4) a.wtt[(static_cast<long long>(g) * a.K + k) * a.mg4 + m] = tile[tx][i];
   }
 }
 
@@ -548,10 +644,10 @@ cudaError_t launch_gd_k(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <typename T, int CFG, bool VB>
+template <typename T, int CFG, int BMODE>
 cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   constexpr FfmaCfg c = kFfmaCfgs[CFG];
-  auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn, VB>;
+  auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn, BMODE>;
   const int ktab_cap = ffma_ktab_entries(a.k_per_split);
   const size_t smem = ffma_smem_bytes(CFG, a.k_per_split);
   cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
@@ -567,10 +663,26 @@ cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
 
 template <typename T, int CFG>
 cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
-  if constexpr (sizeof(T) == 4) {
-    if (plan.ffma_vec && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) return launch_cfg_vb<T, CFG, true>(plan, a, s);
+  if (a.xw) return launch_cfg_vb<T, CFG, kBUnfolded>(plan, a, s);
+  if constexpr (CFG >= kFfmaFirstWide) {
+    return cudaErrorInvalidConfiguration;  // wide tiles are planned with unfolded B only
+  } else {
+    if constexpr (sizeof(T) == 4) {
+      if (plan.ffma_vec && reinterpret_cast<uintptr_t>(a.x) % 16 == 0)
+        return launch_cfg_vb<T, CFG, kBPointwise>(plan, a, s);
+    }
+    return launch_cfg_vb<T, CFG, kBGather>(plan, a, s);
   }
-  return launch_cfg_vb<T, CFG, false>(plan, a, s);
+}
+
+template <typename T>
+cudaError_t launch_unfold(const UnfPlan& u, const ConvArgs& a, cudaStream_t s) {
+  const long long planes = static_cast<long long>(a.n) * a.c_in;
+  const int tk = (a.K + 31) / 32, tm = (u.mg4 + 31) / 32;
+  const long long blocks = planes + static_cast<long long>(a.groups) * tk * tm;
+  if (blocks > 2147483647LL) return cudaErrorInvalidConfiguration;
+  ffma_unfold<T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a, planes, tk, tm);
+  return cudaGetLastError();
 }
 
 template <typename T>
@@ -585,6 +697,8 @@ cudaError_t launch_typed(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
     case 6: return launch_cfg<T, 6>(plan, a, s);
     case 7: return launch_cfg<T, 7>(plan, a, s);
     case 8: return launch_cfg<T, 8>(plan, a, s);
+    case 9: return launch_cfg<T, 9>(plan, a, s);
+    case 10: return launch_cfg<T, 10>(plan, a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -609,6 +723,20 @@ size_t ffma_smem_bytes(int cfg, int k_per_block) {
   const FfmaCfg c = kFfmaCfgs[cfg];
   return static_cast<size_t>(kFfmaStages) * kFfmaBK * (c.bm + 4 + c.bn) * sizeof(float) +
          static_cast<size_t>(ffma_ktab_entries(k_per_block)) * sizeof(int2);
+}
+
+bool unf_plan(const conv_problem* p, long long ho, long long wo, UnfPlan* u) {
+  memset(u, 0, sizeof(*u));
+  if (wo % 4 != 0) return false;  // 4-pixel groups within one output row
+  const long long hu = (ho - 1) * p->stride_h + (p->kh - 1) * p->dil_h + 1;
+  const long long cg = p->c_in / p->groups, mg = p->c_out / p->groups;
+  const long long per_group = cg * p->kw * hu * wo;  // the largest term offset (int32)
+  if (hu > 2147483647LL || per_group > 2147483647LL || p->c_in * p->kw * hu * wo > 2147483647LL) return false;
+  u->hu = static_cast<int>(hu);
+  u->mg4 = static_cast<int>((mg + 3) / 4 * 4);
+  u->xw_elems = p->n * p->c_in * p->kw * hu * wo;
+  u->wt_elems = p->groups * cg * p->kh * p->kw * u->mg4;
+  return true;
 }
 
 bool gd_plan(const conv_problem* p, long long ho, long long wo, GdPlan* g) {
@@ -637,6 +765,16 @@ cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStre
   if (plan.gd.ok && dtype == CONV_F32 && reinterpret_cast<uintptr_t>(a.y) % 16 == 0 &&
       (a.residual == nullptr || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0))
     return plan.gd.k == 3 ? launch_gd_k<3>(plan, a, s) : launch_gd_k<5>(plan, a, s);
+  if (a.xw) {
+    cudaError_t err = cudaErrorInvalidValue;
+    switch (dtype) {
+      case CONV_F32: err = launch_unfold<float>(plan.unf, a, s); break;
+      case CONV_F16: err = launch_unfold<__half>(plan.unf, a, s); break;
+      case CONV_BF16: err = launch_unfold<__nv_bfloat16>(plan.unf, a, s); break;
+      default: break;
+    }
+    if (err != cudaSuccess) return err;
+  }
   switch (dtype) {
     case CONV_F32: return launch_typed<float>(plan, a, s);
     case CONV_F16: return launch_typed<__half>(plan, a, s);

@@ -20,13 +20,36 @@ struct FfmaCfg {
 constexpr int kFfmaBK = 8;          // k terms per pipeline stage
 constexpr int kFfmaStages = 4;      // pipeline depth
 constexpr int kFfmaKTab = 2304;     // k entries of the window table per segment
-constexpr int kNumFfmaCfgs = 9;
+constexpr int kNumFfmaCfgs = 11;
+constexpr int kFfmaFirstWide = 9;   // configs from here on: 8 x 12 register tiles, unfolded B only
 constexpr FfmaCfg kFfmaCfgs[kNumFfmaCfgs] = {
     {128, 128, 8, 8}, {64, 128, 8, 8}, {128, 64, 8, 8}, {64, 64, 4, 4}, {32, 256, 4, 8},
-    {16, 256, 4, 8},  {40, 128, 8, 4}, {16, 64, 4, 4},  {40, 64, 8, 4}};
+    {16, 256, 4, 8},  {40, 128, 8, 4}, {16, 64, 4, 4},  {40, 64, 8, 4},
+    {128, 168, 8, 12}, {128, 96, 8, 12}};
 
 size_t ffma_smem_bytes(int cfg, int k_per_block);  // k_per_block: terms one block sums
 int ffma_ktab_entries(int k_per_block);
+
+// The B operand of the CUDA-core kernel.
+constexpr int kBGather = 0;    // per-k gather from x with 4-byte copies and bounds tests
+constexpr int kBPointwise = 1; // 1x1 / stride 1 / no pad: 16-byte copies straight from x
+constexpr int kBUnfolded = 2;  // 16-byte copies from a column-unfolded copy of x (below)
+
+// Unfolded B: a pre-pass writes, in float32,
+//   xw[n][c][v][r][ow] = x[n][c][r - pad_top][ow*sw - pad_left + v*dw]  (0 outside x)
+// for every kernel column v, padded input row r < hu and output column ow,
+// and the weights transposed to wt[g][k][m] (m padded to mg4 with zeros).
+// The B value of output (n, oh, ow) and term (c, u, v) is then
+// xw[n][c][v][oh*sh + u*dh][ow]: a pixel part plus a term part, so four
+// consecutive output columns of one row are 16 contiguous bytes (Wo a
+// multiple of 4) and need no bounds test.
+struct UnfPlan {
+  int hu;              // padded input rows: (Ho-1)*sh + (kh-1)*dh + 1
+  int mg4;             // output channels per group, rounded up to 4
+  long long xw_elems;  // N * Cin * kw * hu * Wo
+  long long wt_elems;  // groups * K * mg4
+  size_t xw_off, wt_off;  // byte offsets of xw and wt in scratch (after any split planes)
+};
 
 // Depthwise (one input channel per group) halo-tiled direct kernel.
 struct DwPlan {
@@ -114,6 +137,8 @@ struct Plan {
   GdPlan gd;
   int ffma_cfg;
   int ffma_vec;     // pointwise fp32 with whole 16-byte pixel groups: vector B loads
+  int ffma_unf;     // the unfolded-B pre-pass and 16-byte copies (UnfPlan)
+  UnfPlan unf;
   int k_per_split;  // terms per k range of the split variant
   DwPlan dw;
   TcPlan tc;
@@ -128,6 +153,9 @@ struct Plan {
 cudaError_t opt_in_smem(const void* func, size_t bytes);
 
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
+// Whether the unfolded-B layout applies to the shape (element type aside),
+// and its sizes; false when a size is past the kernel's 32-bit offsets.
+bool unf_plan(const conv_problem* p, long long ho, long long wo, UnfPlan* u);
 cudaError_t launch_split_reduce(const ConvArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_depthwise(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_tc(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);

@@ -81,6 +81,9 @@ typedef enum conv_act {
 #define CONV_FLAG_FORCE_FFMA 0x1u   /* the CUDA-core implicit GEMM for every shape   */
 #define CONV_FLAG_NO_SPLIT_K 0x2u   /* never split k                                 */
 #define CONV_FLAG_NO_WINDOW 0x4u    /* never the shifted-window tcgen05 variant       */
+#define CONV_FLAG_NO_UNFOLD 0x8u    /* CUDA-core kernel: never the unfolded-input pre-pass */
+#define CONV_FLAG_FORCE_UNFOLD 0x10u /* CUDA-core kernel: the unfolded-input pre-pass
+                                        wherever it applies (output width a multiple of 4) */
 #define CONV_FLAG_SPLIT_K_SHIFT 8   /* bits 8..13: force this many ranges of k (1-63) */
 #define CONV_FLAG_SPLIT_K_MASK 0x3f00u
 
@@ -177,7 +180,9 @@ CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_pla
  * ("Convolution, pooling and resize", Layout and operands: the scratch
  * query): the float32 partial planes of split k (ranges x output elements),
  * the repacked weights of the shifted-window variant (channel tiles x k
- * blocks x tile channels x 16 bytes), 0 for the other variants.
+ * blocks x tile channels x 16 bytes), the CUDA-core kernel's unfolded input
+ * (float32, n x c_in x kw x padded rows x Wo) and transposed weights when it
+ * uses them, 0 for the other variants.
  * Errors: as conv_plan, and CONV_ERR_DEVICE without a usable device. */
 CONV_API conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes);
 
@@ -218,16 +223,18 @@ CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
  * must not enter the allocator, or a caller whose only CUDA code is this
  * library.  Such a caller still passes x, w, bias, residual and y (device
  * memory it was given), exactly as for conv_forward; the scratch conv_forward
- * would take from the caller -- the float32 planes of split k, or the repacked
- * weights of the shifted-window tensor-core variant -- lives instead in one
+ * would take from the caller -- the float32 planes of split k, the repacked
+ * weights of the shifted-window tensor-core variant, or the unfolded input
+ * and transposed weights of the CUDA-core kernel -- lives instead in one
  * fixed array of CONV_FIXED_SCRATCH_BYTES that the library declares in device
  * memory.  Every GPU that loads the library holds that array until the
  * process exits.
  *
  * When that scratch would exceed the array, the call runs the problem on a
  * variant that needs none, if there is one: the gather tensor-core kernel in
- * place of the shifted-window one, or k summed in one range in place of an
- * automatic split.  Such a call gives results within the same error bound as
+ * place of the shifted-window one, the CUDA-core kernel gathering its input
+ * from x in place of the unfolded copy, or k summed in one range in place of
+ * an automatic split.  Such a call gives results within the same error bound as
  * conv_forward's, but not necessarily the same bits (another summation order).
  *
  * Nothing is allocated by this call.  The first call on each device looks up

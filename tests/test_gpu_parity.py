@@ -49,7 +49,7 @@ REDUCED = {
     "mbv3_pw1x1_f16": (2, 28, 28),
     "grouped_dil2_f32": (1, 28, 28),
     "late_1x1_splitk_f32": (1, 7, 7),
-    "strided_3x3_s2_f32": (1, 30, 30),
+    "strided_3x3_s2_f32": (1, 32, 32),
 }
 
 EXPECTED = {
@@ -157,12 +157,23 @@ EDGE = [
 ]
 
 
+def _out_width(xs, ws, g):
+    st = g.get("stride", 1)
+    sw = st if isinstance(st, int) else st[1]
+    d = g.get("dilation", 1)
+    dw = d if isinstance(d, int) else d[1]
+    pd = g.get("pads", 0)
+    pl, pr = (pd, pd) if isinstance(pd, int) else ((pd[1], pd[1]) if len(pd) == 2 else (pd[1], pd[3]))
+    return (xs[3] + pl + pr - dw * (ws[3] - 1) - 1) // sw + 1
+
+
 def _edge_params():
     """(case, dtype, path) combinations that run distinct code: every case in
     every element type on the planned variant; the forced CUDA-core kernel
     where the plan is something else (16-bit types, depthwise shapes); the
     gather tensor-core kernel in place of the shifted-window one on the
-    win_* shapes."""
+    win_* shapes; the CUDA-core kernel with its unfolded-input pre-pass
+    wherever the output width is a multiple of 4."""
     out = []
     for case in EDGE:
         name = case[0]
@@ -172,6 +183,8 @@ def _edge_params():
                 out.append(pytest.param(case, dtype, "ffma", id=f"ffma-{name}-{dtype}"))
             if dtype != "f32" and name.startswith("win_"):
                 out.append(pytest.param(case, dtype, "gather", id=f"gather-{name}-{dtype}"))
+            if _out_width(case[1], case[2], case[3]) % 4 == 0:
+                out.append(pytest.param(case, dtype, "unfold", id=f"unfold-{name}-{dtype}"))
     return out
 
 
@@ -183,11 +196,15 @@ def test_edge_cases(case, dtype, path):
     ho, wo = conv.conv_output_shape(p)
     rs = (xs[0], ws[0], ho, wo) if res else None
     inp = random_layer_inputs(xs, ws, dtype, seed=zlib.crc32(name.encode()) % 10000, bias=bias, residual_shape=rs)
-    flags = {"auto": 0, "ffma": conv.FLAG_FORCE_FFMA, "gather": conv.FLAG_NO_WINDOW}[path]
+    flags = {"auto": 0, "ffma": conv.FLAG_FORCE_FFMA, "gather": conv.FLAG_NO_WINDOW,
+             "unfold": conv.FLAG_FORCE_FFMA | conv.FLAG_FORCE_UNFOLD}[path]
     if name.startswith("win_") and dtype != "f32" and path == "auto":
         desc = conv.conv_describe_variant(p)
         assert desc.startswith("igemm_tcgen05_window"), desc
-    if name.startswith("gd_") and dtype == "f32":
+    if path == "unfold":
+        desc = conv.conv_describe_variant(conv.make_problem(xs, ws, dtype=dtype, flags=flags, **g))
+        assert "B=unfolded" in desc, desc
+    if name.startswith("gd_") and dtype == "f32" and path == "auto":
         desc = conv.conv_describe_variant(p)
         assert desc.startswith("igemm_ffma grouped"), desc
     y = run_gpu(inp, flags=flags, **g)
@@ -199,13 +216,16 @@ def test_edge_cases(case, dtype, path):
         assert out["max_scaled_err"] < 1e-5, out
 
 
+@pytest.mark.parametrize("unfold", [False, True])
 @pytest.mark.parametrize("split", [2, 3, 7])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_forced_split_k(split, dtype):
-    xs, ws = (2, 64, 9, 9), (24, 64, 3, 3)
+def test_forced_split_k(split, dtype, unfold):
+    xs, ws = (2, 64, 9, 12), (24, 64, 3, 3)
     g = dict(pads=1, act="silu")
-    inp = random_layer_inputs(xs, ws, dtype, seed=split, bias=True, residual_shape=(2, 24, 9, 9))
+    inp = random_layer_inputs(xs, ws, dtype, seed=split, bias=True, residual_shape=(2, 24, 9, 12))
     flags = conv.FLAG_FORCE_FFMA | (split << conv.SPLIT_K_SHIFT)
+    if unfold:
+        flags |= conv.FLAG_FORCE_UNFOLD
     y = run_gpu(inp, flags=flags, **g)
     out = check_full(inp, dtype, y, **g)
     assert out["ok"], out

@@ -1,8 +1,9 @@
 """conv_forward_fixed_scratch: the forward call for callers that cannot
 allocate device memory (a plug-in whose host framework owns all allocations,
-a path that must not enter the allocator).  Its scratch -- split-k planes or
-the shifted-window kernel's repacked weights -- lives in the library's own
-fixed device array instead of caller memory.
+a path that must not enter the allocator).  Its scratch -- split-k planes,
+the shifted-window kernel's repacked weights, the CUDA-core kernel's
+unfolded input -- lives in the library's own fixed device array instead of
+caller memory.
 
 This file is collected last on purpose.  Every call here is compared bit for
 bit with the ordinary entry point on the same inputs, and calls alternate
@@ -111,6 +112,16 @@ def test_fixed_scratch_split_too_large_runs_unsplit():
     p = c[0]
     assert conv.conv_scratch_bytes(p) > conv.FIXED_SCRATCH_BYTES
     _check(c, extra_flags=conv.FLAG_NO_SPLIT_K)
+
+
+def test_fixed_scratch_unfolded_too_large_runs_gathered():
+    """The CUDA-core kernel's unfolded input copy past the array: the same
+    kernel with its B operand gathered from x, which needs no scratch."""
+    c = _case((4, 256, 28, 28), (512, 256, 3, 3), "f32", seed=48, pads=1, act="relu")
+    p = c[0]
+    assert "B=unfolded" in conv.conv_describe_variant(p)
+    assert conv.conv_scratch_bytes(p) > conv.FIXED_SCRATCH_BYTES
+    _check(c, extra_flags=conv.FLAG_NO_UNFOLD)
 
 
 def test_fixed_scratch_refuses_oversize_forced_split():
