@@ -138,6 +138,9 @@ EXPECTED_VARIANT = {
 }
 
 
+UNFOLDED = {"strided_3x3_s2_f32"}   # CUDA-core layers planned with the unfolded-input pre-pass
+
+
 @pytest.mark.parametrize("name", sorted(LAYERS))
 def test_plans_of_the_workloads(lib, name):
     L = LAYERS[name]
@@ -160,6 +163,17 @@ def test_plans_of_the_workloads(lib, name):
         assert plan["ctas"] <= 152
         p2 = _layer_problem(L, flags=conv.FLAG_NO_WINDOW)
         assert conv.conv_plan(p2, 152)["variant_name"] == "igemm_tcgen05"
+        assert conv.conv_plan(p2, 152)["scratch_bytes"] == 0
+    elif name in UNFOLDED:
+        # the unfolded input (float32 n x c_in x kw x hu x Wo, hu the padded
+        # rows the windows reach) on a 256-byte boundary, then the transposed
+        # weights (groups x k x channels rounded to 4)
+        hu = (plan["ho"] - 1) * L.stride[0] + (L.kh - 1) * L.dilation[0] + 1
+        xw = L.n * L.c_in * L.kw * hu * plan["wo"] * 4
+        mg4 = (L.c_out // L.groups + 3) // 4 * 4
+        wt = L.groups * plan["gemm_k"] * mg4 * 4
+        assert plan["scratch_bytes"] == (xw + 255) // 256 * 256 + wt
+        p2 = _layer_problem(L, flags=conv.FLAG_NO_UNFOLD)
         assert conv.conv_plan(p2, 152)["scratch_bytes"] == 0
     else:
         assert plan["scratch_bytes"] == 0
