@@ -238,9 +238,11 @@ def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
     variant = conv.conv_describe_variant(p)
     need = conv.conv_scratch_bytes(p)
     plan = conv.conv_plan(p, torch.cuda.get_device_properties(local_rank).multi_processor_count)
-    # kernels one call launches: split k adds the ordered-sum pass, the
-    # shifted-window variant its weight repack
-    launches_per_step = 2 if (plan["split_k"] > 1 or variant.startswith("igemm_tcgen05_window")) else 1
+    # kernels one call launches, as the library describes its plan
+    m = re.search(r"launches=(\d+)", variant)
+    if not m:
+        raise RuntimeError(f"variant description without a launch count: {variant}")
+    launches_per_step = int(m.group(1))
     set_bytes = layer_bytes(L)
     nsets = max(1, min(256, math.ceil(2 * L2_BYTES / set_bytes)))  # tiny layers stay L2-resident
     sets = []

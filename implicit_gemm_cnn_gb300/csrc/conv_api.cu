@@ -76,12 +76,19 @@ conv_status validate(const conv_problem* p, Shape* s) {
   return CONV_OK;
 }
 
+// Resident blocks of a CUDA-core config per SM: threads (2048), shared memory,
+// and registers -- each of the SM's four schedulers has a 16K-register file,
+// allocated per warp in units of 256, and a block's warps are spread over the
+// four, so a block of w warps fits as long as every scheduler can hold its
+// share.
 int occupancy_estimate(const FfmaCfg& c, size_t smem) {
   const int t = c.threads();
-  const int regs = c.tm * c.tn + 48;
+  const int warps = (t + 31) / 32;
+  const int per_warp = (ffma_cfg_regs(c) * 32 + 255) / 256 * 256;
+  const int warps_per_quarter = 16384 / per_warp;
   int occ = 2048 / t;
   occ = std::min(occ, static_cast<int>(kMaxDynSmem / std::max<size_t>(smem, 1)));
-  occ = std::min(occ, 65536 / (t * regs));
+  occ = std::min(occ, 4 * warps_per_quarter / warps);
   return std::max(occ, 1);
 }
 
@@ -109,36 +116,51 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   // Per-SM time model: an SM runs ceil(blocks / SMs) tiles of bm x bn outputs
   // (padding included) at a rate set by the register tile, slowed when fewer
   // than 8 warps are resident to hide latency.  Lowest time wins; ties go to
-  // the earlier (larger) tile.  With unfolded B the model follows the waves:
-  // the resident blocks of an SM run in rounds of `occupancy`, the last
-  // round perhaps partly filled, each round at a speed set by its warps
-  // (12 resident warps to hide the pipeline's latency).
+  // the earlier (larger) tile.  With unfolded B the model follows the rounds
+  // of resident blocks (`occupancy` per SM) and prices the tail split below:
+  // the tiles of a last round that would fill at most half the device run as
+  // s k ranges each, s = min(8, slots / tail tiles, k / 128).
   double best = 0.0;
-  int bi = -1;
+  int bi = -1, best_tail = 0;
   for (int i = 0; i < kNumFfmaCfgs; ++i) {
     const FfmaCfg& c = kFfmaCfgs[i];
-    if (!unf && i >= kFfmaFirstWide) continue;
     const long long tm = (s.mg + c.bm - 1) / c.bm, tn = (s.npix + c.bn - 1) / c.bn;
     const long long ctas = tm * tn * p->groups;
     if (tm * p->groups > 65535) continue;
     const long long per_sm = (ctas + sm - 1) / sm;
     const int occ = occupancy_estimate(c, ffma_smem_bytes(i, static_cast<int>(s.K)));
-    const double base = c.tm * c.tn >= 64 ? (c.tn == 12 ? 1.05 : 1.0) : (c.tm * c.tn == 32 ? 0.85 : 0.6);
+    const double base = c.tm * c.tn >= 64 ? 1.0 : (c.tm * c.tn == 32 ? 0.85 : 0.6);
     double t;
+    int tail = 0;
     if (!unf) {
       const double warps = static_cast<double>(std::min<long long>(per_sm, occ)) * c.threads() / 32.0;
       const double speed = base * std::min(1.0, warps / 8.0);
       t = static_cast<double>(per_sm) * c.bm * c.bn / speed;
     } else {
-      const long long rounds = (per_sm + occ - 1) / occ;
-      const long long last = per_sm - (rounds - 1) * occ;
       auto speed = [&](long long blocks) {
         return base * std::min(1.0, static_cast<double>(blocks) * c.threads() / 32.0 / 12.0);
       };
       const double work = static_cast<double>(c.bm) * c.bn;
-      t = static_cast<double>(rounds - 1) * occ * work / speed(occ) + static_cast<double>(last) * work / speed(last);
+      const long long slots = static_cast<long long>(sm) * occ;
+      const double t_round = occ * work / speed(occ);
+      const long long full = ctas / slots, rest = ctas % slots;
+      // whole rounds plus the last one as it is ...
+      const long long last_per_sm = (rest + sm - 1) / sm;
+      t = full * t_round + (rest ? last_per_sm * work / speed(last_per_sm) : 0.0);
+      // ... or its tiles split in k
+      if (full >= 1 && rest > 0 && 2 * rest <= slots && s.K >= 256 && p->groups == 1) {
+        const long long ts = std::min<long long>({8, slots / rest, s.K / 128});
+        if (ts >= 2) {
+          const long long units_per_sm = (rest * ts + sm - 1) / sm;
+          const double t_tail = full * t_round + units_per_sm * (work / ts) / speed(units_per_sm);
+          if (t_tail < t) {
+            t = t_tail;
+            tail = static_cast<int>(ts);
+          }
+        }
+      }
     }
-    if (bi < 0 || t < best * (1.0 - 1e-9)) { best = t; bi = i; }
+    if (bi < 0 || t < best * (1.0 - 1e-9)) { best = t; bi = i; best_tail = tail; }
   }
   if (bi < 0) bi = 0;
   const FfmaCfg& c = kFfmaCfgs[bi];
@@ -182,10 +204,24 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   out->info.ctas = ctas * split;
   uint64_t scratch = split > 1 ? static_cast<uint64_t>(split) * s.y_elems * sizeof(float) : 0;
   if (unf) {
-    // after the split planes: the unfolded x, then the transposed weights
+    // after the split planes: the unfolded x, then the transposed weights,
+    // then the raw tiles of a tail split
     u.xw_off = (scratch + 255) / 256 * 256;
     u.wt_off = (u.xw_off + static_cast<uint64_t>(u.xw_elems) * sizeof(float) + 255) / 256 * 256;
     scratch = u.wt_off + static_cast<uint64_t>(u.wt_elems) * sizeof(float);
+    u.tiles = ctas;
+    if (split == 1 && best_tail > 0) {
+      const int occ = occupancy_estimate(c, ffma_smem_bytes(bi, static_cast<int>(s.K)));
+      const long long slots = static_cast<long long>(sm) * occ;
+      const long long rest = ctas % slots;
+      u.tail_split = best_tail;
+      u.tail_len = static_cast<int>(((s.K + best_tail - 1) / best_tail + kFfmaBK - 1) / kFfmaBK * kFfmaBK);
+      u.tail_split = static_cast<int>((s.K + u.tail_len - 1) / u.tail_len);  // ranges that hold terms
+      u.tail_first = ctas - rest;
+      u.tail_off = (scratch + 255) / 256 * 256;
+      scratch = u.tail_off + static_cast<uint64_t>(rest) * u.tail_split * c.bm * c.bn * sizeof(float);
+      out->info.ctas = u.tail_first + rest * u.tail_split;
+    }
     out->unf = u;
   }
   out->info.scratch_bytes = scratch;
@@ -437,6 +473,9 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
   st = make_plan(p, sm, &plan, nullptr);
   if (st != CONV_OK) return st;
   const conv_plan_info& i = plan.info;
+  const int launches = (i.variant == CONV_VARIANT_IGEMM_FFMA || i.variant == CONV_VARIANT_IGEMM_FFMA_SPLIT)
+                           ? ffma_launch_count(plan)
+                           : (i.variant == CONV_VARIANT_IGEMM_TC_WINDOW ? 2 : 1);
   if (i.variant == CONV_VARIANT_IGEMM_TC) {
     static const char* orders[] = {"tap/8-channel", "channel/row/8-tap", "channel/tap"};
     snprintf(buf, len, "%s tile=128px x %dco k=%lld (padded %d, %s order) stages=%d blocks=%lld sms=%d",
@@ -463,11 +502,18 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
              plan.dw.th, plan.dw.in_rows, plan.dw.row, static_cast<long long>(i.ctas), sm);
   } else {
     const FfmaCfg& c = kFfmaCfgs[plan.ffma_cfg];
-    snprintf(buf, len, "%s tile=%dco x %dpx (%dx%d per thread) B=%s split_k=%d blocks=%lld scratch=%llu sms=%d",
+    char tail[64] = "";
+    if (plan.ffma_unf && plan.unf.tail_split > 0)
+      snprintf(tail, sizeof(tail), " tail=%lld tiles x %d k ranges", static_cast<long long>(plan.unf.tiles - plan.unf.tail_first),
+               plan.unf.tail_split);
+    snprintf(buf, len, "%s tile=%dco x %dpx (%dx%d per thread) B=%s split_k=%d%s blocks=%lld scratch=%llu sms=%d",
              variant_name(i.variant), i.tile_m, i.tile_n, c.tm, c.tn,
-             plan.ffma_unf ? "unfolded" : (plan.ffma_vec ? "pointwise" : "gathered"), i.split_k,
+             plan.ffma_unf ? "unfolded" : (plan.ffma_vec ? "pointwise" : "gathered"), i.split_k, tail,
              static_cast<long long>(i.ctas), static_cast<unsigned long long>(i.scratch_bytes), sm);
   }
+  // the number of kernels one call launches, last
+  const size_t used = strlen(buf);
+  if (used + 1 < len) snprintf(buf + used, len - used, " launches=%d", launches);
   return CONV_OK;
 }
 
@@ -543,6 +589,15 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
         a.wtt = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan.unf.wt_off);
         a.hu = plan.unf.hu;
         a.mg4 = plan.unf.mg4;
+        if (plan.unf.tail_split > 0) {
+          const FfmaCfg& c = kFfmaCfgs[plan.ffma_cfg];
+          a.tail_split = plan.unf.tail_split;
+          a.tail_len = plan.unf.tail_len;
+          a.tiles_gy = static_cast<int>((s.mg + c.bm - 1) / c.bm * p->groups);
+          a.tail_first = plan.unf.tail_first;
+          a.tail_tiles = plan.unf.tiles - plan.unf.tail_first;
+          a.tailbuf = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan.unf.tail_off);
+        }
       }
       err = launch_ffma(plan, a, p->dtype, cs);
       if (err == cudaSuccess && a.split > 1) err = launch_split_reduce(a, p->dtype, cs);

@@ -38,6 +38,11 @@ struct ConvArgs {
   float* xw;               // unfolded B: the column-unfolded x (float32), or nullptr
   float* wtt;              // unfolded B: the transposed weights [g][k][mg4]
   int hu, mg4;             // unfolded B: padded input rows, channels per group rounded to 4
+  // tail split (unfolded B): 1-D grid of tail_first whole tiles, then
+  // tail_tiles x tail_split k ranges of tail_len terms into tailbuf
+  int tail_split, tail_len, tiles_gy;
+  long long tail_first, tail_tiles;
+  float* tailbuf;
 };
 
 enum Act {

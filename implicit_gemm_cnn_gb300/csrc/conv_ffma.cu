@@ -122,12 +122,36 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
   const T* __restrict__ x = static_cast<const T*>(a.x);
   const T* __restrict__ wt = static_cast<const T*>(a.wt);
   const int tid = threadIdx.x;
-  const long long pix0 = static_cast<long long>(blockIdx.x) * BN;
+  // ---- the block's tile and k range ------------------------------------------
+  // A 3-D grid (pixel tile, group x channel tile, k range), or with a tail
+  // split a 1-D grid: tiles [0, tail_first) whole, then tail_split k ranges of
+  // each remaining tile (tile index = pixel tile x tiles_gy + channel tile).
+  long long px_tile;
+  int gy, k_begin, k_end, tail_part = -1;
+  long long tail_tile = 0;
+  if (BMODE == kBUnfolded && a.tail_split > 0) {
+    const long long b = blockIdx.x;
+    long long t = b;
+    if (b >= a.tail_first) {
+      const long long u = b - a.tail_first;
+      t = a.tail_first + u / a.tail_split;
+      tail_part = static_cast<int>(u % a.tail_split);
+      tail_tile = t - a.tail_first;
+    }
+    px_tile = t / a.tiles_gy;
+    gy = static_cast<int>(t % a.tiles_gy);
+    k_begin = tail_part < 0 ? 0 : tail_part * a.tail_len;
+    k_end = tail_part < 0 ? a.K : min(a.K, k_begin + a.tail_len);
+  } else {
+    px_tile = blockIdx.x;
+    gy = blockIdx.y;
+    k_begin = blockIdx.z * a.k_per_split;
+    k_end = min(a.K, k_begin + a.k_per_split);
+  }
+  const long long pix0 = px_tile * BN;
   const int co_tiles = (a.mg + BM - 1) / BM;
-  const int g = blockIdx.y / co_tiles;
-  const int m0 = (blockIdx.y % co_tiles) * BM;
-  const int k_begin = blockIdx.z * a.k_per_split;
-  const int k_end = min(a.K, k_begin + a.k_per_split);
+  const int g = gy / co_tiles;
+  const int m0 = (gy % co_tiles) * BM;
   const int khw = a.kh * a.kw;
 
   // ---- the pixel columns this thread stages (gathered B) -------------------
@@ -310,7 +334,20 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
     cp_async_wait<0>();
   }
 
-  // ---- store: raw partial planes (split k) or the fused epilogue -----------
+  // ---- store: a raw tail range, raw partial planes (split k), or the fused
+  // epilogue ----------------------------------------------------------------
+  if (tail_part >= 0) {
+    float* tb = a.tailbuf + (tail_tile * a.tail_split + tail_part) * static_cast<long long>(BM * BN);
+#pragma unroll
+    for (int jg = 0; jg < TN / 4; ++jg)
+#pragma unroll
+      for (int i = 0; i < TM; ++i) {
+        const int ml = i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4);
+        *reinterpret_cast<float4*>(tb + ml * BN + jg * GN + tx * 4) =
+            make_float4(acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]);
+      }
+    return;
+  }
   const long long total = static_cast<long long>(a.n) * a.c_out * a.howo;
   T* y = static_cast<T*>(a.y);
 #pragma unroll
@@ -375,19 +412,26 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
 }
 
 // The unfolded-B pre-pass.  Blocks [0, planes) unfold one input plane (n, c)
-// each into xw[n][c][v][r][ow] (float32, 16-byte stores, zeros outside x);
-// the blocks after them transpose the weights into wtt[g][k][m] (float32,
-// channels padded to mg4 with zeros) through 32 x 32 shared-memory tiles.
+// each into xw[n][c][v][r][ow] (float32, 16-byte stores, zeros outside x),
+// reading the plane once, coalesced, into shared memory when it fits
+// (`staged`); the blocks after them transpose the weights into wtt[g][k][m]
+// (float32, channels padded to mg4 with zeros) through 32 x 32 tiles.
 template <typename T>
 __global__ void __launch_bounds__(256) ffma_unfold(const ConvArgs a, long long planes, int wt_tiles_k,
-                                                   int wt_tiles_m) {
+                                                   int wt_tiles_m, int staged) {
   __shared__ float tile[32][33];
+  extern __shared__ float plane_s[];  // the input plane when staged
   const T* __restrict__ x = static_cast<const T*>(a.x);
   const T* __restrict__ w = static_cast<const T*>(a.wt);
   const int tid = threadIdx.x;
   if (blockIdx.x < planes) {
     const long long nc = blockIdx.x;
     const T* __restrict__ plane = x + nc * a.hw;
+    const int hw = static_cast<int>(a.hw);
+    if (staged) {
+      for (int e = tid; e < hw; e += 256) plane_s[e] = to_f32(plane[e]);
+      __syncthreads();
+    }
     const int wq = a.wo / 4;
     const int units = a.kw * a.hu * wq;
     float* out = a.xw + nc * static_cast<long long>(a.kw) * a.hu * a.wo;
@@ -397,12 +441,13 @@ __global__ void __launch_bounds__(256) ffma_unfold(const ConvArgs a, long long p
       const int r = t % a.hu, v = t / a.hu;
       const int ih = r - a.pt;
       const bool rok = static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
-      const T* __restrict__ row = plane + static_cast<long long>(rok ? ih : 0) * a.w;
+      const int row = (rok ? ih : 0) * a.w;
       float o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int iw = (ow4 * 4 + j) * a.sw - a.pl + v * a.dw;
-        o[j] = rok && static_cast<unsigned>(iw) < static_cast<unsigned>(a.w) ? to_f32(row[iw]) : 0.0f;
+        const bool ok = rok && static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
+        o[j] = ok ? (staged ? plane_s[row + iw] : to_f32(plane[row + iw])) : 0.0f;
       }
       *reinterpret_cast<float4*>(out + static_cast<long long>(t) * a.wo + 4 * ow4) = make_float4(o[0], o[1], o[2], o[3]);
     }
@@ -423,6 +468,56 @@ __global__ void __launch_bounds__(256) ffma_unfold(const ConvArgs a, long long p
   for (int i = ty; i < 32; i += 8) {       // write along m
     const int k = kb * 32 + i, m = mb * 32 + tx;
     if (k < a.K && m < a.mg4) a.wtt[(static_cast<long long>(g) * a.K + k) * a.mg4 + m] = tile[tx][i];
+  }
+}
+
+// The tail of a tail-split launch: for every tile of the last round, the
+// float32 sums of its tail_split k ranges added in range order, then the fused
+// epilogue, four pixels of one channel at a time (the output width is a
+// multiple of 4, so four consecutive tile pixels share an image row).
+template <typename T, int BM, int BN>
+__global__ void __launch_bounds__(256) ffma_tail_reduce(const ConvArgs a) {
+  constexpr int Q = BN / 4;
+  const long long units = a.tail_tiles * BM * Q;
+  const int co_tiles = (a.mg + BM - 1) / BM;
+  T* y = static_cast<T*>(a.y);
+  const T* __restrict__ bp = static_cast<const T*>(a.bias);
+  const T* __restrict__ rp = static_cast<const T*>(a.residual);
+  for (long long u = blockIdx.x * 256LL + threadIdx.x; u < units; u += static_cast<long long>(gridDim.x) * 256) {
+    const long long tt = u / (BM * Q);
+    const int rem = static_cast<int>(u - tt * (BM * Q));
+    const int ml = rem / Q, c4 = rem - (rem / Q) * Q;
+    const long long t = a.tail_first + tt;
+    const long long px_tile = t / a.tiles_gy;
+    const int gy = static_cast<int>(t % a.tiles_gy);
+    const int g = gy / co_tiles;
+    const int m = (gy % co_tiles) * BM + ml;
+    const long long p = px_tile * BN + 4 * c4;
+    if (m >= a.mg || p >= a.npix) continue;
+    const float* src = a.tailbuf + tt * a.tail_split * static_cast<long long>(BM * BN) + ml * BN + 4 * c4;
+    float4 sum = *reinterpret_cast<const float4*>(src);
+    for (int r = 1; r < a.tail_split; ++r) {
+      const float4 t4 = *reinterpret_cast<const float4*>(src + r * static_cast<long long>(BM * BN));
+      sum.x = __fadd_rn(sum.x, t4.x); sum.y = __fadd_rn(sum.y, t4.y);
+      sum.z = __fadd_rn(sum.z, t4.z); sum.w = __fadd_rn(sum.w, t4.w);
+    }
+    const int co = g * a.mg + m;
+    const long long n = p / a.howo;
+    const long long out = (n * a.c_out + co) * a.howo + (p - n * a.howo);
+    float v[4] = {sum.x, sum.y, sum.z, sum.w}, bv[4], rv[4];
+    const float bco = bp ? to_f32(bp[co]) : 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      bv[q] = bco;
+      rv[q] = rp ? to_f32(rp[out + q]) : 0.0f;
+    }
+    epilogue_n<4>(v, bv, rv, bp != nullptr, rp != nullptr, a.act, a.alpha, a.beta);
+    if (a.vec_out) {
+      store4<T>(y, out, v);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) y[out + q] = from_f32<T>(v[q]);
+    }
   }
 }
 
@@ -654,6 +749,18 @@ cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   const long long gx = (a.npix + c.bn - 1) / c.bn;
   const int co_tiles = (a.mg + c.bm - 1) / c.bm;
+  if constexpr (BMODE == kBUnfolded) {
+    if (a.tail_split > 0) {
+      const long long blocks = a.tail_first + a.tail_tiles * a.tail_split;
+      kern<<<static_cast<unsigned>(blocks), c.threads(), smem, s>>>(a, ktab_cap);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+      const long long units = a.tail_tiles * c.bm * (c.bn / 4);
+      const long long rblocks = std::min<long long>((units + 255) / 256, 65535LL * 8);
+      ffma_tail_reduce<T, c.bm, c.bn><<<static_cast<unsigned>(rblocks), 256, 0, s>>>(a);
+      return cudaGetLastError();
+    }
+  }
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(co_tiles * a.groups),
             static_cast<unsigned>(a.split));
   kern<<<grid, c.threads(), smem, s>>>(a, ktab_cap);
@@ -664,16 +771,14 @@ cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
 template <typename T, int CFG>
 cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   if (a.xw) return launch_cfg_vb<T, CFG, kBUnfolded>(plan, a, s);
-  if constexpr (CFG >= kFfmaFirstWide) {
-    return cudaErrorInvalidConfiguration;  // wide tiles are planned with unfolded B only
-  } else {
-    if constexpr (sizeof(T) == 4) {
-      if (plan.ffma_vec && reinterpret_cast<uintptr_t>(a.x) % 16 == 0)
-        return launch_cfg_vb<T, CFG, kBPointwise>(plan, a, s);
-    }
-    return launch_cfg_vb<T, CFG, kBGather>(plan, a, s);
+  if constexpr (sizeof(T) == 4) {
+    if (plan.ffma_vec && reinterpret_cast<uintptr_t>(a.x) % 16 == 0)
+      return launch_cfg_vb<T, CFG, kBPointwise>(plan, a, s);
   }
+  return launch_cfg_vb<T, CFG, kBGather>(plan, a, s);
 }
+
+constexpr long long kUnfoldStageMax = 12288;  // plane elements staged in shared memory (48 KB)
 
 template <typename T>
 cudaError_t launch_unfold(const UnfPlan& u, const ConvArgs& a, cudaStream_t s) {
@@ -681,7 +786,9 @@ cudaError_t launch_unfold(const UnfPlan& u, const ConvArgs& a, cudaStream_t s) {
   const int tk = (a.K + 31) / 32, tm = (u.mg4 + 31) / 32;
   const long long blocks = planes + static_cast<long long>(a.groups) * tk * tm;
   if (blocks > 2147483647LL) return cudaErrorInvalidConfiguration;
-  ffma_unfold<T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a, planes, tk, tm);
+  const int staged = a.hw <= kUnfoldStageMax ? 1 : 0;
+  const size_t smem = staged ? static_cast<size_t>(a.hw) * sizeof(float) : 0;
+  ffma_unfold<T><<<static_cast<unsigned>(blocks), 256, smem, s>>>(a, planes, tk, tm, staged);
   return cudaGetLastError();
 }
 
@@ -697,8 +804,6 @@ cudaError_t launch_typed(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
     case 6: return launch_cfg<T, 6>(plan, a, s);
     case 7: return launch_cfg<T, 7>(plan, a, s);
     case 8: return launch_cfg<T, 8>(plan, a, s);
-    case 9: return launch_cfg<T, 9>(plan, a, s);
-    case 10: return launch_cfg<T, 10>(plan, a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -723,6 +828,14 @@ size_t ffma_smem_bytes(int cfg, int k_per_block) {
   const FfmaCfg c = kFfmaCfgs[cfg];
   return static_cast<size_t>(kFfmaStages) * kFfmaBK * (c.bm + 4 + c.bn) * sizeof(float) +
          static_cast<size_t>(ffma_ktab_entries(k_per_block)) * sizeof(int2);
+}
+
+int ffma_launch_count(const Plan& plan) {
+  if (plan.gd.ok) return 1;
+  int n = 1;
+  if (plan.ffma_unf) n += 1 + (plan.unf.tail_split > 0 ? 1 : 0);
+  if (plan.info.split_k > 1) n += 1;
+  return n;
 }
 
 bool unf_plan(const conv_problem* p, long long ho, long long wo, UnfPlan* u) {

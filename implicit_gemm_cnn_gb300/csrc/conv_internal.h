@@ -20,12 +20,14 @@ struct FfmaCfg {
 constexpr int kFfmaBK = 8;          // k terms per pipeline stage
 constexpr int kFfmaStages = 4;      // pipeline depth
 constexpr int kFfmaKTab = 2304;     // k entries of the window table per segment
-constexpr int kNumFfmaCfgs = 11;
-constexpr int kFfmaFirstWide = 9;   // configs from here on: 8 x 12 register tiles, unfolded B only
+constexpr int kNumFfmaCfgs = 9;
 constexpr FfmaCfg kFfmaCfgs[kNumFfmaCfgs] = {
     {128, 128, 8, 8}, {64, 128, 8, 8}, {128, 64, 8, 8}, {64, 64, 4, 4}, {32, 256, 4, 8},
-    {16, 256, 4, 8},  {40, 128, 8, 4}, {16, 64, 4, 4},  {40, 64, 8, 4},
-    {128, 168, 8, 12}, {128, 96, 8, 12}};
+    {16, 256, 4, 8},  {40, 128, 8, 4}, {16, 64, 4, 4},  {40, 64, 8, 4}};
+// Registers a thread of a config is planned with (the kernel's cap).
+constexpr int ffma_cfg_regs(const FfmaCfg& c) {
+  return c.tm * c.tn + 64 > 255 ? 255 : c.tm * c.tn + 64;
+}
 
 size_t ffma_smem_bytes(int cfg, int k_per_block);  // k_per_block: terms one block sums
 int ffma_ktab_entries(int k_per_block);
@@ -49,6 +51,13 @@ struct UnfPlan {
   long long xw_elems;  // N * Cin * kw * hu * Wo
   long long wt_elems;  // groups * K * mg4
   size_t xw_off, wt_off;  // byte offsets of xw and wt in scratch (after any split planes)
+  // The last, partly filled round of tiles split in k: tiles [tail_first,
+  // tiles) run as tail_split ranges of tail_len terms each, writing raw float32
+  // tiles to scratch at tail_off; a second kernel adds the ranges in order and
+  // applies the epilogue.  tail_split = 0: no tail split.
+  int tail_split, tail_len;
+  long long tiles, tail_first;
+  size_t tail_off;
 };
 
 // Depthwise (one input channel per group) halo-tiled direct kernel.
@@ -153,6 +162,8 @@ struct Plan {
 cudaError_t opt_in_smem(const void* func, size_t bytes);
 
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
+// Kernels one conv_forward of the CUDA-core variant launches for `plan`.
+int ffma_launch_count(const Plan& plan);
 // Whether the unfolded-B layout applies to the shape (element type aside),
 // and its sizes; false when a size is past the kernel's 32-bit offsets.
 bool unf_plan(const conv_problem* p, long long ho, long long wo, UnfPlan* u);

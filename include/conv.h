@@ -187,7 +187,8 @@ CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_pla
 CONV_API conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes);
 
 /* Writes a one-line description of what conv_forward runs for `p` on the
- * current device into buf (NUL-terminated, truncated to len). */
+ * current device into buf (NUL-terminated, truncated to len), ending with
+ * "launches=N", the number of kernels one conv_forward call launches. */
 CONV_API conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len);
 
 /* Enqueue y = conv(x, w) + bias + residual, activated, on `stream`.

@@ -172,7 +172,17 @@ def test_plans_of_the_workloads(lib, name):
         xw = L.n * L.c_in * L.kw * hu * plan["wo"] * 4
         mg4 = (L.c_out // L.groups + 3) // 4 * 4
         wt = L.groups * plan["gemm_k"] * mg4 * 4
-        assert plan["scratch_bytes"] == (xw + 255) // 256 * 256 + wt
+        base = (xw + 255) // 256 * 256 + wt
+        # a tail split: the tiles of the last, partly filled round (2 blocks of
+        # 128 x 128 per SM) run as s k ranges each, their raw tiles after the
+        # weights
+        tiles = -(-plan["gemm_n"] // plan["tile_n"]) * -(-plan["gemm_m"] // plan["tile_m"])
+        if plan["ctas"] > tiles:
+            rest = tiles % (2 * 152)
+            s_ranges = 1 + (plan["ctas"] - tiles) // rest
+            assert plan["ctas"] == tiles - rest + rest * s_ranges and 2 <= s_ranges <= 8
+            base = (base + 255) // 256 * 256 + rest * s_ranges * plan["tile_m"] * plan["tile_n"] * 4
+        assert plan["scratch_bytes"] == base
         p2 = _layer_problem(L, flags=conv.FLAG_NO_UNFOLD)
         assert conv.conv_plan(p2, 152)["scratch_bytes"] == 0
     else:

@@ -172,3 +172,20 @@ def test_chained_pair(first, second, size):
         rb = check_sampled(ib_chained, B.dtype, yb.cpu(), count=1500, seed=4, **_geo(B))
     assert ra["ok"], ra
     assert rb["ok"], rb
+
+
+def test_unfolded_tail_split():
+    """The CUDA-core kernel with its unfolded input and the last round of
+    tiles split in k (a second kernel adds the ranges in order)."""
+    xs, ws = (11, 32, 64, 64), (128, 32, 3, 3)
+    g = dict(pads=1, act="silu")
+    p = conv.make_problem(xs, ws, dtype="f32", has_bias=True, has_residual=True, **g)
+    desc = conv.conv_describe_variant(p)
+    assert "B=unfolded" in desc and "tail=" in desc and "launches=3" in desc, desc
+    inp = random_layer_inputs(xs, ws, "f32", seed=91, bias=True, residual_shape=(11, 128, 64, 64))
+    y, _ = _run_offsets(inp, "f32", (0, 0, 0), **g)
+    out = check_full(inp, "f32", y, **g)
+    assert out["ok"], out
+    assert out["max_scaled_err"] < 1e-5, out
+    y2, _ = _run_offsets(inp, "f32", (0, 0, 0), **g)
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))   # fixed order, no atomics
