@@ -778,7 +778,8 @@ cudaError_t launch_cfg(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   return launch_cfg_vb<T, CFG, kBGather>(plan, a, s);
 }
 
-constexpr long long kUnfoldStageMax = 12288;  // plane elements staged in shared memory (48 KB)
+constexpr long long kUnfoldStageMax = 11000;  // plane elements staged in shared memory (with the
+                                              // 4.2 KB transpose tile, under 48 KB)
 
 template <typename T>
 cudaError_t launch_unfold(const UnfPlan& u, const ConvArgs& a, cudaStream_t s) {
