@@ -433,23 +433,31 @@ __global__ void __launch_bounds__(256) ffma_unfold(const ConvArgs a, long long p
       __syncthreads();
     }
     const int wq = a.wo / 4;
-    const int units = a.kw * a.hu * wq;
     float* out = a.xw + nc * static_cast<long long>(a.kw) * a.hu * a.wo;
-    for (int e = tid; e < units; e += 256) {
-      const int ow4 = e % wq;
-      const int t = e / wq;
-      const int r = t % a.hu, v = t / a.hu;
-      const int ih = r - a.pt;
-      const bool rok = static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
-      const int row = (rok ? ih : 0) * a.w;
-      float o[4];
+    // thread = one 4-column group of `rows_per_pass` rows at a time; the
+    // output rows (v, r) are walked without divisions
+    const int tpr = min(wq, 256);
+    const int rows_per_pass = 256 / tpr;
+    const int r0 = tid / tpr;
+    if (r0 >= rows_per_pass) return;
+    for (int ow4 = tid - r0 * tpr; ow4 < wq; ow4 += tpr) {
+      for (int v = 0; v < a.kw; ++v) {
+        const int col0 = ow4 * 4 * a.sw - a.pl + v * a.dw;
+        float* ov = out + static_cast<long long>(v) * a.hu * a.wo + 4 * ow4;
+        for (int r = r0; r < a.hu; r += rows_per_pass) {
+          const int ih = r - a.pt;
+          const bool rok = static_cast<unsigned>(ih) < static_cast<unsigned>(a.h);
+          const int row = (rok ? ih : 0) * a.w;
+          float o[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int iw = (ow4 * 4 + j) * a.sw - a.pl + v * a.dw;
-        const bool ok = rok && static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
-        o[j] = ok ? (staged ? plane_s[row + iw] : to_f32(plane[row + iw])) : 0.0f;
+          for (int j = 0; j < 4; ++j) {
+            const int iw = col0 + j * a.sw;
+            const bool ok = rok && static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
+            o[j] = ok ? (staged ? plane_s[row + iw] : to_f32(plane[row + iw])) : 0.0f;
+          }
+          *reinterpret_cast<float4*>(ov + static_cast<long long>(r) * a.wo) = make_float4(o[0], o[1], o[2], o[3]);
+        }
       }
-      *reinterpret_cast<float4*>(out + static_cast<long long>(t) * a.wo + 4 * ow4) = make_float4(o[0], o[1], o[2], o[3]);
     }
     return;
   }
