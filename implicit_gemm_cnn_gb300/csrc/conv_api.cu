@@ -128,7 +128,7 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
     const long long ctas = tm * tn * p->groups;
     if (tm * p->groups > 65535) continue;
     const long long per_sm = (ctas + sm - 1) / sm;
-    const int occ = occupancy_estimate(c, ffma_smem_bytes(i, static_cast<int>(s.K)));
+    const int occ = occupancy_estimate(c, ffma_smem_bytes(i, static_cast<int>(s.K), unf));
     const double base = c.tm * c.tn >= 64 ? 1.0 : (c.tm * c.tn == 32 ? 0.85 : 0.6);
     double t;
     int tail = 0;
@@ -182,7 +182,8 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   }
   long long len = s.K;
   if (split > 1) {
-    len = ((s.K + split - 1) / split + kFfmaBK - 1) / kFfmaBK * kFfmaBK;
+    const int bk = unf ? kFfmaBKU : kFfmaBK;  // ranges of whole stages
+    len = ((s.K + split - 1) / split + bk - 1) / bk * bk;
     split = static_cast<int>((s.K + len - 1) / len);
   }
   if (split <= 1) { split = 1; len = s.K; }
@@ -211,11 +212,11 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
     scratch = u.wt_off + static_cast<uint64_t>(u.wt_elems) * sizeof(float);
     u.tiles = ctas;
     if (split == 1 && best_tail > 0) {
-      const int occ = occupancy_estimate(c, ffma_smem_bytes(bi, static_cast<int>(s.K)));
+      const int occ = occupancy_estimate(c, ffma_smem_bytes(bi, static_cast<int>(s.K), true));
       const long long slots = static_cast<long long>(sm) * occ;
       const long long rest = ctas % slots;
       u.tail_split = best_tail;
-      u.tail_len = static_cast<int>(((s.K + best_tail - 1) / best_tail + kFfmaBK - 1) / kFfmaBK * kFfmaBK);
+      u.tail_len = static_cast<int>(((s.K + best_tail - 1) / best_tail + kFfmaBKU - 1) / kFfmaBKU * kFfmaBKU);
       u.tail_split = static_cast<int>((s.K + u.tail_len - 1) / u.tail_len);  // ranges that hold terms
       u.tail_first = ctas - rest;
       u.tail_off = (scratch + 255) / 256 * 256;

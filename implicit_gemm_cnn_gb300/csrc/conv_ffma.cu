@@ -96,6 +96,51 @@ __host__ __device__ constexpr int pow2_floor(int v) {
 //    each term's offset, no bounds tests; the weights come transposed (wtt), so
 //    the A tile arrives by 16-byte copies too.
 // TN = 12 (three 4-pixel groups per thread) is used with unfolded B only.
+// The block index, read again where it is used (an asm volatile read cannot be
+// merged with an earlier one): the tile decode below is recomputed for the
+// epilogue instead of keeping its results in registers through the k loop.
+__device__ __forceinline__ unsigned ctaid_x() {
+  unsigned v;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(v));
+  return v;
+}
+__device__ __forceinline__ unsigned ctaid_y() {
+  unsigned v;
+  asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(v));
+  return v;
+}
+
+// A block's tile: a 3-D grid (pixel tile, group x channel tile, k range), or
+// with a tail split a 1-D grid: tiles [0, tail_first) whole, then tail_split
+// k ranges of each remaining tile (tile = pixel tile x tiles_gy + channel tile).
+struct FfmaTile {
+  long long px_tile;
+  int gy;
+  int part;            // tail k range (-1: not a tail block)
+  long long tail_tile; // tile - tail_first for tail blocks
+};
+template <int BMODE>
+__device__ __forceinline__ FfmaTile ffma_tile(const ConvArgs& a, unsigned bx, unsigned by) {
+  FfmaTile r;
+  r.part = -1;
+  r.tail_tile = 0;
+  if (BMODE == kBUnfolded && a.tail_split > 0) {
+    long long t = bx;
+    if (t >= a.tail_first) {
+      const long long u = t - a.tail_first;
+      t = a.tail_first + u / a.tail_split;
+      r.part = static_cast<int>(u % a.tail_split);
+      r.tail_tile = t - a.tail_first;
+    }
+    r.px_tile = t / a.tiles_gy;
+    r.gy = static_cast<int>(t % a.tiles_gy);
+  } else {
+    r.px_tile = bx;
+    r.gy = static_cast<int>(by);
+  }
+  return r;
+}
+
 // Registers per thread for a block of nt threads: two blocks per SM from 192
 // threads on, three from 128 (multiples of 8, the allocation unit).
 __host__ __device__ constexpr int ffma_maxreg(int nt) {
@@ -106,7 +151,7 @@ template <typename T, int BM, int BN, int TM, int TN, int BMODE>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg((BM / TM) * (BN / TN)))
     igemm_ffma(const ConvArgs a, const int ktab_cap) {
   constexpr int NT = (BM / TM) * (BN / TN);
-  constexpr int BK = kFfmaBK;
+  constexpr int BK = BMODE == kBUnfolded ? kFfmaBKU : kFfmaBK;
   constexpr int S = kFfmaStages;
   constexpr int AS = BM + 4;  // padded weight-tile row: conflict-free transposed stores
   constexpr bool VEC = BMODE != kBGather;
@@ -123,35 +168,23 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
   const T* __restrict__ wt = static_cast<const T*>(a.wt);
   const int tid = threadIdx.x;
   // ---- the block's tile and k range ------------------------------------------
-  // A 3-D grid (pixel tile, group x channel tile, k range), or with a tail
-  // split a 1-D grid: tiles [0, tail_first) whole, then tail_split k ranges of
-  // each remaining tile (tile index = pixel tile x tiles_gy + channel tile).
-  long long px_tile;
-  int gy, k_begin, k_end, tail_part = -1;
-  long long tail_tile = 0;
-  if (BMODE == kBUnfolded && a.tail_split > 0) {
-    const long long b = blockIdx.x;
-    long long t = b;
-    if (b >= a.tail_first) {
-      const long long u = b - a.tail_first;
-      t = a.tail_first + u / a.tail_split;
-      tail_part = static_cast<int>(u % a.tail_split);
-      tail_tile = t - a.tail_first;
-    }
-    px_tile = t / a.tiles_gy;
-    gy = static_cast<int>(t % a.tiles_gy);
-    k_begin = tail_part < 0 ? 0 : tail_part * a.tail_len;
-    k_end = tail_part < 0 ? a.K : min(a.K, k_begin + a.tail_len);
-  } else {
-    px_tile = blockIdx.x;
-    gy = blockIdx.y;
-    k_begin = blockIdx.z * a.k_per_split;
-    k_end = min(a.K, k_begin + a.k_per_split);
-  }
-  const long long pix0 = px_tile * BN;
+  int k_begin, k_end;
+  long long pix0;
+  int g, m0;
   const int co_tiles = (a.mg + BM - 1) / BM;
-  const int g = gy / co_tiles;
-  const int m0 = (gy % co_tiles) * BM;
+  {
+    const FfmaTile t = ffma_tile<BMODE>(a, blockIdx.x, blockIdx.y);
+    if (BMODE == kBUnfolded && a.tail_split > 0) {
+      k_begin = t.part < 0 ? 0 : t.part * a.tail_len;
+      k_end = t.part < 0 ? a.K : min(a.K, k_begin + a.tail_len);
+    } else {
+      k_begin = blockIdx.z * a.k_per_split;
+      k_end = min(a.K, k_begin + a.k_per_split);
+    }
+    pix0 = t.px_tile * BN;
+    g = t.gy / co_tiles;
+    m0 = (t.gy % co_tiles) * BM;
+  }
   const int khw = a.kh * a.kw;
 
   // ---- the pixel columns this thread stages (gathered B) -------------------
@@ -189,7 +222,8 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
   // q / (BN/4), pixels pix0 + 4*(q % (BN/4)) .. +3, all in one image row (the
   // plane length, or the output row, is a multiple of 4)
   constexpr int QV = VEC ? (BK * BN / 4 + NT - 1) / NT : 1;
-  long long vbase[QV];
+  long long vbase[BMODE == kBPointwise ? QV : 1];
+  int uoff[BMODE == kBUnfolded ? QV : 1];  // unfolded: 32-bit element offsets into xw
   bool vok[QV];
   if constexpr (VEC) {
     const long long unf_img = static_cast<long long>(a.c_in) * a.kw * a.hu * a.wo;  // xw per image
@@ -205,12 +239,20 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
         vbase[i] = (n * a.c_in + static_cast<long long>(g) * a.cg) * a.hw + rem;
       } else {
         const long long oh = rem / a.wo, ow = rem - oh * a.wo;
-        vbase[i] = n * unf_img + static_cast<long long>(g) * a.cg * a.kw * a.hu * a.wo + oh * a.sh * a.wo + ow;
+        uoff[i] = static_cast<int>(n * unf_img + static_cast<long long>(g) * a.cg * a.kw * a.hu * a.wo +
+                                   oh * a.sh * a.wo + ow);
       }
     }
   }
-  // unfolded A: 16-byte copies of the transposed weights
+  // unfolded A: 16-byte copies of the transposed weights.  Unfolded copies
+  // address xw and wtt with 32-bit element offsets (both hold fewer than 2^31
+  // elements): the pixel part of each B copy (uoff) and the group's first
+  // weight of the block's channel tile (aoff) are fixed for the whole k loop.
   constexpr int QA = BMODE == kBUnfolded ? (BK * BM / 4 + NT - 1) / NT : 1;
+  const int aoff = BMODE == kBUnfolded ? g * a.K * a.mg4 + m0 : 0;
+  bool aok[QA];  // unfolded A: the copy's four channels are real (else zeros)
+#pragma unroll
+  for (int i = 0; i < QA; ++i) aok[i] = m0 + 4 * ((tid + i * NT) % (BM / 4)) < a.mg4;
 
   float acc[TM][TN];
 #pragma unroll
@@ -245,11 +287,11 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
 #pragma unroll
         for (int i = 0; i < QA; ++i) {
           const int q = tid + i * NT;
-          const int kk = q / (BM / 4), m4 = q - (q / (BM / 4)) * (BM / 4);
+          const int kk = q / (BM / 4), m4 = q % (BM / 4);
           const int k = k0 + kk;
-          const bool ok = q < BK * BM / 4 && k < seg_end && m0 + 4 * m4 < a.mg4;
-          const float* src = ok ? a.wtt + (static_cast<long long>(g) * a.K + k) * a.mg4 + m0 + 4 * m4 : a.wtt;
-          if (q < BK * BM / 4) cp_async16(as + kk * AS + 4 * m4, src, ok);
+          const bool ok = k < seg_end && aok[i];
+          const float* src = a.wtt + (ok ? aoff + k * a.mg4 + 4 * m4 : 0);
+          if ((BK * BM / 4) % NT == 0 || q < BK * BM / 4) cp_async16(as + kk * AS + 4 * m4, src, ok);
         }
       } else {
         constexpr int AE = (BM * BK + NT - 1) / NT;
@@ -265,8 +307,18 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
           }
         }
       }
-      if constexpr (VEC) {
-        const float* xb = BMODE == kBPointwise ? reinterpret_cast<const float*>(x) : a.xw;
+      if constexpr (BMODE == kBUnfolded) {
+#pragma unroll
+        for (int i = 0; i < QV; ++i) {
+          const int q = tid + i * NT;
+          const int kk = q / (BN / 4), c4 = q % (BN / 4);
+          const int k = k0 + kk;
+          const bool ok = vok[i] && k < seg_end;
+          const float* src = a.xw + (ok ? uoff[i] + ktab[k - kseg].x : 0);
+          if ((BK * BN / 4) % NT == 0 || q < BK * BN / 4) cp_async16(bs + kk * BN + 4 * c4, src, ok);
+        }
+      } else if constexpr (BMODE == kBPointwise) {
+        const float* xb = reinterpret_cast<const float*>(x);
 #pragma unroll
         for (int i = 0; i < QV; ++i) {
           const int q = tid + i * NT;
@@ -336,8 +388,12 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
 
   // ---- store: a raw tail range, raw partial planes (split k), or the fused
   // epilogue ----------------------------------------------------------------
-  if (tail_part >= 0) {
-    float* tb = a.tailbuf + (tail_tile * a.tail_split + tail_part) * static_cast<long long>(BM * BN);
+  const FfmaTile te = ffma_tile<BMODE>(a, ctaid_x(), ctaid_y());
+  pix0 = te.px_tile * BN;
+  g = te.gy / co_tiles;
+  m0 = (te.gy % co_tiles) * BM;
+  if (te.part >= 0) {
+    float* tb = a.tailbuf + (te.tail_tile * a.tail_split + te.part) * static_cast<long long>(BM * BN);
 #pragma unroll
     for (int jg = 0; jg < TN / 4; ++jg)
 #pragma unroll
@@ -752,7 +808,7 @@ cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   constexpr FfmaCfg c = kFfmaCfgs[CFG];
   auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn, BMODE>;
   const int ktab_cap = ffma_ktab_entries(a.k_per_split);
-  const size_t smem = ffma_smem_bytes(CFG, a.k_per_split);
+  const size_t smem = ffma_smem_bytes(CFG, a.k_per_split, BMODE == kBUnfolded);
   cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   const long long gx = (a.npix + c.bn - 1) / c.bn;
@@ -833,9 +889,9 @@ int ffma_ktab_entries(int k_per_block) {
   return k_per_block < kFfmaKTab ? (k_per_block + 7) / 8 * 8 : kFfmaKTab;
 }
 
-size_t ffma_smem_bytes(int cfg, int k_per_block) {
+size_t ffma_smem_bytes(int cfg, int k_per_block, bool unfolded) {
   const FfmaCfg c = kFfmaCfgs[cfg];
-  return static_cast<size_t>(kFfmaStages) * kFfmaBK * (c.bm + 4 + c.bn) * sizeof(float) +
+  return static_cast<size_t>(kFfmaStages) * (unfolded ? kFfmaBKU : kFfmaBK) * (c.bm + 4 + c.bn) * sizeof(float) +
          static_cast<size_t>(ffma_ktab_entries(k_per_block)) * sizeof(int2);
 }
 
@@ -853,11 +909,13 @@ bool unf_plan(const conv_problem* p, long long ho, long long wo, UnfPlan* u) {
   const long long hu = (ho - 1) * p->stride_h + (p->kh - 1) * p->dil_h + 1;
   const long long cg = p->c_in / p->groups, mg = p->c_out / p->groups;
   const long long per_group = cg * p->kw * hu * wo;  // the largest term offset (int32)
-  if (hu > 2147483647LL || per_group > 2147483647LL || p->c_in * p->kw * hu * wo > 2147483647LL) return false;
+  if (hu > 2147483647LL || per_group > 2147483647LL) return false;
   u->hu = static_cast<int>(hu);
   u->mg4 = static_cast<int>((mg + 3) / 4 * 4);
   u->xw_elems = p->n * p->c_in * p->kw * hu * wo;
   u->wt_elems = p->groups * cg * p->kh * p->kw * u->mg4;
+  // the kernel addresses both with 32-bit element offsets
+  if (u->xw_elems >= 2147483647LL || u->wt_elems >= 2147483647LL) return false;
   return true;
 }
 

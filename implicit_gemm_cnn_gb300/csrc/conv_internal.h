@@ -18,6 +18,7 @@ struct FfmaCfg {
   int threads() const { return (bm / tm) * (bn / tn); }
 };
 constexpr int kFfmaBK = 8;          // k terms per pipeline stage
+constexpr int kFfmaBKU = 8;         // k terms per stage with unfolded B (16-byte copies only)
 constexpr int kFfmaStages = 4;      // pipeline depth
 constexpr int kFfmaKTab = 2304;     // k entries of the window table per segment
 constexpr int kNumFfmaCfgs = 9;
@@ -29,7 +30,7 @@ constexpr int ffma_cfg_regs(const FfmaCfg& c) {
   return c.tm * c.tn + 64 > 255 ? 255 : c.tm * c.tn + 64;
 }
 
-size_t ffma_smem_bytes(int cfg, int k_per_block);  // k_per_block: terms one block sums
+size_t ffma_smem_bytes(int cfg, int k_per_block, bool unfolded);  // k_per_block: terms one block sums
 int ffma_ktab_entries(int k_per_block);
 
 // The B operand of the CUDA-core kernel.
