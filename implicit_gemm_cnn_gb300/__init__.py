@@ -24,6 +24,7 @@ __all__ = [
     "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "FLAG_NO_UNFOLD", "FLAG_FORCE_UNFOLD", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
     "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
+    "conv_apply_auto_pad", "AUTO_PAD",
     "make_problem", "conv2d", "library_path", "load",
 ]
 
@@ -118,8 +119,9 @@ def load() -> ctypes.CDLL:
         lib.conv_forward.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_device_error.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         lib.conv_forward_fixed_scratch.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp]
+        lib.conv_apply_auto_pad.argtypes = [P(ConvProblem), ctypes.c_int32]
         for f in ("conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
-                  "conv_forward", "conv_device_error", "conv_forward_fixed_scratch"):
+                  "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "conv_apply_auto_pad"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -152,6 +154,15 @@ def conv_output_shape(p: ConvProblem) -> tuple[int, int]:
     _check(load().conv_output_shape(ctypes.byref(p), ctypes.byref(ho), ctypes.byref(wo)),
            "conv_output_shape")
     return ho.value, wo.value
+
+
+AUTO_PAD = {"NOTSET": 0, "SAME_UPPER": 1, "SAME_LOWER": 2, "VALID": 3}
+
+
+def conv_apply_auto_pad(p: ConvProblem, mode: str) -> ConvProblem:
+    """Set p's pads from ONNX auto_pad `mode` (in place; p is returned)."""
+    _check(load().conv_apply_auto_pad(ctypes.byref(p), AUTO_PAD[mode]), "conv_apply_auto_pad")
+    return p
 
 
 def conv_plan(p: ConvProblem, sm_count: int) -> dict:
@@ -230,15 +241,18 @@ def _pads(v) -> tuple[int, int, int, int]:
 
 def make_problem(x_shape, w_shape, *, dtype="f32", stride=1, pads=0, dilation=1, groups=1,
                  act="identity", alpha=0.0, beta=0.0, has_bias=False, has_residual=False,
-                 flags=0) -> ConvProblem:
+                 flags=0, auto_pad="NOTSET") -> ConvProblem:
     n, c_in, h, w = (int(v) for v in x_shape)
     c_out, _, kh, kw = (int(v) for v in w_shape)
     sh, sw = _pair(stride)
     dh, dw = _pair(dilation)
     pt, pl, pb, pr = _pads(pads)
-    return ConvProblem(n, c_in, h, w, c_out, kh, kw, pt, pl, pb, pr, sh, sw, dh, dw, int(groups),
-                       ACTIVATIONS[act], float(alpha), float(beta), DTYPES[dtype],
-                       1 if has_bias else 0, 1 if has_residual else 0, int(flags))
+    p = ConvProblem(n, c_in, h, w, c_out, kh, kw, pt, pl, pb, pr, sh, sw, dh, dw, int(groups),
+                    ACTIVATIONS[act], float(alpha), float(beta), DTYPES[dtype],
+                    1 if has_bias else 0, 1 if has_residual else 0, int(flags))
+    if auto_pad != "NOTSET":
+        conv_apply_auto_pad(p, auto_pad)
+    return p
 
 
 _TORCH_DT = None
@@ -255,11 +269,12 @@ def _dtype_name(t) -> str:
 
 
 def conv2d(x, w, bias=None, residual=None, *, stride=1, pads=0, dilation=1, groups=1,
-           act="identity", alpha=0.0, beta=0.0, out=None, scratch=None, flags=0, stream=None):
+           act="identity", alpha=0.0, beta=0.0, out=None, scratch=None, flags=0, stream=None,
+           auto_pad="NOTSET"):
     """y = act(conv(x, w) + bias + residual) on CUDA tensors (NCHW / OIHW,
-    contiguous, one element type).  Allocates y (and the scratch the plan needs:
-    split-k planes or repacked weights) with torch unless ``out`` / ``scratch``
-    are given."""
+    contiguous, one element type).  ``auto_pad`` (ONNX: SAME_UPPER, SAME_LOWER,
+    VALID) replaces ``pads`` when set.  Allocates y (and the scratch the plan
+    needs) with torch unless ``out`` / ``scratch`` are given."""
     import torch
     dt = _dtype_name(x)
     for t in (w, bias, residual, out):
@@ -269,7 +284,7 @@ def conv2d(x, w, bias=None, residual=None, *, stride=1, pads=0, dilation=1, grou
         raise ValueError("x must be contiguous NCHW")
     p = make_problem(x.shape, w.shape, dtype=dt, stride=stride, pads=pads, dilation=dilation,
                      groups=groups, act=act, alpha=alpha, beta=beta, has_bias=bias is not None,
-                     has_residual=residual is not None, flags=flags)
+                     has_residual=residual is not None, flags=flags, auto_pad=auto_pad)
     ho, wo = conv_output_shape(p)
     if out is None:
         out = torch.empty((p.n, p.c_out, ho, wo), dtype=x.dtype, device=x.device)

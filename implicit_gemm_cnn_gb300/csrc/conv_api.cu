@@ -440,6 +440,37 @@ conv_status conv_output_shape(const conv_problem* p, int64_t* ho, int64_t* wo) {
   return CONV_OK;
 }
 
+conv_status conv_apply_auto_pad(conv_problem* p, int32_t mode) {
+  if (!p) return CONV_ERR_NULL;
+  if (mode < CONV_AUTO_PAD_NOTSET || mode > CONV_AUTO_PAD_VALID) return CONV_ERR_ARG;
+  conv_problem q = *p;
+  if (mode == CONV_AUTO_PAD_VALID) {
+    q.pad_top = q.pad_left = q.pad_bottom = q.pad_right = 0;
+  } else if (mode != CONV_AUTO_PAD_NOTSET) {
+    // one axis: (input, kernel, stride, dilation) -> (begin, end)
+    auto axis = [mode](long long in, long long k, long long s, long long d, int64_t* b, int64_t* e) {
+      if (in < 1 || k < 1 || s < 1 || d < 1 || k > (1LL << 40) || d > (1LL << 20)) return false;
+      const long long out = (in + s - 1) / s;
+      long long total = 0;
+      if (__builtin_mul_overflow(out - 1, s, &total) || __builtin_add_overflow(total, d * (k - 1) + 1 - in, &total))
+        return false;
+      if (total < 0) total = 0;
+      const long long small = total / 2, large = total - total / 2;
+      *b = mode == CONV_AUTO_PAD_SAME_UPPER ? small : large;
+      *e = mode == CONV_AUTO_PAD_SAME_UPPER ? large : small;
+      return true;
+    };
+    if (!axis(q.h, q.kh, q.stride_h, q.dil_h, &q.pad_top, &q.pad_bottom) ||
+        !axis(q.w, q.kw, q.stride_w, q.dil_w, &q.pad_left, &q.pad_right))
+      return CONV_ERR_SHAPE;
+  }
+  Shape s;
+  const conv_status st = validate(&q, &s);
+  if (st != CONV_OK) return st;
+  *p = q;
+  return CONV_OK;
+}
+
 conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_plan_info* out) {
   if (!out) return CONV_ERR_NULL;
   Plan plan;

@@ -155,6 +155,16 @@ typedef struct conv_plan_info {
   uint64_t scratch_bytes; /* device scratch conv_forward needs                */
 } conv_plan_info;
 
+/* ONNX Conv auto_pad values ("Convolution, pooling and resize", Layout and
+ * operands: auto_pad is turned into explicit pads). */
+typedef enum conv_auto_pad {
+  CONV_AUTO_PAD_NOTSET = 0,      /* the explicit pads stay                          */
+  CONV_AUTO_PAD_SAME_UPPER = 1,  /* Ho = ceil(H / stride); an odd pad's extra row /
+                                    column at the end (bottom, right)               */
+  CONV_AUTO_PAD_SAME_LOWER = 2,  /* the same, the extra row / column at the start   */
+  CONV_AUTO_PAD_VALID = 3        /* no padding                                      */
+} conv_auto_pad;
+
 /* Library ABI version (CONV_ABI_VERSION). */
 CONV_API int32_t conv_abi_version(void);
 
@@ -167,6 +177,16 @@ CONV_API const char* conv_status_string(conv_status status);
  * Errors: CONV_ERR_NULL (p, ho or wo NULL), CONV_ERR_SHAPE, CONV_ERR_OVERFLOW,
  * CONV_ERR_DTYPE, CONV_ERR_ACT. */
 CONV_API conv_status conv_output_shape(const conv_problem* p, int64_t* ho, int64_t* wo);
+
+/* Writes into p's four pads what ONNX auto_pad `mode` prescribes for p's
+ * input size, kernel, stride and dilation ("Convolution, pooling and resize",
+ * Layout and operands).  For SAME_UPPER / SAME_LOWER the total padding of an
+ * axis is max(0, (ceil(H/s) - 1)*s + d*(k-1) + 1 - H), split into halves, the
+ * odd one at the end (UPPER) or the start (LOWER); VALID sets zeros; NOTSET
+ * leaves the pads.  Host only.
+ * Errors: CONV_ERR_NULL (p NULL), CONV_ERR_ARG (unknown mode), and the shape
+ * checks of conv_output_shape on the result (p is not modified then). */
+CONV_API conv_status conv_apply_auto_pad(conv_problem* p, int32_t mode);
 
 /* The plan for a device with `sm_count` SMs: variant, k split, tile, grid and
  * scratch bytes.  Host only and a pure function of (p, sm_count), so split

@@ -27,3 +27,24 @@ def depthwise_separable_ratio(cin, cout, k, ho, wo):
     sep = macs(1, cin, cin, k, k, ho, wo, groups=cin) + macs(1, cin, cout, 1, 1, ho, wo)
     std = macs(1, cin, cout, k, k, ho, wo)
     return sep, std
+
+
+def auto_pad(size: int, k: int, stride: int, dilation: int, mode: str) -> tuple[int, int]:
+    """ONNX Conv auto_pad ("Convolution, pooling and resize", Layout and
+    operands: auto_pad is turned into explicit pads), one axis.
+
+    VALID: no padding.  SAME_UPPER / SAME_LOWER: pad so that the output has
+    ceil(size / stride) positions; the total padding is what the last window
+    needs beyond the input, split in two halves, the odd one at the end
+    (SAME_UPPER) or at the beginning (SAME_LOWER).  Returns (begin, end)."""
+    if mode == "VALID":
+        return 0, 0
+    out = -(-size // stride)
+    span = dilation * (k - 1) + 1
+    total = max(0, (out - 1) * stride + span - size)
+    small, large = total // 2, total - total // 2
+    if mode == "SAME_UPPER":
+        return small, large
+    if mode == "SAME_LOWER":
+        return large, small
+    raise ValueError(mode)

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 9, names
+    assert len(names) == 10, names
     for name in names:
         assert hasattr(lib, name), name           # dlsym succeeds
     assert conv.conv_abi_version() == 1
@@ -289,3 +289,70 @@ def test_planner_rules_on_random_shapes(lib):
         else:
             assert plan["split_k"] == 1
     assert {"igemm_ffma", "depthwise_halo", "igemm_tcgen05_window"} <= seen, seen
+
+
+# ---- ONNX auto_pad ----------------------------------------------------------
+AUTO_PAD_HAND = [
+    # (size, k, stride, dilation) -> SAME_UPPER (begin, end), SAME_LOWER (begin, end);
+    # worked by hand: out = ceil(size / stride), total = (out-1)*s + d(k-1) + 1 - size
+    ((224, 7, 2, 1), (2, 3), (3, 2)),     # out 112, total 5 (the ResNet-50 stem)
+    ((56, 3, 1, 1), (1, 1), (1, 1)),      # out 56, total 2
+    ((5, 2, 1, 1), (0, 1), (1, 0)),       # out 5, total 1
+    ((7, 3, 2, 2), (2, 2), (2, 2)),       # out 4, total 4
+    ((8, 1, 2, 1), (0, 0), (0, 0)),       # out 4, total max(0, -1) = 0
+    ((10, 4, 3, 1), (1, 2), (2, 1)),      # out 4, total 3
+]
+
+
+@pytest.mark.parametrize("case", AUTO_PAD_HAND)
+def test_auto_pad_oracle_hand_values(case):
+    """The oracle's auto_pad against values worked by hand from ONNX's rule."""
+    from oracle import arith
+    (size, k, s, d), upper, lower = case
+    assert arith.auto_pad(size, k, s, d, "SAME_UPPER") == upper
+    assert arith.auto_pad(size, k, s, d, "SAME_LOWER") == lower
+    assert arith.auto_pad(size, k, s, d, "VALID") == (0, 0)
+
+
+def test_auto_pad_oracle_same_output_size():
+    """SAME padding's defining property: the output has ceil(size / stride)
+    positions (ONNX), and the two sides differ by at most one."""
+    from oracle import arith
+    o = oracle.Oracle()
+    for size in range(1, 30):
+        for k in (1, 2, 3, 5, 7):
+            for s in (1, 2, 3):
+                for d in (1, 2):
+                    for mode in ("SAME_UPPER", "SAME_LOWER"):
+                        b, e = arith.auto_pad(size, k, s, d, mode)
+                        assert abs(b - e) <= 1 and b >= 0 and e >= 0
+                        assert (b <= e) == (mode == "SAME_UPPER" or b == e)
+                        if size + b + e >= d * (k - 1) + 1:
+                            assert o.output_extent(size, k, b, e, s, d) == -(-size // s), (size, k, s, d)
+
+
+def test_auto_pad_c_abi_matches_oracle(lib):
+    from oracle import arith
+    for (h, w) in ((224, 224), (13, 9), (5, 40), (1, 17)):
+        for (kh, kw) in ((7, 7), (3, 2), (1, 5)):
+            for (sh, sw) in ((1, 1), (2, 2), (3, 1)):
+                for (dh, dw) in ((1, 1), (2, 1)):
+                    for mode in ("SAME_UPPER", "SAME_LOWER", "VALID"):
+                        p = conv.make_problem((2, 3, h, w), (4, 3, kh, kw), stride=(sh, sw),
+                                              dilation=(dh, dw), pads=(9, 9, 9, 9))
+                        if mode == "VALID" and (h < (kh - 1) * dh + 1 or w < (kw - 1) * dw + 1):
+                            st = lib.conv_apply_auto_pad(ctypes.byref(p), conv.AUTO_PAD[mode])
+                            assert conv.STATUS[st] == "CONV_ERR_SHAPE"
+                            assert (p.pad_top, p.pad_left) == (9, 9)    # unchanged on error
+                            continue
+                        conv.conv_apply_auto_pad(p, mode)
+                        pt, pb = arith.auto_pad(h, kh, sh, dh, mode)
+                        pl, pr = arith.auto_pad(w, kw, sw, dw, mode)
+                        assert (p.pad_top, p.pad_left, p.pad_bottom, p.pad_right) == (pt, pl, pb, pr)
+                        if mode != "VALID":
+                            assert conv.conv_output_shape(p) == (-(-h // sh), -(-w // sw))
+    p = conv.make_problem((1, 1, 8, 8), (1, 1, 3, 3), pads=(1, 2, 3, 4))
+    conv.conv_apply_auto_pad(p, "NOTSET")
+    assert (p.pad_top, p.pad_left, p.pad_bottom, p.pad_right) == (1, 2, 3, 4)
+    assert conv.STATUS[lib.conv_apply_auto_pad(ctypes.byref(p), 7)] == "CONV_ERR_ARG"
+    assert conv.STATUS[lib.conv_apply_auto_pad(None, 1)] == "CONV_ERR_NULL"

@@ -189,3 +189,28 @@ def test_unfolded_tail_split():
     assert out["max_scaled_err"] < 1e-5, out
     y2, _ = _run_offsets(inp, "f32", (0, 0, 0), **g)
     assert torch.equal(y.view(torch.int32), y2.view(torch.int32))   # fixed order, no atomics
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("mode", ["SAME_UPPER", "SAME_LOWER", "VALID"])
+@pytest.mark.parametrize("xs,ws,stride,dil", [
+    ((2, 3, 37, 30), (8, 3, 7, 7), (2, 2), (1, 1)),
+    ((1, 8, 20, 24), (16, 8, 4, 3), (1, 3), (2, 1)),
+    ((2, 16, 9, 16), (16, 1, 5, 5), (1, 1), (1, 1)),
+])
+def test_auto_pad_convolution(dtype, mode, xs, ws, stride, dil):
+    """ONNX auto_pad through the library against the oracle given the pads
+    that the oracle's own auto_pad restatement computes."""
+    from oracle import arith
+    groups = xs[1] if ws[1] == 1 else 1
+    dev = random_layer_inputs(xs, ws, dtype, seed=hash((mode, xs)) % 1000, bias=True)
+    y = conv.conv2d(dev["x"].cuda(), dev["w"].cuda(), dev["bias"].cuda(), stride=stride, dilation=dil,
+                    groups=groups, act="relu", auto_pad=mode)
+    torch.cuda.synchronize()
+    pt, pb = arith.auto_pad(xs[2], ws[2], stride[0], dil[0], mode)
+    pl, pr = arith.auto_pad(xs[3], ws[3], stride[1], dil[1], mode)
+    if mode != "VALID":
+        assert tuple(y.shape[2:]) == (-(-xs[2] // stride[0]), -(-xs[3] // stride[1]))
+    out = check_full(dev, dtype, y.cpu(), stride=stride, pads=(pt, pl, pb, pr), dilation=dil,
+                     groups=groups, act="relu")
+    assert out["ok"], out
