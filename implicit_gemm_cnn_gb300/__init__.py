@@ -24,7 +24,7 @@ __all__ = [
     "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "FLAG_NO_UNFOLD", "FLAG_FORCE_UNFOLD", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
     "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
-    "conv_apply_auto_pad", "AUTO_PAD",
+    "conv_apply_auto_pad", "AUTO_PAD", "conv_scratch_bytes_per_image",
     "make_problem", "conv2d", "library_path", "load",
 ]
 
@@ -120,8 +120,10 @@ def load() -> ctypes.CDLL:
         lib.conv_device_error.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         lib.conv_forward_fixed_scratch.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp]
         lib.conv_apply_auto_pad.argtypes = [P(ConvProblem), ctypes.c_int32]
+        lib.conv_scratch_bytes_per_image.argtypes = [P(ConvProblem), P(ctypes.c_size_t)]
         for f in ("conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
-                  "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "conv_apply_auto_pad"):
+                  "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "conv_apply_auto_pad",
+                  "conv_scratch_bytes_per_image"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -174,6 +176,12 @@ def conv_plan(p: ConvProblem, sm_count: int) -> dict:
 def conv_scratch_bytes(p: ConvProblem) -> int:
     n = ctypes.c_size_t()
     _check(load().conv_scratch_bytes(ctypes.byref(p), ctypes.byref(n)), "conv_scratch_bytes")
+    return n.value
+
+
+def conv_scratch_bytes_per_image(p: ConvProblem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().conv_scratch_bytes_per_image(ctypes.byref(p), ctypes.byref(n)), "conv_scratch_bytes_per_image")
     return n.value
 
 

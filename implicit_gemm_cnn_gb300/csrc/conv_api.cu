@@ -92,6 +92,35 @@ int occupancy_estimate(const FfmaCfg& c, size_t smem) {
   return std::max(occ, 1);
 }
 
+// Scratch of the CUDA-core variant for a chunk of `images` whole images:
+// split planes, then (256-byte aligned) the unfolded input, the transposed
+// weights and the raw tiles of a tail split.  Only the planes and the
+// unfolded input grow with the images; images = n gives the whole batch.
+struct FfmaLayout {
+  uint64_t xw_off, wt_off, tail_off, total;
+};
+FfmaLayout ffma_layout(const Plan& plan, const Shape& s, long long n, long long images) {
+  auto align = [](uint64_t v) { return (v + 255) / 256 * 256; };
+  FfmaLayout L{};
+  uint64_t off = plan.info.split_k > 1
+                     ? static_cast<uint64_t>(plan.info.split_k) * (s.y_elems / n) * images * sizeof(float)
+                     : 0;
+  if (plan.ffma_unf) {
+    const UnfPlan& u = plan.unf;
+    L.xw_off = align(off);
+    off = L.xw_off + static_cast<uint64_t>(u.xw_elems / n) * images * sizeof(float);
+    L.wt_off = align(off);
+    off = L.wt_off + static_cast<uint64_t>(u.wt_elems) * sizeof(float);
+    if (u.tail_split > 0) {
+      const FfmaCfg& c = kFfmaCfgs[plan.ffma_cfg];
+      L.tail_off = align(off);
+      off = L.tail_off + static_cast<uint64_t>(u.tiles - u.tail_first) * u.tail_split * c.bm * c.bn * sizeof(float);
+    }
+  }
+  L.total = off;
+  return L;
+}
+
 // Whether the unfolded-B pre-pass pays for a CUDA-core layer: it moves x once
 // and writes and reads the unfolded copy once, so it is taken when the
 // layer's arithmetic is at least 64 FLOP per byte of that traffic (the
@@ -203,13 +232,7 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   out->info.tile_m = c.bm;
   out->info.tile_n = c.bn;
   out->info.ctas = ctas * split;
-  uint64_t scratch = split > 1 ? static_cast<uint64_t>(split) * s.y_elems * sizeof(float) : 0;
   if (unf) {
-    // after the split planes: the unfolded x, then the transposed weights,
-    // then the raw tiles of a tail split
-    u.xw_off = (scratch + 255) / 256 * 256;
-    u.wt_off = (u.xw_off + static_cast<uint64_t>(u.xw_elems) * sizeof(float) + 255) / 256 * 256;
-    scratch = u.wt_off + static_cast<uint64_t>(u.wt_elems) * sizeof(float);
     u.tiles = ctas;
     if (split == 1 && best_tail > 0) {
       const int occ = occupancy_estimate(c, ffma_smem_bytes(bi, static_cast<int>(s.K), true));
@@ -219,13 +242,15 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
       u.tail_len = static_cast<int>(((s.K + best_tail - 1) / best_tail + kFfmaBKU - 1) / kFfmaBKU * kFfmaBKU);
       u.tail_split = static_cast<int>((s.K + u.tail_len - 1) / u.tail_len);  // ranges that hold terms
       u.tail_first = ctas - rest;
-      u.tail_off = (scratch + 255) / 256 * 256;
-      scratch = u.tail_off + static_cast<uint64_t>(rest) * u.tail_split * c.bm * c.bn * sizeof(float);
       out->info.ctas = u.tail_first + rest * u.tail_split;
     }
     out->unf = u;
   }
-  out->info.scratch_bytes = scratch;
+  const FfmaLayout L = ffma_layout(*out, s, p->n, p->n);
+  out->unf.xw_off = L.xw_off;
+  out->unf.wt_off = L.wt_off;
+  out->unf.tail_off = L.tail_off;
+  out->info.scratch_bytes = L.total;
   out->k_per_split = static_cast<int>(len);
   if (out->gd.ok) {
     out->info.tile_m = static_cast<int>(s.mg);
@@ -290,6 +315,7 @@ void shape_args(const conv_problem* p, const Shape& s, ConvArgs* a) {
   a->ho = static_cast<int>(s.ho); a->wo = static_cast<int>(s.wo);
   a->K = static_cast<int>(s.K);
   a->hw = p->h * p->w; a->howo = s.ho * s.wo; a->npix = s.npix;
+  a->pix_lo = 0; a->pix_hi = s.npix; a->img0 = 0; a->part_total = s.y_elems;  // the whole batch
   a->act = p->act; a->alpha = p->act_alpha; a->beta = p->act_beta;
 }
 
@@ -493,6 +519,22 @@ conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes) {
   return st;
 }
 
+conv_status conv_scratch_bytes_per_image(const conv_problem* p, size_t* bytes) {
+  if (!bytes) return CONV_ERR_NULL;
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  int dev, sm;
+  st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  Plan plan;
+  st = make_plan(p, sm, &plan, nullptr);
+  if (st != CONV_OK) return st;
+  const bool ffma = plan.info.variant == CONV_VARIANT_IGEMM_FFMA || plan.info.variant == CONV_VARIANT_IGEMM_FFMA_SPLIT;
+  *bytes = static_cast<size_t>(ffma ? ffma_layout(plan, s, p->n, 1).total : plan.info.scratch_bytes);
+  return CONV_OK;
+}
+
 conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) {
   if (!buf || !len) return CONV_ERR_NULL;
   Shape s;
@@ -571,7 +613,23 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
   Plan plan;
   st = make_plan(p, sm, &plan, nullptr);
   if (st != CONV_OK) return st;
-  const size_t need = plan.info.scratch_bytes;
+  size_t need = plan.info.scratch_bytes;
+  // chunks of whole images when the CUDA-core variant's scratch is smaller
+  // than the whole batch needs ("Convolution, pooling and resize", Layout and
+  // operands: a smaller buffer makes the batch run in chunks of whole
+  // images, which changes no bit of the result)
+  const bool ffma = plan.info.variant == CONV_VARIANT_IGEMM_FFMA || plan.info.variant == CONV_VARIANT_IGEMM_FFMA_SPLIT;
+  long long chunk = p->n;
+  if (need && ffma && scratch && scratch_bytes < need) {
+    chunk = 0;
+    for (long long lo = 1, hi = p->n - 1; lo <= hi;) {  // the most images whose scratch fits
+      const long long mid = lo + (hi - lo) / 2;
+      if (ffma_layout(plan, s, p->n, mid).total <= scratch_bytes) { chunk = mid; lo = mid + 1; }
+      else hi = mid - 1;
+    }
+    if (chunk == 0) return CONV_ERR_SCRATCH;
+    need = ffma_layout(plan, s, p->n, chunk).total;
+  }
   if (need) {
     if (!scratch || scratch_bytes < need || reinterpret_cast<uintptr_t>(scratch) % 16) return CONV_ERR_SCRATCH;
     for (int i = 0; i < 4; ++i)
@@ -616,9 +674,10 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
       a.split = plan.info.split_k;
       a.k_per_split = plan.k_per_split;
       a.partial = static_cast<float*>(scratch);
+      const FfmaLayout L = ffma_layout(plan, s, p->n, chunk);
       if (plan.ffma_unf) {
-        a.xw = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan.unf.xw_off);
-        a.wtt = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan.unf.wt_off);
+        a.xw = reinterpret_cast<float*>(static_cast<char*>(scratch) + L.xw_off);
+        a.wtt = reinterpret_cast<float*>(static_cast<char*>(scratch) + L.wt_off);
         a.hu = plan.unf.hu;
         a.mg4 = plan.unf.mg4;
         if (plan.unf.tail_split > 0) {
@@ -628,11 +687,20 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
           a.tiles_gy = static_cast<int>((s.mg + c.bm - 1) / c.bm * p->groups);
           a.tail_first = plan.unf.tail_first;
           a.tail_tiles = plan.unf.tiles - plan.unf.tail_first;
-          a.tailbuf = reinterpret_cast<float*>(static_cast<char*>(scratch) + plan.unf.tail_off);
+          a.tailbuf = reinterpret_cast<float*>(static_cast<char*>(scratch) + L.tail_off);
         }
       }
-      err = launch_ffma(plan, a, p->dtype, cs);
-      if (err == cudaSuccess && a.split > 1) err = launch_split_reduce(a, p->dtype, cs);
+      // the whole batch, or chunks of whole images: every output is computed
+      // by the whole problem's tile, k ranges and order either way
+      for (long long n0 = 0; n0 < p->n && err == cudaSuccess; n0 += chunk) {
+        const long long n1 = std::min<long long>(p->n, n0 + chunk);
+        a.pix_lo = n0 * a.howo;
+        a.pix_hi = n1 * a.howo;
+        a.img0 = static_cast<int>(n0);
+        a.part_total = (n1 - n0) * a.c_out * a.howo;
+        err = launch_ffma(plan, a, p->dtype, cs);
+        if (err == cudaSuccess && a.split > 1) err = launch_split_reduce(a, p->dtype, cs);
+      }
       break;
     }
   }

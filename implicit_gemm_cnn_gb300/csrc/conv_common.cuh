@@ -43,6 +43,16 @@ struct ConvArgs {
   int tail_split, tail_len, tiles_gy;
   long long tail_first, tail_tiles;
   float* tailbuf;
+  // CUDA-core kernel, a chunk of whole images: only output pixels in
+  // [pix_lo, pix_hi) are loaded (unfolded B) and stored; the unfolded copy and
+  // the split planes hold the chunk's images only, from image img0 on (planes
+  // of part_total elements).  The launch keeps the whole problem's tiles.
+  long long pix_lo, pix_hi, part_total;
+  int img0;
+  // grid offsets of a chunk: the first pixel tile (3-D grid) or, with a tail
+  // split, the whole tiles [blk_whole_lo, + blk_whole_n) and the tail blocks
+  // from blk_tail_lo on (1-D grid)
+  long long px_tile0, blk_whole_lo, blk_whole_n, blk_tail_lo;
 };
 
 enum Act {

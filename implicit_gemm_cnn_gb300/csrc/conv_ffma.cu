@@ -125,9 +125,11 @@ __device__ __forceinline__ FfmaTile ffma_tile(const ConvArgs& a, unsigned bx, un
   r.part = -1;
   r.tail_tile = 0;
   if (BMODE == kBUnfolded && a.tail_split > 0) {
-    long long t = bx;
-    if (t >= a.tail_first) {
-      const long long u = t - a.tail_first;
+    long long t;
+    if (bx < a.blk_whole_n) {
+      t = a.blk_whole_lo + bx;
+    } else {
+      const long long u = (a.blk_tail_lo - a.tail_first) * a.tail_split + (bx - a.blk_whole_n);
       t = a.tail_first + u / a.tail_split;
       r.part = static_cast<int>(u % a.tail_split);
       r.tail_tile = t - a.tail_first;
@@ -135,7 +137,7 @@ __device__ __forceinline__ FfmaTile ffma_tile(const ConvArgs& a, unsigned bx, un
     r.px_tile = t / a.tiles_gy;
     r.gy = static_cast<int>(t % a.tiles_gy);
   } else {
-    r.px_tile = bx;
+    r.px_tile = a.px_tile0 + bx;
     r.gy = static_cast<int>(by);
   }
   return r;
@@ -231,15 +233,15 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
     for (int i = 0; i < QV; ++i) {
       const int q = tid + i * NT;
       const long long p = pix0 + 4 * (q % (BN / 4));
-      vok[i] = q < BK * BN / 4 && p < a.npix;
-      const long long pp = vok[i] ? p : 0;
+      vok[i] = q < BK * BN / 4 && p < a.npix && (BMODE != kBUnfolded || (p >= a.pix_lo && p < a.pix_hi));
+      const long long pp = vok[i] ? p : (BMODE == kBUnfolded ? a.pix_lo : 0);
       const long long n = pp / a.howo;
       const long long rem = pp - n * a.howo;
       if constexpr (BMODE == kBPointwise) {
         vbase[i] = (n * a.c_in + static_cast<long long>(g) * a.cg) * a.hw + rem;
       } else {
         const long long oh = rem / a.wo, ow = rem - oh * a.wo;
-        uoff[i] = static_cast<int>(n * unf_img + static_cast<long long>(g) * a.cg * a.kw * a.hu * a.wo +
+        uoff[i] = static_cast<int>((n - a.img0) * unf_img + static_cast<long long>(g) * a.cg * a.kw * a.hu * a.wo +
                                    oh * a.sh * a.wo + ow);
       }
     }
@@ -404,15 +406,18 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
       }
     return;
   }
-  const long long total = static_cast<long long>(a.n) * a.c_out * a.howo;
+  // only pixels in [pix_lo, pix_hi) (the whole batch, or a chunk of images)
+  // are stored; split planes hold the chunk's outputs from image img0 on
+  const long long out0 = static_cast<long long>(a.img0) * a.c_out * a.howo;
   T* y = static_cast<T*>(a.y);
 #pragma unroll
   for (int jg = 0; jg < TN / 4; ++jg) {
     const long long p = pix0 + jg * GN + tx * 4;
-    if (p >= a.npix) continue;
+    if (p >= a.pix_hi || p + 3 < a.pix_lo) continue;
+    const long long pf = p >= a.pix_lo ? p : a.pix_lo;  // a stored pixel of the group
     const int n = static_cast<int>(p / a.howo);
     const long long rem = p - static_cast<long long>(n) * a.howo;
-    const bool whole4 = a.vec_out && (p + 3 < a.npix) && (rem + 3 < a.howo) && ((a.howo & 3) == 0);
+    const bool whole4 = a.vec_out && p >= a.pix_lo && (p + 3 < a.pix_hi) && (rem + 3 < a.howo) && ((a.howo & 3) == 0);
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
       const int m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
@@ -420,17 +425,17 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
       const int co = g * a.mg + m;
       const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo + rem;
       if (a.split > 1) {
-        float* part = a.partial + static_cast<long long>(blockIdx.z) * total;
+        float* part = a.partial + static_cast<long long>(blockIdx.z) * a.part_total;  // chunk-local
         if (whole4) {
-          *reinterpret_cast<float4*>(part + out) =
+          *reinterpret_cast<float4*>(part + (out - out0)) =
               make_float4(acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]);
         } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const long long pq = p + q;
-            if (pq >= a.npix) break;
+            if (pq < a.pix_lo || pq >= a.pix_hi) continue;
             const int nq = static_cast<int>(pq / a.howo);
-            part[(static_cast<long long>(nq) * a.c_out + co) * a.howo + (pq - nq * a.howo)] =
+            part[(static_cast<long long>(nq) * a.c_out + co) * a.howo + (pq - nq * a.howo) - out0] =
                 acc[i][jg * 4 + q];
           }
         }
@@ -440,19 +445,21 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
         const float bco = a.bias ? to_f32(static_cast<const T*>(a.bias)[co]) : 0.0f;
         float v[4], bv[4], rv[4];
         long long oq[4];
+        bool in[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const long long pq = p + q;
-          const bool ok = pq < a.npix;
+          in[q] = pq >= a.pix_lo && pq < a.pix_hi;
           if (whole4) {
             oq[q] = out + q;
           } else {
-            const int nq = static_cast<int>((ok ? pq : p) / a.howo);
-            oq[q] = (static_cast<long long>(nq) * a.c_out + co) * a.howo + ((ok ? pq : p) - static_cast<long long>(nq) * a.howo);
+            const long long pa = in[q] ? pq : pf;
+            const int nq = static_cast<int>(pa / a.howo);
+            oq[q] = (static_cast<long long>(nq) * a.c_out + co) * a.howo + (pa - static_cast<long long>(nq) * a.howo);
           }
           v[q] = acc[i][jg * 4 + q];
           bv[q] = bco;
-          rv[q] = (resp && ok) ? to_f32(resp[oq[q]]) : 0.0f;
+          rv[q] = (resp && in[q]) ? to_f32(resp[oq[q]]) : 0.0f;
         }
         epilogue_n<4>(v, bv, rv, a.bias != nullptr, resp != nullptr, a.act, a.alpha, a.beta);
         if (whole4) {
@@ -460,7 +467,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
         } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (p + q < a.npix) y[oq[q]] = from_f32<T>(v[q]);
+            if (in[q]) y[oq[q]] = from_f32<T>(v[q]);
         }
       }
     }
@@ -481,8 +488,8 @@ __global__ void __launch_bounds__(256) ffma_unfold(const ConvArgs a, long long p
   const T* __restrict__ w = static_cast<const T*>(a.wt);
   const int tid = threadIdx.x;
   if (blockIdx.x < planes) {
-    const long long nc = blockIdx.x;
-    const T* __restrict__ plane = x + nc * a.hw;
+    const long long nc = blockIdx.x;  // the chunk's planes, from image img0 on
+    const T* __restrict__ plane = x + (static_cast<long long>(a.img0) * a.c_in + nc) * a.hw;
     const int hw = static_cast<int>(a.hw);
     if (staged) {
       for (int e = tid; e < hw; e += 256) plane_s[e] = to_f32(plane[e]);
@@ -557,7 +564,7 @@ __global__ void __launch_bounds__(256) ffma_tail_reduce(const ConvArgs a) {
     const int g = gy / co_tiles;
     const int m = (gy % co_tiles) * BM + ml;
     const long long p = px_tile * BN + 4 * c4;
-    if (m >= a.mg || p >= a.npix) continue;
+    if (m >= a.mg || p < a.pix_lo || p >= a.pix_hi) continue;
     const float* src = a.tailbuf + tt * a.tail_split * static_cast<long long>(BM * BN) + ml * BN + 4 * c4;
     float4 sum = *reinterpret_cast<const float4*>(src);
     for (int r = 1; r < a.tail_split; ++r) {
@@ -589,11 +596,15 @@ __global__ void __launch_bounds__(256) ffma_tail_reduce(const ConvArgs a) {
 // consecutive outputs per thread when the plane length allows vector loads.
 template <typename T>
 __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
-  const long long total = static_cast<long long>(a.n) * a.c_out * a.howo;
-  T* y = static_cast<T*>(a.y);
+  // the planes hold the outputs of images [img0, img0 + chunk): part_total
+  // elements each, output out0 + i at element i
+  const long long total = a.part_total;
+  const long long out0 = static_cast<long long>(a.img0) * a.c_out * a.howo;
+  T* y = static_cast<T*>(a.y) + out0;
+  const T* __restrict__ rbase = a.residual ? static_cast<const T*>(a.residual) + out0 : nullptr;
   const float* part = a.partial;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  if ((total & 3) == 0) {
+  if ((total & 3) == 0 && (out0 & 3) == 0) {
     const long long q = total >> 2;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < q; i += stride) {
       float4 s = reinterpret_cast<const float4*>(part)[i];
@@ -604,11 +615,11 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
       }
       const long long o = i * 4;
       const T* __restrict__ bp = static_cast<const T*>(a.bias);
-      const T* __restrict__ rp = static_cast<const T*>(a.residual);
+      const T* __restrict__ rp = rbase;
       float v[4] = {s.x, s.y, s.z, s.w}, bv[4], rv[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int ck = static_cast<int>(((o + k) / a.howo) % a.c_out);
+        const int ck = static_cast<int>(((out0 + o + k) / a.howo) % a.c_out);
         bv[k] = bp ? to_f32(bp[ck]) : 0.0f;
         rv[k] = rp ? to_f32(rp[o + k]) : 0.0f;
       }
@@ -622,11 +633,11 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
     }
   } else {
     const T* __restrict__ bp = static_cast<const T*>(a.bias);
-    const T* __restrict__ rp = static_cast<const T*>(a.residual);
+    const T* __restrict__ rp = rbase;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total; i += stride) {
       float v[1] = {part[i]};
       for (int z = 1; z < a.split; ++z) v[0] = __fadd_rn(v[0], part[z * total + i]);
-      const int co = static_cast<int>((i / a.howo) % a.c_out);
+      const int co = static_cast<int>(((out0 + i) / a.howo) % a.c_out);
       float bv[1] = {bp ? to_f32(bp[co]) : 0.0f}, rv[1] = {rp ? to_f32(rp[i]) : 0.0f};
       epilogue_n<1>(v, bv, rv, bp != nullptr, rp != nullptr, a.act, a.alpha, a.beta);
       y[i] = from_f32<T>(v[0]);
@@ -804,21 +815,36 @@ cudaError_t launch_gd_k(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
 }
 
 template <typename T, int CFG, int BMODE>
-cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
+cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& args, cudaStream_t s) {
   constexpr FfmaCfg c = kFfmaCfgs[CFG];
   auto kern = igemm_ffma<T, c.bm, c.bn, c.tm, c.tn, BMODE>;
+  ConvArgs a = args;
   const int ktab_cap = ffma_ktab_entries(a.k_per_split);
   const size_t smem = ffma_smem_bytes(CFG, a.k_per_split, BMODE == kBUnfolded);
   cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  const long long gx = (a.npix + c.bn - 1) / c.bn;
+  // the tiles that hold pixels of [pix_lo, pix_hi)
   const int co_tiles = (a.mg + c.bm - 1) / c.bm;
+  const long long px_lo = a.pix_lo / c.bn, px_hi = (a.pix_hi + c.bn - 1) / c.bn;
+  const long long gx = px_hi - px_lo;
+  a.px_tile0 = px_lo;
   if constexpr (BMODE == kBUnfolded) {
     if (a.tail_split > 0) {
-      const long long blocks = a.tail_first + a.tail_tiles * a.tail_split;
+      // tiles are pixel-tile major: the chunk's tiles are [t_lo, t_hi); whole
+      // tiles below tail_first, the rest as tail_split blocks each
+      const long long gyn = static_cast<long long>(a.tiles_gy);
+      const long long t_lo = px_lo * gyn, t_hi = px_hi * gyn;
+      a.blk_whole_lo = t_lo;
+      a.blk_whole_n = std::max(0LL, std::min(t_hi, a.tail_first) - t_lo);
+      const long long tail_lo = std::max(t_lo, a.tail_first);
+      const long long tail_n = std::max(0LL, t_hi - tail_lo);
+      a.blk_tail_lo = tail_lo;
+      const long long blocks = a.blk_whole_n + tail_n * a.tail_split;
+      if (blocks < 1 || blocks > 2147483647LL) return cudaErrorInvalidConfiguration;
       kern<<<static_cast<unsigned>(blocks), c.threads(), smem, s>>>(a, ktab_cap);
       err = cudaGetLastError();
       if (err != cudaSuccess) return err;
+      if (tail_n == 0) return cudaSuccess;
       const long long units = a.tail_tiles * c.bm * (c.bn / 4);
       const long long rblocks = std::min<long long>((units + 255) / 256, 65535LL * 8);
       ffma_tail_reduce<T, c.bm, c.bn><<<static_cast<unsigned>(rblocks), 256, 0, s>>>(a);
@@ -847,7 +873,7 @@ constexpr long long kUnfoldStageMax = 11000;  // plane elements staged in shared
 
 template <typename T>
 cudaError_t launch_unfold(const UnfPlan& u, const ConvArgs& a, cudaStream_t s) {
-  const long long planes = static_cast<long long>(a.n) * a.c_in;
+  const long long planes = (a.pix_hi - a.pix_lo) / a.howo * a.c_in;  // the chunk's images
   const int tk = (a.K + 31) / 32, tm = (u.mg4 + 31) / 32;
   const long long blocks = planes + static_cast<long long>(a.groups) * tk * tm;
   if (blocks > 2147483647LL) return cudaErrorInvalidConfiguration;
@@ -875,7 +901,7 @@ cudaError_t launch_typed(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_reduce_typed(const ConvArgs& a, cudaStream_t s) {
-  const long long total = static_cast<long long>(a.n) * a.c_out * a.howo;
+  const long long total = a.part_total;
   const long long work = (total & 3) == 0 ? total / 4 : total;
   long long blocks = (work + 255) / 256;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;

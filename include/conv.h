@@ -206,6 +206,19 @@ CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_pla
  * Errors: as conv_plan, and CONV_ERR_DEVICE without a usable device. */
 CONV_API conv_status conv_scratch_bytes(const conv_problem* p, size_t* bytes);
 
+/* Scratch bytes conv_forward needs on the current device to run `p` one
+ * image at a time ("Convolution, pooling and resize", Layout and operands: the
+ * scratch query reports the whole batch and one image).  The CUDA-core
+ * variant's split planes and unfolded input grow with the images it runs at
+ * once: given less scratch than conv_scratch_bytes but at least this,
+ * conv_forward runs the batch in chunks of as many whole images as fit, and
+ * every output is computed by the same tile, k ranges and summation order as
+ * in the whole-batch call -- the result is bit-identical.  The other variants'
+ * scratch (repacked weights) does not depend on the batch: for them this
+ * equals conv_scratch_bytes.
+ * Errors: as conv_scratch_bytes. */
+CONV_API conv_status conv_scratch_bytes_per_image(const conv_problem* p, size_t* bytes);
+
 /* Writes a one-line description of what conv_forward runs for `p` on the
  * current device into buf (NUL-terminated, truncated to len), ending with
  * "launches=N", the number of kernels one conv_forward call launches. */
@@ -216,8 +229,11 @@ CONV_API conv_status conv_describe_variant(const conv_problem* p, char* buf, siz
  *   bias        device pointer, read iff p->has_bias (then required);
  *   residual    device pointer, read iff p->has_residual (then required);
  *   scratch     device memory of scratch_bytes bytes, at least
- *               conv_scratch_bytes(p); may be NULL when that is 0.  Its range
- *               must overlap no operand; y must overlap no input.
+ *               conv_scratch_bytes(p) -- or, for the CUDA-core variant, at
+ *               least conv_scratch_bytes_per_image(p), which runs the batch in
+ *               chunks of whole images with bit-identical results; may be
+ *               NULL when that is 0.  The range conv_forward uses must overlap
+ *               no operand; y must overlap no input.
  *   stream      cudaStream_t (NULL: legacy default stream).
  * Errors: those of conv_plan; CONV_ERR_NULL, CONV_ERR_SCRATCH, CONV_ERR_ALIAS
  * before anything is enqueued; CONV_ERR_DEVICE; CONV_ERR_CUDA when a launch
