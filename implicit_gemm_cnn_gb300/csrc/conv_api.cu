@@ -291,6 +291,22 @@ bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   const long long nw_bytes = 8LL * 2 * (s.ho + p->kh - 1) * (s.wo + p->kw + 2) * es;
   d.narrow = p->stride_h == 1 && p->stride_w == 1 && p->dil_h == 1 && p->dil_w == 1 && p->kh == p->kw &&
              (p->kh == 3 || p->kh == 5 || p->kh == 7) && s.wo <= 32 && nw_bytes <= 96 * 1024;
+  // four output columns per lane: the column groups x row blocks of a plane
+  // fill one warp, with at most 8 rows per lane (the compiled row counts
+  // 2, 4, 7, 8: the smallest that covers the plane)
+  d.cols4_r = 0;
+  if (d.narrow) {
+    const long long groups = (s.wo + 3) / 4, rblocks = 32 / groups;
+    const long long r = (s.ho + rblocks - 1) / rblocks;
+    for (int rt : {2, 4, 7, 8}) {
+      if (rt >= r) { d.cols4_r = rt; break; }
+    }
+    const long long nv = (p->kw + 6) / 4 * 4;
+    const long long unit = 16 / es;
+    const long long pitch = (std::max<long long>(p->pad_left + p->w, 4 * (groups - 1) + nv) + unit - 1) / unit * unit;
+    const long long rows = rblocks * d.cols4_r + p->kh - 1;
+    if (d.cols4_r && 8LL * 2 * pitch * rows * es > 100 * 1024) d.cols4_r = 0;  // two blocks per SM
+  }
   out->dw = d;
   out->info.variant = CONV_VARIANT_DEPTHWISE;
   out->info.split_k = 1;
@@ -568,6 +584,9 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
              "%s grouped: input rows staged once per (group, image, %d output rows), %d staged rows of %d, "
              "8co x 4px per thread, items=%lld sms=%d",
              variant_name(i.variant), kGdRows, plan.gd.rows_in, plan.gd.pitch, static_cast<long long>(plan.gd.items), sm);
+  } else if (i.variant == CONV_VARIANT_DEPTHWISE && plan.dw.cols4_r) {
+    snprintf(buf, len, "%s one warp per plane, 4 columns x %d rows per lane, double-buffered planes sms=%d",
+             variant_name(i.variant), plan.dw.cols4_r, sm);
   } else if (i.variant == CONV_VARIANT_DEPTHWISE && plan.dw.narrow) {
     snprintf(buf, len, "%s one warp per plane, window in registers, double-buffered planes sms=%d",
              variant_name(i.variant), sm);

@@ -25,9 +25,10 @@
 // each output is summed in one float32 chain in (kernel column, kernel row)
 // order.  Bias, residual and activation are applied at the store.
 //
-// Planes at most 32 output columns wide at stride 1 take a leaner path (one
-// warp per plane, below): no work-item arithmetic per output, the window in
-// registers, the next plane copied while the current one is computed.
+// Planes at most 32 output columns wide at stride 1 take leaner paths (one
+// warp per plane, below): no work-item arithmetic per output, the next plane
+// copied while the current one is computed -- four output columns per lane
+// where the plane's rows divide among the lanes, else one column per lane.
 #include <algorithm>
 
 #include "conv_internal.h"
@@ -373,6 +374,215 @@ __global__ void __launch_bounds__(kNwWarps * 32, K == 7 ? 2 : 3) depthwise_narro
   }
 }
 
+// ---- narrow planes, four output columns per lane -----------------------------
+// One warp per plane (image, output channel) at a time; lane = (group of 4
+// output columns, block of R output rows).  The zero-bordered plane sits in
+// shared memory, two buffers per warp: the next plane arrives by cp.async
+// (16-, 8- or 4-byte copies; each lane keeps one copy column and strides down
+// the rows) while this one is computed.  A lane streams the R + K - 1 input
+// rows its outputs read, each as K + 3 consecutive values fetched with vector
+// shared loads, and adds the row's taps to the 4 x R accumulators it feeds:
+// input row i serves output row i - u with kernel row u, so each output is
+// summed in one float32 chain in (u, v) order, the order of every other
+// kernel here.  Weights sit in registers; bias, residual and activation are
+// applied at the store, four outputs per vector store where aligned.
+struct Cols4Geo {
+  int pitch;       // elements per staged row (a multiple of 16 bytes)
+  int rows;        // staged rows: rblocks * R + K - 1 (rows past the plane stay zero)
+  int copy;        // bytes per cp.async copy of an image row (16, 8, 4), 0: element loads
+  int groups;      // column groups: ceil(Wo / 4)
+  int rblocks;     // row blocks: 32 / groups
+  int vec_io;      // y (and the residual) take 4-output vector accesses
+};
+
+template <typename T, int N>
+__device__ __forceinline__ void load_row_vals(const T* src, float (&v)[N]) {
+  // N consecutive elements starting at a 4-element boundary of shared memory
+  static_assert(N % 4 == 0, "whole quads");
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+      const float4 t = reinterpret_cast<const float4*>(src)[q];
+      v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+      const uint2 t = reinterpret_cast<const uint2*>(src)[q];
+      const T* h = reinterpret_cast<const T*>(&t);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[4 * q + e] = to_f32(h[e]);
+    }
+  }
+}
+
+template <typename T, int K, int R>
+__global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvArgs a, const Cols4Geo g) {
+  constexpr int NV = (K + 3 + 3) / 4 * 4;  // values read per input row (K + 3, rounded to quads)
+  extern __shared__ __align__(16) unsigned char dsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bufsz = g.pitch * g.rows;
+  T* buf0 = reinterpret_cast<T*>(dsm) + static_cast<size_t>(warp) * 2 * bufsz;
+  for (int i = lane; i < 2 * bufsz; i += 32) buf0[i] = from_f32<T>(0.0f);  // the border stays zero
+  __syncwarp();
+  const T* __restrict__ xg = static_cast<const T*>(a.x);
+  const T* __restrict__ wg = static_cast<const T*>(a.wt);
+  const T* __restrict__ bg = static_cast<const T*>(a.bias);
+  const T* __restrict__ rg = static_cast<const T*>(a.residual);
+  T* __restrict__ y = static_cast<T*>(a.y);
+  const long long planes = static_cast<long long>(a.n) * a.c_out;
+  const long long first = static_cast<long long>(blockIdx.x) * kNwWarps + warp;
+  const long long stride = static_cast<long long>(gridDim.x) * kNwWarps;
+  const int m = a.mg;
+  // staging: image rows land at buffer row pt + r, column pl + c
+  const int rows_s = min(a.h, g.rows - a.pt);
+  const int ce = g.copy ? g.copy / static_cast<int>(sizeof(T)) : 1;  // elements per copy
+  const int units = (a.w + ce - 1) / ce;                            // copies per image row
+  const int rpp = units <= 32 ? 32 / units : 1;                      // rows per pass of the warp
+  const int my_r0 = units <= 32 ? lane / units : 0;
+  const int my_q = units <= 32 ? lane - my_r0 * units : lane;
+  const bool stager = units <= 32 ? my_r0 < rpp : true;
+  auto stage = [&](long long pl, T* buf) {
+    const int n = static_cast<int>(pl / a.c_out);
+    const int co = static_cast<int>(pl - static_cast<long long>(n) * a.c_out);
+    const T* src = xg + (static_cast<long long>(n) * a.c_in + co / m) * a.hw;
+    if (!stager) return;
+    for (int r = my_r0; r < rows_s; r += rpp) {
+      T* drow = buf + (a.pt + r) * g.pitch + a.pl;
+      const T* srow = src + static_cast<long long>(r) * a.w;
+      for (int q = my_q; q < units; q += (units <= 32 ? units : 32)) {
+        if (g.copy == 16) cp_async_n<16>(drow + q * ce, srow + q * ce);
+        else if (g.copy == 8) cp_async_n<8>(drow + q * ce, srow + q * ce);
+        else if (g.copy == 4) cp_async_n<4>(drow + q * ce, srow + q * ce);
+        else drow[q] = srow[q];
+      }
+    }
+  };
+  // this lane's outputs: columns 4j .. 4j+3, rows rb*R .. rb*R + R - 1
+  const int j = lane % g.groups, rb = lane / g.groups;
+  const bool worker = rb < g.rblocks && 4 * j < a.wo;
+  int k = 0;
+  if (first < planes) stage(first, buf0);
+  cp_async_commit();
+  for (long long pl = first; pl < planes; pl += stride, ++k) {
+    T* buf = buf0 + (k & 1) * bufsz;
+    if (pl + stride < planes) stage(pl + stride, buf0 + ((k + 1) & 1) * bufsz);
+    cp_async_commit();
+    const int n = static_cast<int>(pl / a.c_out);
+    const int co = static_cast<int>(pl - static_cast<long long>(n) * a.c_out);
+    float wv[K][K];
+#pragma unroll
+    for (int u = 0; u < K; ++u)
+#pragma unroll
+      for (int v = 0; v < K; ++v) wv[u][v] = to_f32(wg[static_cast<long long>(co) * K * K + u * K + v]);
+    const float bv = bg ? to_f32(bg[co]) : 0.0f;
+    cp_async_wait<1>();  // this plane's copies (the next plane's may still fly)
+    __syncwarp();
+    if (worker) {
+      float acc[R][4];
+#pragma unroll
+      for (int o = 0; o < R; ++o)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[o][c] = 0.0f;
+      const T* base = buf + (rb * R) * g.pitch + 4 * j;  // buffer row rb*R, the group's first window column
+#pragma unroll
+      for (int i = 0; i < R + K - 1; ++i) {
+        float xv[NV];
+        load_row_vals<T, NV>(base + i * g.pitch, xv);
+#pragma unroll
+        for (int u = 0; u < K; ++u) {
+          const int o = i - u;  // the output row this input row feeds with kernel row u
+          if (o < 0 || o >= R) continue;
+#pragma unroll
+          for (int v = 0; v < K; ++v)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[o][c] = fmaf(xv[c + v], wv[u][v], acc[o][c]);
+        }
+      }
+      const long long pbase = (static_cast<long long>(n) * a.c_out + co) * a.howo;
+      const int ow = 4 * j;
+#pragma unroll
+      for (int o = 0; o < R; ++o) {
+        const int oh = rb * R + o;
+        if (oh >= a.ho) break;
+        const long long off = pbase + static_cast<long long>(oh) * a.wo + ow;
+        const bool full = g.vec_io && ow + 3 < a.wo;
+        float v[4] = {acc[o][0], acc[o][1], acc[o][2], acc[o][3]}, bb[4] = {bv, bv, bv, bv}, rr[4] = {0, 0, 0, 0};
+        if (rg) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) rr[c] = ow + c < a.wo ? to_f32(rg[off + c]) : 0.0f;
+        }
+        epilogue_n<4>(v, bb, rr, bg != nullptr, rg != nullptr, a.act, a.alpha, a.beta);
+        if (full) {
+          if constexpr (sizeof(T) == 4) {
+            *reinterpret_cast<float4*>(y + off) = make_float4(v[0], v[1], v[2], v[3]);
+          } else {
+            T h[4] = {from_f32<T>(v[0]), from_f32<T>(v[1]), from_f32<T>(v[2]), from_f32<T>(v[3])};
+            *reinterpret_cast<uint2*>(y + off) = *reinterpret_cast<const uint2*>(h);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (ow + c < a.wo) y[off + c] = from_f32<T>(v[c]);
+        }
+      }
+    }
+    __syncwarp();  // this buffer's reads are done before it is refilled
+  }
+  cp_async_wait<0>();
+}
+
+// Rows per lane the four-column kernel is compiled for.
+constexpr int kCols4Rows[] = {2, 4, 7, 8};
+
+template <typename T, int K, int R>
+cudaError_t launch_cols4_r(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  Cols4Geo g;
+  constexpr int es = static_cast<int>(sizeof(T));
+  constexpr int NV = (K + 3 + 3) / 4 * 4;
+  g.groups = (a.wo + 3) / 4;
+  g.rblocks = 32 / g.groups;
+  g.rows = g.rblocks * R + K - 1;
+  // rows of whole 16-byte units: every row (and every warp's buffer) starts on
+  // 16 bytes, as 16-byte copies and the vector reads need
+  constexpr int unit = 16 / es;
+  g.pitch = (std::max(a.pl + a.w, 4 * (g.groups - 1) + NV) + unit - 1) / unit * unit;
+  // the widest copy that keeps every row start and the buffer column aligned
+  g.copy = 0;
+  for (int cb = 16; cb >= 4; cb /= 2) {
+    if (reinterpret_cast<uintptr_t>(a.x) % cb == 0 && (static_cast<long long>(a.w) * es) % cb == 0 &&
+        (a.hw * es) % cb == 0 && (a.pl * es) % cb == 0) {
+      g.copy = cb;
+      break;
+    }
+  }
+  g.vec_io = reinterpret_cast<uintptr_t>(a.y) % 16 == 0 && (a.wo % 4) == 0 &&
+             (!a.residual || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0);
+  const size_t smem = static_cast<size_t>(kNwWarps) * 2 * g.pitch * g.rows * es;
+  auto kern = depthwise_cols4<T, K, R>;
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
+  if (err != cudaSuccess) return err;
+  const long long planes = static_cast<long long>(a.n) * a.c_out;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNwWarps * 32, smem);
+  if (err != cudaSuccess) return err;
+  const long long blocks = std::min<long long>((planes + kNwWarps - 1) / kNwWarps,
+                                               static_cast<long long>(d.sm) * std::max(per_sm, 1));
+  kern<<<static_cast<unsigned>(blocks), kNwWarps * 32, smem, s>>>(a, g);
+  return cudaGetLastError();
+}
+
+template <typename T, int K>
+cudaError_t launch_cols4(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  switch (d.cols4_r) {
+    case 2: return launch_cols4_r<T, K, 2>(d, a, s);
+    case 4: return launch_cols4_r<T, K, 4>(d, a, s);
+    case 7: return launch_cols4_r<T, K, 7>(d, a, s);
+    case 8: return launch_cols4_r<T, K, 8>(d, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <typename T, int K>
 cudaError_t launch_narrow(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
   NarrowGeo g;
@@ -412,6 +622,11 @@ cudaError_t launch_kh(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_typed(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  if (d.cols4_r) {
+    if (a.kh == 3) return launch_cols4<T, 3>(d, a, s);
+    if (a.kh == 5) return launch_cols4<T, 5>(d, a, s);
+    if (a.kh == 7) return launch_cols4<T, 7>(d, a, s);
+  }
   if (d.narrow) {
     if (a.kh == 3) return launch_narrow<T, 3>(d, a, s);
     if (a.kh == 5) return launch_narrow<T, 5>(d, a, s);

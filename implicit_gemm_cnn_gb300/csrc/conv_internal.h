@@ -70,6 +70,7 @@ struct DwPlan {
   int vec;       // bytes per cp.async copy of input rows (16/8/4; 0: element copies)
   int sm;        // SMs of the device (blocks loop over the work items)
   int narrow;    // one warp per plane (stride 1, dilation 1, square 3/5/7, Wo <= 32)
+  int cols4_r;   // narrow planes, four columns per lane: output rows per lane (2, 4, 7, 8), 0: not used
 };
 size_t depthwise_smem_bytes(const DwPlan& d, int mg, int kh, int kw, int dtype);
 

@@ -114,6 +114,11 @@ EDGE = [
      dict(pads=(2, 1, 0, 3), groups=5, act="hard_sigmoid", alpha=0.2, beta=0.5), True, True),
     ("depthwise_narrow_tall", (1, 3, 60, 7), (3, 1, 7, 7), dict(pads=3, groups=3, act="leaky_relu", alpha=0.1),
      True, False),
+    # more rows than 8 per lane: the one-column-per-lane narrow kernel
+    ("depthwise_narrow_very_tall", (1, 4, 70, 30), (4, 1, 3, 3), dict(pads=1, groups=4, act="relu"), True, True),
+    # four columns per lane with a ragged last column group and 2 rows per lane
+    ("depthwise_cols4_ragged", (3, 5, 10, 18), (10, 1, 5, 5), dict(pads=(2, 1, 2, 3), groups=5, act="silu"),
+     True, True),
     ("one_d", (3, 4, 1, 37), (6, 4, 1, 5), dict(pads=(0, 2, 0, 2), act="leaky_relu", alpha=0.1),
      True, False),
     ("single_output", (2, 3, 5, 5), (4, 3, 5, 5), dict(act="sigmoid"), True, False),
