@@ -392,7 +392,8 @@ struct Cols4Geo {
   int copy;        // bytes per cp.async copy of an image row (16, 8, 4), 0: element loads
   int groups;      // column groups: ceil(Wo / 4)
   int rblocks;     // row blocks: 32 / groups
-  int vec_io;      // y (and the residual) take 4-output vector accesses
+  int vec_io;      // Ho*Wo and Wo multiples of 4, y (and the residual) 16-byte aligned
+  int out_stride;  // floats of one warp's staged sums (Ho*Wo rounded up to 4)
 };
 
 template <typename T, int N>
@@ -416,6 +417,44 @@ __device__ __forceinline__ void load_row_vals(const T* src, float (&v)[N]) {
   }
 }
 
+// The epilogue of one plane, after its sums are in `out` (float32, the plane's
+// Ho x Wo outputs in order): bias, residual, activation, one rounding, stores
+// of 4 consecutive outputs by consecutive lanes (coalesced).
+template <typename T, int ACT>
+__device__ __forceinline__ void cols4_store_plane(const ConvArgs& a, const float* out, long long pbase, float bv,
+                                                  bool has_bias, int vec_io) {
+  const int lane = threadIdx.x & 31;
+  const T* __restrict__ rg = static_cast<const T*>(a.residual);
+  T* __restrict__ y = static_cast<T*>(a.y);
+  const int hw = a.ho * a.wo;
+  if (vec_io) {  // Ho*Wo a multiple of 4, y (and the residual) 16-byte aligned
+    for (int e = 4 * lane; e < hw; e += 128) {
+      float v[4];
+      const float4 t = *reinterpret_cast<const float4*>(out + e);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (has_bias) v[c] = __fadd_rn(v[c], bv);
+        if (rg) v[c] = __fadd_rn(v[c], to_f32(rg[pbase + e + c]));
+        v[c] = act_fn<ACT>(v[c], a.alpha, a.beta);
+      }
+      if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4*>(y + pbase + e) = make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+        T h[4] = {from_f32<T>(v[0]), from_f32<T>(v[1]), from_f32<T>(v[2]), from_f32<T>(v[3])};
+        *reinterpret_cast<uint2*>(y + pbase + e) = *reinterpret_cast<const uint2*>(h);
+      }
+    }
+  } else {
+    for (int e = lane; e < hw; e += 32) {
+      float v = out[e];
+      if (has_bias) v = __fadd_rn(v, bv);
+      if (rg) v = __fadd_rn(v, to_f32(rg[pbase + e]));
+      y[pbase + e] = from_f32<T>(act_fn<ACT>(v, a.alpha, a.beta));
+    }
+  }
+}
+
 template <typename T, int K, int R>
 __global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvArgs a, const Cols4Geo g) {
   constexpr int NV = (K + 3 + 3) / 4 * 4;  // values read per input row (K + 3, rounded to quads)
@@ -423,39 +462,48 @@ __global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvAr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bufsz = g.pitch * g.rows;
   T* buf0 = reinterpret_cast<T*>(dsm) + static_cast<size_t>(warp) * 2 * bufsz;
+  // the plane's float32 sums (Ho x Wo), staged for the coalesced epilogue
+  float* outs = reinterpret_cast<float*>(dsm + static_cast<size_t>(kNwWarps) * 2 * bufsz * sizeof(T)) +
+                static_cast<size_t>(warp) * g.out_stride;
   for (int i = lane; i < 2 * bufsz; i += 32) buf0[i] = from_f32<T>(0.0f);  // the border stays zero
   __syncwarp();
   const T* __restrict__ xg = static_cast<const T*>(a.x);
   const T* __restrict__ wg = static_cast<const T*>(a.wt);
   const T* __restrict__ bg = static_cast<const T*>(a.bias);
-  const T* __restrict__ rg = static_cast<const T*>(a.residual);
-  T* __restrict__ y = static_cast<T*>(a.y);
-  const long long planes = static_cast<long long>(a.n) * a.c_out;
-  const long long first = static_cast<long long>(blockIdx.x) * kNwWarps + warp;
-  const long long stride = static_cast<long long>(gridDim.x) * kNwWarps;
+  const int planes = a.n * a.c_out;  // fits int32 (checked by the planner)
+  // planes are dealt round-robin over the blocks first, so the last, partly
+  // filled round of planes spreads over all SMs
+  const int first = warp * gridDim.x + blockIdx.x;
+  const int stride = gridDim.x * kNwWarps;
   const int m = a.mg;
-  // staging: image rows land at buffer row pt + r, column pl + c
+  // staging: image rows land at buffer row pt + r, column pl + c; a lane keeps
+  // one copy column and strides down the rows
   const int rows_s = min(a.h, g.rows - a.pt);
   const int ce = g.copy ? g.copy / static_cast<int>(sizeof(T)) : 1;  // elements per copy
   const int units = (a.w + ce - 1) / ce;                            // copies per image row
   const int rpp = units <= 32 ? 32 / units : 1;                      // rows per pass of the warp
   const int my_r0 = units <= 32 ? lane / units : 0;
   const int my_q = units <= 32 ? lane - my_r0 * units : lane;
+  const int q_step = units <= 32 ? units : 32;
   const bool stager = units <= 32 ? my_r0 < rpp : true;
-  auto stage = [&](long long pl, T* buf) {
-    const int n = static_cast<int>(pl / a.c_out);
-    const int co = static_cast<int>(pl - static_cast<long long>(n) * a.c_out);
-    const T* src = xg + (static_cast<long long>(n) * a.c_in + co / m) * a.hw;
+  auto stage = [&](int pl, T* buf) {
     if (!stager) return;
-    for (int r = my_r0; r < rows_s; r += rpp) {
-      T* drow = buf + (a.pt + r) * g.pitch + a.pl;
-      const T* srow = src + static_cast<long long>(r) * a.w;
-      for (int q = my_q; q < units; q += (units <= 32 ? units : 32)) {
-        if (g.copy == 16) cp_async_n<16>(drow + q * ce, srow + q * ce);
-        else if (g.copy == 8) cp_async_n<8>(drow + q * ce, srow + q * ce);
-        else if (g.copy == 4) cp_async_n<4>(drow + q * ce, srow + q * ce);
-        else drow[q] = srow[q];
-      }
+    const int n = pl / a.c_out;
+    const int co = pl - n * a.c_out;
+    const T* src = xg + (static_cast<long long>(n) * a.c_in + co / m) * a.hw;
+    T* dst = buf + a.pt * g.pitch + a.pl;
+    if (g.copy == 16) {
+      for (int r = my_r0; r < rows_s; r += rpp)
+        for (int q = my_q; q < units; q += q_step) cp_async_n<16>(dst + r * g.pitch + q * ce, src + r * a.w + q * ce);
+    } else if (g.copy == 8) {
+      for (int r = my_r0; r < rows_s; r += rpp)
+        for (int q = my_q; q < units; q += q_step) cp_async_n<8>(dst + r * g.pitch + q * ce, src + r * a.w + q * ce);
+    } else if (g.copy == 4) {
+      for (int r = my_r0; r < rows_s; r += rpp)
+        for (int q = my_q; q < units; q += q_step) cp_async_n<4>(dst + r * g.pitch + q * ce, src + r * a.w + q * ce);
+    } else {
+      for (int r = my_r0; r < rows_s; r += rpp)
+        for (int q = my_q; q < units; q += q_step) dst[r * g.pitch + q] = src[r * a.w + q];
     }
   };
   // this lane's outputs: columns 4j .. 4j+3, rows rb*R .. rb*R + R - 1
@@ -464,12 +512,12 @@ __global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvAr
   int k = 0;
   if (first < planes) stage(first, buf0);
   cp_async_commit();
-  for (long long pl = first; pl < planes; pl += stride, ++k) {
+  for (int pl = first; pl < planes; pl += stride, ++k) {
     T* buf = buf0 + (k & 1) * bufsz;
     if (pl + stride < planes) stage(pl + stride, buf0 + ((k + 1) & 1) * bufsz);
     cp_async_commit();
-    const int n = static_cast<int>(pl / a.c_out);
-    const int co = static_cast<int>(pl - static_cast<long long>(n) * a.c_out);
+    const int n = pl / a.c_out;
+    const int co = pl - n * a.c_out;
     float wv[K][K];
 #pragma unroll
     for (int u = 0; u < K; ++u)
@@ -489,45 +537,51 @@ __global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvAr
       for (int i = 0; i < R + K - 1; ++i) {
         float xv[NV];
         load_row_vals<T, NV>(base + i * g.pitch, xv);
+        // input row i feeds output row i - u with kernel row u; v outermost
+        // interleaves the independent output rows (each output's terms still
+        // arrive in (u, v) order: one u per input row, v ascending)
 #pragma unroll
-        for (int u = 0; u < K; ++u) {
-          const int o = i - u;  // the output row this input row feeds with kernel row u
-          if (o < 0 || o >= R) continue;
+        for (int v = 0; v < K; ++v)
 #pragma unroll
-          for (int v = 0; v < K; ++v)
+          for (int u = 0; u < K; ++u) {
+            const int o = i - u;
+            if (o < 0 || o >= R) continue;
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[o][c] = fmaf(xv[c + v], wv[u][v], acc[o][c]);
-        }
+          }
       }
-      const long long pbase = (static_cast<long long>(n) * a.c_out + co) * a.howo;
-      const int ow = 4 * j;
+      // the sums into the plane's staging area (rows past Ho, columns past Wo dropped)
 #pragma unroll
       for (int o = 0; o < R; ++o) {
         const int oh = rb * R + o;
         if (oh >= a.ho) break;
-        const long long off = pbase + static_cast<long long>(oh) * a.wo + ow;
-        const bool full = g.vec_io && ow + 3 < a.wo;
-        float v[4] = {acc[o][0], acc[o][1], acc[o][2], acc[o][3]}, bb[4] = {bv, bv, bv, bv}, rr[4] = {0, 0, 0, 0};
-        if (rg) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) rr[c] = ow + c < a.wo ? to_f32(rg[off + c]) : 0.0f;
-        }
-        epilogue_n<4>(v, bb, rr, bg != nullptr, rg != nullptr, a.act, a.alpha, a.beta);
-        if (full) {
-          if constexpr (sizeof(T) == 4) {
-            *reinterpret_cast<float4*>(y + off) = make_float4(v[0], v[1], v[2], v[3]);
-          } else {
-            T h[4] = {from_f32<T>(v[0]), from_f32<T>(v[1]), from_f32<T>(v[2]), from_f32<T>(v[3])};
-            *reinterpret_cast<uint2*>(y + off) = *reinterpret_cast<const uint2*>(h);
-          }
+        float* dst = outs + oh * a.wo + 4 * j;
+        if (g.vec_io && 4 * j + 3 < a.wo) {
+          *reinterpret_cast<float4*>(dst) = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            if (ow + c < a.wo) y[off + c] = from_f32<T>(v[c]);
+            if (4 * j + c < a.wo) dst[c] = acc[o][c];
         }
       }
     }
-    __syncwarp();  // this buffer's reads are done before it is refilled
+    __syncwarp();  // this plane's sums are staged and its input buffer is read
+    const long long pbase = (static_cast<long long>(n) * a.c_out + co) * a.howo;
+    switch (a.act) {
+#define CONV_C4_CASE(A) \
+  case A: cols4_store_plane<T, A>(a, outs, pbase, bv, bg != nullptr, g.vec_io); break;
+      CONV_C4_CASE(ACT_RELU)
+      CONV_C4_CASE(ACT_SILU)
+      CONV_C4_CASE(ACT_SIGMOID)
+      CONV_C4_CASE(ACT_TANH)
+      CONV_C4_CASE(ACT_HARD_SWISH)
+      CONV_C4_CASE(ACT_HARD_SIGMOID)
+      CONV_C4_CASE(ACT_CLIP)
+      CONV_C4_CASE(ACT_LEAKY_RELU)
+#undef CONV_C4_CASE
+      default: cols4_store_plane<T, ACT_IDENTITY>(a, outs, pbase, bv, bg != nullptr, g.vec_io);
+    }
+    __syncwarp();  // the staging area is free for the next plane
   }
   cp_async_wait<0>();
 }
@@ -558,7 +612,8 @@ cudaError_t launch_cols4_r(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
   }
   g.vec_io = reinterpret_cast<uintptr_t>(a.y) % 16 == 0 && (a.wo % 4) == 0 &&
              (!a.residual || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0);
-  const size_t smem = static_cast<size_t>(kNwWarps) * 2 * g.pitch * g.rows * es;
+  g.out_stride = (a.ho * a.wo + 3) / 4 * 4;
+  const size_t smem = static_cast<size_t>(kNwWarps) * (2 * g.pitch * g.rows * es + g.out_stride * 4);
   auto kern = depthwise_cols4<T, K, R>;
   cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
