@@ -455,24 +455,6 @@ __device__ __forceinline__ void cols4_store_plane(const ConvArgs& a, const float
   }
 }
 
-// Two float32 lanes in one 64-bit register, and the packed fused multiply-add
-// of sm_100-class GPUs: each half is an ordinary IEEE fp32 FMA rounded to
-// nearest, so a packed chain gives the same bits as two scalar chains.
-__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpack_f2(unsigned long long v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ unsigned long long fma_f2(unsigned long long a, unsigned long long b,
-                                                     unsigned long long c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
 template <typename T, int K, int R>
 __global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvArgs a, const Cols4Geo g) {
   constexpr int NV = (K + 3 + 3) / 4 * 4;  // values read per input row (K + 3, rounded to quads)
@@ -536,64 +518,50 @@ __global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvAr
     cp_async_commit();
     const int n = pl / a.c_out;
     const int co = pl - n * a.c_out;
-    unsigned long long w2[K][K];  // each weight twice: the multiplier of a column pair
+    float wv[K][K];
 #pragma unroll
     for (int u = 0; u < K; ++u)
 #pragma unroll
-      for (int v = 0; v < K; ++v) {
-        const float wt = to_f32(wg[static_cast<long long>(co) * K * K + u * K + v]);
-        w2[u][v] = pack_f2(wt, wt);
-      }
+      for (int v = 0; v < K; ++v) wv[u][v] = to_f32(wg[static_cast<long long>(co) * K * K + u * K + v]);
     const float bv = bg ? to_f32(bg[co]) : 0.0f;
     cp_async_wait<1>();  // this plane's copies (the next plane's may still fly)
     __syncwarp();
     if (worker) {
-      // accumulators as column pairs: acc[o][0] = columns (0, 1), acc[o][1] = (2, 3)
-      unsigned long long acc[R][2];
+      float acc[R][4];
 #pragma unroll
-      for (int o = 0; o < R; ++o) acc[o][0] = acc[o][1] = 0ull;
+      for (int o = 0; o < R; ++o)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[o][c] = 0.0f;
       const T* base = buf + (rb * R) * g.pitch + 4 * j;  // buffer row rb*R, the group's first window column
 #pragma unroll
       for (int i = 0; i < R + K - 1; ++i) {
         float xv[NV];
         load_row_vals<T, NV>(base + i * g.pitch, xv);
-        // column pairs of the row: ev[q] = (x[2q], x[2q+1]), od[q] = (x[2q+1], x[2q+2])
-        unsigned long long ev[NV / 2], od[NV / 2 - 1];
-#pragma unroll
-        for (int q = 0; q < NV / 2; ++q) ev[q] = pack_f2(xv[2 * q], xv[2 * q + 1]);
-#pragma unroll
-        for (int q = 0; q < NV / 2 - 1; ++q) od[q] = pack_f2(xv[2 * q + 1], xv[2 * q + 2]);
         // input row i feeds output row i - u with kernel row u; v outermost
         // interleaves the independent output rows (each output's terms still
         // arrive in (u, v) order: one u per input row, v ascending)
 #pragma unroll
-        for (int v = 0; v < K; ++v) {
-          const unsigned long long x01 = (v & 1) ? od[v / 2] : ev[v / 2];          // columns v, v+1
-          const unsigned long long x23 = (v & 1) ? od[v / 2 + 1] : ev[v / 2 + 1];  // columns v+2, v+3
+        for (int v = 0; v < K; ++v)
 #pragma unroll
           for (int u = 0; u < K; ++u) {
             const int o = i - u;
             if (o < 0 || o >= R) continue;
-            acc[o][0] = fma_f2(x01, w2[u][v], acc[o][0]);
-            acc[o][1] = fma_f2(x23, w2[u][v], acc[o][1]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[o][c] = fmaf(xv[c + v], wv[u][v], acc[o][c]);
           }
-        }
       }
       // the sums into the plane's staging area (rows past Ho, columns past Wo dropped)
 #pragma unroll
       for (int o = 0; o < R; ++o) {
         const int oh = rb * R + o;
         if (oh >= a.ho) break;
-        float sv[4];
-        unpack_f2(acc[o][0], sv[0], sv[1]);
-        unpack_f2(acc[o][1], sv[2], sv[3]);
         float* dst = outs + oh * a.wo + 4 * j;
         if (g.vec_io && 4 * j + 3 < a.wo) {
-          *reinterpret_cast<float4*>(dst) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+          *reinterpret_cast<float4*>(dst) = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            if (4 * j + c < a.wo) dst[c] = sv[c];
+            if (4 * j + c < a.wo) dst[c] = acc[o][c];
         }
       }
     }
