@@ -306,7 +306,7 @@ bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
     const long long pitch = (std::max<long long>(p->pad_left + p->w, 4 * (groups - 1) + nv) + unit - 1) / unit * unit;
     const long long rows = rblocks * d.cols4_r + p->kh - 1;
     const long long outs = (s.ho * s.wo + 3) / 4 * 4 * 4;  // one warp's staged sums
-    if (d.cols4_r && 8LL * (2 * pitch * rows * es + outs) > 100 * 1024) d.cols4_r = 0;  // two blocks per SM
+    if (d.cols4_r && 4LL * (2 * pitch * rows * es + outs) > 45 * 1024) d.cols4_r = 0;  // five blocks per SM
     if (p->n * p->c_out > 2000000000LL) d.cols4_r = 0;  // plane indices (and the stride past them) in 32 bits
   }
   out->dw = d;

@@ -455,15 +455,17 @@ __device__ __forceinline__ void cols4_store_plane(const ConvArgs& a, const float
   }
 }
 
+constexpr int kC4Warps = 4;  // warps per block of the four-column kernel (five blocks per SM)
+
 template <typename T, int K, int R>
-__global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvArgs a, const Cols4Geo g) {
+__global__ void __launch_bounds__(kC4Warps * 32, 5) depthwise_cols4(const ConvArgs a, const Cols4Geo g) {
   constexpr int NV = (K + 3 + 3) / 4 * 4;  // values read per input row (K + 3, rounded to quads)
   extern __shared__ __align__(16) unsigned char dsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bufsz = g.pitch * g.rows;
   T* buf0 = reinterpret_cast<T*>(dsm) + static_cast<size_t>(warp) * 2 * bufsz;
   // the plane's float32 sums (Ho x Wo), staged for the coalesced epilogue
-  float* outs = reinterpret_cast<float*>(dsm + static_cast<size_t>(kNwWarps) * 2 * bufsz * sizeof(T)) +
+  float* outs = reinterpret_cast<float*>(dsm + static_cast<size_t>(kC4Warps) * 2 * bufsz * sizeof(T)) +
                 static_cast<size_t>(warp) * g.out_stride;
   for (int i = lane; i < 2 * bufsz; i += 32) buf0[i] = from_f32<T>(0.0f);  // the border stays zero
   __syncwarp();
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(kNwWarps * 32, 2) depthwise_cols4(const ConvAr
   // planes are dealt round-robin over the blocks first, so the last, partly
   // filled round of planes spreads over all SMs
   const int first = warp * gridDim.x + blockIdx.x;
-  const int stride = gridDim.x * kNwWarps;
+  const int stride = gridDim.x * kC4Warps;
   const int m = a.mg;
   // staging: image rows land at buffer row pt + r, column pl + c; a lane keeps
   // one copy column and strides down the rows
@@ -613,17 +615,17 @@ cudaError_t launch_cols4_r(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
   g.vec_io = reinterpret_cast<uintptr_t>(a.y) % 16 == 0 && (a.wo % 4) == 0 &&
              (!a.residual || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0);
   g.out_stride = (a.ho * a.wo + 3) / 4 * 4;
-  const size_t smem = static_cast<size_t>(kNwWarps) * (2 * g.pitch * g.rows * es + g.out_stride * 4);
+  const size_t smem = static_cast<size_t>(kC4Warps) * (2 * g.pitch * g.rows * es + g.out_stride * 4);
   auto kern = depthwise_cols4<T, K, R>;
   cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   const long long planes = static_cast<long long>(a.n) * a.c_out;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNwWarps * 32, smem);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kC4Warps * 32, smem);
   if (err != cudaSuccess) return err;
-  const long long blocks = std::min<long long>((planes + kNwWarps - 1) / kNwWarps,
+  const long long blocks = std::min<long long>((planes + kC4Warps - 1) / kC4Warps,
                                                static_cast<long long>(d.sm) * std::max(per_sm, 1));
-  kern<<<static_cast<unsigned>(blocks), kNwWarps * 32, smem, s>>>(a, g);
+  kern<<<static_cast<unsigned>(blocks), kC4Warps * 32, smem, s>>>(a, g);
   return cudaGetLastError();
 }
 
