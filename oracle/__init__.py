@@ -26,6 +26,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "conv_oracle.c")
+_SRC_INT = os.path.join(_HERE, "conv_integer_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _lock = threading.Lock()
 _libs: dict[int, ctypes.CDLL] = {}
@@ -47,12 +48,13 @@ def build(mutant: int = 0, force: bool = False) -> str:
     epilogue rounds each step on every host).  ``mutant`` > 0 plants one
     deliberate mistake; the pin tests use those builds to show they catch it."""
     out = library_path(mutant)
-    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_INT))
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= newest:
         return out
     os.makedirs(_BUILD, exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-           "-shared", "-pthread", f"-DORACLE_MUTANT={mutant}", _SRC, "-o", tmp, "-lm"]
+           "-shared", "-pthread", f"-DORACLE_MUTANT={mutant}", _SRC, _SRC_INT, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -86,6 +88,10 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
                                           ctypes.c_float]
         lib.oracle_activation.restype = ctypes.c_float
         lib.oracle_mutant.restype = ctypes.c_int
+        lib.oracle_conv_integer.argtypes = [i64p, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_int32,
+                                            ctypes.POINTER(ctypes.c_int32), ctypes.c_int, i64p,
+                                            ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
+        lib.oracle_conv_integer.restype = ctypes.c_int
         _libs[mutant] = lib
         return lib
 
@@ -164,6 +170,49 @@ class Oracle:
         if rc != 0:
             raise ValueError("geometry outside the definition")
         return {"y": y, "t": t, "acc": acc, "scale": scale}
+
+    def conv_integer(self, x, w, x_zero=0, w_zero=0, *, stride=(1, 1), pads=(0, 0, 0, 0),
+                     dilation=(1, 1), groups=1, nthreads=None, index=None):
+        """ONNX ConvInteger by its definition ("Convolution, pooling and resize",
+        ConvInteger): sum over the window of (x - x_zero) * (w - w_zero[co])
+        in int32 with wrap-around, a padded tap being x_zero (adding nothing).
+
+        x: (N, Cin, H, W) and w: (Cout, Cin/groups, kh, kw) numpy arrays of
+        uint8 or int8 (any mix); x_zero: one value of x's type; w_zero: one
+        value or Cout values of w's type.  Returns int32 (N, Cout, Ho, Wo),
+        or the listed NCHW outputs (index) as a flat array."""
+        for a in (x, w):
+            if a.dtype not in (np.uint8, np.int8):
+                raise TypeError(f"ConvInteger operands are uint8 or int8, not {a.dtype}")
+        geom, ho, wo = self.geometry(x.shape, w.shape, stride, pads, dilation, groups)
+        xs, ws = int(x.dtype == np.int8), int(w.dtype == np.int8)
+        wz = np.atleast_1d(np.asarray(w_zero)).astype(np.int64)
+        per_channel = wz.size > 1
+        if per_channel and wz.size != w.shape[0]:
+            raise ValueError("w_zero: one value or one per output channel")
+        lo, hi = (-128, 127) if xs else (0, 255)
+        if not lo <= int(x_zero) <= hi:
+            raise ValueError("x_zero outside x's type")
+        lo, hi = (-128, 127) if ws else (0, 255)
+        if wz.min() < lo or wz.max() > hi:
+            raise ValueError("w_zero outside w's type")
+        wz32 = np.ascontiguousarray(wz, dtype=np.int32)
+        xa, wa = np.ascontiguousarray(x), np.ascontiguousarray(w)
+        n, cout = x.shape[0], w.shape[0]
+        shape = (n, cout, ho, wo) if index is None else (len(index),)
+        y = np.empty(shape, dtype=np.int32)
+        g = (ctypes.c_int64 * 16)(*geom)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        idx = None
+        if index is not None:
+            idx = np.ascontiguousarray(index, dtype=np.int64)
+        rc = self.lib.oracle_conv_integer(
+            g, xs, ws, xa.ctypes.data, wa.ctypes.data, int(x_zero), wz32.ctypes.data_as(i32p),
+            int(per_channel), idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if idx is not None else None,
+            len(idx) if idx is not None else 0, y.ctypes.data_as(i32p), nthreads or os.cpu_count() or 1)
+        if rc != 0:
+            raise ValueError("geometry outside the definition")
+        return y
 
     def geometry(self, xshape, wshape, stride, pads, dilation, groups):
         n, cin, h, w_ = xshape
