@@ -25,6 +25,7 @@ __all__ = [
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
     "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
     "conv_apply_auto_pad", "AUTO_PAD", "conv_scratch_bytes_per_image",
+    "conv_integer_scratch_bytes", "conv_integer_forward", "conv_integer2d", "INT_TYPES",
     "make_problem", "conv2d", "library_path", "load",
 ]
 
@@ -121,9 +122,13 @@ def load() -> ctypes.CDLL:
         lib.conv_forward_fixed_scratch.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp]
         lib.conv_apply_auto_pad.argtypes = [P(ConvProblem), ctypes.c_int32]
         lib.conv_scratch_bytes_per_image.argtypes = [P(ConvProblem), P(ctypes.c_size_t)]
+        lib.conv_integer_scratch_bytes.argtypes = [P(ConvProblem), ctypes.c_int32, ctypes.c_int32,
+                                                   P(ctypes.c_size_t)]
+        lib.conv_integer_forward.argtypes = [P(ConvProblem), ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
+                                             ctypes.c_int32, vp, vp, ctypes.c_size_t, vp]
         for f in ("conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
                   "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "conv_apply_auto_pad",
-                  "conv_scratch_bytes_per_image"):
+                  "conv_scratch_bytes_per_image", "conv_integer_scratch_bytes", "conv_integer_forward"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -225,6 +230,56 @@ def conv_forward_fixed_scratch(p: ConvProblem, x, w, bias, residual, y, stream=N
     _check(load().conv_forward_fixed_scratch(ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias),
                                              _ptr(residual), _ptr(y), stream or None),
            "conv_forward_fixed_scratch")
+
+
+INT_TYPES = {"u8": 0, "i8": 1}
+
+
+def conv_integer_scratch_bytes(p: ConvProblem, x_type: str, w_type: str) -> int:
+    n = ctypes.c_size_t()
+    _check(load().conv_integer_scratch_bytes(ctypes.byref(p), INT_TYPES[x_type], INT_TYPES[w_type],
+                                             ctypes.byref(n)), "conv_integer_scratch_bytes")
+    return n.value
+
+
+def conv_integer_forward(p: ConvProblem, x_type: str, w_type: str, x, w, x_zero, w_zero, w_zero_count: int,
+                         y, scratch, scratch_bytes: int, stream=None) -> None:
+    """Enqueue ConvInteger (int32 output with wrap-around)."""
+    if stream is None:
+        try:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream
+        except Exception:  # noqa: BLE001 - no torch / no CUDA: the legacy default stream
+            stream = 0
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    _check(load().conv_integer_forward(ctypes.byref(p), INT_TYPES[x_type], INT_TYPES[w_type], _ptr(x), _ptr(w),
+                                       _ptr(x_zero), _ptr(w_zero), int(w_zero_count), _ptr(y), _ptr(scratch),
+                                       scratch_bytes, stream or None), "conv_integer_forward")
+
+
+def conv_integer2d(x, w, x_zero, w_zero, *, stride=1, pads=0, dilation=1, groups=1, out=None, scratch=None,
+                   stream=None, auto_pad="NOTSET"):
+    """ConvInteger on CUDA tensors: x, w uint8 / int8 (NCHW / OIHW), x_zero a
+    one-element tensor of x's type, w_zero one element or one per output
+    channel of w's type.  Returns int32 y (allocated unless ``out``)."""
+    import torch
+    tn = {torch.uint8: "u8", torch.int8: "i8"}
+    if x.dtype not in tn or w.dtype not in tn:
+        raise TypeError("ConvInteger operands are uint8 or int8")
+    if x_zero.dtype != x.dtype or w_zero.dtype != w.dtype or x_zero.numel() != 1:
+        raise ValueError("zero points: one element of x's type; one or c_out elements of w's type")
+    p = make_problem(x.shape, w.shape, stride=stride, pads=pads, dilation=dilation, groups=groups,
+                     auto_pad=auto_pad)
+    ho, wo = conv_output_shape(p)
+    if out is None:
+        out = torch.empty((p.n, p.c_out, ho, wo), dtype=torch.int32, device=x.device)
+    need = conv_integer_scratch_bytes(p, tn[x.dtype], tn[w.dtype])
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=x.device)
+    conv_integer_forward(p, tn[x.dtype], tn[w.dtype], x, w, x_zero, w_zero, w_zero.numel(), out, scratch,
+                         scratch.numel() * scratch.element_size(), stream)
+    return out
 
 
 def conv_device_error(reset: bool = True) -> int:

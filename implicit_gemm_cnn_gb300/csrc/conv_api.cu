@@ -732,6 +732,76 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
   return CONV_OK;
 }
 
+// ---- ConvInteger -------------------------------------------------------------
+// The geometry of conv_problem; no bias, residual or activation.
+static conv_status ci_validate(const conv_problem* p, int32_t x_type, int32_t w_type, Shape* s) {
+  conv_status st = validate(p, s);
+  if (st != CONV_OK) return st;
+  if (x_type < CONV_U8 || x_type > CONV_I8 || w_type < CONV_U8 || w_type > CONV_I8) return CONV_ERR_DTYPE;
+  if (p->act != CONV_ACT_IDENTITY || p->has_bias || p->has_residual) return CONV_ERR_ARG;
+  if ((s->mg + 127) / 128 * p->groups > 65535 || p->groups > 65535) return CONV_ERR_SHAPE;  // grid limits
+  return CONV_OK;
+}
+
+conv_status conv_integer_scratch_bytes(const conv_problem* p, int32_t x_type, int32_t w_type, size_t* bytes) {
+  if (!bytes) return CONV_ERR_NULL;
+  Shape s;
+  conv_status st = ci_validate(p, x_type, w_type, &s);
+  if (st != CONV_OK) return st;
+  ConvArgs a;
+  shape_args(p, s, &a);
+  *bytes = ci_plan(a).scratch_bytes;
+  return CONV_OK;
+}
+
+conv_status conv_integer_forward(const conv_problem* p, int32_t x_type, int32_t w_type, const void* x,
+                                 const void* w, const void* x_zero, const void* w_zero, int32_t w_zero_count,
+                                 int32_t* y, void* scratch, size_t scratch_bytes, void* stream) {
+  Shape s;
+  conv_status st = ci_validate(p, x_type, w_type, &s);
+  if (st != CONV_OK) return st;
+  if (!x || !w || !x_zero || !w_zero || !y) return CONV_ERR_NULL;
+  if (w_zero_count != 1 && w_zero_count != p->c_out) return CONV_ERR_ARG;
+  int dev, sm;
+  st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  ConvArgs a;
+  shape_args(p, s, &a);
+  const CiPlan pl = ci_plan(a);
+  const size_t yb = s.y_elems * 4;
+  const void* in_ptr[] = {x, w, x_zero, w_zero};
+  const size_t in_len[] = {static_cast<size_t>(s.x_elems), static_cast<size_t>(s.w_elems), 1,
+                           static_cast<size_t>(w_zero_count)};
+  for (int i = 0; i < 4; ++i)
+    if (overlap(y, yb, in_ptr[i], in_len[i])) return CONV_ERR_ALIAS;
+  if (!scratch || scratch_bytes < pl.scratch_bytes || reinterpret_cast<uintptr_t>(scratch) % 256)
+    return CONV_ERR_SCRATCH;
+  for (int i = 0; i < 4; ++i)
+    if (overlap(scratch, pl.scratch_bytes, in_ptr[i], in_len[i])) return CONV_ERR_ALIAS;
+  if (overlap(scratch, pl.scratch_bytes, y, yb)) return CONV_ERR_ALIAS;
+  a.x = x; a.wt = w; a.y = y;
+  CiArgs c;
+  memset(&c, 0, sizeof(c));
+  c.x_signed = x_type == CONV_I8;
+  c.w_signed = w_type == CONV_I8;
+  c.x_zero = static_cast<const uint8_t*>(x_zero);
+  c.w_zero = static_cast<const uint8_t*>(w_zero);
+  c.wz_per_channel = w_zero_count > 1;
+  c.kq = pl.kq;
+  c.p4 = pl.p4;
+  c.mg4 = pl.mg4;
+  char* sc = static_cast<char*>(scratch);
+  c.cols = reinterpret_cast<uint32_t*>(sc + pl.cols_off);
+  c.sx = reinterpret_cast<int32_t*>(sc + pl.sx_off);
+  c.wq = reinterpret_cast<uint32_t*>(sc + pl.wq_off);
+  c.sw = reinterpret_cast<int32_t*>(sc + pl.sw_off);
+  if (launch_conv_integer(a, pl, c, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return CONV_ERR_CUDA;
+  }
+  return CONV_OK;
+}
+
 conv_status conv_device_error(uint32_t* word, int32_t reset) {
   if (!word) return CONV_ERR_NULL;
   int dev, sm;

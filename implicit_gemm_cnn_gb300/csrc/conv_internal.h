@@ -163,6 +163,31 @@ struct Plan {
 // it under another thread's launch.
 cudaError_t opt_in_smem(const void* func, size_t bytes);
 
+// ConvInteger (conv_integer.cu): the unfolded byte matrix cols[g][q][p]
+// (k words of 4 terms x pixels), per-pixel byte sums sx[g][p], the weight
+// words wq[g][q][m] and per-channel byte sums sw[co], all in scratch.
+struct CiPlan {
+  int kq;            // k words: ceil(K / 4)
+  long long p4;      // pixels (N*Ho*Wo) rounded up to 4
+  int mg4;           // channels per group rounded up to 4
+  size_t cols_off, sx_off, wq_off, sw_off, scratch_bytes;
+};
+struct CiArgs {
+  int x_signed, w_signed;      // int8 (1) or uint8 (0)
+  const uint8_t* x_zero;       // one element of x's type (device)
+  const uint8_t* w_zero;       // one, or c_out, elements of w's type (device)
+  int wz_per_channel;
+  int kq;
+  long long p4;
+  int mg4;
+  uint32_t* cols;
+  int32_t* sx;
+  uint32_t* wq;
+  int32_t* sw;
+};
+CiPlan ci_plan(const ConvArgs& a);
+cudaError_t launch_conv_integer(const ConvArgs& a, const CiPlan& plan, const CiArgs& c, cudaStream_t s);
+
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
 // Kernels one conv_forward of the CUDA-core variant launches for `plan`.
 int ffma_launch_count(const Plan& plan);

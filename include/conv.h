@@ -249,6 +249,49 @@ CONV_API conv_status conv_forward(const conv_problem* p, const void* x, const vo
  * diagnostics. */
 CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
 
+/* ---- ConvInteger ----------------------------------------------------------
+ * ONNX ConvInteger ("Convolution, pooling and resize", ConvInteger):
+ *
+ *   y[n,co,oh,ow] = sum_{c,u,v} (x[n, g*Cin/G + c, oh*sh - pt + u*dh, ow*sw - pl + v*dw] - x_zero)
+ *                             * (w[co,c,u,v] - w_zero[co])
+ *
+ * in int32 with wrap-around (the exact sum modulo 2^32), with x and w each
+ * uint8 or int8 in any mix; a tap outside the image is the quantized value
+ * x_zero (the real value zero) and adds nothing.  The geometry is that of
+ * conv_problem (pads, stride, dilation, groups; one-dimensional as h = 1);
+ * act must be identity and has_bias / has_residual 0; dtype is ignored.
+ * Layouts as for conv_forward (x NCHW, w OIHW, y NCHW int32). */
+typedef enum conv_int_type {
+  CONV_U8 = 0,  /* uint8, values 0..255 */
+  CONV_I8 = 1   /* int8, two's complement, values -128..127 */
+} conv_int_type;
+
+/* Scratch bytes conv_integer_forward needs for p: the unfolded byte matrix
+ * (groups x ceil(K/4) words x N*Ho*Wo pixels rounded to 4, K = Cin/G*kh*kw),
+ * per-pixel and per-channel byte sums, and the weights as 4-byte words.
+ * Host only.  Errors: those of conv_output_shape, CONV_ERR_DTYPE (x_type or
+ * w_type not a conv_int_type), CONV_ERR_ARG (an activation, bias or residual
+ * requested). */
+CONV_API conv_status conv_integer_scratch_bytes(const conv_problem* p, int32_t x_type, int32_t w_type,
+                                                size_t* bytes);
+
+/* Enqueue ConvInteger on `stream`.
+ *   x, w      device arrays of x_type / w_type elements (conv_int_type);
+ *   x_zero    device pointer to one element of x_type;
+ *   w_zero    device pointer to w_zero_count elements of w_type: 1 (one zero
+ *             point) or c_out (one per output channel);
+ *   y         device int32 array N x c_out x Ho x Wo;
+ *   scratch   device memory of at least conv_integer_scratch_bytes, 256-byte
+ *             aligned, overlapping no operand; y overlaps no input.
+ * Results are exact and bit-identical across runs, devices and variants.
+ * Errors: those of conv_integer_scratch_bytes; CONV_ERR_NULL, CONV_ERR_ARG
+ * (w_zero_count), CONV_ERR_SCRATCH, CONV_ERR_ALIAS before anything is
+ * enqueued; CONV_ERR_DEVICE; CONV_ERR_CUDA when a launch fails. */
+CONV_API conv_status conv_integer_forward(const conv_problem* p, int32_t x_type, int32_t w_type,
+                                          const void* x, const void* w, const void* x_zero,
+                                          const void* w_zero, int32_t w_zero_count, int32_t* y,
+                                          void* scratch, size_t scratch_bytes, void* stream);
+
 /* Bytes of the library-owned scratch array of conv_forward_fixed_scratch. */
 #define CONV_FIXED_SCRATCH_BYTES (8u << 20) /* 8 MiB */
 

@@ -149,3 +149,54 @@ def to_numpy_operand(t: torch.Tensor | None, dtype: str):
     if dtype == "f32":
         return t.numpy()
     return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# ---- ConvInteger layers ------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class IntLayer:
+    """A ConvInteger layer: uint8 / int8 operands, zero points, int32 output."""
+    name: str
+    n: int
+    c_in: int
+    h: int
+    w: int
+    c_out: int
+    kh: int
+    kw: int
+    stride: tuple = (1, 1)
+    pads: tuple = (0, 0, 0, 0)
+    dilation: tuple = (1, 1)
+    groups: int = 1
+    x_type: str = "u8"
+    w_type: str = "i8"
+    per_channel: bool = True      # one weight zero point per output channel
+    seed: int = 0
+    description: str = ""
+
+    def with_(self, **kw) -> "IntLayer":
+        return dataclasses.replace(self, **kw)
+
+
+INT_LAYERS: dict[str, IntLayer] = {}
+# the second convolution of a Whisper-small-like audio front end (1-D as
+# height 1): 768 -> 768 channels, kernel 3, stride 2, over 3000 frames, batch 8
+INT_LAYERS["whisper_conv2_u8i8"] = IntLayer(
+    "whisper_conv2_u8i8", 8, 768, 1, 3000, 768, 1, 3, stride=(1, 2), pads=(0, 1, 0, 1), seed=1100,
+    description="ConvInteger 768->768 1x3 stride 2 over 3000 frames (1-D), N=8, uint8 x, int8 w, "
+                "per-channel weight zero points")
+
+_INT_RANGE = {"u8": (0, 256, torch.uint8), "i8": (-128, 128, torch.int8)}
+
+
+def make_int_inputs(layer: IntLayer, seed_offset: int = 0) -> dict:
+    """CPU tensors x, w (uniform over their type), x_zero (one value) and
+    w_zero (one per output channel, within +-8 of zero, or one value)."""
+    gen = torch.Generator().manual_seed(layer.seed * 1000 + seed_offset)
+    xl, xh, xt = _INT_RANGE[layer.x_type]
+    wl, wh, wt = _INT_RANGE[layer.w_type]
+    x = torch.randint(xl, xh, (layer.n, layer.c_in, layer.h, layer.w), generator=gen).to(xt)
+    w = torch.randint(wl, wh, (layer.c_out, layer.c_in // layer.groups, layer.kh, layer.kw), generator=gen).to(wt)
+    xz = torch.randint(xl, xh, (1,), generator=gen).to(xt)
+    nz = layer.c_out if layer.per_channel else 1
+    wz = torch.randint(max(wl, -8), min(wh, 9), (nz,), generator=gen).to(wt)
+    return {"x": x, "w": w, "x_zero": xz, "w_zero": wz}
