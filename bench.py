@@ -437,6 +437,80 @@ def run_reference(L, steps: int, warmup: int) -> dict:
     return {"value": value, "secs": secs, "per_step": per_step, "cores": cores, "total": total}
 
 
+# ---- ConvInteger ---------------------------------------------------------------
+# dp4a issue rate: one instruction per FP32 lane per clock (4 multiply-adds),
+# 152 SMs x 128 lanes at 2.07 GHz; the rate measured on this GB300 is stated
+# with the roofline in the design notes
+DP4A_PEAK_TOPS = 152 * 128 * 4 * 2 * 2.07e9 / 1e12
+
+
+def int_layer_ops(L) -> int:
+    ho = (L.h + L.pads[0] + L.pads[2] - L.dilation[0] * (L.kh - 1) - 1) // L.stride[0] + 1
+    wo = (L.w + L.pads[1] + L.pads[3] - L.dilation[1] * (L.kw - 1) - 1) // L.stride[1] + 1
+    return 2 * L.n * ho * wo * L.c_out * (L.c_in // L.groups) * L.kh * L.kw
+
+
+def run_integer(L, steps: int, warmup: int, world: int, local_rank: int) -> dict:
+    """conv_integer_forward timed like run_ours: CUDA graphs of back-to-back
+    calls over input sets rotated past L2, events on the launching stream."""
+    import torch
+
+    import implicit_gemm_cnn_gb300 as conv
+    from workloads import make_int_inputs
+    dev = torch.device("cuda", local_rank)
+    geo = dict(stride=L.stride, pads=L.pads, dilation=L.dilation, groups=L.groups)
+    p = conv.make_problem((L.n, L.c_in, L.h, L.w), (L.c_out, L.c_in // L.groups, L.kh, L.kw), **geo)
+    ho, wo = conv.conv_output_shape(p)
+    need = conv.conv_integer_scratch_bytes(p, L.x_type, L.w_type)
+    set_bytes = L.n * L.c_in * L.h * L.w + L.c_out * (L.c_in // L.groups) * L.kh * L.kw + 4 * L.n * L.c_out * ho * wo
+    nsets = max(1, min(64, math.ceil(2 * L2_BYTES / set_bytes)))
+    sets = []
+    for i in range(nsets):
+        t = {k: v.to(dev) for k, v in make_int_inputs(L, seed_offset=i + 1).items()}
+        t["y"] = torch.empty((L.n, L.c_out, ho, wo), dtype=torch.int32, device=dev)
+        sets.append(t)
+    scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def step(i):
+        t = sets[i % nsets]
+        conv.conv_integer_forward(p, L.x_type, L.w_type, t["x"], t["w"], t["x_zero"], t["w_zero"],
+                                  t["w_zero"].numel(), t["y"], scratch, need)
+
+    for i in range(max(warmup, nsets)):
+        step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for i in range(steps):
+            step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank).start()
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        g.replay()
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    us = secs * 1e6 / steps
+    ops = int_layer_ops(L)
+    value = aggregate(ops * steps, world, secs) / 1e12
+    return {"value": value, "us": us, "clocks": clocks, "launches": 3 * steps,
+            "roofline": {"bound": "alu", "achieved": round(ops / (us / 1e6) / 1e12, 2), "peak": DP4A_PEAK_TOPS,
+                         "unit": "TOP/s", "frac": round(ops / (us / 1e6) / 1e12 / DP4A_PEAK_TOPS, 4),
+                         "traffic": None, "tensor_or_alu_frac": round(ops / (us / 1e6) / 1e12 / DP4A_PEAK_TOPS, 4)}}
+
+
 def nested_layers(headline: str, args, world: int, rank: int, local_rank: int) -> list:
     """Every other workload layer, timed like the headline (graphs of
     back-to-back calls, inputs rotated past L2, events on the launching
@@ -459,6 +533,15 @@ def nested_layers(headline: str, args, world: int, rank: int, local_rank: int) -
                "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
                "clock_reasons": r["clocks"].get("reasons")}
         out.append(rec)
+    from workloads import INT_LAYERS
+    for name in sorted(INT_LAYERS):
+        L = INT_LAYERS[name]
+        r = run_integer(L, args.layer_steps, args.warmup, world, local_rank)
+        out.append({"layer": name, "workload": L.description, "dtype": f"{L.x_type}x{L.w_type}->i32",
+                    "variant": "conv_integer dp4a (unfold + weights + product)", "steps": args.layer_steps,
+                    "us_per_call": round(r["us"], 3), "tops": round(r["value"], 3), "roofline": r["roofline"],
+                    "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
+                    "clock_reasons": r["clocks"].get("reasons")})
     return out
 
 
