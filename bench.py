@@ -438,10 +438,10 @@ def run_reference(L, steps: int, warmup: int) -> dict:
 
 
 # ---- ConvInteger ---------------------------------------------------------------
-# dp4a issue rate: one instruction per FP32 lane per clock (4 multiply-adds),
-# 152 SMs x 128 lanes at 2.07 GHz; the rate measured on this GB300 is stated
-# with the roofline in the design notes
-DP4A_PEAK_TOPS = 152 * 128 * 4 * 2 * 2.07e9 / 1e12
+# dp4a (4 multiply-adds of bytes into an int32) issues on 64 lanes per SM per
+# clock on GB300 -- half the FP32 FFMA rate, measured at 20.0 G instructions/s
+# against 39.0 G for FFMA -- so 152 SMs x 64 x 8 ops x 2.07 GHz
+DP4A_PEAK_TOPS = 152 * 64 * 4 * 2 * 2.07e9 / 1e12
 
 
 def int_layer_ops(L) -> int:

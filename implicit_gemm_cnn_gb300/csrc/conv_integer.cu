@@ -58,9 +58,11 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Unfold: block (32 pixels, group); thread (pixel lane, word row ty of 8):
-// words q = ty, ty + 8, ... of its pixel into cols[g][q][p], the pixel's byte
-// sum reduced over the 8 rows into sx[g][p].
+// Unfold: block (32 pixels, group); thread (pixel lane, row ty of 8): the
+// words q in [ty*qc, (ty+1)*qc) of its pixel into cols[g][q][p] (a warp
+// writes 32 consecutive words per q), the terms' (channel, tap) walked
+// without divisions, and the pixel's byte sum reduced over the 8 rows into
+// sx[g][p].
 __global__ void __launch_bounds__(256) ci_unfold(const ConvArgs a, const CiArgs c) {
   __shared__ int32_t part[8][32];
   const int lane = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -69,30 +71,40 @@ __global__ void __launch_bounds__(256) ci_unfold(const ConvArgs a, const CiArgs 
   const uint8_t* __restrict__ x = static_cast<const uint8_t*>(a.x);
   const int32_t xz = load_byte(c.x_zero, 0, c.x_signed);
   int32_t sum = 0;
-  if (p < a.npix) {
+  const int qc = (c.kq + 7) / 8;
+  const int q0 = ty * qc, q1 = min(c.kq, q0 + qc);
+  if (p < a.npix && q0 < q1) {
     const long long n = p / a.howo;
     const int rem = static_cast<int>(p - n * a.howo);
     const int oh = rem / a.wo, ow = rem - (rem / a.wo) * a.wo;
     const int ih0 = oh * a.sh - a.pt, iw0 = ow * a.sw - a.pl;
     const uint8_t* xg = x + (n * a.c_in + static_cast<long long>(g) * a.cg) * a.hw;
+    // term k = 4*q0 as (channel, kernel row, kernel column)
     const int khw = a.kh * a.kw;
-    for (int q = ty; q < c.kq; q += 8) {
+    int k = 4 * q0;
+    int ch = k / khw;
+    int u = (k - ch * khw) / a.kw;
+    int v = k - ch * khw - u * a.kw;
+    for (int q = q0; q < q1; ++q) {
       uint32_t word = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const int k = 4 * q + b;
-        int32_t v = 0;  // terms past K: 0 (their weight bytes are 0 too)
+        int32_t val = 0;  // terms past K: 0 (their weight bytes are 0 too)
         if (k < a.K) {
-          const int ch = k / khw, tap = k - (k / khw) * khw;
-          const int u = tap / a.kw, vv = tap - (tap / a.kw) * a.kw;
-          const int ih = ih0 + u * a.dh, iw = iw0 + vv * a.dw;
+          const int ih = ih0 + u * a.dh, iw = iw0 + v * a.dw;
           const bool in = static_cast<unsigned>(ih) < static_cast<unsigned>(a.h) &&
                           static_cast<unsigned>(iw) < static_cast<unsigned>(a.w);
-          v = in ? load_byte(xg, static_cast<long long>(ch) * a.hw + static_cast<long long>(ih) * a.w + iw, c.x_signed)
-                 : xz;
-          sum += v;
+          val = in ? load_byte(xg, static_cast<long long>(ch) * a.hw + static_cast<long long>(ih) * a.w + iw,
+                               c.x_signed)
+                   : xz;
+          sum += val;
         }
-        word |= (static_cast<uint32_t>(v) & 0xffu) << (8 * b);
+        word |= (static_cast<uint32_t>(val) & 0xffu) << (8 * b);
+        ++k;  // the next term: kernel column, then row, then channel
+        if (++v == a.kw) {
+          v = 0;
+          if (++u == a.kh) { u = 0; ++ch; }
+        }
       }
       c.cols[(static_cast<long long>(g) * c.kq + q) * c.p4 + p] = word;
     }
@@ -107,31 +119,40 @@ __global__ void __launch_bounds__(256) ci_unfold(const ConvArgs a, const CiArgs 
   }
 }
 
-// Weights: thread per (group, channel m): words wq[g][q][m] (channels padded
-// to mg4 with zero words) and the channel's byte sum sw[co].
-__global__ void __launch_bounds__(256) ci_weights(const ConvArgs a, const CiArgs c) {
-  const long long t = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
-  if (t >= static_cast<long long>(a.groups) * c.mg4) return;
-  const int g = static_cast<int>(t / c.mg4), m = static_cast<int>(t - static_cast<long long>(g) * c.mg4);
+// Weights.  Blocks [0, word_blocks): one thread per word wq[g][q][m]
+// (channels padded to mg4 with zero words; a warp writes 32 consecutive
+// channels).  The blocks after them: one warp per output channel, the
+// channel's K bytes read by consecutive lanes and summed into sw[co].
+__global__ void __launch_bounds__(256) ci_weights(const ConvArgs a, const CiArgs c, long long word_blocks) {
   const uint8_t* __restrict__ w = static_cast<const uint8_t*>(a.wt);
-  const bool real = m < a.mg;
-  const long long row = (static_cast<long long>(g) * a.mg + m) * a.K;
-  int32_t sum = 0;
-  for (int q = 0; q < c.kq; ++q) {
+  if (blockIdx.x < word_blocks) {
+    const long long t = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+    const long long words = static_cast<long long>(a.groups) * c.kq * c.mg4;
+    if (t >= words) return;
+    const int m = static_cast<int>(t % c.mg4);
+    const long long gq = t / c.mg4;
+    const int q = static_cast<int>(gq % c.kq), g = static_cast<int>(gq / c.kq);
     uint32_t word = 0;
+    if (m < a.mg) {
+      const long long row = (static_cast<long long>(g) * a.mg + m) * a.K;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int k = 4 * q + b;
-      int32_t v = 0;
-      if (real && k < a.K) {
-        v = load_byte(w, row + k, c.w_signed);
-        sum += v;
+      for (int b = 0; b < 4; ++b) {
+        const int k = 4 * q + b;
+        const int32_t v = k < a.K ? load_byte(w, row + k, c.w_signed) : 0;
+        word |= (static_cast<uint32_t>(v) & 0xffu) << (8 * b);
       }
-      word |= (static_cast<uint32_t>(v) & 0xffu) << (8 * b);
     }
-    c.wq[(static_cast<long long>(g) * c.kq + q) * c.mg4 + m] = word;
+    c.wq[t] = word;
+    return;
   }
-  if (real) c.sw[g * a.mg + m] = sum;
+  const long long co = (static_cast<long long>(blockIdx.x) - word_blocks) * 8 + (threadIdx.x >> 5);
+  if (co >= a.c_out) return;
+  const int lane = threadIdx.x & 31;
+  int32_t s = 0;
+  for (int k = lane; k < a.K; k += 32) s += load_byte(w, co * a.K + k, c.w_signed);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) c.sw[co] = s;
 }
 
 // The product: block = 128 channels x 128 pixels of one group, k in stages of
@@ -245,8 +266,11 @@ cudaError_t launch_conv_integer(const ConvArgs& a, const CiPlan& pl, const CiArg
   ci_unfold<<<ug, 256, 0, s>>>(a, c);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const long long wthreads = static_cast<long long>(a.groups) * pl.mg4;
-  ci_weights<<<static_cast<unsigned>((wthreads + 255) / 256), 256, 0, s>>>(a, c);
+  const long long words = static_cast<long long>(a.groups) * pl.kq * pl.mg4;
+  const long long word_blocks = (words + 255) / 256;
+  const long long sum_blocks = (static_cast<long long>(a.c_out) + 7) / 8;
+  if (word_blocks + sum_blocks > 2147483647LL) return cudaErrorInvalidConfiguration;
+  ci_weights<<<static_cast<unsigned>(word_blocks + sum_blocks), 256, 0, s>>>(a, c, word_blocks);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int co_tiles = (a.mg + kCiBM - 1) / kCiBM;
