@@ -92,6 +92,12 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
                                             ctypes.POINTER(ctypes.c_int32), ctypes.c_int, i64p,
                                             ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
         lib.oracle_conv_integer.restype = ctypes.c_int
+        lib.oracle_transpose_extent.argtypes = [ctypes.c_int64] * 7
+        lib.oracle_transpose_extent.restype = ctypes.c_int64
+        lib.oracle_conv_transpose2d.argtypes = [i64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                                ctypes.c_float, ctypes.c_float, ctypes.c_int, vp, vp, vp, vp,
+                                                i64p, ctypes.c_int64, vp, vp, vp, vp, ctypes.c_int]
+        lib.oracle_conv_transpose2d.restype = ctypes.c_int
         _libs[mutant] = lib
         return lib
 
@@ -167,6 +173,52 @@ class Oracle:
             rc = self.lib.oracle_conv2d_at(
                 *common, idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(idx),
                 ptr(y), ptr(t), ptr(acc), ptr(scale), nthreads)
+        if rc != 0:
+            raise ValueError("geometry outside the definition")
+        return {"y": y, "t": t, "acc": acc, "scale": scale}
+
+    def transpose_extent(self, size, k, pad_begin, pad_end, stride=1, dilation=1, out_pad=0) -> int:
+        return int(self.lib.oracle_transpose_extent(size, k, pad_begin, pad_end, stride, dilation, out_pad))
+
+    def conv_transpose2d(self, x, w, bias=None, residual=None, *, dtype="f32", stride=(1, 1),
+                         pads=(0, 0, 0, 0), dilation=(1, 1), out_pad=(0, 0), groups=1, act="identity",
+                         alpha=0.0, beta=0.0, nthreads=None, index=None):
+        """The transposed convolution (ONNX ConvTranspose) by its gathering
+        definition (see conv_oracle.c).  x: (N, Cin, H, W); w: (Cin, Cout/groups,
+        kh, kw); element types and the returned dict as for conv2d."""
+        n, cin, h, wd = x.shape
+        cin_w, mg, kh, kw = w.shape
+        if cin_w != cin or cin % groups:
+            raise ValueError("weights [Cin][Cout/groups][kh][kw]")
+        cout = mg * groups
+        pt, pl, pb, pr = pads
+        ho = self.transpose_extent(h, kh, pt, pb, stride[0], dilation[0], out_pad[0])
+        wo = self.transpose_extent(wd, kw, pl, pr, stride[1], dilation[1], out_pad[1])
+        if ho < 1 or wo < 1:
+            raise ValueError("no output position")
+        geom = [n, cin, h, wd, cout, kh, kw, pt, pl, pb, pr, stride[0], stride[1], dilation[0], dilation[1],
+                groups]
+        want = np.float32 if dtype == "f32" else np.uint16
+        arrs = [np.ascontiguousarray(a) if a is not None else None for a in (x, w, bias, residual)]
+        for a in arrs:
+            if a is not None and a.dtype != want:
+                raise TypeError(f"oracle operand dtype {a.dtype}, expected {want} for {dtype}")
+        if arrs[3] is not None and arrs[3].shape != (n, cout, ho, wo):
+            raise ValueError("residual shape")
+        shape = (n, cout, ho, wo) if index is None else (len(index),)
+        y = np.empty(shape, dtype=want)
+        t = np.empty(shape, dtype=np.float32)
+        acc = np.empty(shape, dtype=np.float64)
+        scale = np.empty(shape, dtype=np.float64)
+        g = (ctypes.c_int64 * 16)(*geom)
+        ptr = lambda a: a.ctypes.data if a is not None else None
+        idx = np.ascontiguousarray(index, dtype=np.int64) if index is not None else None
+        rc = self.lib.oracle_conv_transpose2d(
+            g, out_pad[0], out_pad[1], _ACT_CODE[act], alpha, beta, _DT_CODE[dtype], ptr(arrs[0]), ptr(arrs[1]),
+            ptr(arrs[2]), ptr(arrs[3]),
+            idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if idx is not None else None,
+            len(idx) if idx is not None else 0, ptr(y), ptr(t), ptr(acc), ptr(scale),
+            nthreads or os.cpu_count() or 1)
         if rc != 0:
             raise ValueError("geometry outside the definition")
         return {"y": y, "t": t, "acc": acc, "scale": scale}

@@ -38,6 +38,20 @@
  *
  * Built with -ffp-contract=off so that no multiply-add is fused: the float32
  * epilogue then rounds each step as written on every host.
+ *
+ * The transposed convolution (ONNX ConvTranspose; "Convolution, pooling and
+ * resize", Layout and operands: weights [Cin][Cout/groups][kh][kw]; output
+ * size from "Convolutions", section 2.1, (H - 1)s - pads + d(kh - 1) + 1 +
+ * output_padding) is the same loop read the other way round:
+ *
+ *   acc[n,co,oh,ow] = sum_{c < Cin/g} sum_{u < kh} sum_{v < kw}
+ *                      X(n, g(co)*Cin/g + c, (oh + pt - u*dh)/sh, (ow + pl - v*dw)/sw)
+ *                      * W[g(co)*Cin/g + c, co - g(co)*Cout/g, u, v]
+ *
+ * where a term exists only when both divisions are exact and land inside the
+ * image (each input pixel spreads the kernel over the output at s-strided
+ * positions; each output gathers the taps that reach it).  The same double
+ * sum, error scale and float32 epilogue as the forward convolution.
  */
 #include <math.h>
 #include <pthread.h>
@@ -193,7 +207,48 @@ typedef struct {
   const int64_t* index; /* NULL: outputs [begin, end) in order */
   int64_t begin, end;
   int64_t ho, wo;
+  int transpose; /* 1: the transposed convolution */
 } job;
+
+/* The transposed sum of one output: see the header. */
+static void transposed_sum(const job* J, int64_t n, int64_t co, int64_t oh, int64_t ow, double* acc_out,
+                           double* scale_out) {
+  const int64_t* g = J->g;
+  const int64_t cg = g[G_CIN] / g[G_GROUPS], mg = g[G_COUT] / g[G_GROUPS];
+  const int64_t grp = co / mg, col = co - grp * mg;
+  double acc = 0.0, scale = 0.0;
+  for (int64_t c = 0; c < cg; ++c) {
+    const int64_t ci = grp * cg + c;
+    for (int64_t u = 0; u < g[G_KH]; ++u) {
+      const int64_t th = oh + g[G_PT] - u * g[G_DH];
+#if ORACLE_MUTANT == 11
+      if (th < 0) continue; /* mutant: the stride's divisibility is not checked */
+      const int64_t ih = th / g[G_SH];
+#else
+      if (th < 0 || th % g[G_SH]) continue;
+      const int64_t ih = th / g[G_SH];
+#endif
+      if (ih >= g[G_H]) continue;
+      for (int64_t v = 0; v < g[G_KW]; ++v) {
+        const int64_t tw = ow + g[G_PL] - v * g[G_DW];
+        if (tw < 0 || tw % g[G_SW]) continue;
+        const int64_t iw = tw / g[G_SW];
+        if (iw >= g[G_W]) continue;
+        const double xv = load_elem(J->x, ((n * g[G_CIN] + ci) * g[G_H] + ih) * g[G_W] + iw, J->dtype);
+#if ORACLE_MUTANT == 12
+        const double wv = load_elem(J->w, ((ci * mg + col) * g[G_KH] + (g[G_KH] - 1 - u)) * g[G_KW] +
+                                           (g[G_KW] - 1 - v), J->dtype); /* mutant: kernel flipped */
+#else
+        const double wv = load_elem(J->w, ((ci * mg + col) * g[G_KH] + u) * g[G_KW] + v, J->dtype);
+#endif
+        acc += xv * wv;
+        scale += fabs(xv * wv);
+      }
+    }
+  }
+  *acc_out = acc;
+  *scale_out = scale;
+}
 
 static void one_output(const job* J, int64_t lin, int64_t slot) {
   const int64_t* g = J->g;
@@ -209,7 +264,8 @@ static void one_output(const job* J, int64_t lin, int64_t slot) {
   grp = 0; /* mutant: every group reads the first channel slice */
 #endif
   double acc = 0.0, scale = 0.0;
-  for (int64_t c = 0; c < cg; ++c) {
+  if (J->transpose) transposed_sum(J, n, co, oh, ow, &acc, &scale);
+  for (int64_t c = 0; c < cg && !J->transpose; ++c) {
     for (int64_t u = 0; u < g[G_KH]; ++u) {
       for (int64_t v = 0; v < g[G_KW]; ++v) {
 #if ORACLE_MUTANT == 5
@@ -347,6 +403,51 @@ int oracle_conv2d_at(const int64_t* geom, int act, float alpha, float beta, int 
   J.x = x; J.w = w; J.b = b; J.r = r; J.y = y; J.index = index;
   J.t_out = t_out; J.acc_out = acc_out; J.scale_out = scale_out;
   J.ho = ho; J.wo = wo;
+  return run(J, count, nthreads);
+}
+
+/* ---- the transposed convolution --------------------------------------------- */
+/* Output extent: s*(in - 1) + output_padding + d*(k - 1) + 1 - pad_begin - pad_end. */
+int64_t oracle_transpose_extent(int64_t in, int64_t k, int64_t pad_begin, int64_t pad_end, int64_t stride,
+                                int64_t dil, int64_t out_pad) {
+  if (in < 1 || k < 1 || stride < 1 || dil < 1 || out_pad < 0 || pad_begin < 0 || pad_end < 0) return 0;
+  int64_t e = stride * (in - 1) + out_pad + dil * (k - 1) + 1 - pad_begin - pad_end;
+  return e > 0 ? e : 0;
+}
+
+static int check_tgeom(const int64_t* g, int64_t oph, int64_t opw, int64_t* ho, int64_t* wo) {
+  for (int i = 0; i < G_COUNT; ++i) {
+    if (i >= G_PT && i <= G_PR) { if (g[i] < 0) return -1; }
+    else if (g[i] < 1) return -1;
+  }
+  if (g[G_CIN] % g[G_GROUPS] || g[G_COUT] % g[G_GROUPS]) return -1;
+  *ho = oracle_transpose_extent(g[G_H], g[G_KH], g[G_PT], g[G_PB], g[G_SH], g[G_DH], oph);
+  *wo = oracle_transpose_extent(g[G_W], g[G_KW], g[G_PL], g[G_PR], g[G_SW], g[G_DW], opw);
+  return (*ho >= 1 && *wo >= 1) ? 0 : -1;
+}
+
+/* Every output (index NULL) or the listed NCHW outputs of the transposed
+ * convolution; geom as for oracle_conv2d with G_COUT the output channels,
+ * w laid out [Cin][Cout/groups][kh][kw]. */
+int oracle_conv_transpose2d(const int64_t* geom, int64_t out_pad_h, int64_t out_pad_w, int act, float alpha,
+                            float beta, int dtype, const void* x, const void* w, const void* b, const void* r,
+                            const int64_t* index, int64_t count, void* y, float* t_out, double* acc_out,
+                            double* scale_out, int nthreads) {
+  int64_t ho, wo;
+  if (check_tgeom(geom, out_pad_h, out_pad_w, &ho, &wo)) return -1;
+  const int64_t total = geom[G_N] * geom[G_COUT] * ho * wo;
+  if (index) {
+    for (int64_t i = 0; i < count; ++i)
+      if (index[i] < 0 || index[i] >= total) return -1;
+  } else {
+    count = total;
+  }
+  job J;
+  memset(&J, 0, sizeof J);
+  J.g = geom; J.act = act; J.alpha = alpha; J.beta = beta; J.dtype = dtype;
+  J.x = x; J.w = w; J.b = b; J.r = r; J.y = y; J.index = index;
+  J.t_out = t_out; J.acc_out = acc_out; J.scale_out = scale_out;
+  J.ho = ho; J.wo = wo; J.transpose = 1;
   return run(J, count, nthreads);
 }
 
