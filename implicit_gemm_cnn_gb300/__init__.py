@@ -26,6 +26,8 @@ __all__ = [
     "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
     "conv_apply_auto_pad", "AUTO_PAD", "conv_scratch_bytes_per_image",
     "conv_integer_scratch_bytes", "conv_integer_forward", "conv_integer2d", "INT_TYPES",
+    "ConvTransposeProblem", "make_transpose_problem", "conv_transpose_output_shape",
+    "conv_transpose_scratch_bytes", "conv_transpose_forward", "conv_transpose2d",
     "make_problem", "conv2d", "library_path", "load",
 ]
 
@@ -72,6 +74,10 @@ class ConvProblem(ctypes.Structure):
         ("act", ctypes.c_int32), ("act_alpha", ctypes.c_float), ("act_beta", ctypes.c_float),
         ("dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32), ("has_residual", ctypes.c_int32),
         ("flags", ctypes.c_uint32)]
+
+
+class ConvTransposeProblem(ctypes.Structure):
+    _fields_ = [("conv", ConvProblem), ("out_pad_h", ctypes.c_int64), ("out_pad_w", ctypes.c_int64)]
 
 
 class ConvPlanInfo(ctypes.Structure):
@@ -122,13 +128,17 @@ def load() -> ctypes.CDLL:
         lib.conv_forward_fixed_scratch.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp]
         lib.conv_apply_auto_pad.argtypes = [P(ConvProblem), ctypes.c_int32]
         lib.conv_scratch_bytes_per_image.argtypes = [P(ConvProblem), P(ctypes.c_size_t)]
+        lib.conv_transpose_output_shape.argtypes = [P(ConvTransposeProblem), P(ctypes.c_int64), P(ctypes.c_int64)]
+        lib.conv_transpose_scratch_bytes.argtypes = [P(ConvTransposeProblem), P(ctypes.c_size_t)]
+        lib.conv_transpose_forward.argtypes = [P(ConvTransposeProblem), vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_integer_scratch_bytes.argtypes = [P(ConvProblem), ctypes.c_int32, ctypes.c_int32,
                                                    P(ctypes.c_size_t)]
         lib.conv_integer_forward.argtypes = [P(ConvProblem), ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
                                              ctypes.c_int32, vp, vp, ctypes.c_size_t, vp]
         for f in ("conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
                   "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "conv_apply_auto_pad",
-                  "conv_scratch_bytes_per_image", "conv_integer_scratch_bytes", "conv_integer_forward"):
+                  "conv_scratch_bytes_per_image", "conv_integer_scratch_bytes", "conv_integer_forward",
+                  "conv_transpose_output_shape", "conv_transpose_scratch_bytes", "conv_transpose_forward"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -230,6 +240,67 @@ def conv_forward_fixed_scratch(p: ConvProblem, x, w, bias, residual, y, stream=N
     _check(load().conv_forward_fixed_scratch(ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias),
                                              _ptr(residual), _ptr(y), stream or None),
            "conv_forward_fixed_scratch")
+
+
+def make_transpose_problem(x_shape, w_shape, *, dtype="f32", stride=1, pads=0, dilation=1, out_pad=0,
+                           groups=1, act="identity", alpha=0.0, beta=0.0, has_bias=False,
+                           has_residual=False) -> ConvTransposeProblem:
+    """x (N, Cin, H, W); w (Cin, Cout/groups, kh, kw)."""
+    n, c_in, h, w = (int(v) for v in x_shape)
+    cin_w, mg, kh, kw = (int(v) for v in w_shape)
+    if cin_w != c_in:
+        raise ValueError("ConvTranspose weights are [Cin][Cout/groups][kh][kw]")
+    q = make_problem((n, c_in, h, w), (mg * int(groups), c_in // int(groups), kh, kw), dtype=dtype,
+                     stride=stride, pads=pads, dilation=dilation, groups=groups, act=act, alpha=alpha,
+                     beta=beta, has_bias=has_bias, has_residual=has_residual)
+    oph, opw = _pair(out_pad)
+    return ConvTransposeProblem(q, oph, opw)
+
+
+def conv_transpose_output_shape(p: ConvTransposeProblem) -> tuple[int, int]:
+    ho, wo = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().conv_transpose_output_shape(ctypes.byref(p), ctypes.byref(ho), ctypes.byref(wo)),
+           "conv_transpose_output_shape")
+    return ho.value, wo.value
+
+
+def conv_transpose_scratch_bytes(p: ConvTransposeProblem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().conv_transpose_scratch_bytes(ctypes.byref(p), ctypes.byref(n)), "conv_transpose_scratch_bytes")
+    return n.value
+
+
+def conv_transpose_forward(p: ConvTransposeProblem, x, w, bias, residual, y, scratch, scratch_bytes: int,
+                           stream=None) -> None:
+    if stream is None:
+        try:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream
+        except Exception:  # noqa: BLE001 - no torch / no CUDA: the legacy default stream
+            stream = 0
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    _check(load().conv_transpose_forward(ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias), _ptr(residual), _ptr(y),
+                                         _ptr(scratch), scratch_bytes, stream or None), "conv_transpose_forward")
+
+
+def conv_transpose2d(x, w, bias=None, residual=None, *, stride=1, pads=0, dilation=1, out_pad=0, groups=1,
+                     act="identity", alpha=0.0, beta=0.0, out=None, scratch=None, stream=None):
+    """ConvTranspose on CUDA tensors (w [Cin][Cout/groups][kh][kw]); allocates
+    y and scratch with torch unless given."""
+    import torch
+    dt = _dtype_name(x)
+    p = make_transpose_problem(x.shape, w.shape, dtype=dt, stride=stride, pads=pads, dilation=dilation,
+                               out_pad=out_pad, groups=groups, act=act, alpha=alpha, beta=beta,
+                               has_bias=bias is not None, has_residual=residual is not None)
+    ho, wo = conv_transpose_output_shape(p)
+    if out is None:
+        out = torch.empty((p.conv.n, p.conv.c_out, ho, wo), dtype=x.dtype, device=x.device)
+    need = conv_transpose_scratch_bytes(p)
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=x.device)
+    conv_transpose_forward(p, x, w, bias, residual, out, scratch, scratch.numel() * scratch.element_size(), stream)
+    return out
 
 
 INT_TYPES = {"u8": 0, "i8": 1}

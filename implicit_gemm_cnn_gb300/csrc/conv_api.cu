@@ -732,6 +732,147 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
   return CONV_OK;
 }
 
+// ---- ConvTranspose -------------------------------------------------------------
+// The transposed problem: its output size, the 1x1 Gemm problem and its plan,
+// the kernel arguments (addresses left empty) and the scratch layout.
+static conv_status t_prepare(const conv_transpose_problem* tp, int sm, TransposePlan* out, ConvArgs* a,
+                             TransposeGeo* geo, Shape* shape) {
+  if (!tp) return CONV_ERR_NULL;
+  const conv_problem* p = &tp->conv;
+  if (p->dtype < CONV_F32 || p->dtype > CONV_BF16) return CONV_ERR_DTYPE;
+  if (p->act < CONV_ACT_IDENTITY || p->act > CONV_ACT_LEAKY_RELU) return CONV_ERR_ACT;
+  const long long pos[] = {p->n, p->c_in, p->h, p->w, p->c_out, p->kh, p->kw,
+                           p->stride_h, p->stride_w, p->dil_h, p->dil_w, p->groups};
+  for (long long v : pos)
+    if (v < 1) return CONV_ERR_SHAPE;
+  if (p->pad_top < 0 || p->pad_left < 0 || p->pad_bottom < 0 || p->pad_right < 0) return CONV_ERR_SHAPE;
+  if (p->c_in % p->groups || p->c_out % p->groups) return CONV_ERR_SHAPE;
+  // ONNX: output_padding below the stride or the dilation of its axis
+  if (tp->out_pad_h < 0 || tp->out_pad_w < 0 || tp->out_pad_h >= std::max(p->stride_h, p->dil_h) ||
+      tp->out_pad_w >= std::max(p->stride_w, p->dil_w))
+    return CONV_ERR_SHAPE;
+  const long long big = 1LL << 31;
+  const long long dims[] = {p->n, p->c_in, p->h, p->w, p->c_out, p->kh, p->kw, p->stride_h, p->stride_w,
+                            p->dil_h, p->dil_w, p->pad_top, p->pad_left, p->pad_bottom, p->pad_right};
+  for (long long v : dims)
+    if (v >= big) return CONV_ERR_SHAPE;
+  const long long ho = p->stride_h * (p->h - 1) + tp->out_pad_h + p->dil_h * (p->kh - 1) + 1 - p->pad_top - p->pad_bottom;
+  const long long wo = p->stride_w * (p->w - 1) + tp->out_pad_w + p->dil_w * (p->kw - 1) + 1 - p->pad_left - p->pad_right;
+  if (ho < 1 || wo < 1) return CONV_ERR_SHAPE;
+  if (ho >= big || wo >= big) return CONV_ERR_SHAPE;
+  long long per_img_out, y_elems, t;
+  if (!mul_ok(p->c_out, ho, &t) || !mul_ok(t, wo, &per_img_out) || per_img_out > kI32) return CONV_ERR_SHAPE;
+  if (!mul_ok(per_img_out, p->n, &y_elems)) return CONV_ERR_OVERFLOW;
+  // the Gemm: a 1x1 convolution of x to Cout*kh*kw channels (groups kept)
+  conv_problem q;
+  memset(&q, 0, sizeof(q));
+  q.n = p->n; q.c_in = p->c_in; q.h = p->h; q.w = p->w;
+  long long cout_k;
+  if (!mul_ok(p->c_out, p->kh * p->kw, &cout_k)) return CONV_ERR_OVERFLOW;
+  q.c_out = cout_k;
+  q.kh = q.kw = 1; q.stride_h = q.stride_w = 1; q.dil_h = q.dil_w = 1; q.groups = p->groups;
+  q.act = CONV_ACT_IDENTITY; q.dtype = p->dtype;
+  q.flags = CONV_FLAG_FORCE_FFMA | CONV_FLAG_NO_SPLIT_K | CONV_FLAG_NO_UNFOLD;
+  Shape sq;
+  conv_status st = make_plan(&q, sm, &out->gemm_plan, &sq);
+  if (st != CONV_OK) return st;
+  if (out->gemm_plan.info.scratch_bytes != 0) return CONV_ERR_SHAPE;  // a plain one-pass Gemm
+  shape_args(&q, sq, &out->gemm_args);
+  out->dtype = p->dtype;
+  const size_t es = p->dtype == CONV_F32 ? 4 : 2;
+  out->wt_off = 0;
+  out->cols_off = (static_cast<size_t>(sq.w_elems) * es + 255) / 256 * 256;
+  long long cols_bytes;
+  if (!mul_ok(sq.y_elems, 4, &cols_bytes)) return CONV_ERR_OVERFLOW;
+  out->scratch_bytes = out->cols_off + static_cast<size_t>(cols_bytes);
+  // the col2im's arguments: the transposed problem's geometry
+  memset(a, 0, sizeof(*a));
+  a->n = static_cast<int>(p->n); a->c_in = static_cast<int>(p->c_in);
+  a->h = static_cast<int>(p->h); a->w = static_cast<int>(p->w);
+  a->c_out = static_cast<int>(p->c_out); a->kh = static_cast<int>(p->kh); a->kw = static_cast<int>(p->kw);
+  a->pt = static_cast<int>(p->pad_top); a->pl = static_cast<int>(p->pad_left);
+  a->sh = static_cast<int>(p->stride_h); a->sw = static_cast<int>(p->stride_w);
+  a->dh = static_cast<int>(p->dil_h); a->dw = static_cast<int>(p->dil_w);
+  a->groups = static_cast<int>(p->groups);
+  a->cg = static_cast<int>(p->c_in / p->groups); a->mg = static_cast<int>(p->c_out / p->groups);
+  a->hw = p->h * p->w;
+  a->act = p->act; a->alpha = p->act_alpha; a->beta = p->act_beta;
+  geo->ho = static_cast<int>(ho);
+  geo->wo = static_cast<int>(wo);
+  if (shape) {
+    memset(shape, 0, sizeof(*shape));
+    shape->ho = ho; shape->wo = wo;
+    shape->x_elems = p->n * p->c_in * p->h * p->w;
+    shape->w_elems = p->c_in * (p->c_out / p->groups) * p->kh * p->kw;
+    shape->y_elems = y_elems;
+  }
+  return CONV_OK;
+}
+
+conv_status conv_transpose_output_shape(const conv_transpose_problem* tp, int64_t* ho, int64_t* wo) {
+  if (!ho || !wo) return CONV_ERR_NULL;
+  TransposePlan pl;
+  ConvArgs a;
+  TransposeGeo g;
+  const conv_status st = t_prepare(tp, 152, &pl, &a, &g, nullptr);
+  if (st != CONV_OK) return st;
+  *ho = g.ho;
+  *wo = g.wo;
+  return CONV_OK;
+}
+
+conv_status conv_transpose_scratch_bytes(const conv_transpose_problem* tp, size_t* bytes) {
+  if (!bytes) return CONV_ERR_NULL;
+  int dev, sm;
+  conv_status st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  TransposePlan pl;
+  ConvArgs a;
+  TransposeGeo g;
+  st = t_prepare(tp, sm, &pl, &a, &g, nullptr);
+  if (st == CONV_OK) *bytes = pl.scratch_bytes;
+  return st;
+}
+
+conv_status conv_transpose_forward(const conv_transpose_problem* tp, const void* x, const void* w,
+                                   const void* bias, const void* residual, void* y, void* scratch,
+                                   size_t scratch_bytes, void* stream) {
+  if (!tp) return CONV_ERR_NULL;
+  const conv_problem* p = &tp->conv;
+  int dev, sm;
+  conv_status st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  TransposePlan pl;
+  ConvArgs a;
+  TransposeGeo g;
+  Shape s;
+  st = t_prepare(tp, sm, &pl, &a, &g, &s);
+  if (st != CONV_OK) return st;
+  if (!x || !w || !y) return CONV_ERR_NULL;
+  if (p->has_bias && !bias) return CONV_ERR_NULL;
+  if (p->has_residual && !residual) return CONV_ERR_NULL;
+  const size_t es = p->dtype == CONV_F32 ? 4 : 2;
+  const size_t xb = s.x_elems * es, wb = s.w_elems * es, yb = s.y_elems * es;
+  const size_t bb = p->has_bias ? p->c_out * es : 0, rb = p->has_residual ? yb : 0;
+  const void* in_ptr[] = {x, w, p->has_bias ? bias : nullptr, p->has_residual ? residual : nullptr};
+  const size_t in_len[] = {xb, wb, bb, rb};
+  for (int i = 0; i < 4; ++i)
+    if (overlap(y, yb, in_ptr[i], in_len[i])) return CONV_ERR_ALIAS;
+  if (!scratch || scratch_bytes < pl.scratch_bytes || reinterpret_cast<uintptr_t>(scratch) % 256)
+    return CONV_ERR_SCRATCH;
+  for (int i = 0; i < 4; ++i)
+    if (overlap(scratch, pl.scratch_bytes, in_ptr[i], in_len[i])) return CONV_ERR_ALIAS;
+  if (overlap(scratch, pl.scratch_bytes, y, yb)) return CONV_ERR_ALIAS;
+  a.x = x; a.wt = w; a.y = y;
+  a.bias = p->has_bias ? bias : nullptr;
+  a.residual = p->has_residual ? residual : nullptr;
+  if (launch_conv_transpose(pl, a, g, w, scratch, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return CONV_ERR_CUDA;
+  }
+  return CONV_OK;
+}
+
 // ---- ConvInteger -------------------------------------------------------------
 // The geometry of conv_problem; no bias, residual or activation.
 static conv_status ci_validate(const conv_problem* p, int32_t x_type, int32_t w_type, Shape* s) {

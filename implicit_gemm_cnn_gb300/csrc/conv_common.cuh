@@ -53,6 +53,7 @@ struct ConvArgs {
   // split, the whole tiles [blk_whole_lo, + blk_whole_n) and the tail blocks
   // from blk_tail_lo on (1-D grid)
   long long px_tile0, blk_whole_lo, blk_whole_n, blk_tail_lo;
+  int raw_out;             // CUDA-core kernel: write the raw float32 sums to `partial` (no epilogue)
 };
 
 enum Act {

@@ -424,7 +424,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
       if (m >= a.mg) continue;
       const int co = g * a.mg + m;
       const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo + rem;
-      if (a.split > 1) {
+      if (a.split > 1 || a.raw_out) {
         float* part = a.partial + static_cast<long long>(blockIdx.z) * a.part_total;  // chunk-local
         if (whole4) {
           *reinterpret_cast<float4*>(part + (out - out0)) =

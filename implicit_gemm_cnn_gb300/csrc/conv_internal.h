@@ -189,6 +189,20 @@ CiPlan ci_plan(const ConvArgs& a);
 cudaError_t launch_conv_integer(const ConvArgs& a, const CiPlan& plan, const CiArgs& c, cudaStream_t s);
 
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s);
+
+// The transposed convolution (conv_transpose.cu): the Gemm as a planned 1x1
+// convolution (raw float32 sums into scratch) and the gathering col2im.
+struct TransposeGeo {
+  int ho, wo;        // output size
+};
+struct TransposePlan {
+  int dtype;
+  Plan gemm_plan;        // the CUDA-core plan of the 1x1 Gemm
+  ConvArgs gemm_args;    // its geometry (addresses filled at launch)
+  size_t wt_off, cols_off, scratch_bytes;
+};
+cudaError_t launch_conv_transpose(const TransposePlan& tp, const ConvArgs& a, const TransposeGeo& t,
+                                  const void* w, void* scratch, cudaStream_t s);
 // Kernels one conv_forward of the CUDA-core variant launches for `plan`.
 int ffma_launch_count(const Plan& plan);
 // Whether the unfolded-B layout applies to the shape (element type aside),

@@ -249,6 +249,49 @@ CONV_API conv_status conv_forward(const conv_problem* p, const void* x, const vo
  * diagnostics. */
 CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
 
+/* ---- ConvTranspose --------------------------------------------------------
+ * The transposed convolution (ONNX ConvTranspose; "Convolution, pooling and
+ * resize": weights [Cin][Cout/groups][kh][kw]; Variants: a Gemm of the
+ * transposed weights with the input, then a gathering col2im with the same
+ * epilogue):
+ *
+ *   Ho = stride_h*(H - 1) + out_pad_h + dil_h*(kh - 1) + 1 - pad_top - pad_bottom
+ *   y[n,co,oh,ow] = act( sum_{c,u,v} x[n, g*Cin/G + c, (oh + pt - u*dh)/sh, (ow + pl - v*dw)/sw]
+ *                                   * w[g*Cin/G + c, co - g*Cout/G, u, v]
+ *                        + bias[co] + residual[n,co,oh,ow] )
+ *
+ * with g = co / (Cout/G) and only the terms whose divisions are exact and
+ * land inside the input ("Convolutions", section 2.5: each input pixel
+ * spreads the kernel over the output at s-strided positions).  The epilogue
+ * and element types are those of conv_forward. */
+typedef struct conv_transpose_problem {
+  conv_problem conv;    /* n, c_in, h, w: the input; c_out: output channels;
+                           kh, kw, pads, stride, dilation, groups, activation,
+                           dtype, has_bias, has_residual as for conv_forward
+                           (flags unused)                                     */
+  int64_t out_pad_h, out_pad_w; /* ONNX output_padding, below max(stride, dilation) */
+} conv_transpose_problem;
+
+/* Output size of a transposed problem.  Host only.  Errors: CONV_ERR_NULL,
+ * CONV_ERR_SHAPE (a size < 1, groups not dividing the channels, an
+ * output_padding at or past max(stride, dilation), no output position, or a
+ * size past a kernel limit), CONV_ERR_OVERFLOW, CONV_ERR_DTYPE, CONV_ERR_ACT. */
+CONV_API conv_status conv_transpose_output_shape(const conv_transpose_problem* p, int64_t* ho, int64_t* wo);
+
+/* Scratch bytes conv_transpose_forward needs on the current device: the
+ * transposed weights, then the float32 Gemm result N x (Cout*kh*kw) x H*W. */
+CONV_API conv_status conv_transpose_scratch_bytes(const conv_transpose_problem* p, size_t* bytes);
+
+/* Enqueue the transposed convolution on `stream`; pointers as for
+ * conv_forward (w laid out [c_in][c_out/groups][kh][kw]), scratch at least
+ * conv_transpose_scratch_bytes, 256-byte aligned.  No atomics: the result
+ * has the same bits on every run.  Errors: those of
+ * conv_transpose_output_shape; CONV_ERR_NULL, CONV_ERR_SCRATCH,
+ * CONV_ERR_ALIAS before anything is enqueued; CONV_ERR_DEVICE; CONV_ERR_CUDA. */
+CONV_API conv_status conv_transpose_forward(const conv_transpose_problem* p, const void* x, const void* w,
+                                            const void* bias, const void* residual, void* y, void* scratch,
+                                            size_t scratch_bytes, void* stream);
+
 /* ---- ConvInteger ----------------------------------------------------------
  * ONNX ConvInteger ("Convolution, pooling and resize", ConvInteger):
  *

@@ -200,3 +200,50 @@ def make_int_inputs(layer: IntLayer, seed_offset: int = 0) -> dict:
     nz = layer.c_out if layer.per_channel else 1
     wz = torch.randint(max(wl, -8), min(wh, 9), (nz,), generator=gen).to(wt)
     return {"x": x, "w": w, "x_zero": xz, "w_zero": wz}
+
+
+# ---- transposed convolution layers ---------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class TransposeLayer:
+    """A ConvTranspose layer: w is [Cin][Cout/groups][kh][kw]."""
+    name: str
+    n: int
+    c_in: int
+    h: int
+    w: int
+    c_out: int
+    kh: int
+    kw: int
+    stride: tuple = (1, 1)
+    pads: tuple = (0, 0, 0, 0)
+    dilation: tuple = (1, 1)
+    out_pad: tuple = (0, 0)
+    groups: int = 1
+    act: str = "identity"
+    dtype: str = "f32"
+    bias: bool = True
+    seed: int = 0
+    description: str = ""
+
+
+TRANSPOSE_LAYERS: dict[str, TransposeLayer] = {}
+for _dt, _s in (("f32", 1200), ("f16", 1201)):
+    # a decoder's 2x upsampling step: k = 2s gives every output the same
+    # number of taps ("Convolutions", section 2.5)
+    TRANSPOSE_LAYERS[f"decoder_up4x4_s2_{_dt}"] = TransposeLayer(
+        f"decoder_up4x4_s2_{_dt}", 8, 256, 28, 28, 128, 4, 4, stride=(2, 2), pads=(1, 1, 1, 1), act="relu",
+        dtype=_dt, seed=_s,
+        description=f"ConvTranspose 256->128 4x4 stride 2 pad 1, 28x28 -> 56x56, N=8, bias, ReLU, {_dt}")
+
+
+def make_transpose_inputs(layer: TransposeLayer, seed_offset: int = 0) -> dict:
+    """x ~ U(-1, 1), w ~ N(0, sqrt(2 / fan_in)) with fan_in = Cin/groups * k^2
+    / stride^2 (the taps that reach one output), bias ~ U(-0.1, 0.1)."""
+    gen = torch.Generator().manual_seed(layer.seed * 1000 + seed_offset)
+    dt = TORCH_DTYPE[layer.dtype]
+    fan = (layer.c_in // layer.groups) * layer.kh * layer.kw / (layer.stride[0] * layer.stride[1])
+    x = _draw((layer.n, layer.c_in, layer.h, layer.w), ("uniform", -1.0, 1.0), gen).to(dt)
+    w = _draw((layer.c_in, layer.c_out // layer.groups, layer.kh, layer.kw), ("normal", 0.0, math.sqrt(2.0 / fan)),
+              gen).to(dt)
+    b = _draw((layer.c_out,), ("uniform", -0.1, 0.1), gen).to(dt) if layer.bias else None
+    return {"x": x, "w": w, "bias": b, "residual": None}
