@@ -511,6 +511,73 @@ def run_integer(L, steps: int, warmup: int, world: int, local_rank: int) -> dict
                          "traffic": None, "tensor_or_alu_frac": round(ops / (us / 1e6) / 1e12 / DP4A_PEAK_TOPS, 4)}}
 
 
+# ---- ConvTranspose ---------------------------------------------------------------
+def transpose_flops(L) -> int:
+    """2 x the multiply-adds of the transposed convolution: every input pixel
+    times its kernel taps times the output channels of its group."""
+    return 2 * L.n * L.c_in * L.h * L.w * (L.c_out // L.groups) * L.kh * L.kw
+
+
+def run_transpose(L, steps: int, warmup: int, world: int, local_rank: int) -> dict:
+    import torch
+
+    import implicit_gemm_cnn_gb300 as conv
+    from workloads import make_transpose_inputs
+    dev = torch.device("cuda", local_rank)
+    p = conv.make_transpose_problem((L.n, L.c_in, L.h, L.w), (L.c_in, L.c_out // L.groups, L.kh, L.kw),
+                                    dtype=L.dtype, stride=L.stride, pads=L.pads, dilation=L.dilation,
+                                    out_pad=L.out_pad, groups=L.groups, act=L.act, has_bias=L.bias)
+    ho, wo = conv.conv_transpose_output_shape(p)
+    need = conv.conv_transpose_scratch_bytes(p)
+    es = 4 if L.dtype == "f32" else 2
+    set_bytes = es * (L.n * L.c_in * L.h * L.w + L.c_in * (L.c_out // L.groups) * L.kh * L.kw + L.n * L.c_out * ho * wo)
+    nsets = max(1, min(64, math.ceil(2 * L2_BYTES / set_bytes)))
+    sets = []
+    for i in range(nsets):
+        t = {k: (v.to(dev) if v is not None else None) for k, v in make_transpose_inputs(L, seed_offset=i + 1).items()}
+        t["y"] = torch.empty((L.n, L.c_out, ho, wo), dtype=t["x"].dtype, device=dev)
+        sets.append(t)
+    scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def step(i):
+        t = sets[i % nsets]
+        conv.conv_transpose_forward(p, t["x"], t["w"], t["bias"], None, t["y"], scratch, need)
+
+    for i in range(max(warmup, nsets)):
+        step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for i in range(steps):
+            step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank).start()
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        g.replay()
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    us = secs * 1e6 / steps
+    fl = transpose_flops(L)
+    rate = fl / (us / 1e6) / 1e12
+    return {"value": aggregate(fl * steps, world, secs) / 1e12, "us": us, "clocks": clocks, "launches": 3 * steps,
+            "roofline": {"bound": "alu", "achieved": round(rate, 2), "peak": FFMA_PEAK_TFLOPS, "unit": "TFLOP/s",
+                         "frac": round(rate / FFMA_PEAK_TFLOPS, 4), "traffic": None,
+                         "tensor_or_alu_frac": round(rate / FFMA_PEAK_TFLOPS, 4)}}
+
+
 def nested_layers(headline: str, args, world: int, rank: int, local_rank: int) -> list:
     """Every other workload layer, timed like the headline (graphs of
     back-to-back calls, inputs rotated past L2, events on the launching
@@ -541,6 +608,15 @@ def nested_layers(headline: str, args, world: int, rank: int, local_rank: int) -
                     "variant": "conv_integer dp4a (unfold + weights + product)", "steps": args.layer_steps,
                     "us_per_call": round(r["us"], 3), "tops": round(r["value"], 3), "roofline": r["roofline"],
                     "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
+                    "clock_reasons": r["clocks"].get("reasons")})
+    from workloads import TRANSPOSE_LAYERS
+    for name in sorted(TRANSPOSE_LAYERS):
+        L = TRANSPOSE_LAYERS[name]
+        r = run_transpose(L, args.layer_steps, args.warmup, world, local_rank)
+        out.append({"layer": name, "workload": L.description, "dtype": L.dtype,
+                    "variant": "conv_transpose (weight transpose + CUDA-core Gemm + gathering col2im)",
+                    "steps": args.layer_steps, "us_per_call": round(r["us"], 3), "tflops": round(r["value"], 3),
+                    "roofline": r["roofline"], "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
                     "clock_reasons": r["clocks"].get("reasons")})
     return out
 
