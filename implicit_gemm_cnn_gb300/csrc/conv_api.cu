@@ -366,6 +366,45 @@ bool plan_tc(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   return true;
 }
 
+// Winograd F(2x2, 3x3): the shapes it covers, and whether it is taken.
+bool wino_applies(const conv_problem* p) {
+  return p->dtype == CONV_F32 && p->kh == 3 && p->kw == 3 && p->stride_h == 1 && p->stride_w == 1 &&
+         p->dil_h == 1 && p->dil_w == 1 && p->groups == 1 && !(p->flags & CONV_FLAG_NO_WINOGRAD) &&
+         !(p->flags & CONV_FLAG_FORCE_FFMA);
+}
+
+conv_status make_plan(const conv_problem* p, int sm, Plan* out, Shape* shape);
+
+// The Winograd plan: tiles, the 16-group 1x1 product's plan and the scratch.
+conv_status wino_prepare(const conv_problem* p, const Shape& s, int sm, WinoPlan* wp) {
+  memset(wp, 0, sizeof(*wp));
+  wp->geo.th = static_cast<int>((s.ho + 1) / 2);
+  wp->geo.tw = static_cast<int>((s.wo + 1) / 2);
+  wp->geo.tiles = p->n * wp->geo.th * wp->geo.tw;
+  wp->geo.p4 = (wp->geo.tiles + 3) / 4 * 4;
+  conv_problem q;
+  memset(&q, 0, sizeof(q));
+  q.n = 1; q.c_in = 16 * p->c_in; q.h = 1; q.w = wp->geo.p4;
+  q.c_out = 16 * p->c_out; q.kh = q.kw = 1; q.stride_h = q.stride_w = 1; q.dil_h = q.dil_w = 1;
+  q.groups = 16; q.act = CONV_ACT_IDENTITY; q.dtype = CONV_F32;
+  q.flags = CONV_FLAG_FORCE_FFMA | CONV_FLAG_NO_SPLIT_K | CONV_FLAG_NO_UNFOLD;
+  Shape sq;
+  conv_status st = make_plan(&q, sm, &wp->gemm_plan, &sq);
+  if (st != CONV_OK) return st;
+  if (wp->gemm_plan.info.scratch_bytes != 0) return CONV_ERR_SHAPE;
+  shape_args(&q, sq, &wp->gemm_args);
+  auto align = [](uint64_t v) { return (v + 255) / 256 * 256; };
+  uint64_t off = 0;
+  wp->u_off = off;
+  off = align(off + 16ull * p->c_out * p->c_in * 4);
+  wp->v_off = off;
+  off = align(off + 16ull * p->c_in * wp->geo.p4 * 4);
+  wp->m_off = off;
+  off += 16ull * p->c_out * wp->geo.p4 * 4;
+  wp->scratch_bytes = off;
+  return CONV_OK;
+}
+
 conv_status make_plan(const conv_problem* p, int sm, Plan* out, Shape* shape) {
   if (sm < 1) return CONV_ERR_ARG;
   Shape s;
@@ -379,7 +418,21 @@ conv_status make_plan(const conv_problem* p, int sm, Plan* out, Shape* shape) {
   out->info.gemm_k = s.K;
   const bool force_ffma = (p->flags & CONV_FLAG_FORCE_FFMA) != 0;
   bool done = false;
-  if (!force_ffma && s.cg == 1) done = plan_depthwise(p, s, sm, out);
+  // Winograd where it is forced, or for 3x3 stride-1 float32 layers with 64 or
+  // more channels each way (the sixteen products then dominate the transforms)
+  if (wino_applies(p) && ((p->flags & CONV_FLAG_WINOGRAD) || (p->c_in >= 64 && p->c_out >= 64))) {
+    WinoPlan wp;
+    if (wino_prepare(p, s, sm, &wp) == CONV_OK) {
+      out->info.variant = CONV_VARIANT_WINOGRAD;
+      out->info.split_k = 1;
+      out->info.tile_m = 2;
+      out->info.tile_n = 2;
+      out->info.ctas = wp.gemm_plan.info.ctas;
+      out->info.scratch_bytes = wp.scratch_bytes;
+      done = true;
+    }
+  }
+  if (!done && !force_ffma && s.cg == 1) done = plan_depthwise(p, s, sm, out);
   if (!done && !force_ffma) done = plan_tc(p, s, sm, out);
   if (!done) plan_ffma(p, s, sm, out);
   if (shape) *shape = s;
@@ -431,6 +484,7 @@ const char* variant_name(int v) {
     case CONV_VARIANT_DEPTHWISE: return "depthwise_halo";
     case CONV_VARIANT_IGEMM_TC: return "igemm_tcgen05";
     case CONV_VARIANT_IGEMM_TC_WINDOW: return "igemm_tcgen05_window";
+    case CONV_VARIANT_WINOGRAD: return "winograd_f2x2_3x3";
     default: return "unknown";
   }
 }
@@ -567,8 +621,16 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
   const conv_plan_info& i = plan.info;
   const int launches = (i.variant == CONV_VARIANT_IGEMM_FFMA || i.variant == CONV_VARIANT_IGEMM_FFMA_SPLIT)
                            ? ffma_launch_count(plan)
-                           : (i.variant == CONV_VARIANT_IGEMM_TC_WINDOW ? 2 : 1);
-  if (i.variant == CONV_VARIANT_IGEMM_TC) {
+                           : (i.variant == CONV_VARIANT_IGEMM_TC_WINDOW ? 2 : (i.variant == CONV_VARIANT_WINOGRAD ? 4 : 1));
+  if (i.variant == CONV_VARIANT_WINOGRAD) {
+    WinoPlan wp;
+    if (wino_prepare(p, s, sm, &wp) != CONV_OK) return CONV_ERR_SHAPE;
+    const FfmaCfg& c = kFfmaCfgs[wp.gemm_plan.ffma_cfg];
+    snprintf(buf, len, "%s tiles=%dx%d per image (%lld in all) products=16 x %lldco x %lldci on CUDA cores "
+             "tile=%dco x %dpx scratch=%llu sms=%d", variant_name(i.variant), wp.geo.th, wp.geo.tw,
+             static_cast<long long>(wp.geo.tiles), static_cast<long long>(p->c_out), static_cast<long long>(p->c_in),
+             c.bm, c.bn, static_cast<unsigned long long>(i.scratch_bytes), sm);
+  } else if (i.variant == CONV_VARIANT_IGEMM_TC) {
     static const char* orders[] = {"tap/8-channel", "channel/row/8-tap", "channel/tap"};
     snprintf(buf, len, "%s tile=128px x %dco k=%lld (padded %d, %s order) stages=%d blocks=%lld sms=%d",
              variant_name(i.variant), plan.tc.bn, static_cast<long long>(i.gemm_k), plan.tc.k_pad,
@@ -691,6 +753,12 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
     case CONV_VARIANT_IGEMM_TC:
       err = launch_tc(plan, a, p->dtype, cs);
       break;
+    case CONV_VARIANT_WINOGRAD: {
+      WinoPlan wp;
+      if (wino_prepare(p, s, sm, &wp) != CONV_OK) return CONV_ERR_SHAPE;
+      err = launch_winograd(wp, a, scratch, cs);
+      break;
+    }
     default: {
       a.split = plan.info.split_k;
       a.k_per_split = plan.k_per_split;
@@ -990,11 +1058,13 @@ extern "C" conv_status conv_forward_fixed_scratch(const conv_problem* p, const v
   // planes), unless the caller forced the split.
   conv_problem q = *p;
   const int forced_split = static_cast<int>((p->flags & CONV_FLAG_SPLIT_K_MASK) >> CONV_FLAG_SPLIT_K_SHIFT);
-  const uint32_t fallbacks[] = {CONV_FLAG_NO_WINDOW, CONV_FLAG_NO_UNFOLD, forced_split ? 0u : CONV_FLAG_NO_SPLIT_K};
+  const uint32_t fallbacks[] = {CONV_FLAG_NO_WINDOW, CONV_FLAG_NO_WINOGRAD, CONV_FLAG_NO_UNFOLD,
+                                forced_split ? 0u : CONV_FLAG_NO_SPLIT_K};
   for (uint32_t f : fallbacks) {
     if (plan.info.scratch_bytes <= CONV_FIXED_SCRATCH_BYTES) break;
     if (!f || (q.flags & f)) continue;
     if (f == CONV_FLAG_NO_UNFOLD && (q.flags & CONV_FLAG_FORCE_UNFOLD)) continue;
+    if (f == CONV_FLAG_NO_WINOGRAD && (q.flags & CONV_FLAG_WINOGRAD)) continue;
     q.flags |= f;
     st = make_plan(&q, sm, &plan, nullptr);
     if (st != CONV_OK) return st;

@@ -203,6 +203,22 @@ struct TransposePlan {
 };
 cudaError_t launch_conv_transpose(const TransposePlan& tp, const ConvArgs& a, const TransposeGeo& t,
                                   const void* w, void* scratch, cudaStream_t s);
+
+// Winograd F(2x2, 3x3) (conv_winograd.cu): transformed weights U[16][K][C],
+// transformed input tiles V[16][C][p4], the sixteen products M[16][K][p4]
+// (a 16-group 1x1 convolution on the CUDA-core kernel), all in scratch.
+struct WinoGeo {
+  int th, tw;          // tiles per image: ceil(Ho/2) x ceil(Wo/2)
+  long long tiles;     // over all images
+  long long p4;        // tiles rounded up to 4 (the product's pixel rows)
+};
+struct WinoPlan {
+  WinoGeo geo;
+  Plan gemm_plan;      // the CUDA-core plan of the 16-group 1x1 product
+  ConvArgs gemm_args;
+  size_t u_off, v_off, m_off, scratch_bytes;
+};
+cudaError_t launch_winograd(const WinoPlan& wp, const ConvArgs& a, void* scratch, cudaStream_t s);
 // Kernels one conv_forward of the CUDA-core variant launches for `plan`.
 int ffma_launch_count(const Plan& plan);
 // Whether the unfolded-B layout applies to the shape (element type aside),

@@ -84,6 +84,9 @@ typedef enum conv_act {
 #define CONV_FLAG_NO_UNFOLD 0x8u    /* CUDA-core kernel: never the unfolded-input pre-pass */
 #define CONV_FLAG_FORCE_UNFOLD 0x10u /* CUDA-core kernel: the unfolded-input pre-pass
                                         wherever it applies (output width a multiple of 4) */
+#define CONV_FLAG_WINOGRAD 0x20u     /* Winograd F(2x2,3x3) wherever it applies (float32,
+                                        3x3, stride 1, dilation 1, one group)      */
+#define CONV_FLAG_NO_WINOGRAD 0x40u  /* never Winograd                                 */
 #define CONV_FLAG_SPLIT_K_SHIFT 8   /* bits 8..13: force this many ranges of k (1-63) */
 #define CONV_FLAG_SPLIT_K_MASK 0x3f00u
 
@@ -135,11 +138,18 @@ typedef enum conv_variant {
                                       per group, any channel multiplier)     */
   CONV_VARIANT_IGEMM_TC = 3,       /* implicit GEMM on tcgen05 tensor cores,
                                       input window gathered into shared memory */
-  CONV_VARIANT_IGEMM_TC_WINDOW = 4 /* tcgen05 implicit GEMM over shifted windows of
+  CONV_VARIANT_IGEMM_TC_WINDOW = 4, /* tcgen05 implicit GEMM over shifted windows of
                                       a zero-padded input band in shared memory
                                       (stride 1, or stride 2 split into 2x2
                                       phases; one group; the output's rows a
                                       multiple of 8 elements)                */
+  CONV_VARIANT_WINOGRAD = 5        /* Winograd F(2x2, 3x3) ("Convolutions",
+                                      section 2.6): weight and input-tile
+                                      transforms, sixteen products summed over
+                                      channels on CUDA cores, output transform
+                                      with the epilogue (float32, 3x3, stride
+                                      1, dilation 1, one group; taken for 64 or
+                                      more channels in and out)              */
 } conv_variant;
 
 /* The host-side plan of a problem for a device with `sm_count` SMs. */

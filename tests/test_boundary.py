@@ -135,6 +135,7 @@ EXPECTED_VARIANT = {
     "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05_window",
     "grouped_dil2_f32": "igemm_ffma", "late_1x1_splitk_f32": "igemm_ffma_split_k",
     "strided_3x3_s2_f32": "igemm_ffma",
+    "resnet50_3x3_256_f32": "winograd_f2x2_3x3",
 }
 
 
@@ -185,6 +186,13 @@ def test_plans_of_the_workloads(lib, name):
         assert plan["scratch_bytes"] == base
         p2 = _layer_problem(L, flags=conv.FLAG_NO_UNFOLD)
         assert conv.conv_plan(p2, 152)["scratch_bytes"] == 0
+    elif plan["variant_name"] == "winograd_f2x2_3x3":
+        # U[16][K][C], V[16][C][tiles rounded to 4], M[16][K][same], 256-byte aligned
+        tiles = L.n * -(-plan["ho"] // 2) * -(-plan["wo"] // 2)
+        p4 = (tiles + 3) // 4 * 4
+        u = (16 * L.c_out * L.c_in * 4 + 255) // 256 * 256
+        v = (16 * L.c_in * p4 * 4 + 255) // 256 * 256
+        assert plan["scratch_bytes"] == u + v + 16 * L.c_out * p4 * 4
     else:
         assert plan["scratch_bytes"] == 0
     assert conv.conv_plan(p, 152) == plan      # a pure function of (problem, SMs)

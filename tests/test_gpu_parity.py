@@ -50,6 +50,7 @@ REDUCED = {
     "grouped_dil2_f32": (1, 28, 28),
     "late_1x1_splitk_f32": (1, 7, 7),
     "strided_3x3_s2_f32": (1, 32, 32),
+    "resnet50_3x3_256_f32": (2, 14, 13),
 }
 
 EXPECTED = {
@@ -59,6 +60,7 @@ EXPECTED = {
     "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05_window",
     "grouped_dil2_f32": "igemm_ffma", "late_1x1_splitk_f32": "igemm_ffma_split_k",
     "strided_3x3_s2_f32": "igemm_ffma",
+    "resnet50_3x3_256_f32": "winograd_f2x2_3x3",
 }
 
 
@@ -240,7 +242,7 @@ def test_forced_split_k(split, dtype, unfold):
 
 
 @pytest.mark.parametrize("name", ["resnet50_3x3_f16", "mbv3_dw5x5_f32", "late_1x1_splitk_f32",
-                                  "grouped_dil2_f32"])
+                                  "grouped_dil2_f32", "resnet50_3x3_256_f32"])
 def test_bit_identical_runs(name):
     """No atomics, fixed summation order: two runs give the same bits
     ("Convolution, pooling and resize", Determinism)."""

@@ -260,3 +260,26 @@ def test_batch_chunks_are_bit_identical(xs, ws, g, dtype):
     st = lib.conv_forward(ctypes.byref(p), dev["x"].data_ptr(), dev["w"].data_ptr(), dev["bias"].data_ptr(),
                           dev["residual"].data_ptr(), y.data_ptr(), scratch.data_ptr(), one - 1, None)
     assert conv.STATUS[st] == "CONV_ERR_SCRATCH"
+
+
+# ---- Winograd F(2x2, 3x3) ------------------------------------------------------
+@pytest.mark.parametrize("xs,ws,g,res", [
+    ((2, 8, 9, 11), (16, 8, 3, 3), dict(pads=1, act="relu"), True),
+    ((1, 5, 12, 7), (6, 5, 3, 3), dict(pads=(2, 0, 1, 1), act="silu"), False),
+    ((3, 4, 6, 6), (4, 4, 3, 3), dict(act="tanh"), True),                # no padding: 4x4 outputs
+    ((1, 16, 1, 9), (8, 16, 3, 3), dict(pads=(1, 1, 1, 1)), False),       # one input row
+    ((2, 64, 14, 14), (64, 64, 3, 3), dict(pads=1, act="leaky_relu", alpha=0.1), True),
+])
+def test_winograd_parity(xs, ws, g, res):
+    """Winograd F(2x2, 3x3) against the oracle's direct sum: the float32 bar,
+    literally (max |err| / sum|w x| < 1e-5)."""
+    flags = conv.FLAG_WINOGRAD
+    p = conv.make_problem(xs, ws, dtype="f32", has_bias=True, has_residual=res, flags=flags, **g)
+    assert conv.conv_describe_variant(p).startswith("winograd_f2x2_3x3"), conv.conv_describe_variant(p)
+    ho, wo = conv.conv_output_shape(p)
+    inp = random_layer_inputs(xs, ws, "f32", seed=xs[1] * 7 + ws[0], bias=True,
+                              residual_shape=(xs[0], ws[0], ho, wo) if res else None)
+    y, _ = _run_offsets(inp, "f32", (0, 0, 0), flags=flags, **g)
+    out = check_full(inp, "f32", y, **g)
+    assert out["ok"], out
+    assert out["max_scaled_err"] < 1e-5, out

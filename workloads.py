@@ -103,6 +103,12 @@ _add(Layer("strided_3x3_s2_f32", 16, 256, 56, 56, 512, 3, 3, stride=(2, 2), pads
            act="leaky_relu", alpha=0.1, bias=False, seed=1010,
            description="N=16 256->512 3x3 s2 p1 at 56x56, leaky-relu 0.1, no bias, fp32"))
 
+# A ResNet-50 stage-3 3x3 layer in float32: the stride-1 3x3 class on which
+# "Convolution, pooling and resize" prices Winograd F(2x2, 3x3).
+_add(Layer("resnet50_3x3_256_f32", 16, 256, 14, 14, 256, 3, 3, pads=(1, 1, 1, 1), act="relu",
+           x_dist=("normal", 0.0, 1.0), w_dist=_he(256 * 9), b_dist=("uniform", -0.1, 0.1), seed=1011,
+           description="ResNet-50 3x3 256->256 s1 p1 at 14x14, N=16, bias, ReLU, fp32"))
+
 TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
