@@ -357,17 +357,18 @@ CONV_API conv_status conv_integer_forward(const conv_problem* p, int32_t x_type,
  * library.  Such a caller still passes x, w, bias, residual and y (device
  * memory it was given), exactly as for conv_forward; the scratch conv_forward
  * would take from the caller -- the float32 planes of split k, the repacked
- * weights of the shifted-window tensor-core variant, or the unfolded input
- * and transposed weights of the CUDA-core kernel -- lives instead in one
+ * weights of the shifted-window tensor-core variant, the unfolded input and
+ * transposed weights of the CUDA-core kernel, or Winograd's transformed
+ * operands -- lives instead in one
  * fixed array of CONV_FIXED_SCRATCH_BYTES that the library declares in device
  * memory.  Every GPU that loads the library holds that array until the
  * process exits.
  *
  * When that scratch would exceed the array, the call runs the problem on a
  * variant that needs none, if there is one: the gather tensor-core kernel in
- * place of the shifted-window one, the CUDA-core kernel gathering its input
- * from x in place of the unfolded copy, or k summed in one range in place of
- * an automatic split.  Such a call gives results within the same error bound as
+ * place of the shifted-window one, the direct CUDA-core kernel in place of
+ * Winograd, the CUDA-core kernel gathering its input from x in place of the
+ * unfolded copy, or k summed in one range in place of an automatic split.  Such a call gives results within the same error bound as
  * conv_forward's, but not necessarily the same bits (another summation order).
  *
  * Nothing is allocated by this call.  The first call on each device looks up

@@ -221,7 +221,7 @@ def test_auto_pad_convolution(dtype, mode, xs, ws, stride, dil):
 # ---- batch chunking ----------------------------------------------------------
 @pytest.mark.parametrize("xs,ws,g,dtype", [
     ((11, 32, 64, 64), (128, 32, 3, 3), dict(pads=1, act="silu"), "f32"),       # unfolded, tail split
-    ((4, 256, 28, 28), (512, 256, 3, 3), dict(pads=1, act="relu"), "f32"),      # unfolded
+    ((4, 256, 28, 28), (512, 256, 3, 3), dict(pads=1, act="relu"), "f32"),      # unfolded (Winograd off)
     ((5, 512, 7, 7), (64, 512, 1, 1), dict(act="leaky_relu", alpha=0.1), "f32"),  # split k, 49 px per image
     ((3, 256, 9, 9), (48, 256, 3, 3), dict(pads=1), "bf16"),                     # forced CUDA-core split k
 ])
@@ -229,7 +229,7 @@ def test_batch_chunks_are_bit_identical(xs, ws, g, dtype):
     """A scratch smaller than the whole batch needs (but at least one image's)
     runs the batch in chunks of whole images; the result has the same bits
     ("Convolution, pooling and resize", Layout and operands)."""
-    flags = conv.FLAG_FORCE_FFMA if dtype != "f32" else 0
+    flags = conv.FLAG_FORCE_FFMA if dtype != "f32" else conv.FLAG_NO_WINOGRAD
     p = conv.make_problem(xs, ws, dtype=dtype, has_bias=True, has_residual=True, flags=flags, **g)
     full = conv.conv_scratch_bytes(p)
     one = conv.conv_scratch_bytes_per_image(p)

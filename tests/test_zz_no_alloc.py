@@ -2,8 +2,8 @@
 allocate device memory (a plug-in whose host framework owns all allocations,
 a path that must not enter the allocator).  Its scratch -- split-k planes,
 the shifted-window kernel's repacked weights, the CUDA-core kernel's
-unfolded input -- lives in the library's own fixed device array instead of
-caller memory.
+unfolded input, Winograd's transformed operands -- lives in the library's own
+fixed device array instead of caller memory.
 
 This file is collected last on purpose.  Every call here is compared bit for
 bit with the ordinary entry point on the same inputs, and calls alternate
@@ -75,7 +75,7 @@ def test_fixed_scratch_split_k_alternating_inputs():
     """Split-k planes in the array: three calls, the middle one on another
     shape and other values, each equal to conv_forward's bits."""
     a = _case((1, 2048, 7, 7), (512, 2048, 1, 1), "f32", seed=41)
-    b = _case((1, 1024, 9, 9), (96, 1024, 3, 3), "f32", seed=42, pads=1, act="relu")
+    b = _case((1, 1024, 9, 9), (96, 1024, 3, 3), "f32", seed=42, flags=conv.FLAG_NO_WINOGRAD, pads=1, act="relu")
     for c in (a, b):
         assert conv.conv_plan(c[0], torch.cuda.get_device_properties(0).multi_processor_count)["split_k"] > 1
         assert 0 < conv.conv_scratch_bytes(c[0]) <= conv.FIXED_SCRATCH_BYTES
@@ -117,11 +117,21 @@ def test_fixed_scratch_split_too_large_runs_unsplit():
 def test_fixed_scratch_unfolded_too_large_runs_gathered():
     """The CUDA-core kernel's unfolded input copy past the array: the same
     kernel with its B operand gathered from x, which needs no scratch."""
-    c = _case((4, 256, 28, 28), (512, 256, 3, 3), "f32", seed=48, pads=1, act="relu")
+    c = _case((4, 256, 28, 28), (512, 256, 3, 3), "f32", seed=48, flags=conv.FLAG_NO_WINOGRAD, pads=1, act="relu")
     p = c[0]
     assert "B=unfolded" in conv.conv_describe_variant(p)
     assert conv.conv_scratch_bytes(p) > conv.FIXED_SCRATCH_BYTES
     _check(c, extra_flags=conv.FLAG_NO_UNFOLD)
+
+
+def test_fixed_scratch_winograd_too_large_runs_direct():
+    """Winograd's transformed operands past the array: the direct CUDA-core
+    kernel with its input gathered from x, which needs no scratch."""
+    c = _case((4, 256, 28, 28), (512, 256, 3, 3), "f32", seed=49, pads=1, act="relu")
+    p = c[0]
+    assert conv.conv_describe_variant(p).startswith("winograd_f2x2_3x3")
+    assert conv.conv_scratch_bytes(p) > conv.FIXED_SCRATCH_BYTES
+    _check(c, extra_flags=conv.FLAG_NO_WINOGRAD | conv.FLAG_NO_UNFOLD)
 
 
 def test_fixed_scratch_refuses_oversize_forced_split():
