@@ -24,7 +24,8 @@ __all__ = [
     "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "FLAG_NO_UNFOLD", "FLAG_FORCE_UNFOLD", "FLAG_WINOGRAD",
     "FLAG_NO_WINOGRAD", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
-    "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "FIXED_SCRATCH_BYTES",
+    "conv_forward", "conv_device_error", "conv_selftest_bounded_wait", "conv_forward_fixed_scratch",
+    "FIXED_SCRATCH_BYTES",
     "conv_apply_auto_pad", "AUTO_PAD", "conv_scratch_bytes_per_image",
     "conv_integer_scratch_bytes", "conv_integer_forward", "conv_integer2d", "INT_TYPES",
     "ConvTransposeProblem", "make_transpose_problem", "conv_transpose_output_shape",
@@ -128,6 +129,7 @@ def load() -> ctypes.CDLL:
         lib.conv_describe_variant.argtypes = [P(ConvProblem), ctypes.c_char_p, ctypes.c_size_t]
         lib.conv_forward.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_device_error.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
+        lib.conv_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P(ctypes.c_uint32)]
         lib.conv_forward_fixed_scratch.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp]
         lib.conv_apply_auto_pad.argtypes = [P(ConvProblem), ctypes.c_int32]
         lib.conv_scratch_bytes_per_image.argtypes = [P(ConvProblem), P(ctypes.c_size_t)]
@@ -139,7 +141,8 @@ def load() -> ctypes.CDLL:
         lib.conv_integer_forward.argtypes = [P(ConvProblem), ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
                                              ctypes.c_int32, vp, vp, ctypes.c_size_t, vp]
         for f in ("conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
-                  "conv_forward", "conv_device_error", "conv_forward_fixed_scratch", "conv_apply_auto_pad",
+                  "conv_forward", "conv_device_error", "conv_selftest_bounded_wait",
+                  "conv_forward_fixed_scratch", "conv_apply_auto_pad",
                   "conv_scratch_bytes_per_image", "conv_integer_scratch_bytes", "conv_integer_forward",
                   "conv_transpose_output_shape", "conv_transpose_scratch_bytes", "conv_transpose_forward"):
             getattr(lib, f).restype = ctypes.c_int
@@ -360,6 +363,13 @@ def conv_device_error(reset: bool = True) -> int:
     word = ctypes.c_uint32()
     _check(load().conv_device_error(ctypes.byref(word), 1 if reset else 0), "conv_device_error")
     return word.value
+
+
+def conv_selftest_bounded_wait(limit_us: int = 1000) -> list[int]:
+    """The five report words of the give-up-path self test (see include/conv.h)."""
+    report = (ctypes.c_uint32 * 5)()
+    _check(load().conv_selftest_bounded_wait(int(limit_us), report), "conv_selftest_bounded_wait")
+    return list(report)
 
 
 # ---- conveniences ---------------------------------------------------------

@@ -1022,6 +1022,19 @@ conv_status conv_device_error(uint32_t* word, int32_t reset) {
   return CONV_OK;
 }
 
+conv_status conv_selftest_bounded_wait(uint32_t limit_us, uint32_t* report) {
+  if (!report) return CONV_ERR_NULL;
+  if (limit_us < 1 || limit_us > 100000) return CONV_ERR_ARG;
+  int dev, sm;
+  conv_status st = device_info(&dev, &sm);
+  if (st != CONV_OK) return st;
+  if (tcw_wait_selftest_run(1000ull * limit_us, report) != cudaSuccess) {
+    cudaGetLastError();
+    return CONV_ERR_CUDA;
+  }
+  return CONV_OK;
+}
+
 }  // extern "C"
 
 // ---- a forward call for callers that cannot allocate device memory ---------

@@ -230,5 +230,6 @@ cudaError_t launch_tc(const Plan& plan, const ConvArgs& a, int dtype, cudaStream
 cudaError_t launch_tcw(const Plan& plan, const ConvArgs& a, int dtype, void* scratch, cudaStream_t s);
 cudaError_t tc_error_word(uint32_t* word, int reset);
 cudaError_t tcw_error_word(uint32_t* word, int reset);
+cudaError_t tcw_wait_selftest_run(unsigned long long limit_ns, uint32_t* report_host);
 
 }  // namespace conv

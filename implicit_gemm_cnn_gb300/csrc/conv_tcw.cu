@@ -853,6 +853,84 @@ cudaError_t launch_tcw(const Plan& plan, const ConvArgs& a, int dtype, void* scr
   return cudaErrorInvalidValue;
 }
 
+// ---- the bounded-wait abort path, run on its own --------------------------
+//
+// The shifted-window kernel's give-up path (a wait that runs out raises the
+// block's abort flag and ORs its code into g_tcw_error; the other roles see the
+// flag and stop; the copies still in flight are waited for; tensor memory is
+// freed) only runs when a partner role stops, which never happens in a correct
+// launch.  This kernel walks the same steps with the same wait helper on a
+// block where nothing else can be outstanding: warp 0 allocates 32 columns of
+// tensor memory; thread 0 starts one 256-byte bulk copy into shared memory;
+// all 64 threads wait, with a short limit, on an mbarrier nothing arrives on;
+// the copy is then drained (its own wait ignores the abort flag, with the
+// usual limit), written back out, and the tensor memory freed.
+constexpr uint32_t kSelftestWaitCode = 256u;   // the withheld arrival's wait ran out
+constexpr uint32_t kSelftestDrainCode = 512u;  // the drain of the copy ran out
+
+__global__ void __launch_bounds__(64) tcw_wait_selftest(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                        unsigned long long limit_ns, uint32_t* __restrict__ report) {
+  __shared__ __align__(128) uint4 buf[16];
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x / 32;
+  const uint32_t never = smem_u32(&bars[0]), copied = smem_u32(&bars[1]);
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(never, 1);
+    mbar_init(copied, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 32);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(copied, sizeof(buf));
+    bulk_load(smem_u32(buf), src, sizeof(buf), copied);
+  }
+  const bool got = tcx::wait_phase(&g_tcw_error, never, 0, &abort_flag, kSelftestWaitCode, false, 0, limit_ns);
+  if (got) atomicAdd(&report[0], 1u);
+  const bool drained = tcx::wait_phase(&g_tcw_error, copied, 0, &abort_flag, kSelftestDrainCode, true);
+  if (drained) atomicAdd(&report[1], 1u);
+  __syncthreads();
+  if (threadIdx.x == 0) report[2] = static_cast<uint32_t>(abort_flag);
+  if (drained && threadIdx.x < 16) dst[threadIdx.x] = buf[threadIdx.x];
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_base, 32);
+  if (threadIdx.x == 0) report[3] = 1;  // reached the end
+}
+
+cudaError_t tcw_wait_selftest_run(unsigned long long limit_ns, uint32_t* report_host) {
+  // device: 256 bytes source, 256 bytes destination, 4 report words
+  void* mem = nullptr;
+  cudaError_t err = cudaMalloc(&mem, 512 + 4 * sizeof(uint32_t));
+  if (err != cudaSuccess) return err;
+  uint4* src = static_cast<uint4*>(mem);
+  uint4* dst = src + 16;
+  uint32_t* report = reinterpret_cast<uint32_t*>(dst + 16);
+  uint32_t pattern[64];
+  for (uint32_t i = 0; i < 64; ++i) pattern[i] = 0x9e3779b9u * (i + 1);
+  err = cudaMemcpy(src, pattern, sizeof(pattern), cudaMemcpyHostToDevice);
+  if (err == cudaSuccess) err = cudaMemset(dst, 0, 256 + 4 * sizeof(uint32_t));
+  if (err == cudaSuccess) {
+    tcw_wait_selftest<<<1, 64>>>(src, dst, limit_ns, report);
+    err = cudaGetLastError();
+  }
+  if (err == cudaSuccess) err = cudaDeviceSynchronize();
+  uint32_t back[64 + 4];
+  if (err == cudaSuccess) err = cudaMemcpy(back, dst, sizeof(back), cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess) {
+    for (int i = 0; i < 4; ++i) report_host[i] = back[64 + i];
+    report_host[4] = memcmp(back, pattern, sizeof(pattern)) == 0 ? 1u : 0u;
+  }
+  const cudaError_t ferr = cudaFree(mem);
+  return err != cudaSuccess ? err : ferr;
+}
+
 cudaError_t tcw_error_word(uint32_t* word, int reset) {
   cudaError_t err = cudaDeviceSynchronize();
   if (err != cudaSuccess) return err;

@@ -47,13 +47,15 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 }
 
 // Wait until the phase of `bar` with parity `parity` has completed.  Gives up
-// (returns false) after kWaitNs or kMaxSpins polls -- then it raises the
-// block's abort flag and ORs `code` into *err -- or as soon as another thread
-// of the block raised the abort flag (unless `ignore_abort`).  A waiter that
-// is not on the critical path passes `sleep_ns`: it then sleeps between polls
-// and leaves the issue slots to the warps that work.
+// (returns false) after `limit_ns` (kWaitNs unless a self-test shortens it) or
+// kMaxSpins polls -- then it raises the block's abort flag and ORs `code` into
+// *err -- or as soon as another thread of the block raised the abort flag
+// (unless `ignore_abort`).  A waiter that is not on the critical path passes
+// `sleep_ns`: it then sleeps between polls and leaves the issue slots to the
+// warps that work.
 static __device__ bool wait_phase(uint32_t* err, uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                  uint32_t code, bool ignore_abort = false, uint32_t sleep_ns = 0) {
+                                  uint32_t code, bool ignore_abort = false, uint32_t sleep_ns = 0,
+                                  unsigned long long limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (unsigned i = 1;; ++i) {
@@ -61,7 +63,7 @@ static __device__ bool wait_phase(uint32_t* err, uint32_t bar, uint32_t parity, 
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (!ignore_abort && *abort_flag) return false;
-      if (globaltimer() - t0 > kWaitNs || i > kMaxSpins) {
+      if (globaltimer() - t0 > limit_ns || i > kMaxSpins) {
         *abort_flag = 1;
         atomicOr(err, code);
         return false;

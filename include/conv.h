@@ -259,6 +259,22 @@ CONV_API conv_status conv_forward(const conv_problem* p, const void* x, const vo
  * diagnostics. */
 CONV_API conv_status conv_device_error(uint32_t* word, int32_t reset);
 
+/* Runs the tensor-core kernels' give-up path on its own, for tests: one block
+ * allocates tensor memory, starts one 256-byte bulk copy, waits `limit_us`
+ * microseconds (1 .. 100000) on an mbarrier that nothing arrives on, raises
+ * its abort flag and reports into the shifted-window error word (bit 24 of
+ * conv_device_error's word: the wait ran out; bit 25: the copy's drain ran
+ * out), drains the copy, frees the tensor memory and returns.  The pages
+ * describe no such call; it exists so that the bounded-wait mechanism the
+ * kernels rely on can be checked without a failing convolution.
+ * `report` (host, 5 words) receives: [0] waits that succeeded (0 expected),
+ * [1] threads whose drain completed (64), [2] the abort flag (1), [3] 1 when
+ * the block reached its end, [4] 1 when the copied bytes arrived intact.
+ * Synchronous; uses the current device and allocates 528 bytes of device
+ * memory for the call.  Errors: CONV_ERR_NULL, CONV_ERR_ARG (limit out of
+ * range), CONV_ERR_DEVICE, CONV_ERR_CUDA. */
+CONV_API conv_status conv_selftest_bounded_wait(uint32_t limit_us, uint32_t* report);
+
 /* ---- ConvTranspose --------------------------------------------------------
  * The transposed convolution (ONNX ConvTranspose; "Convolution, pooling and
  * resize": weights [Cin][Cout/groups][kh][kw]; Variants: a Gemm of the

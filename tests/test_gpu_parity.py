@@ -6,7 +6,8 @@
   benchmark times (sampled outputs, borders included);
 * an edge-case sweep over geometry, activations, optional operands, element
   types and variants (forced CUDA-core path, forced k split);
-* run-to-run bit identity and a clean device error word.
+* run-to-run bit identity, a clean device error word, and the bounded-wait
+  give-up path run on its own with the device usable after it.
 """
 import dataclasses
 import zlib
@@ -255,4 +256,25 @@ def test_bit_identical_runs(name):
 
 
 def test_device_error_word_clear():
+    assert conv.conv_device_error(reset=True) == 0
+
+
+def test_bounded_wait_gives_up_and_device_stays_usable():
+    """The tensor-core kernels' give-up path, run on its own: a wait with a
+    1 ms limit on an mbarrier nothing arrives on runs out, raises the abort
+    flag and its error bit, the bulk copy in flight is drained intact, tensor
+    memory is freed; then a shifted-window convolution on the same device
+    still matches the oracle and leaves the word clear."""
+    assert conv.conv_device_error(reset=True) == 0
+    for _ in range(2):  # twice: the tensor memory of the first run was freed
+        report = conv.conv_selftest_bounded_wait(1000)
+        assert report == [0, 64, 1, 1, 1], report
+        word = conv.conv_device_error(reset=True)
+        assert word == 1 << 24, hex(word)  # the withheld wait's bit, no drain failure
+    L = _reduced(LAYERS["resnet50_3x3_f16"])
+    assert conv.conv_describe_variant(_problem(L)).startswith("igemm_tcgen05_window")
+    inp = make_inputs(L)
+    y = run_gpu(inp, **_geo(L))
+    res = check_full(inp, L.dtype, y, **_geo(L))
+    assert res["ok"], res
     assert conv.conv_device_error(reset=True) == 0
