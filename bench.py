@@ -600,25 +600,30 @@ def nested_layers(headline: str, args, world: int, rank: int, local_rank: int) -
                "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
                "clock_reasons": r["clocks"].get("reasons")}
         out.append(rec)
-    from workloads import INT_LAYERS
-    for name in sorted(INT_LAYERS):
+    from workloads import INT_LAYERS, TRANSPOSE_LAYERS
+    for name in sorted(INT_LAYERS) + sorted(TRANSPOSE_LAYERS):
+        out.append(other_op_record(name, args, world, local_rank))
+    return out
+
+
+def other_op_record(name: str, args, world: int, local_rank: int) -> dict:
+    """The record of one ConvInteger or ConvTranspose workload layer."""
+    from workloads import INT_LAYERS, TRANSPOSE_LAYERS
+    if name in INT_LAYERS:
         L = INT_LAYERS[name]
         r = run_integer(L, args.layer_steps, args.warmup, world, local_rank)
-        out.append({"layer": name, "workload": L.description, "dtype": f"{L.x_type}x{L.w_type}->i32",
-                    "variant": "conv_integer dp4a (unfold + weights + product)", "steps": args.layer_steps,
-                    "us_per_call": round(r["us"], 3), "tops": round(r["value"], 3), "roofline": r["roofline"],
-                    "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
-                    "clock_reasons": r["clocks"].get("reasons")})
-    from workloads import TRANSPOSE_LAYERS
-    for name in sorted(TRANSPOSE_LAYERS):
-        L = TRANSPOSE_LAYERS[name]
-        r = run_transpose(L, args.layer_steps, args.warmup, world, local_rank)
-        out.append({"layer": name, "workload": L.description, "dtype": L.dtype,
-                    "variant": "conv_transpose (weight transpose + CUDA-core Gemm + gathering col2im)",
-                    "steps": args.layer_steps, "us_per_call": round(r["us"], 3), "tflops": round(r["value"], 3),
-                    "roofline": r["roofline"], "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
-                    "clock_reasons": r["clocks"].get("reasons")})
-    return out
+        return {"layer": name, "workload": L.description, "dtype": f"{L.x_type}x{L.w_type}->i32",
+                "variant": "conv_integer dp4a (unfold + weights + product)", "steps": args.layer_steps,
+                "us_per_call": round(r["us"], 3), "tops": round(r["value"], 3), "roofline": r["roofline"],
+                "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
+                "clock_reasons": r["clocks"].get("reasons")}
+    L = TRANSPOSE_LAYERS[name]
+    r = run_transpose(L, args.layer_steps, args.warmup, world, local_rank)
+    return {"layer": name, "workload": L.description, "dtype": L.dtype,
+            "variant": "conv_transpose (weight transpose + CUDA-core Gemm + gathering col2im)",
+            "steps": args.layer_steps, "us_per_call": round(r["us"], 3), "tflops": round(r["value"], 3),
+            "roofline": r["roofline"], "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
+            "clock_reasons": r["clocks"].get("reasons")}
 
 
 # ---- main ----------------------------------------------------------------
@@ -645,9 +650,12 @@ def main(argv=None) -> int:
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
-    from workloads import LAYERS
+    from workloads import INT_LAYERS, LAYERS, TRANSPOSE_LAYERS
     rank, world, local_rank = dist_env()
     names = sorted(LAYERS) if args.layers == "all" else [args.layer]
+    other_op = args.layer in INT_LAYERS or args.layer in TRANSPOSE_LAYERS
+    if other_op and args.impl != "ours":
+        ap.error("--impl reference times the Conv layers only")
 
     if args.impl == "reference":
         if rank != 0:
@@ -676,6 +684,14 @@ def main(argv=None) -> int:
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if other_op:
+        # one ConvInteger / ConvTranspose layer on its own (for profiler captures): its record only
+        rec = other_op_record(args.layer, args, world, local_rank)
+        if rank == 0:
+            print(json.dumps(rec), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
     nested = args.layers != "all" and not args.quick and not args.no_layers
     for name in names:
         L = LAYERS[name]
