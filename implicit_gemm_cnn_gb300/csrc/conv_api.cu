@@ -839,7 +839,11 @@ static conv_status t_prepare(const conv_transpose_problem* tp, int sm, Transpose
   if (!mul_ok(p->c_out, p->kh * p->kw, &cout_k)) return CONV_ERR_OVERFLOW;
   q.c_out = cout_k;
   q.kh = q.kw = 1; q.stride_h = q.stride_w = 1; q.dil_h = q.dil_w = 1; q.groups = p->groups;
-  q.act = CONV_ACT_IDENTITY; q.dtype = p->dtype;
+  // The Gemm runs in float32 for every element type: 16-bit x is widened
+  // into scratch first (exact), so the pointwise kernel's 16-byte copies apply;
+  // its products and sums are those of the 16-bit kernel, which widens each
+  // element as it stages it.
+  q.act = CONV_ACT_IDENTITY; q.dtype = CONV_F32;
   q.flags = CONV_FLAG_FORCE_FFMA | CONV_FLAG_NO_SPLIT_K | CONV_FLAG_NO_UNFOLD;
   Shape sq;
   conv_status st = make_plan(&q, sm, &out->gemm_plan, &sq);
@@ -847,9 +851,10 @@ static conv_status t_prepare(const conv_transpose_problem* tp, int sm, Transpose
   if (out->gemm_plan.info.scratch_bytes != 0) return CONV_ERR_SHAPE;  // a plain one-pass Gemm
   shape_args(&q, sq, &out->gemm_args);
   out->dtype = p->dtype;
-  const size_t es = p->dtype == CONV_F32 ? 4 : 2;
+  auto up256 = [](size_t v) { return (v + 255) / 256 * 256; };
   out->wt_off = 0;
-  out->cols_off = (static_cast<size_t>(sq.w_elems) * es + 255) / 256 * 256;
+  out->xf_off = up256(static_cast<size_t>(sq.w_elems) * 4);
+  out->cols_off = out->xf_off + (p->dtype == CONV_F32 ? 0 : up256(static_cast<size_t>(sq.x_elems) * 4));
   long long cols_bytes;
   if (!mul_ok(sq.y_elems, 4, &cols_bytes)) return CONV_ERR_OVERFLOW;
   out->scratch_bytes = out->cols_off + static_cast<size_t>(cols_bytes);

@@ -46,6 +46,15 @@ __device__ __forceinline__ void cp_async_n(void* smem, const void* gmem) {
   const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(s), "l"(gmem), "n"(BYTES) : "memory");
 }
+// n copies of BYTES each, the k-th from s + k * sstep to shared address d + k * dstep.
+template <int BYTES>
+__device__ __forceinline__ void cp_async_run(uint32_t d, const char* s, int n, uint32_t dstep, long long sstep) {
+  for (int k = 0; k < n; ++k) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(d), "l"(s), "n"(BYTES) : "memory");
+    d += dstep;
+    s += sstep;
+  }
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -428,6 +437,7 @@ __device__ __forceinline__ void cols4_store_plane(const ConvArgs& a, const float
   T* __restrict__ y = static_cast<T*>(a.y);
   const int hw = a.ho * a.wo;
   if (vec_io) {  // Ho*Wo a multiple of 4, y (and the residual) 16-byte aligned
+#pragma unroll 2
     for (int e = 4 * lane; e < hw; e += 128) {
       float v[4];
       const float4 t = *reinterpret_cast<const float4*>(out + e);
@@ -467,7 +477,11 @@ __global__ void __launch_bounds__(kC4Warps * 32, 5) depthwise_cols4(const ConvAr
   // the plane's float32 sums (Ho x Wo), staged for the coalesced epilogue
   float* outs = reinterpret_cast<float*>(dsm + static_cast<size_t>(kC4Warps) * 2 * bufsz * sizeof(T)) +
                 static_cast<size_t>(warp) * g.out_stride;
-  for (int i = lane; i < 2 * bufsz; i += 32) buf0[i] = from_f32<T>(0.0f);  // the border stays zero
+  {  // the border stays zero (a buffer is a whole number of 16-byte units)
+    uint4* z = reinterpret_cast<uint4*>(buf0);
+    const int units16 = 2 * bufsz * static_cast<int>(sizeof(T)) / 16;
+    for (int i = lane; i < units16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   __syncwarp();
   const T* __restrict__ xg = static_cast<const T*>(a.x);
   const T* __restrict__ wg = static_cast<const T*>(a.wt);
@@ -488,11 +502,27 @@ __global__ void __launch_bounds__(kC4Warps * 32, 5) depthwise_cols4(const ConvAr
   const int my_q = units <= 32 ? lane - my_r0 * units : lane;
   const int q_step = units <= 32 ? units : 32;
   const bool stager = units <= 32 ? my_r0 < rpp : true;
-  auto stage = [&](int pl, T* buf) {
+  // with at most 32 copies per image row a lane's copies are one column q and
+  // the rows my_r0, my_r0 + rpp, ...: the same shared and global offsets for
+  // every plane, stepped by constants (no per-copy index arithmetic)
+  const bool prog = units <= 32 && g.copy != 0;
+  const int ncp = prog && stager && rows_s > my_r0 ? (rows_s - my_r0 + rpp - 1) / rpp : 0;
+  const uint32_t dst_first =
+      static_cast<uint32_t>(((a.pt + my_r0) * g.pitch + a.pl + my_q * ce) * static_cast<int>(sizeof(T)));
+  const uint32_t dst_step = static_cast<uint32_t>(rpp * g.pitch * static_cast<int>(sizeof(T)));
+  const long long src_first = (static_cast<long long>(my_r0) * a.w + my_q * ce) * static_cast<long long>(sizeof(T));
+  const long long src_step = static_cast<long long>(rpp) * a.w * static_cast<long long>(sizeof(T));
+  auto stage = [&](int n, int co, T* buf) {
     if (!stager) return;
-    const int n = pl / a.c_out;
-    const int co = pl - n * a.c_out;
-    const T* src = xg + (static_cast<long long>(n) * a.c_in + co / m) * a.hw;
+    const T* src = xg + (static_cast<long long>(n) * a.c_in + (m == 1 ? co : co / m)) * a.hw;
+    if (prog) {
+      const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(buf)) + dst_first;
+      const char* sp = reinterpret_cast<const char*>(src) + src_first;
+      if (g.copy == 16) cp_async_run<16>(d, sp, ncp, dst_step, src_step);
+      else if (g.copy == 8) cp_async_run<8>(d, sp, ncp, dst_step, src_step);
+      else cp_async_run<4>(d, sp, ncp, dst_step, src_step);
+      return;
+    }
     T* dst = buf + a.pt * g.pitch + a.pl;
     if (g.copy == 16) {
       for (int r = my_r0; r < rows_s; r += rpp)
@@ -512,14 +542,22 @@ __global__ void __launch_bounds__(kC4Warps * 32, 5) depthwise_cols4(const ConvAr
   const int j = lane % g.groups, rb = lane / g.groups;
   const bool worker = rb < g.rblocks && 4 * j < a.wo;
   int k = 0;
-  if (first < planes) stage(first, buf0);
+  // (image, channel) of plane pl, stepped by `stride` planes without a division
+  const int step_n = stride / a.c_out, step_c = stride - (stride / a.c_out) * a.c_out;
+  int n = first / a.c_out, co = first - (first / a.c_out) * a.c_out;
+  auto next_plane = [&](int& pn, int& pc) {
+    pn += step_n;
+    pc += step_c;
+    if (pc >= a.c_out) { pc -= a.c_out; ++pn; }
+  };
+  if (first < planes) stage(n, co, buf0);
   cp_async_commit();
   for (int pl = first; pl < planes; pl += stride, ++k) {
     T* buf = buf0 + (k & 1) * bufsz;
-    if (pl + stride < planes) stage(pl + stride, buf0 + ((k + 1) & 1) * bufsz);
+    int n_next = n, co_next = co;
+    next_plane(n_next, co_next);
+    if (pl + stride < planes) stage(n_next, co_next, buf0 + ((k + 1) & 1) * bufsz);
     cp_async_commit();
-    const int n = pl / a.c_out;
-    const int co = pl - n * a.c_out;
     float wv[K][K];
 #pragma unroll
     for (int u = 0; u < K; ++u)
@@ -584,6 +622,8 @@ __global__ void __launch_bounds__(kC4Warps * 32, 5) depthwise_cols4(const ConvAr
       default: cols4_store_plane<T, ACT_IDENTITY>(a, outs, pbase, bv, bg != nullptr, g.vec_io);
     }
     __syncwarp();  // the staging area is free for the next plane
+    n = n_next;
+    co = co_next;
   }
   cp_async_wait<0>();
 }

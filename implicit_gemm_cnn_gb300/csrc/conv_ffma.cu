@@ -414,10 +414,21 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
   for (int jg = 0; jg < TN / 4; ++jg) {
     const long long p = pix0 + jg * GN + tx * 4;
     if (p >= a.pix_hi || p + 3 < a.pix_lo) continue;
-    const long long pf = p >= a.pix_lo ? p : a.pix_lo;  // a stored pixel of the group
     const int n = static_cast<int>(p / a.howo);
     const long long rem = p - static_cast<long long>(n) * a.howo;
     const bool whole4 = a.vec_out && p >= a.pix_lo && (p + 3 < a.pix_hi) && (rem + 3 < a.howo) && ((a.howo & 3) == 0);
+    // output offset (image, position) of pixel p + q, stepped from p's
+    // without a division: the 4 pixels may cross image boundaries
+    long long oo[4];
+    int on[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      long long o = rem + q;
+      int nq = n;
+      while (o >= a.howo) { o -= a.howo; ++nq; }
+      oo[q] = o;
+      on[q] = nq;
+    }
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
       const int m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
@@ -434,9 +445,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
           for (int q = 0; q < 4; ++q) {
             const long long pq = p + q;
             if (pq < a.pix_lo || pq >= a.pix_hi) continue;
-            const int nq = static_cast<int>(pq / a.howo);
-            part[(static_cast<long long>(nq) * a.c_out + co) * a.howo + (pq - nq * a.howo) - out0] =
-                acc[i][jg * 4 + q];
+            part[(static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q] - out0] = acc[i][jg * 4 + q];
           }
         }
       } else {
@@ -450,13 +459,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
         for (int q = 0; q < 4; ++q) {
           const long long pq = p + q;
           in[q] = pq >= a.pix_lo && pq < a.pix_hi;
-          if (whole4) {
-            oq[q] = out + q;
-          } else {
-            const long long pa = in[q] ? pq : pf;
-            const int nq = static_cast<int>(pa / a.howo);
-            oq[q] = (static_cast<long long>(nq) * a.c_out + co) * a.howo + (pa - static_cast<long long>(nq) * a.howo);
-          }
+          oq[q] = whole4 ? out + q : (static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q];
           v[q] = acc[i][jg * 4 + q];
           bv[q] = bco;
           rv[q] = (resp && in[q]) ? to_f32(resp[oq[q]]) : 0.0f;
@@ -607,9 +610,23 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
   if ((total & 3) == 0 && (out0 & 3) == 0) {
     const long long q = total >> 2;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < q; i += stride) {
-      float4 s = reinterpret_cast<const float4*>(part)[i];
-      for (int z = 1; z < a.split; ++z) {
-        const float4 t = reinterpret_cast<const float4*>(part + z * total)[i];
+      const float4* p4 = reinterpret_cast<const float4*>(part) + i;
+      const long long zs = q;  // float4s per plane
+      float4 s = p4[0];
+      int z = 1;
+      // four planes' loads in flight at a time; the adds stay in range order
+      for (; z + 3 < a.split; z += 4) {
+        float4 t[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) t[j] = p4[(z + j) * zs];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s.x = __fadd_rn(s.x, t[j].x); s.y = __fadd_rn(s.y, t[j].y);
+          s.z = __fadd_rn(s.z, t[j].z); s.w = __fadd_rn(s.w, t[j].w);
+        }
+      }
+      for (; z < a.split; ++z) {
+        const float4 t = p4[z * zs];
         s.x = __fadd_rn(s.x, t.x); s.y = __fadd_rn(s.y, t.y);
         s.z = __fadd_rn(s.z, t.z); s.w = __fadd_rn(s.w, t.w);
       }
@@ -617,9 +634,16 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
       const T* __restrict__ bp = static_cast<const T*>(a.bias);
       const T* __restrict__ rp = rbase;
       float v[4] = {s.x, s.y, s.z, s.w}, bv[4], rv[4];
+      // the channel of output out0 + o, then stepped (4 outputs may cross planes)
+      const long long plane = (out0 + o) / a.howo;
+      long long pos = out0 + o - plane * a.howo;
+      int ck = static_cast<int>(plane % a.c_out);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int ck = static_cast<int>(((out0 + o + k) / a.howo) % a.c_out);
+        if (k > 0 && ++pos >= a.howo) {
+          pos = 0;
+          if (++ck == a.c_out) ck = 0;
+        }
         bv[k] = bp ? to_f32(bp[ck]) : 0.0f;
         rv[k] = rp ? to_f32(rp[o + k]) : 0.0f;
       }
@@ -903,9 +927,11 @@ template <typename T>
 cudaError_t launch_reduce_typed(const ConvArgs& a, cudaStream_t s) {
   const long long total = a.part_total;
   const long long work = (total & 3) == 0 ? total / 4 : total;
-  long long blocks = (work + 255) / 256;
+  // small reductions in 64-thread blocks, so that they spread over more SMs
+  const int threads = work < 152LL * 256 ? 64 : 256;
+  long long blocks = (work + threads - 1) / threads;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  split_reduce<T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  split_reduce<T><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

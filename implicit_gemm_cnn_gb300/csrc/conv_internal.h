@@ -199,7 +199,9 @@ struct TransposePlan {
   int dtype;
   Plan gemm_plan;        // the CUDA-core plan of the 1x1 Gemm
   ConvArgs gemm_args;    // its geometry (addresses filled at launch)
-  size_t wt_off, cols_off, scratch_bytes;
+  size_t wt_off;          // float32 transposed weights
+  size_t xf_off;          // 16-bit types: x widened to float32
+  size_t cols_off, scratch_bytes;
 };
 cudaError_t launch_conv_transpose(const TransposePlan& tp, const ConvArgs& a, const TransposeGeo& t,
                                   const void* w, void* scratch, cudaStream_t s);
