@@ -343,37 +343,35 @@ def run_ours(L, steps: int, warmup: int, world: int, rank: int, local_rank: int,
 
 
 def e2e_rate(L, p, t, need, steps, dev) -> dict:
-    """Through the public API: pinned host input -> device, conv2d, result ->
-    pinned host, every step."""
+    """Through the public API, every step: the step's x from pinned host memory
+    to the device, the convolution, its y back to pinned host memory.  The
+    library's HostPipeline overlaps one step's copies with its neighbours'
+    convolutions (three streams, two device buffers each of x and y)."""
     import torch
 
     import implicit_gemm_cnn_gb300 as conv
     x_host = t["x"].cpu().pin_memory()
-    y_host = torch.empty(t["y"].shape, dtype=t["y"].dtype).pin_memory()
-    x_dev = torch.empty_like(t["x"])
+    y_hosts = [torch.empty(t["y"].shape, dtype=t["y"].dtype).pin_memory() for _ in range(2)]
     geo = dict(stride=L.stride, pads=L.pads, dilation=L.dilation, groups=L.groups, act=L.act,
                alpha=L.alpha, beta=L.beta)
-    scratch = t["scratch"] if need else None
+    pipe = conv.HostPipeline(tuple(t["x"].shape), t["w"], t["bias"], t["residual"], **geo)
 
-    def step():
-        x_dev.copy_(x_host, non_blocking=True)
-        conv.conv2d(x_dev, t["w"], t["bias"], t["residual"], out=t["y"], scratch=scratch, **geo)
-        y_host.copy_(t["y"], non_blocking=True)
+    def run(n):
+        pipe.run([x_host] * n, [y_hosts[i % 2] for i in range(n)])
 
-    for _ in range(3):
-        step()
+    run(4)
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
-    for _ in range(steps):
-        step()
+    run(steps)
     e1.record(s)
     torch.cuda.synchronize()
     secs = e0.elapsed_time(e1) / 1e3
     return {"value": layer_flops(L) * steps / secs / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
-            "d2h_bytes_per_step": y_host.numel() * y_host.element_size(), "steps": steps}
+            "d2h_bytes_per_step": y_hosts[0].numel() * y_hosts[0].element_size(), "steps": steps,
+            "overlap": "HostPipeline: copies of one step overlap the neighbouring steps' convolutions"}
 
 
 # ---- the CPU oracle (reported baseline / reference arm) -------------------

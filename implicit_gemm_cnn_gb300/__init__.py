@@ -30,7 +30,7 @@ __all__ = [
     "conv_integer_scratch_bytes", "conv_integer_forward", "conv_integer2d", "INT_TYPES",
     "ConvTransposeProblem", "make_transpose_problem", "conv_transpose_output_shape",
     "conv_transpose_scratch_bytes", "conv_transpose_forward", "conv_transpose2d",
-    "make_problem", "conv2d", "library_path", "load",
+    "make_problem", "conv2d", "HostPipeline", "library_path", "load",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -370,6 +370,69 @@ def conv_selftest_bounded_wait(limit_us: int = 1000) -> list[int]:
     report = (ctypes.c_uint32 * 5)()
     _check(load().conv_selftest_bounded_wait(int(limit_us), report), "conv_selftest_bounded_wait")
     return list(report)
+
+
+
+class HostPipeline:
+    """conv2d over batches that live in (pinned) host memory, with the copies
+    overlapped: the host->device copy of one batch, the convolution of the
+    previous one and the device->host copy of the one before run at the same
+    time on three CUDA streams, over two device buffers of x and of y used in
+    turn.  Each batch's result is the one conv2d gives.  w, bias and residual
+    are device tensors shared by every batch; the scratch is allocated once.
+
+    ``run`` enqueues and returns; the caller's current stream waits for all of
+    it, so a synchronize (or any later work on that stream) sees the results.
+    """
+
+    def __init__(self, x_shape, w, bias=None, residual=None, *, stride=1, pads=0, dilation=1, groups=1,
+                 act="identity", alpha=0.0, beta=0.0, flags=0, auto_pad="NOTSET"):
+        import torch
+        self._torch = torch
+        dt = _dtype_name(w)
+        self.p = make_problem(tuple(x_shape), w.shape, dtype=dt, stride=stride, pads=pads, dilation=dilation,
+                              groups=groups, act=act, alpha=alpha, beta=beta, has_bias=bias is not None,
+                              has_residual=residual is not None, flags=flags, auto_pad=auto_pad)
+        ho, wo = conv_output_shape(self.p)
+        dev = w.device
+        self.w, self.bias, self.residual = w, bias, residual
+        self.x_dev = [torch.empty(tuple(x_shape), dtype=w.dtype, device=dev) for _ in range(2)]
+        self.y_dev = [torch.empty((self.p.n, self.p.c_out, ho, wo), dtype=w.dtype, device=dev) for _ in range(2)]
+        self.need = conv_scratch_bytes(self.p)
+        self.scratch = torch.empty(self.need, dtype=torch.uint8, device=dev) if self.need else None
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_comp = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+        self.turn = 0
+
+    def run(self, x_hosts, y_hosts) -> None:
+        torch = self._torch
+        cur = torch.cuda.current_stream()
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.wait_stream(cur)
+        for xh, yh in zip(x_hosts, y_hosts):
+            b = self.turn
+            self.turn ^= 1
+            with torch.cuda.stream(self.s_in):
+                if self.used[b]:
+                    self.s_in.wait_event(self.ev_comp[b])  # the convolution that read x_dev[b] is done
+                self.x_dev[b].copy_(xh, non_blocking=True)
+                self.ev_in[b].record(self.s_in)
+            self.s_comp.wait_event(self.ev_in[b])
+            if self.used[b]:
+                self.s_comp.wait_event(self.ev_out[b])  # y_dev[b] has been copied out
+            conv_forward(self.p, self.x_dev[b], self.w, self.bias, self.residual, self.y_dev[b], self.scratch,
+                         self.need, self.s_comp)
+            self.ev_comp[b].record(self.s_comp)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(self.ev_comp[b])
+                yh.copy_(self.y_dev[b], non_blocking=True)
+                self.ev_out[b].record(self.s_out)
+            self.used[b] = True
+        for s in (self.s_in, self.s_comp, self.s_out):
+            cur.wait_stream(s)
 
 
 # ---- conveniences ---------------------------------------------------------

@@ -283,3 +283,27 @@ def test_winograd_parity(xs, ws, g, res):
     out = check_full(inp, "f32", y, **g)
     assert out["ok"], out
     assert out["max_scaled_err"] < 1e-5, out
+
+
+# ---- host batches with the copies overlapped -------------------------------------
+@pytest.mark.parametrize("dtype,xs,ws,geo,res", [
+    ("f32", (2, 16, 18, 20), (24, 16, 3, 3), dict(pads=1, act="relu"), True),
+    ("f16", (2, 16, 16, 16), (32, 16, 3, 3), dict(pads=1, act="silu"), False),
+])
+def test_host_pipeline_matches_conv2d(dtype, xs, ws, geo, res):
+    """HostPipeline over five host batches gives, bit for bit, what conv2d
+    gives on each batch (two device buffers in turn, three streams)."""
+    tdt = {"f32": torch.float32, "f16": torch.float16}[dtype]
+    w = random_layer_inputs(xs, ws, dtype, seed=5, bias=True)["w"].cuda()
+    b = random_layer_inputs(xs, ws, dtype, seed=6, bias=True)["bias"].cuda()
+    ho, wo = conv.conv_output_shape(conv.make_problem(xs, ws, dtype=dtype, **{k: v for k, v in geo.items() if k != "act"}))
+    r = torch.randn((xs[0], ws[0], ho, wo), generator=torch.Generator().manual_seed(9)).to(tdt).cuda() if res else None
+    xh = [torch.randn(xs, generator=torch.Generator().manual_seed(100 + i)).to(tdt).pin_memory() for i in range(5)]
+    yh = [torch.empty((xs[0], ws[0], ho, wo), dtype=tdt).pin_memory() for _ in range(5)]
+    pipe = conv.HostPipeline(xs, w, b, r, **geo)
+    pipe.run(xh, yh)
+    torch.cuda.synchronize()
+    for i in range(5):
+        ref = conv.conv2d(xh[i].cuda(), w, b, r, **geo)
+        torch.cuda.synchronize()
+        assert torch.equal(yh[i], ref.cpu()), i
