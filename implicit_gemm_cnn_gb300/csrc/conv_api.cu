@@ -309,6 +309,28 @@ bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
     if (d.cols4_r && 4LL * (2 * pitch * rows * es + outs) > 45 * 1024) d.cols4_r = 0;  // five blocks per SM
     if (p->n * p->c_out > 2000000000LL) d.cols4_r = 0;  // plane indices (and the stride past them) in 32 bits
   }
+  // 16-bit planes up to 64 columns wide on the tensor cores (band matrices,
+  // mma.sync): the staged plane per warp, 16-byte rows with an odd number of
+  // 16-byte units per row (conflict-free ldmatrix), eight warps, two buffers
+  d.mma = 0;
+  d.mma_pitch = d.mma_rows = 0;
+  if (p->dtype != CONV_F32 && !(p->flags & CONV_FLAG_NO_DW_MMA) && p->stride_h == 1 && p->stride_w == 1 &&
+      p->dil_h == 1 && p->dil_w == 1 && p->kh == p->kw && (p->kh == 3 || p->kh == 5 || p->kh == 7) &&
+      s.wo <= 64 && p->n * p->c_out < 2000000000LL && p->n < 2000000000LL) {
+    long long ntiles = (s.wo + 7) / 8;  // compiled for 1, 2, 4 or 8 column blocks
+    ntiles = ntiles <= 1 ? 1 : ntiles <= 2 ? 2 : ntiles <= 4 ? 4 : 8;
+    const long long mtiles = (s.ho + 15) / 16;
+    const long long delta = p->pad_left & 1;
+    long long pitch = std::max<long long>(8 * ntiles + 8, p->pad_left + delta + p->w);
+    pitch = (pitch + 7) / 8 * 8;
+    if ((pitch / 8) % 2 == 0) pitch += 8;
+    const long long rows = 16 * mtiles + p->kh - 1;
+    if (8LL * 2 * pitch * rows * 2 <= 110 * 1024) {
+      d.mma = 1;
+      d.mma_pitch = static_cast<int>(pitch);
+      d.mma_rows = static_cast<int>(rows);
+    }
+  }
   out->dw = d;
   out->info.variant = CONV_VARIANT_DEPTHWISE;
   out->info.split_k = 1;
@@ -648,6 +670,11 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
              "%s grouped: input rows staged once per (group, image, %d output rows), %d staged rows of %d, "
              "8co x 4px per thread, items=%lld sms=%d",
              variant_name(i.variant), kGdRows, plan.gd.rows_in, plan.gd.pitch, static_cast<long long>(plan.gd.items), sm);
+  } else if (i.variant == CONV_VARIANT_DEPTHWISE && plan.dw.mma) {
+    snprintf(buf, len,
+             "%s tensor cores: per channel %d band matrices, mma.sync m16n8k16 over 16 x 8 output blocks, "
+             "one warp per plane, staged plane %dx%d sms=%d",
+             variant_name(i.variant), static_cast<int>(p->kh), plan.dw.mma_rows, plan.dw.mma_pitch, sm);
   } else if (i.variant == CONV_VARIANT_DEPTHWISE && plan.dw.cols4_r) {
     snprintf(buf, len, "%s one warp per plane, 4 columns x %d rows per lane, double-buffered planes sms=%d",
              variant_name(i.variant), plan.dw.cols4_r, sm);

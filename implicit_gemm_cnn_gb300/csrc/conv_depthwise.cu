@@ -30,6 +30,7 @@
 // copied while the current one is computed -- four output columns per lane
 // where the plane's rows divide among the lanes, else one column per lane.
 #include <algorithm>
+#include <type_traits>
 
 #include "conv_internal.h"
 
@@ -628,6 +629,287 @@ __global__ void __launch_bounds__(kC4Warps * 32, 5) depthwise_cols4(const ConvAr
   cp_async_wait<0>();
 }
 
+// ---- 16-bit depthwise planes on the tensor cores ---------------------------
+// With Xp the zero-padded input plane (stride 1, dilation 1), output row oh of
+// a depthwise plane is sum_u Xp[oh + u][:] . T_u, where T_u[j][ow] =
+// w[u][j - ow] (zero outside 0 .. K-1): K products with band matrices.  The
+// plane sits in shared memory with padded column j at staged column
+// j + delta (delta = 0 or 1, so image column 0 starts on a 4-byte boundary).
+// A block of 8 output columns 8nt .. 8nt+7 reads staged columns
+// 8nt .. 8nt + 7 + K - 1 + delta < 8nt + 16, so each (kernel row u, block of
+// 16 output rows mt, block of 8 output columns nt) is one
+// mma.sync.m16n8k16 with float32 accumulation: A = staged rows
+// 16mt + u .. 16mt + u + 15, columns 8nt .. 8nt + 15 (ldmatrix), and B_u[k][n]
+// = w[u][k - n - delta], the same for every column block, held in registers
+// per channel (two per kernel row).  Products of 16-bit values are exact in
+// float32; the sums run in the MMA's float32 order.  Then bias, residual and
+// activation in float32, one rounding.  One warp per plane at a time, planes
+// in channel-major order (a warp's planes share their band matrices), the
+// next plane staged by cp.async while this one is computed.
+struct DwMmaGeo {
+  int pitch;   // staged row length in elements: a multiple of 8 with pitch / 8 odd (conflict-free ldmatrix)
+  int rows;    // staged rows: mtiles * 16 + K - 1
+  int mtiles;  // blocks of 16 output rows
+  int ntiles;  // blocks of 8 output columns computed: 1, 2, 4 or 8 (those past Wo are dropped)
+  int delta;   // staged column of padded column j: j + delta
+  int copy4;   // 4-byte cp.async copies of image rows (else element copies)
+  int pair_out;  // two outputs per store (Wo even, y and the residual 4-byte aligned)
+  long long warps;  // warps sharing the planes (contiguous runs in channel-major order)
+};
+constexpr int kDmWarps = 8;
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack_t2(T lo, T hi) {
+  return static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&lo)) |
+         (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&aq)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same<T, __half>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(aq[0]), "r"(aq[1]), "r"(aq[2]), "r"(aq[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(aq[0]), "r"(aq[1]), "r"(aq[2]), "r"(aq[3]), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+template <typename T, int K, int NT>
+__global__ void __launch_bounds__(kDmWarps * 32, NT >= 4 ? 2 : 3) depthwise_mma(const ConvArgs a, const DwMmaGeo g) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bufsz = g.pitch * g.rows;  // elements of one staged plane
+  T* buf0 = reinterpret_cast<T*>(dsm) + static_cast<size_t>(warp) * 2 * bufsz;
+  {  // the border stays zero (two buffers: a whole number of 16-byte units, pitch a multiple of 8)
+    uint4* z = reinterpret_cast<uint4*>(buf0);
+    const int units16 = 2 * bufsz * static_cast<int>(sizeof(T)) / 16;
+    for (int i = lane; i < units16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncwarp();
+  const T* __restrict__ xg = static_cast<const T*>(a.x);
+  const T* __restrict__ wg = static_cast<const T*>(a.wt);
+  const T* __restrict__ bg = static_cast<const T*>(a.bias);
+  const T* __restrict__ rg = static_cast<const T*>(a.residual);
+  T* __restrict__ y = static_cast<T*>(a.y);
+  // this warp's planes: an even share of the planes in channel-major order
+  const long long planes = static_cast<long long>(a.n) * a.c_out;
+  const long long gw = static_cast<long long>(blockIdx.x) * kDmWarps + warp;
+  const long long p_begin = gw * planes / g.warps;
+  const long long p_end = (gw + 1) * planes / g.warps;
+  if (gw >= g.warps || p_begin >= p_end) return;
+  const int m = a.mg;  // channel multiplier: output channel co reads input channel co / m
+  // staging: image row r lands at staged row pt + r, image column c at staged
+  // column pl + delta + c
+  const int rows_s = min(a.h, g.rows - a.pt);
+  const int col0 = a.pl + g.delta;
+  const int wq = a.w / 2;  // 4-byte copies per image row
+  // with at most 32 copies per image row a lane's copies are one column pair
+  // and rows r0, r0 + rpp, ...: constant shared and global strides
+  const bool prog = g.copy4 && wq <= 32;
+  const int rpp = prog ? 32 / wq : 1, r0 = prog ? lane / wq : 0, q0 = prog ? lane - (lane / wq) * wq : 0;
+  const int ncp = prog && r0 < rpp && rows_s > r0 ? (rows_s - r0 + rpp - 1) / rpp : 0;
+  const uint32_t dst_first = static_cast<uint32_t>(((a.pt + r0) * g.pitch + col0 + 2 * q0) * sizeof(T));
+  const uint32_t dst_step = static_cast<uint32_t>(rpp * g.pitch * sizeof(T));
+  const long long src_first = (static_cast<long long>(r0) * a.w + 2 * q0) * static_cast<long long>(sizeof(T));
+  const long long src_step = static_cast<long long>(rpp) * a.w * static_cast<long long>(sizeof(T));
+  auto stage = [&](int n, int co, T* buf) {
+    const T* src = xg + (static_cast<long long>(n) * a.c_in + (m == 1 ? co : co / m)) * a.hw;
+    if (prog) {
+      cp_async_run<4>(static_cast<uint32_t>(__cvta_generic_to_shared(buf)) + dst_first,
+                      reinterpret_cast<const char*>(src) + src_first, ncp, dst_step, src_step);
+      return;
+    }
+    T* dst = buf + a.pt * g.pitch + col0;
+    if (g.copy4) {
+      {
+        for (int r = 0; r < rows_s; ++r)
+          for (int q = lane; q < wq; q += 32) cp_async_n<4>(dst + r * g.pitch + 2 * q, src + r * a.w + 2 * q);
+      }
+    } else {
+      for (int r = 0; r < rows_s; ++r)
+        for (int c = lane; c < a.w; c += 32) dst[r * g.pitch + c] = src[r * a.w + c];
+    }
+  };
+  // band matrices of channel co: thread t holds B_u[k][n] for n = t / 4 and
+  // k = 2(t % 4) + {0, 1} (bq[u][0]) and + 8 (bq[u][1])
+  uint32_t bq[K][2];
+  int bq_co = -1;
+  auto build_b = [&](int co) {
+    const T* wc = wg + static_cast<long long>(co) * K * K;
+    const int nn = lane >> 2, k0 = 2 * (lane & 3);
+#pragma unroll
+    for (int u = 0; u < K; ++u) {
+      T e[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = k0 + (i & 1) + (i >> 1) * 8;
+        const int d = k - nn - g.delta;
+        e[i] = (d >= 0 && d < K) ? wc[u * K + d] : from_f32<T>(0.0f);
+      }
+      bq[u][0] = pack_t2<T>(e[0], e[1]);
+      bq[u][1] = pack_t2<T>(e[2], e[3]);
+    }
+    bq_co = co;
+  };
+  // plane pl = co * N + n
+  int co = static_cast<int>(p_begin / a.n), n = static_cast<int>(p_begin - static_cast<long long>(co) * a.n);
+  stage(n, co, buf0);
+  cp_async_commit();
+  // accumulator (t, q): output row 16 mt + lane / 4 (+ 8 for q >= 2), column
+  // 8 t + 2 (lane % 4) + (q & 1)
+  const int ow_l = 2 * (lane & 3);
+  int k = 0;
+  for (long long pl = p_begin; pl < p_end; ++pl, ++k) {
+    T* buf = buf0 + (k & 1) * bufsz;
+    int n_next = n + 1, co_next = co;
+    if (n_next == a.n) { n_next = 0; ++co_next; }
+    if (pl + 1 < p_end) stage(n_next, co_next, buf0 + ((k + 1) & 1) * bufsz);
+    cp_async_commit();
+    if (co != bq_co) build_b(co);
+    cp_async_wait<1>();  // this plane's copies (the next plane's may still fly)
+    __syncwarp();
+    const float bv = bg ? to_f32(bg[co]) : 0.0f;
+    const long long pbase = (static_cast<long long>(n) * a.c_out + co) * a.howo;
+    // ldmatrix row address of this lane: staged row (lane & 15) of the block,
+    // columns 8 (lane >> 4) ..
+    const uint32_t lane_addr = static_cast<uint32_t>(__cvta_generic_to_shared(buf)) +
+                               static_cast<uint32_t>(((lane & 15) * g.pitch + (lane >> 4) * 8) * sizeof(T));
+    // two blocks of 16 rows at a time: 2 * NT independent accumulators
+    for (int mt0 = 0; mt0 < g.mtiles; mt0 += 2) {
+      const bool second = mt0 + 1 < g.mtiles;
+      float acc[2][NT][4];
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[b][t][q] = 0.0f;
+#pragma unroll
+      for (int u = 0; u < K; ++u) {
+        const uint32_t rowa = lane_addr + static_cast<uint32_t>((mt0 * 16 + u) * g.pitch * sizeof(T));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          uint32_t aq[4];
+          ldmatrix_x4(aq, rowa + static_cast<uint32_t>(t * 8 * sizeof(T)));
+          mma_16816<T>(acc[0][t], aq, bq[u][0], bq[u][1]);
+        }
+        if (second) {
+          const uint32_t rowb = rowa + static_cast<uint32_t>(16 * g.pitch * sizeof(T));
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            uint32_t aq[4];
+            ldmatrix_x4(aq, rowb + static_cast<uint32_t>(t * 8 * sizeof(T)));
+            mma_16816<T>(acc[1][t], aq, bq[u][0], bq[u][1]);
+          }
+        }
+      }
+      // the epilogue: bias, residual, activation over a block's outputs at
+      // once (one dispatch), then the stores
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        if (b == 1 && !second) break;
+        const int oh0 = (mt0 + b) * 16 + (lane >> 2);
+        float* v = &acc[b][0][0];
+        float bb[NT * 4], rr[NT * 4];
+#pragma unroll
+        for (int i = 0; i < NT * 4; ++i) { bb[i] = bv; rr[i] = 0.0f; }
+        if (rg) {
+#pragma unroll
+          for (int i = 0; i < NT * 4; ++i) {
+            const int oh = oh0 + 8 * ((i & 3) >> 1), ow = 8 * (i >> 2) + ow_l + (i & 1);
+            if (oh < a.ho && ow < a.wo) rr[i] = to_f32(rg[pbase + static_cast<long long>(oh) * a.wo + ow]);
+          }
+        }
+        epilogue_n<NT * 4>(*reinterpret_cast<float(*)[NT * 4]>(v), bb, rr, bg != nullptr, rg != nullptr, a.act,
+                           a.alpha, a.beta);
+        T* yrow = y + pbase + static_cast<long long>(oh0) * a.wo + ow_l;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (oh0 + 8 * h >= a.ho) continue;
+          T* yr = yrow + 8 * h * a.wo;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int ow = 8 * t + ow_l;
+            if (ow >= a.wo) continue;
+            const float v0 = acc[b][t][2 * h], v1 = acc[b][t][2 * h + 1];
+            if (g.pair_out) {  // Wo even: ow + 1 < Wo too
+              *reinterpret_cast<uint32_t*>(yr + 8 * t) = pack_t2<T>(from_f32<T>(v0), from_f32<T>(v1));
+            } else {
+              yr[8 * t] = from_f32<T>(v0);
+              if (ow + 1 < a.wo) yr[8 * t + 1] = from_f32<T>(v1);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();  // this buffer is read; it is refilled two planes on
+    n = n_next;
+    co = co_next;
+  }
+  cp_async_wait<0>();
+}
+
+template <typename T, int K, int NT>
+cudaError_t launch_mma_nt(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  DwMmaGeo g;
+  g.pitch = d.mma_pitch;
+  g.rows = d.mma_rows;
+  g.mtiles = (a.ho + 15) / 16;
+  g.ntiles = NT;
+  g.delta = a.pl & 1;
+  g.copy4 = (a.w % 2 == 0) && (a.hw % 2 == 0) && reinterpret_cast<uintptr_t>(a.x) % 4 == 0;
+  g.pair_out = (a.wo % 2 == 0) && reinterpret_cast<uintptr_t>(a.y) % 4 == 0 &&
+               (!a.residual || reinterpret_cast<uintptr_t>(a.residual) % 4 == 0);
+  const size_t smem = static_cast<size_t>(kDmWarps) * 2 * g.pitch * g.rows * sizeof(T);
+  auto kern = depthwise_mma<T, K, NT>;
+  cudaError_t err = opt_in_smem(reinterpret_cast<const void*>(kern), smem);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDmWarps * 32, smem);
+  if (err != cudaSuccess) return err;
+  const long long planes = static_cast<long long>(a.n) * a.c_out;
+  // every resident warp slot of the device, or one warp per plane
+  const long long slots = static_cast<long long>(d.sm) * std::max(per_sm, 1);
+  const long long blocks = std::min<long long>(slots, (planes + kDmWarps - 1) / kDmWarps);
+  g.warps = std::min<long long>(planes, blocks * kDmWarps);
+  kern<<<static_cast<unsigned>(blocks), kDmWarps * 32, smem, s>>>(a, g);
+  return cudaGetLastError();
+}
+
+template <typename T, int K>
+cudaError_t launch_mma_k(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  const int nt = (a.wo + 7) / 8;  // compiled for 1, 2, 4 or 8 column blocks (extra blocks are masked)
+  if (nt <= 1) return launch_mma_nt<T, K, 1>(d, a, s);
+  if (nt <= 2) return launch_mma_nt<T, K, 2>(d, a, s);
+  if (nt <= 4) return launch_mma_nt<T, K, 4>(d, a, s);
+  return launch_mma_nt<T, K, 8>(d, a, s);
+}
+
+template <typename T>
+cudaError_t launch_mma(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  if constexpr (std::is_same<T, float>::value) {
+    return cudaErrorInvalidValue;  // 16-bit operands only
+  } else {
+    if (a.kh == 3) return launch_mma_k<T, 3>(d, a, s);
+    if (a.kh == 5) return launch_mma_k<T, 5>(d, a, s);
+    if (a.kh == 7) return launch_mma_k<T, 7>(d, a, s);
+    return cudaErrorInvalidValue;
+  }
+}
+
 // Rows per lane the four-column kernel is compiled for.
 constexpr int kCols4Rows[] = {2, 4, 7, 8};
 
@@ -719,6 +1001,7 @@ cudaError_t launch_kh(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_typed(const DwPlan& d, const ConvArgs& a, cudaStream_t s) {
+  if (d.mma) return launch_mma<T>(d, a, s);
   if (d.cols4_r) {
     if (a.kh == 3) return launch_cols4<T, 3>(d, a, s);
     if (a.kh == 5) return launch_cols4<T, 5>(d, a, s);

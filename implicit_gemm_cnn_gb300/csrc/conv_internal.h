@@ -71,6 +71,8 @@ struct DwPlan {
   int sm;        // SMs of the device (blocks loop over the work items)
   int narrow;    // one warp per plane (stride 1, dilation 1, square 3/5/7, Wo <= 32)
   int cols4_r;   // narrow planes, four columns per lane: output rows per lane (2, 4, 7, 8), 0: not used
+  int mma;       // 16-bit planes on the tensor cores (band-matrix mma.sync), one warp per plane
+  int mma_pitch, mma_rows;  // its staged plane: row length (elements) and rows
 };
 size_t depthwise_smem_bytes(const DwPlan& d, int mg, int kh, int kw, int dtype);
 

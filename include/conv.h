@@ -87,6 +87,8 @@ typedef enum conv_act {
 #define CONV_FLAG_WINOGRAD 0x20u     /* Winograd F(2x2,3x3) wherever it applies (float32,
                                         3x3, stride 1, dilation 1, one group)      */
 #define CONV_FLAG_NO_WINOGRAD 0x40u  /* never Winograd                                 */
+#define CONV_FLAG_NO_DW_MMA 0x80u    /* 16-bit depthwise: the CUDA-core kernels, not the
+                                        tensor-core band-matrix kernel              */
 #define CONV_FLAG_SPLIT_K_SHIFT 8   /* bits 8..13: force this many ranges of k (1-63) */
 #define CONV_FLAG_SPLIT_K_MASK 0x3f00u
 

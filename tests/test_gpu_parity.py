@@ -189,6 +189,9 @@ def _edge_params():
             out.append(pytest.param(case, dtype, "auto", id=f"auto-{name}-{dtype}"))
             if dtype != "f32" or name.startswith("depthwise"):
                 out.append(pytest.param(case, dtype, "ffma", id=f"ffma-{name}-{dtype}"))
+            if dtype != "f32" and name.startswith("depthwise"):
+                # the CUDA-core depthwise kernels in place of the tensor-core one
+                out.append(pytest.param(case, dtype, "dwcc", id=f"dwcc-{name}-{dtype}"))
             if dtype != "f32" and name.startswith("win_"):
                 out.append(pytest.param(case, dtype, "gather", id=f"gather-{name}-{dtype}"))
             g = case[3]
@@ -208,13 +211,16 @@ def test_edge_cases(case, dtype, path):
     rs = (xs[0], ws[0], ho, wo) if res else None
     inp = random_layer_inputs(xs, ws, dtype, seed=zlib.crc32(name.encode()) % 10000, bias=bias, residual_shape=rs)
     flags = {"auto": 0, "ffma": conv.FLAG_FORCE_FFMA, "gather": conv.FLAG_NO_WINDOW,
-             "unfold": conv.FLAG_FORCE_FFMA | conv.FLAG_FORCE_UNFOLD}[path]
+             "unfold": conv.FLAG_FORCE_FFMA | conv.FLAG_FORCE_UNFOLD, "dwcc": conv.FLAG_NO_DW_MMA}[path]
     if name.startswith("win_") and dtype != "f32" and path == "auto":
         desc = conv.conv_describe_variant(p)
         assert desc.startswith("igemm_tcgen05_window"), desc
     if path == "unfold":
         desc = conv.conv_describe_variant(conv.make_problem(xs, ws, dtype=dtype, flags=flags, **g))
         assert "B=unfolded" in desc, desc
+    if path == "dwcc":
+        desc = conv.conv_describe_variant(conv.make_problem(xs, ws, dtype=dtype, flags=flags, **g))
+        assert desc.startswith("depthwise_halo") and "tensor cores" not in desc, desc
     if name.startswith("gd_") and dtype == "f32" and path == "auto":
         desc = conv.conv_describe_variant(p)
         assert desc.startswith("igemm_ffma grouped"), desc
@@ -253,6 +259,20 @@ def test_bit_identical_runs(name):
     b = run_gpu(inp, **_geo(L))
     assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a.view(torch.int32),
                        b.view(torch.int16) if b.dtype != torch.float32 else b.view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_depthwise_16bit_on_tensor_cores(dtype):
+    """16-bit depthwise planes with stride 1 take the band-matrix tensor-core
+    kernel (the MobileNetV3 layer's shape, reduced batch), all outputs against
+    the oracle; the same shape in float32 stays on the CUDA cores."""
+    L = dataclasses.replace(_reduced(LAYERS["mbv3_dw5x5_f16"]), dtype=dtype)
+    assert "tensor cores" in conv.conv_describe_variant(_problem(L))
+    assert "tensor cores" not in conv.conv_describe_variant(_problem(dataclasses.replace(L, dtype="f32")))
+    inp = make_inputs(L)
+    y = run_gpu(inp, **_geo(L))
+    res = check_full(inp, L.dtype, y, **_geo(L))
+    assert res["ok"], res
 
 
 def test_device_error_word_clear():
