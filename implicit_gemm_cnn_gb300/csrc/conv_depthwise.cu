@@ -688,7 +688,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
 }
 
 template <typename T, int K, int NT>
-__global__ void __launch_bounds__(kDmWarps * 32, NT >= 4 ? 2 : 3) depthwise_mma(const ConvArgs a, const DwMmaGeo g) {
+__global__ void __launch_bounds__(kDmWarps * 32, NT >= 2 ? 2 : 3) depthwise_mma(const ConvArgs a, const DwMmaGeo g) {
   extern __shared__ __align__(16) unsigned char dsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bufsz = g.pitch * g.rows;  // elements of one staged plane
@@ -797,23 +797,26 @@ __global__ void __launch_bounds__(kDmWarps * 32, NT >= 4 ? 2 : 3) depthwise_mma(
         for (int t = 0; t < NT; ++t)
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[b][t][q] = 0.0f;
+      // per kernel row: the fragment loads first, then the MMAs (the asm
+      // statements keep their order, so this is the order they issue in)
 #pragma unroll
       for (int u = 0; u < K; ++u) {
         const uint32_t rowa = lane_addr + static_cast<uint32_t>((mt0 * 16 + u) * g.pitch * sizeof(T));
+        uint32_t aq[NT][4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          uint32_t aq[4];
-          ldmatrix_x4(aq, rowa + static_cast<uint32_t>(t * 8 * sizeof(T)));
-          mma_16816<T>(acc[0][t], aq, bq[u][0], bq[u][1]);
-        }
+        for (int t = 0; t < NT; ++t) ldmatrix_x4(aq[t], rowa + static_cast<uint32_t>(t * 8 * sizeof(T)));
         if (second) {
           const uint32_t rowb = rowa + static_cast<uint32_t>(16 * g.pitch * sizeof(T));
+          uint32_t aq2[NT][4];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            uint32_t aq[4];
-            ldmatrix_x4(aq, rowb + static_cast<uint32_t>(t * 8 * sizeof(T)));
-            mma_16816<T>(acc[1][t], aq, bq[u][0], bq[u][1]);
-          }
+          for (int t = 0; t < NT; ++t) ldmatrix_x4(aq2[t], rowb + static_cast<uint32_t>(t * 8 * sizeof(T)));
+#pragma unroll
+          for (int t = 0; t < NT; ++t) mma_16816<T>(acc[0][t], aq[t], bq[u][0], bq[u][1]);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) mma_16816<T>(acc[1][t], aq2[t], bq[u][0], bq[u][1]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) mma_16816<T>(acc[0][t], aq[t], bq[u][0], bq[u][1]);
         }
       }
       // the epilogue: bias, residual, activation over a block's outputs at

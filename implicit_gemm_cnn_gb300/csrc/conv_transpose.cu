@@ -88,21 +88,35 @@ __global__ void __launch_bounds__(256) col2im_rows(const ConvArgs a, const Trans
       const int tw0 = ow + a.pl;
       const int qw0 = tw0 / a.sw, rw0 = tw0 - (tw0 / a.sw) * a.sw;
       float acc = 0.0f;
-      int qh = qh0, rh = rh0;
-      for (int u = 0; u < a.kh; ++u) {
-        if (rh == 0 && qh >= 0 && qh < a.h) {
-          const float* brow = base + static_cast<long long>(u) * a.kw * a.hw + static_cast<long long>(qh) * a.w;
-          int qw = qw0, rw = rw0;
-          for (int v = 0; v < a.kw; ++v) {
-            if (rw == 0 && qw >= 0 && qw < a.w) acc = __fadd_rn(acc, brow[static_cast<long long>(v) * a.hw + qw]);
-            rw -= dwr;
-            qw -= dwq;
-            if (rw < 0) { rw += a.sw; qw -= 1; }
+      if (a.dh == 1 && a.dw == 1) {
+        // dilation 1: the taps used are u = rh0, rh0 + sh, ... (input rows qh0,
+        // qh0 - 1, ...) and v = rw0, rw0 + sw, ... -- visited directly, in (u, v) order
+        for (int u = rh0, ih = qh0; u < a.kh; u += a.sh, --ih) {
+          if (ih < 0) break;
+          if (ih >= a.h) continue;
+          const float* brow = base + static_cast<long long>(u) * a.kw * a.hw + static_cast<long long>(ih) * a.w;
+          for (int v = rw0, iw = qw0; v < a.kw; v += a.sw, --iw) {
+            if (iw < 0) break;
+            if (iw < a.w) acc = __fadd_rn(acc, brow[static_cast<long long>(v) * a.hw + iw]);
           }
         }
-        rh -= dhr;
-        qh -= dhq;
-        if (rh < 0) { rh += a.sh; qh -= 1; }
+      } else {
+        int qh = qh0, rh = rh0;
+        for (int u = 0; u < a.kh; ++u) {
+          if (rh == 0 && qh >= 0 && qh < a.h) {
+            const float* brow = base + static_cast<long long>(u) * a.kw * a.hw + static_cast<long long>(qh) * a.w;
+            int qw = qw0, rw = rw0;
+            for (int v = 0; v < a.kw; ++v) {
+              if (rw == 0 && qw >= 0 && qw < a.w) acc = __fadd_rn(acc, brow[static_cast<long long>(v) * a.hw + qw]);
+              rw -= dwr;
+              qw -= dwq;
+              if (rw < 0) { rw += a.sw; qw -= 1; }
+            }
+          }
+          rh -= dhr;
+          qh -= dhq;
+          if (rh < 0) { rh += a.sh; qh -= 1; }
+        }
       }
       float v = acc;
       if (bp) v = __fadd_rn(v, bv);
