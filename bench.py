@@ -98,6 +98,8 @@ def roofline_bound(L, variant: str, pk: dict) -> tuple[str, float, str]:
         return "hbm", pk["hbm_gbs"], "GB/s"
     if variant.startswith("igemm_tcgen05"):
         compute, kind = pk["bf16_tflops"], "tensor"  # fp16 and bf16 share the dense rate
+    elif variant.startswith("pointwise_mma"):
+        compute, kind = MMA_SYNC_PEAK_TFLOPS, "tensor"  # the warp-level MMA path's own rate
     else:
         compute, kind = FFMA_PEAK_TFLOPS, "alu"
     ridge = compute * 1e12 / (pk["hbm_gbs"] * 1e9)
@@ -108,7 +110,8 @@ def roofline_bound(L, variant: str, pk: dict) -> tuple[str, float, str]:
 
 def kernel_source(variant: str) -> str:
     name = {"igemm_tcgen05": "conv_tc.cu", "igemm_tcgen05_window": "conv_tcw.cu",
-            "depthwise_halo": "conv_depthwise.cu"}.get(variant.split()[0], "conv_ffma.cu")
+            "depthwise_halo": "conv_depthwise.cu", "pointwise_mma": "conv_pointwise.cu"}.get(variant.split()[0],
+                                                                                             "conv_ffma.cu")
     return os.path.join(ROOT, "implicit_gemm_cnn_gb300", "csrc", name)
 
 
@@ -440,6 +443,10 @@ def run_reference(L, steps: int, warmup: int) -> dict:
 # clock on GB300 -- half the FP32 FFMA rate, measured at 20.0 G instructions/s
 # against 39.0 G for FFMA -- so 152 SMs x 64 x 8 ops x 2.07 GHz
 DP4A_PEAK_TOPS = 152 * 64 * 4 * 2 * 2.07e9 / 1e12
+# Warp-level mma.sync m16n8k16 (f16 in, f32 accumulate) on this GPU: 147.8 G
+# MMAs/s x 8192 FLOP = 1210 TFLOP/s, measured by a probe of independent MMA
+# chains on every SM (the rate of the kernels that use it, below tcgen05's).
+MMA_SYNC_PEAK_TFLOPS = 1210.0
 
 
 def int_layer_ops(L) -> int:

@@ -22,7 +22,7 @@ import threading
 __all__ = [
     "ConvError", "ConvLibraryError", "ConvProblem", "ConvPlanInfo", "ACTIVATIONS", "DTYPES",
     "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "FLAG_NO_UNFOLD", "FLAG_FORCE_UNFOLD", "FLAG_WINOGRAD",
-    "FLAG_NO_WINOGRAD", "FLAG_NO_DW_MMA", "VARIANTS", "conv_abi_version", "conv_status_string",
+    "FLAG_NO_WINOGRAD", "FLAG_NO_DW_MMA", "FLAG_NO_PW_MMA", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
     "conv_forward", "conv_device_error", "conv_selftest_bounded_wait", "conv_forward_fixed_scratch",
     "FIXED_SCRATCH_BYTES",
@@ -40,7 +40,7 @@ ACTIVATIONS = {"identity": 0, "relu": 1, "silu": 2, "sigmoid": 3, "tanh": 4, "ha
                "hard_sigmoid": 6, "clip": 7, "leaky_relu": 8}
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 VARIANTS = {0: "igemm_ffma", 1: "igemm_ffma_split_k", 2: "depthwise_halo", 3: "igemm_tcgen05",
-            4: "igemm_tcgen05_window", 5: "winograd_f2x2_3x3"}
+            4: "igemm_tcgen05_window", 5: "winograd_f2x2_3x3", 6: "pointwise_mma"}
 FIXED_SCRATCH_BYTES = 8 << 20  # CONV_FIXED_SCRATCH_BYTES
 FLAG_FORCE_FFMA = 0x1
 FLAG_NO_SPLIT_K = 0x2
@@ -50,6 +50,7 @@ FLAG_FORCE_UNFOLD = 0x10
 FLAG_WINOGRAD = 0x20
 FLAG_NO_WINOGRAD = 0x40
 FLAG_NO_DW_MMA = 0x80
+FLAG_NO_PW_MMA = 0x4000
 SPLIT_K_SHIFT = 8
 STATUS = {0: "CONV_OK", 1: "CONV_ERR_SHAPE", 2: "CONV_ERR_OVERFLOW", 3: "CONV_ERR_DTYPE",
           4: "CONV_ERR_ACT", 5: "CONV_ERR_NULL", 6: "CONV_ERR_SCRATCH", 7: "CONV_ERR_ALIAS",

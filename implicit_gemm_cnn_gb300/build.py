@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libconv.so")
-SOURCES = ["conv_api.cu", "conv_ffma.cu", "conv_depthwise.cu", "conv_tc.cu", "conv_tcw.cu", "conv_integer.cu", "conv_transpose.cu", "conv_winograd.cu"]
+SOURCES = ["conv_api.cu", "conv_ffma.cu", "conv_depthwise.cu", "conv_tc.cu", "conv_tcw.cu", "conv_integer.cu", "conv_transpose.cu", "conv_winograd.cu", "conv_pointwise.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -259,6 +259,36 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   }
 }
 
+// 16-bit 1x1 layers (stride 1, no padding, dilation 1, one group, Cin <=
+// 256, Cout <= 64) as channel x pixel tiles on the tensor cores, BM = the
+// channels rounded up to 16.  Wider layers stay on the shifted-window kernel
+// (its 1x1 view), which streams them better: a 64 -> 256 layer with a
+// residual measured 84 us here against 39 us there.
+bool plan_pointwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
+  (void)sm;
+  if (p->dtype == CONV_F32 || (p->flags & CONV_FLAG_NO_PW_MMA)) return false;
+  if (p->kh != 1 || p->kw != 1 || p->stride_h != 1 || p->stride_w != 1 || p->groups != 1) return false;
+  if (p->pad_top || p->pad_left || p->pad_bottom || p->pad_right) return false;
+  if (p->c_in > 256 || p->c_out > 64 || s.ho * s.wo > (1LL << 30)) return false;
+  const long long pblocks = (s.ho * s.wo + 127) / 128;
+  if (p->n * pblocks > 2000000000LL) return false;
+  PwPlan pp;
+  pp.ok = 1;
+  pp.kp = static_cast<int>((p->c_in + 15) / 16 * 16);
+  pp.cfg = static_cast<int>((p->c_out + 15) / 16);
+  const int bm = 16 * pp.cfg;
+  if ((p->c_out + bm - 1) / bm > 65535) return false;
+  if (pw_smem_bytes(pp) > 110 * 1024) return false;  // two blocks per SM
+  out->pw = pp;
+  out->info.variant = CONV_VARIANT_POINTWISE_MMA;
+  out->info.split_k = 1;
+  out->info.tile_m = bm;
+  out->info.tile_n = 128;
+  out->info.ctas = p->n * pblocks * ((p->c_out + bm - 1) / bm);
+  out->info.scratch_bytes = 0;
+  return true;
+}
+
 bool plan_depthwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   constexpr int QH = 8;                       // output rows per thread (one column)
   const int es = p->dtype == CONV_F32 ? 4 : 2;
@@ -455,6 +485,7 @@ conv_status make_plan(const conv_problem* p, int sm, Plan* out, Shape* shape) {
     }
   }
   if (!done && !force_ffma && s.cg == 1) done = plan_depthwise(p, s, sm, out);
+  if (!done && !force_ffma) done = plan_pointwise(p, s, sm, out);
   if (!done && !force_ffma) done = plan_tc(p, s, sm, out);
   if (!done) plan_ffma(p, s, sm, out);
   if (shape) *shape = s;
@@ -507,6 +538,7 @@ const char* variant_name(int v) {
     case CONV_VARIANT_IGEMM_TC: return "igemm_tcgen05";
     case CONV_VARIANT_IGEMM_TC_WINDOW: return "igemm_tcgen05_window";
     case CONV_VARIANT_WINOGRAD: return "winograd_f2x2_3x3";
+    case CONV_VARIANT_POINTWISE_MMA: return "pointwise_mma";
     default: return "unknown";
   }
 }
@@ -670,6 +702,10 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
              "%s grouped: input rows staged once per (group, image, %d output rows), %d staged rows of %d, "
              "8co x 4px per thread, items=%lld sms=%d",
              variant_name(i.variant), kGdRows, plan.gd.rows_in, plan.gd.pitch, static_cast<long long>(plan.gd.items), sm);
+  } else if (i.variant == CONV_VARIANT_POINTWISE_MMA) {
+    snprintf(buf, len,
+             "%s tile=%dco x 128px (one image), k=%d in shared memory, mma.sync m16n8k16, blocks=%lld sms=%d",
+             variant_name(i.variant), i.tile_m, plan.pw.kp, static_cast<long long>(i.ctas), sm);
   } else if (i.variant == CONV_VARIANT_DEPTHWISE && plan.dw.mma) {
     snprintf(buf, len,
              "%s tensor cores: per channel %d band matrices, mma.sync m16n8k16 over 16 x 8 output blocks, "
@@ -779,6 +815,9 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
       break;
     case CONV_VARIANT_IGEMM_TC:
       err = launch_tc(plan, a, p->dtype, cs);
+      break;
+    case CONV_VARIANT_POINTWISE_MMA:
+      err = launch_pointwise(plan.pw, a, p->dtype, cs);
       break;
     case CONV_VARIANT_WINOGRAD: {
       WinoPlan wp;

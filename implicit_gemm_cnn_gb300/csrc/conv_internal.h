@@ -145,6 +145,24 @@ struct GdPlan {
 };
 bool gd_plan(const conv_problem* p, long long ho, long long wo, GdPlan* g);
 
+// 16-bit 1x1 convolutions on the tensor cores (conv_pointwise.cu): one block
+// per tile of BM = 16 * cfg output channels (cfg 1-4) x 128 pixels of one
+// image, all of k in shared memory, eight warps across the pixels.
+struct PwPlan {
+  int ok;
+  int cfg;
+  int kp;  // Cin rounded up to 16
+};
+struct PwGeo {
+  int kp, wpitch, xpitch;  // k rows staged; row lengths (elements) of the weight and pixel tiles
+  int pblocks;             // 128-pixel blocks per image
+  int vec_w, vec_x;        // 16-byte copies of weight rows / pixel rows
+  int pair_io;             // two outputs (and residual values) per access
+  int vec_r;               // the residual tile staged in shared memory by 16-byte copies
+};
+size_t pw_smem_bytes(const PwPlan& pp);
+cudaError_t launch_pointwise(const PwPlan& pp, const ConvArgs& a, int dtype, cudaStream_t s);
+
 struct Plan {
   conv_plan_info info;
   GdPlan gd;
@@ -157,6 +175,7 @@ struct Plan {
   TcPlan tc;
   WinPlan tcw;
   int tcw_ok;       // tcw holds a plan (the variant may still fall back to tc at launch)
+  PwPlan pw;
 };
 
 // Opt `func` in to `bytes` of dynamic shared memory on the current device.

@@ -89,6 +89,8 @@ typedef enum conv_act {
 #define CONV_FLAG_NO_WINOGRAD 0x40u  /* never Winograd                                 */
 #define CONV_FLAG_NO_DW_MMA 0x80u    /* 16-bit depthwise: the CUDA-core kernels, not the
                                         tensor-core band-matrix kernel              */
+#define CONV_FLAG_NO_PW_MMA 0x4000u  /* 16-bit 1x1 layers: not the pointwise tensor-core
+                                        tile kernel                                 */
 #define CONV_FLAG_SPLIT_K_SHIFT 8   /* bits 8..13: force this many ranges of k (1-63) */
 #define CONV_FLAG_SPLIT_K_MASK 0x3f00u
 
@@ -145,13 +147,17 @@ typedef enum conv_variant {
                                       (stride 1, or stride 2 split into 2x2
                                       phases; one group; the output's rows a
                                       multiple of 8 elements)                */
-  CONV_VARIANT_WINOGRAD = 5        /* Winograd F(2x2, 3x3) ("Convolutions",
+  CONV_VARIANT_WINOGRAD = 5,       /* Winograd F(2x2, 3x3) ("Convolutions",
                                       section 2.6): weight and input-tile
                                       transforms, sixteen products summed over
                                       channels on CUDA cores, output transform
                                       with the epilogue (float32, 3x3, stride
                                       1, dilation 1, one group; taken for 64 or
                                       more channels in and out)              */
+  CONV_VARIANT_POINTWISE_MMA = 6   /* 16-bit 1x1 layers (stride 1, no padding, one
+                                      group, Cin <= 256, Cout <= 64): tiles of
+                                      output channels x 128 pixels on the tensor
+                                      cores (warp-level mma.sync, float32 sums) */
 } conv_variant;
 
 /* The host-side plan of a problem for a device with `sm_count` SMs. */

@@ -36,6 +36,7 @@ def test_binding_rooflines_of_the_workloads():
     expect = {"resnet50_stem_f16": ("igemm_tcgen05_window", "hbm"),
               "resnet50_3x3_f16": ("igemm_tcgen05_window", "tensor"),
               "resnet50_1x1_res_f16": ("igemm_tcgen05_window", "hbm"),
+              "mbv3_pw1x1_f16": ("pointwise_mma", "hbm"),
               "mbv3_dw5x5_f32": ("depthwise_halo", "hbm"),
               "mbv3_pw1x1_f32": ("igemm_ffma", "alu"),
               "strided_3x3_s2_f32": ("igemm_ffma", "alu"),

@@ -132,7 +132,7 @@ EXPECTED_VARIANT = {
     "small_3x3_f32": "igemm_ffma", "resnet50_stem_f16": "igemm_tcgen05_window",
     "resnet50_3x3_f16": "igemm_tcgen05_window", "resnet50_1x1_res_f16": "igemm_tcgen05_window",
     "mbv3_dw5x5_f32": "depthwise_halo", "mbv3_dw5x5_f16": "depthwise_halo",
-    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05_window",
+    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "pointwise_mma",
     "grouped_dil2_f32": "igemm_ffma", "late_1x1_splitk_f32": "igemm_ffma_split_k",
     "strided_3x3_s2_f32": "igemm_ffma",
     "resnet50_3x3_256_f32": "winograd_f2x2_3x3",
@@ -165,6 +165,16 @@ def test_plans_of_the_workloads(lib, name):
         p2 = _layer_problem(L, flags=conv.FLAG_NO_WINDOW)
         assert conv.conv_plan(p2, 152)["variant_name"] == "igemm_tcgen05"
         assert conv.conv_plan(p2, 152)["scratch_bytes"] == 0
+    elif plan["variant_name"] == "pointwise_mma":
+        # one block per 128-pixel block of an image and channel block, no scratch
+        assert plan["scratch_bytes"] == 0 and plan["tile_n"] == 128
+        bm = plan["tile_m"]
+        assert L.c_out <= 64 and bm == (L.c_out + 15) // 16 * 16
+        hw = plan["ho"] * plan["wo"]
+        assert plan["ctas"] == L.n * -(-hw // 128) * -(-L.c_out // bm)
+        # with the kernel turned off: the shifted-window kernel's 1x1 view
+        p2 = _layer_problem(L, flags=conv.FLAG_NO_PW_MMA)
+        assert conv.conv_plan(p2, 152)["variant_name"] == "igemm_tcgen05_window"
     elif name in UNFOLDED:
         # the unfolded input (float32 n x c_in x kw x hu x Wo, hu the padded
         # rows the windows reach) on a 256-byte boundary, then the transposed
@@ -284,6 +294,9 @@ def test_planner_rules_on_random_shapes(lib):
             assert v == "depthwise_halo", (p, plan)
         if dt == "f32":
             assert v in ("igemm_ffma", "igemm_ffma_split_k", "depthwise_halo"), (p, plan)
+        if v == "pointwise_mma":
+            assert dt != "f32" and kh == kw == 1 and s == 1 and not any(pads) and groups == 1 and mg <= 64, (p, plan)
+            assert plan["scratch_bytes"] == 0
         if v == "igemm_tcgen05_window":
             # rows of 8-element multiples: the output's, or for a 1x1 layer
             # read as it lies, a row length dividing the plane
@@ -296,7 +309,7 @@ def test_planner_rules_on_random_shapes(lib):
             assert plan["split_k"] > 1 and plan["scratch_bytes"] == plan["split_k"] * n * mg * groups * ho * wo * 4
         else:
             assert plan["split_k"] == 1
-    assert {"igemm_ffma", "depthwise_halo", "igemm_tcgen05_window"} <= seen, seen
+    assert {"igemm_ffma", "depthwise_halo", "pointwise_mma", "igemm_tcgen05"} <= seen, seen
 
 
 # ---- ONNX auto_pad ----------------------------------------------------------

@@ -58,7 +58,7 @@ EXPECTED = {
     "small_3x3_f32": "igemm_ffma", "resnet50_stem_f16": "igemm_tcgen05_window",
     "resnet50_3x3_f16": "igemm_tcgen05_window", "resnet50_1x1_res_f16": "igemm_tcgen05_window",
     "mbv3_dw5x5_f32": "depthwise_halo", "mbv3_dw5x5_f16": "depthwise_halo",
-    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "igemm_tcgen05_window",
+    "mbv3_pw1x1_f32": "igemm_ffma", "mbv3_pw1x1_f16": "pointwise_mma",
     "grouped_dil2_f32": "igemm_ffma", "late_1x1_splitk_f32": "igemm_ffma_split_k",
     "strided_3x3_s2_f32": "igemm_ffma",
     "resnet50_3x3_256_f32": "winograd_f2x2_3x3",
@@ -194,6 +194,9 @@ def _edge_params():
                 out.append(pytest.param(case, dtype, "dwcc", id=f"dwcc-{name}-{dtype}"))
             if dtype != "f32" and name.startswith("win_"):
                 out.append(pytest.param(case, dtype, "gather", id=f"gather-{name}-{dtype}"))
+            if dtype != "f32" and name.startswith("win_1x1"):
+                # the shifted-window kernel's 1x1 view in place of the pointwise tile kernel
+                out.append(pytest.param(case, dtype, "nopw", id=f"nopw-{name}-{dtype}"))
             g = case[3]
             pointwise_f32 = (dtype == "f32" and case[2][2:] == (1, 1) and g.get("stride", 1) in (1, (1, 1))
                              and g.get("pads", 0) in (0, (0, 0), (0, 0, 0, 0)))
@@ -210,11 +213,14 @@ def test_edge_cases(case, dtype, path):
     ho, wo = conv.conv_output_shape(p)
     rs = (xs[0], ws[0], ho, wo) if res else None
     inp = random_layer_inputs(xs, ws, dtype, seed=zlib.crc32(name.encode()) % 10000, bias=bias, residual_shape=rs)
-    flags = {"auto": 0, "ffma": conv.FLAG_FORCE_FFMA, "gather": conv.FLAG_NO_WINDOW,
-             "unfold": conv.FLAG_FORCE_FFMA | conv.FLAG_FORCE_UNFOLD, "dwcc": conv.FLAG_NO_DW_MMA}[path]
-    if name.startswith("win_") and dtype != "f32" and path == "auto":
-        desc = conv.conv_describe_variant(p)
-        assert desc.startswith("igemm_tcgen05_window"), desc
+    flags = {"auto": 0, "ffma": conv.FLAG_FORCE_FFMA, "gather": conv.FLAG_NO_WINDOW | conv.FLAG_NO_PW_MMA,
+             "unfold": conv.FLAG_FORCE_FFMA | conv.FLAG_FORCE_UNFOLD, "dwcc": conv.FLAG_NO_DW_MMA,
+             "nopw": conv.FLAG_NO_PW_MMA}[path]
+    if name.startswith("win_") and dtype != "f32" and path in ("auto", "nopw"):
+        desc = conv.conv_describe_variant(conv.make_problem(xs, ws, dtype=dtype, flags=flags, **g))
+        pw = name.startswith("win_1x1") and path == "auto" and ws[0] <= 64
+        expect = "pointwise_mma" if pw else "igemm_tcgen05_window"
+        assert desc.startswith(expect), desc
     if path == "unfold":
         desc = conv.conv_describe_variant(conv.make_problem(xs, ws, dtype=dtype, flags=flags, **g))
         assert "B=unfolded" in desc, desc

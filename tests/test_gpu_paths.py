@@ -71,7 +71,10 @@ OFFSET_CASES = [
     ("window_y_off", (2, 16, 12, 16), (40, 16, 3, 3), dict(pads=1, act="silu"), ("f16", "bf16"), (0, 1, 1), True),
     ("window_stem_x_off", (2, 3, 40, 48), (16, 3, 7, 7), dict(stride=2, pads=3, act="relu"), ("f16",), (3, 5, 0),
      False),
-    ("window_1x1_res_off", (2, 32, 8, 16), (64, 32, 1, 1), dict(act="relu"), ("bf16",), (0, 0, 1), True),
+    # the pointwise tensor-core kernel: residual, x (element staging) and y (single stores) off 4 bytes
+    ("pw_1x1_res_off", (2, 32, 8, 16), (64, 32, 1, 1), dict(act="relu"), ("bf16",), (0, 0, 1), True),
+    ("pw_1x1_x_off", (2, 40, 9, 12), (48, 40, 1, 1), dict(act="silu"), ("f16",), (1, 0, 0), False),
+    ("pw_1x1_y_off", (2, 24, 8, 10), (56, 24, 1, 1), dict(), ("f16", "bf16"), (0, 1, 0), True),
     # general depthwise kernel: 16-, 8-, 4-byte and element copies of x rows
     ("dw_general_f32_off2", (2, 6, 12, 10), (18, 1, 3, 3), dict(stride=(2, 1), pads=1, groups=6, act="relu"),
      ("f32",), (2, 1, 0), False),
@@ -115,6 +118,8 @@ def test_operands_at_element_offsets(case, dtype):
                               residual_shape=(xs[0], ws[0], ho, wo) if res else None)
     if name.startswith("window"):
         assert _desc(p0).startswith("igemm_tcgen05_window"), _desc(p0)
+    if name.startswith("pw_"):
+        assert _desc(p0).startswith("pointwise_mma"), _desc(p0)
     y, _ = _run_offsets(inp, dtype, offs, **g)
     out = check_full(inp, dtype, y, **g)
     assert out["ok"], out
