@@ -165,15 +165,54 @@ __global__ void __launch_bounds__(kPwThreads, 2) pointwise_mma(const ConvArgs a,
         pw_mma<T>(acc[i][j], af[i], bf[j >> 1][2 * (j & 1)], bf[j >> 1][2 * (j & 1) + 1]);
   }
   // ---- epilogue: accumulator (i, j, q) is channel m0 + 16 (wm TMW + i) +
-  // lane / 4 (+ 8 for q >= 2) and pixel p0 + 8 (wn TNW + j) + 2 (lane % 4) + (q & 1)
+  // lane / 4 (+ 8 for q >= 2) and pixel p0 + 8 (wn TNW + j) + 2 (lane % 4) + (q & 1).
+  // Bias and residual per value, then the activation over all of the thread's
+  // values in one dispatch (a dispatch per pair would be if-converted into
+  // evaluating every activation), then the stores.
   const long long img = static_cast<long long>(n) * a.c_out;
+  float* v = &acc[0][0][0];
+  constexpr int NV = TMW * TNW * 4;
+  if (bg || rg) {
+#pragma unroll
+    for (int i = 0; i < TMW; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rl = (wm * TMW + i) * 16 + (lane >> 2) + 8 * h;
+        const int co = m0 + rl;
+        if (co >= a.c_out) continue;
+        const float bv = bg ? to_f32(bg[co]) : 0.0f;
+        const long long rowo = (img + co) * hw;
+#pragma unroll
+        for (int j = 0; j < TNW; ++j) {
+          const int cl = (wn * TNW + j) * 8 + 2 * (lane & 3);
+          const int p = p0 + cl;
+          if (p >= hw) continue;
+          float& v0 = acc[i][j][2 * h];
+          float& v1 = acc[i][j][2 * h + 1];
+          if (bg) {
+            v0 = __fadd_rn(v0, bv);
+            v1 = __fadd_rn(v1, bv);
+          }
+          if (g.vec_r) {  // from the staged tile (pairs: H*W is a multiple of 8)
+            const uint32_t rw = *reinterpret_cast<const uint32_t*>(rs + rl * g.xpitch + cl);
+            const uint16_t lo = static_cast<uint16_t>(rw & 0xffffu), hi = static_cast<uint16_t>(rw >> 16);
+            v0 = __fadd_rn(v0, to_f32(*reinterpret_cast<const T*>(&lo)));
+            v1 = __fadd_rn(v1, to_f32(*reinterpret_cast<const T*>(&hi)));
+          } else if (rg) {
+            v0 = __fadd_rn(v0, to_f32(rg[rowo + p]));
+            if (p + 1 < hw) v1 = __fadd_rn(v1, to_f32(rg[rowo + p + 1]));
+          }
+        }
+      }
+    }
+  }
+  activate_n<NV>(*reinterpret_cast<float(*)[NV]>(v), a.act, a.alpha, a.beta);
 #pragma unroll
   for (int i = 0; i < TMW; ++i) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int co = m0 + (wm * TMW + i) * 16 + (lane >> 2) + 8 * h;
       if (co >= a.c_out) continue;
-      const float bv = bg ? to_f32(bg[co]) : 0.0f;
       const long long rowo = (img + co) * hw;
 #pragma unroll
       for (int j = 0; j < TNW; ++j) {
@@ -181,30 +220,11 @@ __global__ void __launch_bounds__(kPwThreads, 2) pointwise_mma(const ConvArgs a,
         if (p >= hw) continue;
         const long long o = rowo + p;
         const bool two = p + 1 < hw;
-        float v[2] = {acc[i][j][2 * h], acc[i][j][2 * h + 1]}, b2[2] = {bv, bv}, r2[2] = {0.0f, 0.0f};
-        if (g.vec_r) {  // from the staged tile (pairs: H*W is a multiple of 8)
-          const int rl = (wm * TMW + i) * 16 + (lane >> 2) + 8 * h, cl = (wn * TNW + j) * 8 + 2 * (lane & 3);
-          const uint32_t rw = *reinterpret_cast<const uint32_t*>(rs + rl * g.xpitch + cl);
-          const uint16_t lo = static_cast<uint16_t>(rw & 0xffffu), hi = static_cast<uint16_t>(rw >> 16);
-          r2[0] = to_f32(*reinterpret_cast<const T*>(&lo));
-          r2[1] = to_f32(*reinterpret_cast<const T*>(&hi));
-        } else if (rg) {
-          if (two && g.pair_io) {
-            const uint32_t rw = *reinterpret_cast<const uint32_t*>(rg + o);
-            const uint16_t lo = static_cast<uint16_t>(rw & 0xffffu), hi = static_cast<uint16_t>(rw >> 16);
-            r2[0] = to_f32(*reinterpret_cast<const T*>(&lo));
-            r2[1] = to_f32(*reinterpret_cast<const T*>(&hi));
-          } else {
-            r2[0] = to_f32(rg[o]);
-            if (two) r2[1] = to_f32(rg[o + 1]);
-          }
-        }
-        epilogue_n<2>(v, b2, r2, bg != nullptr, rg != nullptr, a.act, a.alpha, a.beta);
         if (two && g.pair_io) {
-          *reinterpret_cast<uint32_t*>(y + o) = pw_pack<T>(v[0], v[1]);
+          *reinterpret_cast<uint32_t*>(y + o) = pw_pack<T>(acc[i][j][2 * h], acc[i][j][2 * h + 1]);
         } else {
-          y[o] = from_f32<T>(v[0]);
-          if (two) y[o + 1] = from_f32<T>(v[1]);
+          y[o] = from_f32<T>(acc[i][j][2 * h]);
+          if (two) y[o + 1] = from_f32<T>(acc[i][j][2 * h + 1]);
         }
       }
     }
