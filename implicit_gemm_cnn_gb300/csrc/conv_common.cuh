@@ -126,6 +126,23 @@ __device__ __forceinline__ float activate(float t, int act, float alpha, float b
   return v[0];
 }
 
+// Bias, residual, then the compiled-in activation ACT, for N values (each
+// step rounded in float32).
+template <int ACT, int N>
+__device__ __forceinline__ void epilogue_t(float (&v)[N], const float (&bias)[N], const float (&res)[N],
+                                           bool has_bias, bool has_res, float alpha, float beta) {
+  if (has_bias) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __fadd_rn(v[i], bias[i]);
+  }
+  if (has_res) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __fadd_rn(v[i], res[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = act_fn<ACT>(v[i], alpha, beta);
+}
+
 // Sum, bias, residual for N values of one output channel or of N channels
 // (bias per value), then the activation: the float32 steps of the epilogue.
 template <int N>

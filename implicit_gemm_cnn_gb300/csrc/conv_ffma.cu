@@ -406,71 +406,170 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
       }
     return;
   }
-  // only pixels in [pix_lo, pix_hi) (the whole batch, or a chunk of images)
-  // are stored; split planes hold the chunk's outputs from image img0 on
-  const long long out0 = static_cast<long long>(a.img0) * a.c_out * a.howo;
-  T* y = static_cast<T*>(a.y);
-#pragma unroll
-  for (int jg = 0; jg < TN / 4; ++jg) {
-    const long long p = pix0 + jg * GN + tx * 4;
-    if (p >= a.pix_hi || p + 3 < a.pix_lo) continue;
-    const int n = static_cast<int>(p / a.howo);
-    const long long rem = p - static_cast<long long>(n) * a.howo;
-    const bool whole4 = a.vec_out && p >= a.pix_lo && (p + 3 < a.pix_hi) && (rem + 3 < a.howo) && ((a.howo & 3) == 0);
-    // output offset (image, position) of pixel p + q, stepped from p's
-    // without a division: the 4 pixels may cross image boundaries
-    long long oo[4];
-    int on[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      long long o = rem + q;
-      int nq = n;
-      while (o >= a.howo) { o -= a.howo; ++nq; }
-      oo[q] = o;
-      on[q] = nq;
-    }
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-      const int m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
-      if (m >= a.mg) continue;
-      const int co = g * a.mg + m;
-      const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo + rem;
-      if (a.split > 1 || a.raw_out) {
-        float* part = a.partial + static_cast<long long>(blockIdx.z) * a.part_total;  // chunk-local
-        if (whole4) {
-          *reinterpret_cast<float4*>(part + (out - out0)) =
-              make_float4(acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]);
+  if constexpr (BM * BN == 128 * 128) {
+    // the 128 x 128 tiles (128 registers a thread) keep the epilogue per run
+    // of 4 pixels: the two-pass form below cost the unfolded kernel 6 % (664
+    // against 627 us) and made the gathered one spill
+    // only pixels in [pix_lo, pix_hi) (the whole batch, or a chunk of images)
+    // are stored; split planes hold the chunk's outputs from image img0 on
+    const long long out0 = static_cast<long long>(a.img0) * a.c_out * a.howo;
+    T* y = static_cast<T*>(a.y);
+  #pragma unroll
+    for (int jg = 0; jg < TN / 4; ++jg) {
+      const long long p = pix0 + jg * GN + tx * 4;
+      if (p >= a.pix_hi || p + 3 < a.pix_lo) continue;
+      const int n = static_cast<int>(p / a.howo);
+      const long long rem = p - static_cast<long long>(n) * a.howo;
+      const bool whole4 = a.vec_out && p >= a.pix_lo && (p + 3 < a.pix_hi) && (rem + 3 < a.howo) && ((a.howo & 3) == 0);
+      // output offset (image, position) of pixel p + q, stepped from p's
+      // without a division: the 4 pixels may cross image boundaries
+      long long oo[4];
+      int on[4];
+  #pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        long long o = rem + q;
+        int nq = n;
+        while (o >= a.howo) { o -= a.howo; ++nq; }
+        oo[q] = o;
+        on[q] = nq;
+      }
+  #pragma unroll
+      for (int i = 0; i < TM; ++i) {
+        const int m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+        if (m >= a.mg) continue;
+        const int co = g * a.mg + m;
+        const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo + rem;
+        if (a.split > 1 || a.raw_out) {
+          float* part = a.partial + static_cast<long long>(blockIdx.z) * a.part_total;  // chunk-local
+          if (whole4) {
+            *reinterpret_cast<float4*>(part + (out - out0)) =
+                make_float4(acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]);
+          } else {
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const long long pq = p + q;
+              if (pq < a.pix_lo || pq >= a.pix_hi) continue;
+              part[(static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q] - out0] = acc[i][jg * 4 + q];
+            }
+          }
         } else {
-#pragma unroll
+          // the epilogue on this run of 4 pixels of one channel
+          const T* __restrict__ resp = static_cast<const T*>(a.residual);
+          const float bco = a.bias ? to_f32(static_cast<const T*>(a.bias)[co]) : 0.0f;
+          float v[4], bv[4], rv[4];
+          long long oq[4];
+          bool in[4];
+  #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const long long pq = p + q;
-            if (pq < a.pix_lo || pq >= a.pix_hi) continue;
-            part[(static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q] - out0] = acc[i][jg * 4 + q];
+            in[q] = pq >= a.pix_lo && pq < a.pix_hi;
+            oq[q] = whole4 ? out + q : (static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q];
+            v[q] = acc[i][jg * 4 + q];
+            bv[q] = bco;
+            rv[q] = (resp && in[q]) ? to_f32(resp[oq[q]]) : 0.0f;
+          }
+          epilogue_n<4>(v, bv, rv, a.bias != nullptr, resp != nullptr, a.act, a.alpha, a.beta);
+          if (whole4) {
+            store4<T>(y, out, v);
+          } else {
+  #pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (in[q]) y[oq[q]] = from_f32<T>(v[q]);
           }
         }
-      } else {
-        // the epilogue on this run of 4 pixels of one channel
-        const T* __restrict__ resp = static_cast<const T*>(a.residual);
-        const float bco = a.bias ? to_f32(static_cast<const T*>(a.bias)[co]) : 0.0f;
-        float v[4], bv[4], rv[4];
-        long long oq[4];
-        bool in[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const long long pq = p + q;
-          in[q] = pq >= a.pix_lo && pq < a.pix_hi;
-          oq[q] = whole4 ? out + q : (static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q];
-          v[q] = acc[i][jg * 4 + q];
-          bv[q] = bco;
-          rv[q] = (resp && in[q]) ? to_f32(resp[oq[q]]) : 0.0f;
+      }
+    }
+    return;
+  } else {
+    // only pixels in [pix_lo, pix_hi) (the whole batch, or a chunk of images)
+    // are stored; split planes hold the chunk's outputs from image img0 on
+    const long long out0 = static_cast<long long>(a.img0) * a.c_out * a.howo;
+    T* y = static_cast<T*>(a.y);
+    const bool raw = a.split > 1 || a.raw_out;
+    // pixel group jg: its first pixel, image and position, and the (image,
+    // position) of each of its 4 pixels, stepped without a division (the 4
+    // pixels may cross image boundaries)
+    auto group = [&](int jg, long long& p, int& n, long long& rem, long long (&oo)[4], int (&on)[4]) {
+      p = pix0 + jg * GN + tx * 4;
+      n = static_cast<int>(p / a.howo);
+      rem = p - static_cast<long long>(n) * a.howo;
+  #pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        long long o = rem + q;
+        int nq = n;
+        while (o >= a.howo) { o -= a.howo; ++nq; }
+        oo[q] = o;
+        on[q] = nq;
+      }
+    };
+    if (!raw) {
+      // the fused epilogue in float32: bias and residual per value, then the
+      // activation over all of the thread's values in one dispatch (a dispatch
+      // per 4 values is if-converted into evaluating every activation)
+      const T* __restrict__ resp = static_cast<const T*>(a.residual);
+      const T* __restrict__ biasp = static_cast<const T*>(a.bias);
+      if (biasp || resp) {
+  #pragma unroll
+        for (int jg = 0; jg < TN / 4; ++jg) {
+          long long p, rem, oo[4];
+          int n, on[4];
+          group(jg, p, n, rem, oo, on);
+          if (p >= a.pix_hi || p + 3 < a.pix_lo) continue;
+  #pragma unroll
+          for (int i = 0; i < TM; ++i) {
+            const int m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+            if (m >= a.mg) continue;
+            const int co = g * a.mg + m;
+            const float bco = biasp ? to_f32(biasp[co]) : 0.0f;
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float& v = acc[i][jg * 4 + q];
+              if (biasp) v = __fadd_rn(v, bco);
+              const long long pq = p + q;
+              if (resp && pq >= a.pix_lo && pq < a.pix_hi)
+                v = __fadd_rn(v, to_f32(resp[(static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q]]));
+            }
+          }
         }
-        epilogue_n<4>(v, bv, rv, a.bias != nullptr, resp != nullptr, a.act, a.alpha, a.beta);
-        if (whole4) {
+      }
+      activate_n<TM * TN>(*reinterpret_cast<float(*)[TM * TN]>(&acc[0][0]), a.act, a.alpha, a.beta);
+    }
+  #pragma unroll
+    for (int jg = 0; jg < TN / 4; ++jg) {
+      long long p, rem, oo[4];
+      int n, on[4];
+      group(jg, p, n, rem, oo, on);
+      if (p >= a.pix_hi || p + 3 < a.pix_lo) continue;
+      const bool whole4 = a.vec_out && p >= a.pix_lo && (p + 3 < a.pix_hi) && (rem + 3 < a.howo) && ((a.howo & 3) == 0);
+  #pragma unroll
+      for (int i = 0; i < TM; ++i) {
+        const int m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+        if (m >= a.mg) continue;
+        const int co = g * a.mg + m;
+        const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo + rem;
+        if (raw) {
+          float* part = a.partial + static_cast<long long>(blockIdx.z) * a.part_total;  // chunk-local
+          if (whole4) {
+            *reinterpret_cast<float4*>(part + (out - out0)) =
+                make_float4(acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]);
+          } else {
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const long long pq = p + q;
+              if (pq < a.pix_lo || pq >= a.pix_hi) continue;
+              part[(static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q] - out0] = acc[i][jg * 4 + q];
+            }
+          }
+        } else if (whole4) {
+          float v[4] = {acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]};
           store4<T>(y, out, v);
         } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (in[q]) y[oq[q]] = from_f32<T>(v[q]);
+  #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const long long pq = p + q;
+            if (pq >= a.pix_lo && pq < a.pix_hi)
+              y[(static_cast<long long>(on[q]) * a.c_out + co) * a.howo + oo[q]] = from_f32<T>(acc[i][jg * 4 + q]);
+          }
         }
       }
     }
@@ -597,7 +696,7 @@ __global__ void __launch_bounds__(256) ffma_tail_reduce(const ConvArgs a) {
 
 // Sum the split planes in range order, then the fused epilogue.  Four
 // consecutive outputs per thread when the plane length allows vector loads.
-template <typename T>
+template <typename T, int ACT>
 __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
   // the planes hold the outputs of images [img0, img0 + chunk): part_total
   // elements each, output out0 + i at element i
@@ -647,7 +746,7 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
         bv[k] = bp ? to_f32(bp[ck]) : 0.0f;
         rv[k] = rp ? to_f32(rp[o + k]) : 0.0f;
       }
-      epilogue_n<4>(v, bv, rv, bp != nullptr, rp != nullptr, a.act, a.alpha, a.beta);
+      epilogue_t<ACT, 4>(v, bv, rv, bp != nullptr, rp != nullptr, a.alpha, a.beta);
       if (a.vec_out) {
         store4<T>(y, o, v);
       } else {
@@ -663,7 +762,7 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
       for (int z = 1; z < a.split; ++z) v[0] = __fadd_rn(v[0], part[z * total + i]);
       const int co = static_cast<int>(((out0 + i) / a.howo) % a.c_out);
       float bv[1] = {bp ? to_f32(bp[co]) : 0.0f}, rv[1] = {rp ? to_f32(rp[i]) : 0.0f};
-      epilogue_n<1>(v, bv, rv, bp != nullptr, rp != nullptr, a.act, a.alpha, a.beta);
+      epilogue_t<ACT, 1>(v, bv, rv, bp != nullptr, rp != nullptr, a.alpha, a.beta);
       y[i] = from_f32<T>(v[0]);
     }
   }
@@ -931,7 +1030,20 @@ cudaError_t launch_reduce_typed(const ConvArgs& a, cudaStream_t s) {
   const int threads = work < 152LL * 256 ? 64 : 256;
   long long blocks = (work + threads - 1) / threads;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  split_reduce<T><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
+  switch (a.act) {  // the activation compiled in: one code path per kernel
+#define CONV_SR_CASE(A) \
+  case A: split_reduce<T, A><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a); break;
+    CONV_SR_CASE(ACT_RELU)
+    CONV_SR_CASE(ACT_SILU)
+    CONV_SR_CASE(ACT_SIGMOID)
+    CONV_SR_CASE(ACT_TANH)
+    CONV_SR_CASE(ACT_HARD_SWISH)
+    CONV_SR_CASE(ACT_HARD_SIGMOID)
+    CONV_SR_CASE(ACT_CLIP)
+    CONV_SR_CASE(ACT_LEAKY_RELU)
+#undef CONV_SR_CASE
+    default: split_reduce<T, ACT_IDENTITY><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a); break;
+  }
   return cudaGetLastError();
 }
 
