@@ -577,10 +577,17 @@ def run_transpose(L, steps: int, warmup: int, world: int, local_rank: int) -> di
     us = secs * 1e6 / steps
     fl = transpose_flops(L)
     rate = fl / (us / 1e6) / 1e12
-    return {"value": aggregate(fl * steps, world, secs) / 1e12, "us": us, "clocks": clocks, "launches": 3 * steps,
-            "roofline": {"bound": "alu", "achieved": round(rate, 2), "peak": FFMA_PEAK_TFLOPS, "unit": "TFLOP/s",
-                         "frac": round(rate / FFMA_PEAK_TFLOPS, 4), "traffic": None,
-                         "tensor_or_alu_frac": round(rate / FFMA_PEAK_TFLOPS, 4)}}
+    # 16-bit layers with one group run their Gemm on the tensor cores (mma.sync,
+    # weight transpose + Gemm + col2im); the others on the CUDA cores in float32
+    # (plus the widening of a 16-bit x)
+    tc = L.dtype != "f32" and L.groups == 1
+    peak = MMA_SYNC_PEAK_TFLOPS if tc else FFMA_PEAK_TFLOPS
+    launches = 3 if (tc or L.dtype == "f32") else 4
+    return {"value": aggregate(fl * steps, world, secs) / 1e12, "us": us, "clocks": clocks,
+            "launches": launches * steps, "tensor_gemm": tc,
+            "roofline": {"bound": "tensor" if tc else "alu", "achieved": round(rate, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(rate / peak, 4), "traffic": None,
+                         "tensor_or_alu_frac": round(rate / peak, 4)}}
 
 
 def nested_layers(headline: str, args, world: int, rank: int, local_rank: int) -> list:
@@ -625,7 +632,9 @@ def other_op_record(name: str, args, world: int, local_rank: int) -> dict:
     L = TRANSPOSE_LAYERS[name]
     r = run_transpose(L, args.layer_steps, args.warmup, world, local_rank)
     return {"layer": name, "workload": L.description, "dtype": L.dtype,
-            "variant": "conv_transpose (weight transpose + CUDA-core Gemm + gathering col2im)",
+            "variant": ("conv_transpose (weight transpose + tensor-core Gemm (mma.sync) + gathering col2im)"
+                        if r["tensor_gemm"] else
+                        "conv_transpose (weight transpose + float32 CUDA-core Gemm + gathering col2im)"),
             "steps": args.layer_steps, "us_per_call": round(r["us"], 3), "tflops": round(r["value"], 3),
             "roofline": r["roofline"], "gpu_launches": r["launches"], "sm_mhz": r["clocks"].get("sm_mhz"),
             "clock_reasons": r["clocks"].get("reasons")}

@@ -252,15 +252,16 @@ def conv_forward_fixed_scratch(p: ConvProblem, x, w, bias, residual, y, stream=N
 
 def make_transpose_problem(x_shape, w_shape, *, dtype="f32", stride=1, pads=0, dilation=1, out_pad=0,
                            groups=1, act="identity", alpha=0.0, beta=0.0, has_bias=False,
-                           has_residual=False) -> ConvTransposeProblem:
-    """x (N, Cin, H, W); w (Cin, Cout/groups, kh, kw)."""
+                           has_residual=False, flags=0) -> ConvTransposeProblem:
+    """x (N, Cin, H, W); w (Cin, Cout/groups, kh, kw).  ``flags``:
+    FLAG_NO_PW_MMA keeps a 16-bit layer's Gemm on the CUDA cores."""
     n, c_in, h, w = (int(v) for v in x_shape)
     cin_w, mg, kh, kw = (int(v) for v in w_shape)
     if cin_w != c_in:
         raise ValueError("ConvTranspose weights are [Cin][Cout/groups][kh][kw]")
     q = make_problem((n, c_in, h, w), (mg * int(groups), c_in // int(groups), kh, kw), dtype=dtype,
                      stride=stride, pads=pads, dilation=dilation, groups=groups, act=act, alpha=alpha,
-                     beta=beta, has_bias=has_bias, has_residual=has_residual)
+                     beta=beta, has_bias=has_bias, has_residual=has_residual, flags=flags)
     oph, opw = _pair(out_pad)
     return ConvTransposeProblem(q, oph, opw)
 
@@ -293,14 +294,14 @@ def conv_transpose_forward(p: ConvTransposeProblem, x, w, bias, residual, y, scr
 
 
 def conv_transpose2d(x, w, bias=None, residual=None, *, stride=1, pads=0, dilation=1, out_pad=0, groups=1,
-                     act="identity", alpha=0.0, beta=0.0, out=None, scratch=None, stream=None):
+                     act="identity", alpha=0.0, beta=0.0, out=None, scratch=None, stream=None, flags=0):
     """ConvTranspose on CUDA tensors (w [Cin][Cout/groups][kh][kw]); allocates
     y and scratch with torch unless given."""
     import torch
     dt = _dtype_name(x)
     p = make_transpose_problem(x.shape, w.shape, dtype=dt, stride=stride, pads=pads, dilation=dilation,
                                out_pad=out_pad, groups=groups, act=act, alpha=alpha, beta=beta,
-                               has_bias=bias is not None, has_residual=residual is not None)
+                               has_bias=bias is not None, has_residual=residual is not None, flags=flags)
     ho, wo = conv_transpose_output_shape(p)
     if out is None:
         out = torch.empty((p.conv.n, p.conv.c_out, ho, wo), dtype=x.dtype, device=x.device)

@@ -278,7 +278,7 @@ bool plan_pointwise(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   pp.cfg = static_cast<int>((p->c_out + 15) / 16);
   const int bm = 16 * pp.cfg;
   if ((p->c_out + bm - 1) / bm > 65535) return false;
-  if (pw_smem_bytes(pp) > 110 * 1024) return false;  // two blocks per SM
+  if (pw_smem_bytes(pp, true) > 110 * 1024) return false;  // two blocks per SM
   out->pw = pp;
   out->info.variant = CONV_VARIANT_POINTWISE_MMA;
   out->info.split_k = 1;
@@ -918,9 +918,31 @@ static conv_status t_prepare(const conv_transpose_problem* tp, int sm, Transpose
   shape_args(&q, sq, &out->gemm_args);
   out->dtype = p->dtype;
   auto up256 = [](size_t v) { return (v + 255) / 256 * 256; };
+  // 16-bit, one group, Cin <= 256: the Gemm on the pointwise tensor-core
+  // kernel with raw float32 sums (x read as it is, the weights transposed in
+  // their own type); else the float32 CUDA-core Gemm above
+  out->mma = 0;
+  memset(&out->pw, 0, sizeof(out->pw));
+  if (p->dtype != CONV_F32 && p->groups == 1 && p->c_in <= 256 && !(p->flags & CONV_FLAG_NO_PW_MMA) &&
+      p->n * ((p->h * p->w + 127) / 128) <= 2000000000LL && (cout_k + 127) / 128 <= 65535) {
+    PwPlan pp;
+    pp.ok = 1;
+    pp.kp = static_cast<int>((p->c_in + 15) / 16 * 16);
+    pp.cfg = cout_k <= 64 ? static_cast<int>((cout_k + 15) / 16) : 5;
+    if (pp.cfg == 5 && pw_smem_bytes(pp, false) > 110 * 1024) pp.cfg = 4;  // 64-channel tiles when k is long
+    if (pw_smem_bytes(pp, false) <= 110 * 1024) {  // two blocks per SM
+      out->mma = 1;
+      out->pw = pp;
+    }
+  }
   out->wt_off = 0;
-  out->xf_off = up256(static_cast<size_t>(sq.w_elems) * 4);
-  out->cols_off = out->xf_off + (p->dtype == CONV_F32 ? 0 : up256(static_cast<size_t>(sq.x_elems) * 4));
+  if (out->mma) {
+    out->xf_off = 0;
+    out->cols_off = up256(static_cast<size_t>(sq.w_elems) * 2);
+  } else {
+    out->xf_off = up256(static_cast<size_t>(sq.w_elems) * 4);
+    out->cols_off = out->xf_off + (p->dtype == CONV_F32 ? 0 : up256(static_cast<size_t>(sq.x_elems) * 4));
+  }
   long long cols_bytes;
   if (!mul_ok(sq.y_elems, 4, &cols_bytes)) return CONV_ERR_OVERFLOW;
   out->scratch_bytes = out->cols_off + static_cast<size_t>(cols_bytes);

@@ -146,8 +146,9 @@ struct GdPlan {
 bool gd_plan(const conv_problem* p, long long ho, long long wo, GdPlan* g);
 
 // 16-bit 1x1 convolutions on the tensor cores (conv_pointwise.cu): one block
-// per tile of BM = 16 * cfg output channels (cfg 1-4) x 128 pixels of one
-// image, all of k in shared memory, eight warps across the pixels.
+// per tile of BM = 16 * cfg output channels (cfg 1-4, eight warps across the
+// pixels; cfg 5: 128 channels, 2 x 4 warps) x 128 pixels of one image, all of
+// k in shared memory.
 struct PwPlan {
   int ok;
   int cfg;
@@ -160,7 +161,7 @@ struct PwGeo {
   int pair_io;             // two outputs (and residual values) per access
   int vec_r;               // the residual tile staged in shared memory by 16-byte copies
 };
-size_t pw_smem_bytes(const PwPlan& pp);
+size_t pw_smem_bytes(const PwPlan& pp, bool residual_tile);  // shared memory of a block
 cudaError_t launch_pointwise(const PwPlan& pp, const ConvArgs& a, int dtype, cudaStream_t s);
 
 struct Plan {
@@ -220,9 +221,11 @@ struct TransposePlan {
   int dtype;
   Plan gemm_plan;        // the CUDA-core plan of the 1x1 Gemm
   ConvArgs gemm_args;    // its geometry (addresses filled at launch)
-  size_t wt_off;          // float32 transposed weights
-  size_t xf_off;          // 16-bit types: x widened to float32
+  size_t wt_off;          // transposed weights: float32, or 16-bit for the tensor-core Gemm
+  size_t xf_off;          // 16-bit types on the CUDA-core Gemm: x widened to float32
   size_t cols_off, scratch_bytes;
+  int mma;                // 16-bit, one group: the Gemm on the pointwise tensor-core kernel
+  PwPlan pw;
 };
 cudaError_t launch_conv_transpose(const TransposePlan& tp, const ConvArgs& a, const TransposeGeo& t,
                                   const void* w, void* scratch, cudaStream_t s);

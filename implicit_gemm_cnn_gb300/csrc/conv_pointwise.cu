@@ -13,7 +13,8 @@
 // weight rows, B fragments by ldmatrix.trans from the pixel rows.  Products
 // of 16-bit values are exact in float32; the sums run in the MMA's float32
 // order.  The epilogue adds bias and residual, applies the activation in
-// float32 and rounds once, two pixels per store.
+// float32 and rounds once, two pixels per store; or (raw_out, the Gemm of a
+// transposed convolution) writes the float32 sums as they are.
 #include <algorithm>
 #include <type_traits>
 
@@ -166,10 +167,34 @@ __global__ void __launch_bounds__(kPwThreads, 2) pointwise_mma(const ConvArgs a,
   }
   // ---- epilogue: accumulator (i, j, q) is channel m0 + 16 (wm TMW + i) +
   // lane / 4 (+ 8 for q >= 2) and pixel p0 + 8 (wn TNW + j) + 2 (lane % 4) + (q & 1).
+  const long long img = static_cast<long long>(n) * a.c_out;
+  if (a.raw_out) {  // the raw float32 sums into the float32 array y (no epilogue)
+    float* __restrict__ yf = static_cast<float*>(a.y);
+#pragma unroll
+    for (int i = 0; i < TMW; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int co = m0 + (wm * TMW + i) * 16 + (lane >> 2) + 8 * h;
+        if (co >= a.c_out) continue;
+        const long long rowo = (img + co) * hw;
+#pragma unroll
+        for (int j = 0; j < TNW; ++j) {
+          const int p = p0 + (wn * TNW + j) * 8 + 2 * (lane & 3);
+          if (p >= hw) continue;
+          if (p + 1 < hw && g.pair_io) {
+            *reinterpret_cast<float2*>(yf + rowo + p) = make_float2(acc[i][j][2 * h], acc[i][j][2 * h + 1]);
+          } else {
+            yf[rowo + p] = acc[i][j][2 * h];
+            if (p + 1 < hw) yf[rowo + p + 1] = acc[i][j][2 * h + 1];
+          }
+        }
+      }
+    }
+    return;
+  }
   // Bias and residual per value, then the activation over all of the thread's
   // values in one dispatch (a dispatch per pair would be if-converted into
   // evaluating every activation), then the stores.
-  const long long img = static_cast<long long>(n) * a.c_out;
   float* v = &acc[0][0][0];
   constexpr int NV = TMW * TNW * 4;
   if (bg || rg) {
@@ -241,7 +266,7 @@ cudaError_t launch_pw_cfg(const PwPlan& pp, const ConvArgs& a, cudaStream_t s) {
   g.pblocks = static_cast<int>((a.hw + kPwBN - 1) / kPwBN);
   g.vec_w = (a.c_in % 8 == 0) && reinterpret_cast<uintptr_t>(a.wt) % 16 == 0;
   g.vec_x = (a.hw % 8 == 0) && reinterpret_cast<uintptr_t>(a.x) % 16 == 0;
-  g.pair_io = (a.hw % 2 == 0) && reinterpret_cast<uintptr_t>(a.y) % 4 == 0 &&
+  g.pair_io = (a.hw % 2 == 0) && reinterpret_cast<uintptr_t>(a.y) % (a.raw_out ? 8 : 4) == 0 &&
               (!a.residual || reinterpret_cast<uintptr_t>(a.residual) % 4 == 0);
   g.vec_r = a.residual && (a.hw % 8 == 0) && reinterpret_cast<uintptr_t>(a.residual) % 16 == 0;
   const size_t smem = (static_cast<size_t>(BM) * g.wpitch + static_cast<size_t>(g.kp) * g.xpitch +
@@ -262,15 +287,17 @@ cudaError_t launch_pw_typed(const PwPlan& pp, const ConvArgs& a, cudaStream_t s)
     case 2: return launch_pw_cfg<T, 2, 1, 8>(pp, a, s);
     case 3: return launch_pw_cfg<T, 3, 1, 8>(pp, a, s);
     case 4: return launch_pw_cfg<T, 4, 1, 8>(pp, a, s);
+    case 5: return launch_pw_cfg<T, 4, 2, 4>(pp, a, s);  // 128 channels: the raw-sum Gemm of ConvTranspose
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-size_t pw_smem_bytes(const PwPlan& pp) {  // with a staged residual tile
-  const int bm = 16 * pp.cfg;
-  return (static_cast<size_t>(bm) * (pp.kp + 8) + static_cast<size_t>(pp.kp + bm) * (kPwBN + 8)) * 2;
+size_t pw_smem_bytes(const PwPlan& pp, bool residual_tile) {
+  const int bm = pp.cfg == 5 ? 128 : 16 * pp.cfg;
+  return (static_cast<size_t>(bm) * (pp.kp + 8) +
+          static_cast<size_t>(pp.kp + (residual_tile ? bm : 0)) * (kPwBN + 8)) * 2;
 }
 
 cudaError_t launch_pointwise(const PwPlan& pp, const ConvArgs& a, int dtype, cudaStream_t s) {

@@ -21,11 +21,11 @@
 namespace conv {
 namespace {
 
-// w [Cin][Cout/G][kh][kw] -> wt [G][(co_l, u, v)][c_l] in float32, the 1x1
-// weights of the Gemm.  Block row r of the grid is one row (g, co_l, tap) of
+// w [Cin][Cout/G][kh][kw] -> wt [G][(co_l, u, v)][c_l] (float32, or the
+// element type for the tensor-core Gemm), the 1x1 weights of the Gemm.  Block row r of the grid is one row (g, co_l, tap) of
 // wt; its threads cover the c_l of that row.
-template <typename T>
-__global__ void __launch_bounds__(256) transpose_weights(const T* __restrict__ w, float* __restrict__ wt, int cg,
+template <typename T, typename U>
+__global__ void __launch_bounds__(256) transpose_weights(const T* __restrict__ w, U* __restrict__ wt, int cg,
                                                          int mg, int khw, long long rows) {
   const int c = blockIdx.x * 256 + threadIdx.x;
   for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
@@ -33,7 +33,11 @@ __global__ void __launch_bounds__(256) transpose_weights(const T* __restrict__ w
     const long long gc = r / khw;
     const int col = static_cast<int>(gc % mg);
     const long long g = gc / mg;
-    if (c < cg) wt[r * cg + c] = to_f32(w[((g * cg + c) * mg + col) * khw + tap]);
+    if (c < cg) {
+      const T v = w[((g * cg + c) * mg + col) * khw + tap];
+      if constexpr (std::is_same<T, U>::value) wt[r * cg + c] = v;
+      else wt[r * cg + c] = to_f32(v);
+    }
   }
 }
 
@@ -127,16 +131,39 @@ __global__ void __launch_bounds__(256) col2im_rows(const ConvArgs a, const Trans
 }
 
 template <typename T>
+cudaError_t launch_col2im(const ConvArgs& a, const TransposeGeo& t, const float* cols, cudaStream_t s);
+
+template <typename T>
 cudaError_t launch_typed(const TransposePlan& tp, const ConvArgs& a, const TransposeGeo& t, const void* w,
                          void* scratch, cudaStream_t s) {
   char* sc = static_cast<char*>(scratch);
-  float* wt = reinterpret_cast<float*>(sc + tp.wt_off);
   float* cols = reinterpret_cast<float*>(sc + tp.cols_off);
   const int khw = a.kh * a.kw;
   const long long wrows = static_cast<long long>(a.groups) * a.mg * khw;
   const dim3 wgrid(static_cast<unsigned>((a.cg + 255) / 256), static_cast<unsigned>(std::min<long long>(wrows, 65535)));
-  transpose_weights<T><<<wgrid, 256, 0, s>>>(static_cast<const T*>(w), wt, a.cg, a.mg, khw, wrows);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = cudaSuccess;
+  if constexpr (!std::is_same<T, float>::value) {
+    if (tp.mma) {  // the Gemm on the tensor cores: weights in the element type, raw float32 sums
+      T* wt16 = reinterpret_cast<T*>(sc + tp.wt_off);
+      transpose_weights<T, T><<<wgrid, 256, 0, s>>>(static_cast<const T*>(w), wt16, a.cg, a.mg, khw, wrows);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+      ConvArgs g = tp.gemm_args;
+      g.x = a.x;
+      g.wt = wt16;
+      g.y = cols;
+      g.bias = nullptr;
+      g.residual = nullptr;
+      g.raw_out = 1;
+      g.act = ACT_IDENTITY;
+      err = launch_pointwise(tp.pw, g, tp.dtype, s);
+      if (err != cudaSuccess) return err;
+      return launch_col2im<T>(a, t, cols, s);
+    }
+  }
+  float* wt = reinterpret_cast<float*>(sc + tp.wt_off);
+  transpose_weights<T, float><<<wgrid, 256, 0, s>>>(static_cast<const T*>(w), wt, a.cg, a.mg, khw, wrows);
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   // the Gemm: a 1x1 convolution of x (widened to float32 for 16-bit types)
   // with wt, raw float32 sums into cols
@@ -161,6 +188,11 @@ cudaError_t launch_typed(const TransposePlan& tp, const ConvArgs& a, const Trans
   g.k_per_split = g.K;
   err = launch_ffma(tp.gemm_plan, g, CONV_F32, s);
   if (err != cudaSuccess) return err;
+  return launch_col2im<T>(a, t, cols, s);
+}
+
+template <typename T>
+cudaError_t launch_col2im(const ConvArgs& a, const TransposeGeo& t, const float* cols, cudaStream_t s) {
   const long long rows = static_cast<long long>(a.n) * a.c_out * t.ho;
   const unsigned blocks = static_cast<unsigned>(std::max<long long>(1, std::min<long long>((rows + 7) / 8, 152LL * 16)));
   switch (a.act) {

@@ -58,12 +58,24 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_transpose_cases(case, dtype):
+def _case_params():
+    """Every case in every element type; 16-bit types also with the Gemm kept
+    on the CUDA cores (the tensor-core Gemm is the default for one group)."""
+    out = []
+    for c in CASES:
+        for dt in ("f32", "f16", "bf16"):
+            out.append(pytest.param(c, dt, 0, id=f"{c[0]}-{dt}"))
+            if dt != "f32":
+                out.append(pytest.param(c, dt, conv.FLAG_NO_PW_MMA, id=f"{c[0]}-{dt}-cudacore"))
+    return out
+
+
+@pytest.mark.parametrize("case,dtype,flags", _case_params())
+def test_transpose_cases(case, dtype, flags):
     name, xs, ws, g, res = case
+    g = dict(g, flags=flags) if flags else g
     p = conv.make_transpose_problem(xs, ws, dtype=dtype, has_bias=True, has_residual=res,
-                                    **{k: v for k, v in g.items() if k not in ("act", "alpha", "beta")})
+                                    **{k: v for k, v in g.items() if k not in ("act", "alpha", "beta", "flags")})
     ho, wo = conv.conv_transpose_output_shape(p)
     cout = ws[1] * g.get("groups", 1)
     seed = zlib.crc32(name.encode()) % 1000
