@@ -119,6 +119,10 @@ EDGE = [
      True, False),
     # more rows than 8 per lane: the one-column-per-lane narrow kernel
     ("depthwise_narrow_very_tall", (1, 4, 70, 30), (4, 1, 3, 3), dict(pads=1, groups=4, act="relu"), True, True),
+    # 16-bit: eight 8-column blocks per row on the tensor-core kernel (Wo = 48); fp32: halo tiles
+    ("depthwise_wide_48", (2, 6, 20, 48), (6, 1, 3, 3), dict(pads=1, groups=6, act="relu"), True, True),
+    # 16-bit, 7x7 over 64 columns: the widest band-matrix variant
+    ("depthwise_wide_64_k7", (1, 4, 18, 64), (4, 1, 7, 7), dict(pads=3, groups=4, act="silu"), True, False),
     # four columns per lane with a ragged last column group and 2 rows per lane
     ("depthwise_cols4_ragged", (3, 5, 10, 18), (10, 1, 5, 5), dict(pads=(2, 1, 2, 3), groups=5, act="silu"),
      True, True),
