@@ -775,10 +775,10 @@ __global__ void __launch_bounds__(256) split_reduce(const ConvArgs a) {
 // zero columns left and right, written once) and its weights, transposed to
 // [channel][tap][output channel], arrive in shared memory by cp.async, the
 // next item's while this one is computed.  A thread holds 8 output channels
-// x 4 consecutive pixels of one row; each k term (channel c, tap u, v) is 4
-// staged inputs at the tap's offset, two broadcast float4 weight loads and 32
+// x 4 pixels of one row, Wo/4 columns apart; each k term (channel c, tap u, v)
+// is 4 staged inputs at the tap's offset, two broadcast float4 weight loads and 32
 // FMAs, k in (c, u, v) order into one float32 chain per output, then the fused
-// epilogue and one 16-byte store per output channel.
+// epilogue.
 template <int K, int ACT>
 __global__ void __launch_bounds__(kGdThreads, 3) grouped_direct(const ConvArgs a, const GdPlan g) {
   extern __shared__ __align__(16) float gsm[];
@@ -847,15 +847,18 @@ __global__ void __launch_bounds__(kGdThreads, 3) grouped_direct(const ConvArgs a
     const float* xs = buf;
     const float* ws = buf + xs_floats;
     for (int u_ = tid; u_ < units; u_ += kGdThreads) {
+      // a thread's 4 pixels are columns cb, cb + Wo/4, cb + 2 Wo/4, cb + 3 Wo/4
+      // of its row: consecutive threads take consecutive cb, so each of the 4
+      // staged-input reads of a tap (and each store) is consecutive across them
       const int h8 = u_ % halves, pg = u_ / halves;
-      const int r = pg / groups4, col0 = 4 * (pg - (pg / groups4) * groups4);
+      const int r = pg / groups4, cb = pg - (pg / groups4) * groups4;
       if (oh0 + r >= a.ho) continue;
       float acc[8][4];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
-      const float* xb = xs + r * g.pitch + g.cofs - a.pl + col0;
+      const float* xb = xs + r * g.pitch + g.cofs - a.pl + cb;
       const float* wb = ws + 8 * h8;
       for (int c = 0; c < a.cg; ++c) {
         const float* xc = xb + c * g.rows_in * g.pitch;
@@ -865,7 +868,7 @@ __global__ void __launch_bounds__(kGdThreads, 3) grouped_direct(const ConvArgs a
 #pragma unroll
           for (int v = 0; v < K; ++v) {
             const float* xp = xc + u * a.dh * g.pitch + v * a.dw;
-            const float xv[4] = {xp[0], xp[1], xp[2], xp[3]};
+            const float xv[4] = {xp[0], xp[groups4], xp[2 * groups4], xp[3 * groups4]};
             const float4 w0 = *reinterpret_cast<const float4*>(wc + (u * K + v) * a.mg);
             const float4 w1 = *reinterpret_cast<const float4*>(wc + (u * K + v) * a.mg + 4);
             const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -879,22 +882,15 @@ __global__ void __launch_bounds__(kGdThreads, 3) grouped_direct(const ConvArgs a
       for (int j = 0; j < 8; ++j) {
         const int co = gi * a.mg + 8 * h8 + j;
         const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo +
-                              static_cast<long long>(oh0 + r) * a.wo + col0;
+                              static_cast<long long>(oh0 + r) * a.wo + cb;
         const float b = bias ? bias[co] : 0.0f;
-        float rv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (res) {
-          const float4 t = *reinterpret_cast<const float4*>(res + out);
-          rv[0] = t.x, rv[1] = t.y, rv[2] = t.z, rv[3] = t.w;
-        }
-        float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float t = acc[j][q];
           if (bias) t = __fadd_rn(t, b);
-          if (res) t = __fadd_rn(t, rv[q]);
-          v[q] = act_fn<ACT>(t, a.alpha, a.beta);
+          if (res) t = __fadd_rn(t, res[out + q * groups4]);
+          y[out + q * groups4] = act_fn<ACT>(t, a.alpha, a.beta);
         }
-        *reinterpret_cast<float4*>(y + out) = make_float4(v[0], v[1], v[2], v[3]);
       }
     }
     __syncthreads();  // this buffer is refilled two items from now
