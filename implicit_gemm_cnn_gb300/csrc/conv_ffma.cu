@@ -1101,9 +1101,9 @@ bool gd_plan(const conv_problem* p, long long ho, long long wo, GdPlan* g) {
 }
 
 cudaError_t launch_ffma(const Plan& plan, const ConvArgs& a, int dtype, cudaStream_t s) {
-  // the grouped path stores (and reads the residual) 16 bytes at a time
-  if (plan.gd.ok && dtype == CONV_F32 && reinterpret_cast<uintptr_t>(a.y) % 16 == 0 &&
-      (a.residual == nullptr || reinterpret_cast<uintptr_t>(a.residual) % 16 == 0))
+  // grouped layers with staged input rows (any alignment of y and the residual;
+  // x rows are copied 16 bytes at a time when x allows it)
+  if (plan.gd.ok && dtype == CONV_F32)
     return plan.gd.k == 3 ? launch_gd_k<3>(plan, a, s) : launch_gd_k<5>(plan, a, s);
   if (a.xw) {
     cudaError_t err = cudaErrorInvalidValue;

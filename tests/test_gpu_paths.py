@@ -95,7 +95,7 @@ OFFSET_CASES = [
      (1, 2, 3), True),
     ("ffma_general_y_off", (1, 5, 19, 17), (20, 5, 4, 3), dict(stride=(1, 2), pads=(1, 1, 2, 0)), ("f32",),
      (2, 1, 1), True),
-    # grouped CUDA-core layer whose y is not 16-byte aligned: the per-k gather kernel
+    # grouped CUDA-core layer with staged input rows, y and the residual off 4 bytes (scalar stores)
     ("grouped_y_off", (2, 32, 13, 12), (32, 16, 3, 3), dict(pads=2, dilation=2, groups=2, act="silu"), ("f32",),
      (0, 1, 1), True),
 ]
