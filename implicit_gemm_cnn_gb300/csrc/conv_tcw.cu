@@ -461,8 +461,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int units = rows * p.wp * nb;  // (row, channel block, column)
         const int per_row = p.wp * nb;
         const int base_slot = static_cast<int>((static_cast<long long>(brow0) * p.wp) % R);
+        bool vec_done = false;
+        if constexpr (PH == 1) {
+          if ((a.cg & 7) == 0) {
+            // whole 8-channel blocks: 4 staged columns of 8 channels at a time
+            // (eight 8-byte reads, a register transpose, four 16-byte
+            // writes), then the padding columns as zeros
+            vec_done = true;
+            const int nq = p.vw / 4;  // 4-column chunks of a staged row
+            const int vunits = rows * nb * nq;
+            for (int e = ptid; e < vunits; e += kProd) {
+              const int q4 = e % nq, t1 = e / nq;
+              const int cbv = t1 % nb, brv = first + t1 / nb;
+              uint32_t o[4][4];  // o[i]: column i's channels (0,1) (2,3) (4,5) (6,7), low half the even one
+              if (cbv * 8 < a.cg) {
+                const uint16_t* src = sg + (static_cast<size_t>(cbv) * 8 * SB + brv) * p.vw + 4 * q4;
+                uint2 r[8];  // r[j]: channel j, columns (0,1) and (2,3)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = *reinterpret_cast<const uint2*>(src + static_cast<size_t>(j) * cstride);
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) {
+                  o[0][pr] = __byte_perm(r[2 * pr].x, r[2 * pr + 1].x, 0x5410);
+                  o[1][pr] = __byte_perm(r[2 * pr].x, r[2 * pr + 1].x, 0x7632);
+                  o[2][pr] = __byte_perm(r[2 * pr].y, r[2 * pr + 1].y, 0x5410);
+                  o[3][pr] = __byte_perm(r[2 * pr].y, r[2 * pr + 1].y, 0x7632);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                  for (int pr = 0; pr < 4; ++pr) o[i][pr] = 0u;
+              }
+              int slot = base_slot + brv * p.wp + a.pl + 4 * q4;  // < 2R: R exceeds a band's positions
+              if (slot >= R) slot -= R;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 u4 = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
+                uint8_t* dst = ring + (static_cast<size_t>(cbv) * RM + slot) * 16u;
+                *reinterpret_cast<uint4*>(dst) = u4;
+                if (slot < p.mirror) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(R) * 16u) = u4;
+                if (++slot == R) slot = 0;
+              }
+            }
+            const int pc = p.wp - p.vw;  // padding columns: [0, pl) and [pl + vw, wp)
+            for (int e = ptid; e < rows * nb * pc; e += kProd) {
+              const int q = e % pc, t1 = e / pc;
+              const int cbv = t1 % nb, brv = first + t1 / nb;
+              int slot = base_slot + brv * p.wp + (q < a.pl ? q : q + p.vw);
+              if (slot >= R) slot -= R;
+              uint8_t* dst = ring + (static_cast<size_t>(cbv) * RM + slot) * 16u;
+              *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+              if (slot < p.mirror) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(R) * 16u) = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        }
         int br = first + ptid / per_row, cb = (ptid % per_row) / p.wp, c = ptid % p.wp;
-        for (int e = ptid; e < units; e += kProd) {
+        for (int e = ptid; !vec_done && e < units; e += kProd) {
           // value j of the unit: channel cb*8 + j (PH 1), or channel
           // cb*2 + j/4, phase row (j/2)%2, phase column j%2 (PH 2); staged at
           // [channel][PH*SB rows][vw columns]
