@@ -115,10 +115,11 @@ def kernel_source(variant: str) -> str:
     return os.path.join(ROOT, "implicit_gemm_cnn_gb300", "csrc", name)
 
 
-def profiled_traffic(layer_name: str, variant: str):
+def profiled_traffic(layer_name: str, variant: str, source: str | None = None):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if the kernel source is unchanged since the capture."""
-    src = kernel_source(variant)
+    workload, if the kernel source is unchanged since the capture (`source`:
+    the dominant kernel's file under csrc/, else the variant's)."""
+    src = (os.path.join(ROOT, "implicit_gemm_cnn_gb300", "csrc", source) if source else kernel_source(variant))
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     except OSError:
@@ -513,7 +514,8 @@ def run_integer(L, steps: int, warmup: int, world: int, local_rank: int) -> dict
     return {"value": value, "us": us, "clocks": clocks, "launches": 3 * steps,
             "roofline": {"bound": "alu", "achieved": round(ops / (us / 1e6) / 1e12, 2), "peak": DP4A_PEAK_TOPS,
                          "unit": "TOP/s", "frac": round(ops / (us / 1e6) / 1e12 / DP4A_PEAK_TOPS, 4),
-                         "traffic": None, "tensor_or_alu_frac": round(ops / (us / 1e6) / 1e12 / DP4A_PEAK_TOPS, 4)}}
+                         "traffic": profiled_traffic(L.name, "", "conv_integer.cu"),
+                         "tensor_or_alu_frac": round(ops / (us / 1e6) / 1e12 / DP4A_PEAK_TOPS, 4)}}
 
 
 # ---- ConvTranspose ---------------------------------------------------------------
@@ -586,7 +588,8 @@ def run_transpose(L, steps: int, warmup: int, world: int, local_rank: int) -> di
     return {"value": aggregate(fl * steps, world, secs) / 1e12, "us": us, "clocks": clocks,
             "launches": launches * steps, "tensor_gemm": tc,
             "roofline": {"bound": "tensor" if tc else "alu", "achieved": round(rate, 2), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(rate / peak, 4), "traffic": None,
+                         "unit": "TFLOP/s", "frac": round(rate / peak, 4),
+                         "traffic": profiled_traffic(L.name, "", "conv_pointwise.cu" if tc else "conv_ffma.cu"),
                          "tensor_or_alu_frac": round(rate / peak, 4)}}
 
 

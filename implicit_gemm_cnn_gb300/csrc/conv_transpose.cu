@@ -6,9 +6,11 @@
 //
 // The Gemm: for every image and group, cols[(co, u, v)][ih*W + iw] =
 // sum_c w[c][co][u][v] * x[c][ih][iw] -- a 1x1 convolution of x whose
-// weights are w transposed to [group][(co, u, v)][c]; it runs in float32 on
-// the CUDA-core implicit-GEMM kernel (16-bit x and w widened first, exactly)
-// with its raw float32 sums written to scratch (no epilogue).  The col2im:
+// weights are w transposed to [group][(co, u, v)][c], with its raw float32
+// sums written to scratch (no epilogue).  16-bit layers with one group run it
+// on the tensor cores (the pointwise tile kernel: products exact, float32
+// accumulation); the others in float32 on the CUDA-core implicit-GEMM kernel
+// (a 16-bit x and w widened first, exactly).  The col2im:
 // output (n, co, oh, ow) gathers the taps (u, v)
 // whose input position (oh + pt - u*dh)/sh, (ow + pl - v*dw)/sw is exact and
 // inside the input, adds them in (u, v) order in float32, then bias,
