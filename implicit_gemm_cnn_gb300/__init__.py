@@ -22,7 +22,7 @@ import threading
 __all__ = [
     "ConvError", "ConvLibraryError", "ConvProblem", "ConvPlanInfo", "ACTIVATIONS", "DTYPES",
     "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "FLAG_NO_UNFOLD", "FLAG_FORCE_UNFOLD", "FLAG_WINOGRAD",
-    "FLAG_NO_WINOGRAD", "FLAG_NO_DW_MMA", "FLAG_NO_PW_MMA", "VARIANTS", "conv_abi_version", "conv_status_string",
+    "FLAG_NO_WINOGRAD", "FLAG_NO_DW_MMA", "FLAG_NO_PW_MMA", "FLAG_NO_CLUSTER_K", "VARIANTS", "conv_abi_version", "conv_status_string",
     "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
     "conv_forward", "conv_device_error", "conv_selftest_bounded_wait", "conv_forward_fixed_scratch",
     "FIXED_SCRATCH_BYTES",
@@ -51,6 +51,7 @@ FLAG_WINOGRAD = 0x20
 FLAG_NO_WINOGRAD = 0x40
 FLAG_NO_DW_MMA = 0x80
 FLAG_NO_PW_MMA = 0x4000
+FLAG_NO_CLUSTER_K = 0x8000
 SPLIT_K_SHIFT = 8
 STATUS = {0: "CONV_OK", 1: "CONV_ERR_SHAPE", 2: "CONV_ERR_OVERFLOW", 3: "CONV_ERR_DTYPE",
           4: "CONV_ERR_ACT", 5: "CONV_ERR_NULL", 6: "CONV_ERR_SCRATCH", 7: "CONV_ERR_ALIAS",

@@ -252,6 +252,10 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   out->unf.tail_off = L.tail_off;
   out->info.scratch_bytes = L.total;
   out->k_per_split = static_cast<int>(len);
+  // the k ranges of a tile reduced within a thread-block cluster (at most 16
+  // blocks; the 128 x 128 tile keeps the planes); the planes stay in the
+  // scratch figure, for a device where no such cluster fits
+  out->cluster_k = split >= 2 && split <= 16 && bi != 0 && !(p->flags & CONV_FLAG_NO_CLUSTER_K) ? 1 : 0;
   if (out->gd.ok) {
     out->info.tile_m = static_cast<int>(s.mg);
     out->info.tile_n = static_cast<int>(kGdRows * s.wo);
@@ -546,7 +550,60 @@ const char* variant_name(int v) {
 std::mutex g_smem_mu;
 std::map<std::pair<const void*, int>, size_t> g_smem_optin;  // (kernel, device) -> bytes
 
+struct ClusterKey {
+  const void* func;
+  int dev, cluster, threads;
+  size_t smem;
+  bool operator<(const ClusterKey& o) const {
+    if (func != o.func) return func < o.func;
+    if (dev != o.dev) return dev < o.dev;
+    if (cluster != o.cluster) return cluster < o.cluster;
+    if (threads != o.threads) return threads < o.threads;
+    return smem < o.smem;
+  }
+};
+std::mutex g_cluster_mu;
+std::map<ClusterKey, bool> g_cluster_fits;
+
 }  // namespace
+
+bool conv::cluster_fits(const void* func, int cluster, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  const ClusterKey key{func, dev, cluster, threads, smem};
+  auto it = g_cluster_fits.find(key);
+  if (it != g_cluster_fits.end()) return it->second;
+  bool ok = true;
+  if (cluster > 8 && cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();  // a refused attribute leaves no error behind for the next launch check
+    ok = false;
+  }
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, static_cast<unsigned>(cluster));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(cluster);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // likewise for a refused query
+      n = 0;
+    }
+    ok = n >= 1;
+  }
+  g_cluster_fits[key] = ok;
+  return ok;
+}
 
 cudaError_t conv::opt_in_smem(const void* func, size_t bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;  // no opt-in needed
@@ -726,9 +783,10 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
     if (plan.ffma_unf && plan.unf.tail_split > 0)
       snprintf(tail, sizeof(tail), " tail=%lld tiles x %d k ranges", static_cast<long long>(plan.unf.tiles - plan.unf.tail_first),
                plan.unf.tail_split);
-    snprintf(buf, len, "%s tile=%dco x %dpx (%dx%d per thread) B=%s split_k=%d%s blocks=%lld scratch=%llu sms=%d",
+    const char* reduce = i.split_k < 2 ? "" : (plan.cluster_k ? " reduce=cluster" : " reduce=planes");
+    snprintf(buf, len, "%s tile=%dco x %dpx (%dx%d per thread) B=%s split_k=%d%s%s blocks=%lld scratch=%llu sms=%d",
              variant_name(i.variant), i.tile_m, i.tile_n, c.tm, c.tn,
-             plan.ffma_unf ? "unfolded" : (plan.ffma_vec ? "pointwise" : "gathered"), i.split_k, tail,
+             plan.ffma_unf ? "unfolded" : (plan.ffma_vec ? "pointwise" : "gathered"), i.split_k, reduce, tail,
              static_cast<long long>(i.ctas), static_cast<unsigned long long>(i.scratch_bytes), sm);
   }
   // the number of kernels one call launches, last
@@ -828,6 +886,7 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
     default: {
       a.split = plan.info.split_k;
       a.k_per_split = plan.k_per_split;
+      a.cluster_k = plan.cluster_k;
       a.partial = static_cast<float*>(scratch);
       const FfmaLayout L = ffma_layout(plan, s, p->n, chunk);
       if (plan.ffma_unf) {
@@ -854,7 +913,7 @@ conv_status conv_forward(const conv_problem* p, const void* x, const void* w, co
         a.img0 = static_cast<int>(n0);
         a.part_total = (n1 - n0) * a.c_out * a.howo;
         err = launch_ffma(plan, a, p->dtype, cs);
-        if (err == cudaSuccess && a.split > 1) err = launch_split_reduce(a, p->dtype, cs);
+        if (err == cudaSuccess && a.split > 1 && !a.cluster_k) err = launch_split_reduce(a, p->dtype, cs);
       }
       break;
     }

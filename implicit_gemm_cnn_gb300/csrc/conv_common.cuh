@@ -54,6 +54,8 @@ struct ConvArgs {
   // from blk_tail_lo on (1-D grid)
   long long px_tile0, blk_whole_lo, blk_whole_n, blk_tail_lo;
   int raw_out;             // CUDA-core kernel: write the raw float32 sums to `partial` (no epilogue)
+  int cluster_k;           // split k: the k ranges of a tile are one thread-block cluster and are
+                           // added through distributed shared memory (no planes, no second kernel)
 };
 
 enum Act {

@@ -14,10 +14,15 @@
 // so y is written once.
 //
 // Split k ("Convolution, pooling and resize", RTX 4070 split k): when the grid
-// is too small to fill the device, k is cut into ranges; each range's block
-// writes its raw float32 sums into its own plane of scratch, and
-// split_reduce adds the planes in range order, then applies the epilogue.
-// No atomics: every output's sum has an order fixed by the shape.
+// is too small to fill the device, k is cut into ranges.  Normally the ranges
+// of a tile are the blocks of one thread-block cluster: each keeps its raw
+// float32 sums in its shared memory and, after a cluster barrier, every block
+// adds a share of the tile's outputs over the ranges in range order (reading
+// the other blocks' shared memory) and applies the epilogue.  Otherwise (more
+// than 16 ranges, the 128 x 128 tile, or no such cluster fits) each range's
+// block writes its sums into its own plane of scratch and split_reduce adds
+// the planes in range order, then applies the epilogue.  Both give the same
+// bits; no atomics: every output's sum has an order fixed by the shape.
 //
 // Pipeline: fp32 tiles arrive by cp.async (4-byte copies with zero fill for
 // padded taps) kFfmaStages deep; 16-bit operands (the fallback for shapes the
@@ -107,6 +112,30 @@ __device__ __forceinline__ unsigned ctaid_x() {
 __device__ __forceinline__ unsigned ctaid_y() {
   unsigned v;
   asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(v));
+  return v;
+}
+
+// Split k within a thread-block cluster: the blocks of one tile's k ranges
+// form one cluster (cluster dims 1 x 1 x split, rank = k range) and read each
+// other's shared memory.
+constexpr int kMaxClusterK = 16;
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned v;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(v));
+  return v;
+}
+// All threads of all blocks of the cluster: shared-memory writes before it are
+// seen by reads after it from any block of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;\n" ::: "memory");
+}
+// The float at this block's shared address `saddr`, read from block `rank`'s
+// shared memory.
+__device__ __forceinline__ float ld_cluster_f32(unsigned saddr, unsigned rank) {
+  unsigned r;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
   return v;
 }
 
@@ -481,6 +510,55 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
     }
     return;
   } else {
+    if (a.cluster_k) {
+      // split k within the cluster: each k range's block writes its raw sums
+      // to its own shared memory; after the cluster barrier, rank r finishes
+      // a 1/split share of the tile: per output the ranges' sums added in rank
+      // (= k) order, then the fused epilogue and one store -- the additions
+      // and roundings of the planes + split_reduce path, bit for bit.
+      __syncthreads();  // every warp is past its last reads of the stages
+#pragma unroll
+      for (int jg = 0; jg < TN / 4; ++jg)
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+          const int ml = i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4);
+          *reinterpret_cast<float4*>(smem + ml * BN + jg * GN + tx * 4) =
+              make_float4(acc[i][jg * 4], acc[i][jg * 4 + 1], acc[i][jg * 4 + 2], acc[i][jg * 4 + 3]);
+        }
+      cluster_sync();
+      const int rank = static_cast<int>(cluster_rank());
+      const int per = (BM * BN + a.split - 1) / a.split;
+      const int e_end = min(BM * BN, (rank + 1) * per);
+      const unsigned sbase = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+      const T* __restrict__ resp = static_cast<const T*>(a.residual);
+      const T* __restrict__ biasp = static_cast<const T*>(a.bias);
+      T* __restrict__ yo = static_cast<T*>(a.y);
+      for (int e = rank * per + tid; e < e_end; e += NT) {
+        const int ml = e / BN, col = e - (e / BN) * BN;
+        const int m = m0 + ml;
+        const long long p = pix0 + col;
+        if (m >= a.mg || p < a.pix_lo || p >= a.pix_hi) continue;
+        const unsigned addr = sbase + static_cast<unsigned>(e) * 4u;
+        float t[kMaxClusterK];
+#pragma unroll
+        for (int z = 0; z < kMaxClusterK; ++z)
+          if (z < a.split) t[z] = ld_cluster_f32(addr, static_cast<unsigned>(z));
+        float v[1] = {t[0]};
+#pragma unroll
+        for (int z = 1; z < kMaxClusterK; ++z)
+          if (z < a.split) v[0] = __fadd_rn(v[0], t[z]);
+        const int n = static_cast<int>(p / a.howo);
+        const long long rem = p - static_cast<long long>(n) * a.howo;
+        const int co = g * a.mg + m;
+        const long long out = (static_cast<long long>(n) * a.c_out + co) * a.howo + rem;
+        float bv[1] = {biasp ? to_f32(biasp[co]) : 0.0f};
+        float rv[1] = {resp ? to_f32(resp[out]) : 0.0f};
+        epilogue_n<1>(v, bv, rv, biasp != nullptr, resp != nullptr, a.act, a.alpha, a.beta);
+        yo[out] = from_f32<T>(v[0]);
+      }
+      cluster_sync();  // no block leaves while another still reads its tile
+      return;
+    }
     // only pixels in [pix_lo, pix_hi) (the whole batch, or a chunk of images)
     // are stored; split planes hold the chunk's outputs from image img0 on
     const long long out0 = static_cast<long long>(a.img0) * a.c_out * a.howo;
@@ -933,6 +1011,9 @@ cudaError_t launch_gd_k(const Plan& plan, const ConvArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_reduce_typed(const ConvArgs& a, cudaStream_t s);
+
 template <typename T, int CFG, int BMODE>
 cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& args, cudaStream_t s) {
   constexpr FfmaCfg c = kFfmaCfgs[CFG];
@@ -972,6 +1053,36 @@ cudaError_t launch_cfg_vb(const Plan& plan, const ConvArgs& args, cudaStream_t s
   }
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(co_tiles * a.groups),
             static_cast<unsigned>(a.split));
+  if (a.cluster_k) {
+    // the k ranges of a tile as one cluster; its shared memory also holds the
+    // block's BM x BN float32 sums
+    const size_t csmem = std::max(smem, static_cast<size_t>(c.bm) * c.bn * sizeof(float));
+    const void* fn = reinterpret_cast<const void*>(kern);
+    err = opt_in_smem(fn, csmem);
+    if (err != cudaSuccess) return err;
+    if (c.bm * c.bn != 128 * 128 && a.split >= 2 && a.split <= kMaxClusterK &&
+        cluster_fits(fn, a.split, c.threads(), csmem)) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = grid;
+      cfg.blockDim = dim3(static_cast<unsigned>(c.threads()), 1, 1);
+      cfg.dynamicSmemBytes = csmem;
+      cfg.stream = s;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = static_cast<unsigned>(a.split);
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, kern, static_cast<const ConvArgs&>(a), ktab_cap);
+    }
+    // no such cluster fits this device: the planes and the reduction kernel
+    a.cluster_k = 0;
+    kern<<<grid, c.threads(), smem, s>>>(a, ktab_cap);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_reduce_typed<T>(a, s);
+  }
   kern<<<grid, c.threads(), smem, s>>>(a, ktab_cap);
   (void)plan;
   return cudaGetLastError();
@@ -1059,7 +1170,7 @@ int ffma_launch_count(const Plan& plan) {
   if (plan.gd.ok) return 1;
   int n = 1;
   if (plan.ffma_unf) n += 1 + (plan.unf.tail_split > 0 ? 1 : 0);
-  if (plan.info.split_k > 1) n += 1;
+  if (plan.info.split_k > 1 && !plan.cluster_k) n += 1;
   return n;
 }
 

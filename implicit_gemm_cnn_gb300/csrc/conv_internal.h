@@ -172,6 +172,7 @@ struct Plan {
   int ffma_unf;     // the unfolded-B pre-pass and 16-byte copies (UnfPlan)
   UnfPlan unf;
   int k_per_split;  // terms per k range of the split variant
+  int cluster_k;    // split k reduced within a cluster of the k ranges' blocks (else planes + split_reduce)
   DwPlan dw;
   TcPlan tc;
   WinPlan tcw;
@@ -184,6 +185,13 @@ struct Plan {
 // check and the update hold one lock, so concurrent host threads never lower
 // it under another thread's launch.
 cudaError_t opt_in_smem(const void* func, size_t bytes);
+
+// Whether `func` can run as clusters of `cluster` blocks (cluster dims 1 x 1 x
+// cluster) of `threads` threads and `smem` bytes of dynamic shared memory on
+// the current device: at least one such cluster fits.  Clusters of more than 8
+// blocks are allowed for `func` first.  The answer is remembered per (kernel,
+// device, cluster, threads, smem).
+bool cluster_fits(const void* func, int cluster, int threads, size_t smem);
 
 // ConvInteger (conv_integer.cu): the unfolded byte matrix cols[g][q][p]
 // (k words of 4 terms x pixels), per-pixel byte sums sx[g][p], the weight

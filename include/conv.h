@@ -91,6 +91,9 @@ typedef enum conv_act {
                                         tensor-core band-matrix kernel              */
 #define CONV_FLAG_NO_PW_MMA 0x4000u  /* 16-bit 1x1 layers: not the pointwise tensor-core
                                         tile kernel                                 */
+#define CONV_FLAG_NO_CLUSTER_K 0x8000u /* split k: the ranges' float32 planes in scratch and a
+                                        second kernel that adds them, not the reduction
+                                        within a thread-block cluster               */
 #define CONV_FLAG_SPLIT_K_SHIFT 8   /* bits 8..13: force this many ranges of k (1-63) */
 #define CONV_FLAG_SPLIT_K_MASK 0x3f00u
 

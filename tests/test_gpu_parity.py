@@ -258,6 +258,47 @@ def test_forced_split_k(split, dtype, unfold):
     assert out["ok"], out
 
 
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int32) if t.dtype == torch.float32 else t.view(torch.int16)
+
+
+@pytest.mark.parametrize("unfold", [False, True])
+@pytest.mark.parametrize("split", [2, 7, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_cluster_split_k_matches_planes(split, dtype, unfold):
+    """Split k reduced within a thread-block cluster (one block per k range,
+    sums read from the other blocks' shared memory) gives the bits of the
+    planes + ordered-reduction kernel, and both pass the oracle bar
+    ("Convolution, pooling and resize", split k; Determinism)."""
+    xs, ws = (2, 64, 9, 12), (24, 64, 3, 3)
+    g = dict(pads=1, act="silu")
+    inp = random_layer_inputs(xs, ws, dtype, seed=40 + split, bias=True, residual_shape=(2, 24, 9, 12))
+    flags = conv.FLAG_FORCE_FFMA | (split << conv.SPLIT_K_SHIFT)
+    if unfold:
+        flags |= conv.FLAG_FORCE_UNFOLD
+    desc = conv.conv_describe_variant(conv.make_problem(xs, ws, dtype=dtype, flags=flags, **g))
+    assert "reduce=cluster" in desc and desc.endswith("launches=%d" % (2 if unfold else 1)), desc
+    desc_p = conv.conv_describe_variant(conv.make_problem(xs, ws, dtype=dtype, flags=flags | conv.FLAG_NO_CLUSTER_K, **g))
+    assert "reduce=planes" in desc_p, desc_p
+    y_c = run_gpu(inp, flags=flags, **g)
+    y_p = run_gpu(inp, flags=flags | conv.FLAG_NO_CLUSTER_K, **g)
+    assert torch.equal(_bits(y_c), _bits(y_p))
+    out = check_full(inp, dtype, y_c, **g)
+    assert out["ok"], out
+
+
+def test_cluster_split_k_workload_layer():
+    """The 2048->512 1x1 layer at 7x7 (N=1) at full size: the cluster reduction
+    is the default there (one launch) and matches the planes bit for bit."""
+    L = LAYERS["late_1x1_splitk_f32"]
+    desc = conv.conv_describe_variant(_problem(L))
+    assert "reduce=cluster" in desc and desc.endswith("launches=1"), desc
+    inp = make_inputs(L, seed_offset=3)
+    a = run_gpu(inp, **_geo(L))
+    b = run_gpu(inp, flags=conv.FLAG_NO_CLUSTER_K, **_geo(L))
+    assert torch.equal(_bits(a), _bits(b))
+
+
 @pytest.mark.parametrize("name", ["resnet50_3x3_f16", "mbv3_dw5x5_f32", "late_1x1_splitk_f32",
                                   "grouped_dil2_f32", "resnet50_3x3_256_f32"])
 def test_bit_identical_runs(name):
