@@ -253,13 +253,18 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
   // q / (BN/4), pixels pix0 + 4*(q % (BN/4)) .. +3, all in one image row (the
   // plane length, or the output row, is a multiple of 4)
   constexpr int QV = VEC ? (BK * BN / 4 + NT - 1) / NT : 1;
-  long long vbase[BMODE == kBPointwise ? QV : 1];
-  int uoff[BMODE == kBUnfolded ? QV : 1];  // unfolded: 32-bit element offsets into xw
-  bool vok[QV];
+  // when the block's threads cover whole k rows (NT a multiple of BN/4) and
+  // every copy is used, a thread's copies share its 4 pixels: one pixel
+  // offset and one validity flag serve all of them
+  constexpr bool VSAME = VEC && NT % (BN / 4) == 0 && (BK * BN / 4) % NT == 0;
+  constexpr int QVS = VSAME ? 1 : QV;
+  long long vbase[BMODE == kBPointwise ? QVS : 1];
+  int uoff[BMODE == kBUnfolded ? QVS : 1];  // unfolded: 32-bit element offsets into xw
+  bool vok[QVS];
   if constexpr (VEC) {
     const long long unf_img = static_cast<long long>(a.c_in) * a.kw * a.hu * a.wo;  // xw per image
 #pragma unroll
-    for (int i = 0; i < QV; ++i) {
+    for (int i = 0; i < QVS; ++i) {
       const int q = tid + i * NT;
       const long long p = pix0 + 4 * (q % (BN / 4));
       vok[i] = q < BK * BN / 4 && p < a.npix && (BMODE != kBUnfolded || (p >= a.pix_lo && p < a.pix_hi));
@@ -280,10 +285,12 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
   // elements): the pixel part of each B copy (uoff) and the group's first
   // weight of the block's channel tile (aoff) are fixed for the whole k loop.
   constexpr int QA = BMODE == kBUnfolded ? (BK * BM / 4 + NT - 1) / NT : 1;
+  constexpr bool ASAME = NT % (BM / 4) == 0;  // a thread's copies share their 4 channels
+  constexpr int QAS = ASAME ? 1 : QA;
   const int aoff = BMODE == kBUnfolded ? g * a.K * a.mg4 + m0 : 0;
-  bool aok[QA];  // unfolded A: the copy's four channels are real (else zeros)
+  bool aok[QAS];  // unfolded A: the copy's four channels are real (else zeros)
 #pragma unroll
-  for (int i = 0; i < QA; ++i) aok[i] = m0 + 4 * ((tid + i * NT) % (BM / 4)) < a.mg4;
+  for (int i = 0; i < QAS; ++i) aok[i] = m0 + 4 * ((tid + i * NT) % (BM / 4)) < a.mg4;
 
   float acc[TM][TN];
 #pragma unroll
@@ -320,7 +327,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
           const int q = tid + i * NT;
           const int kk = q / (BM / 4), m4 = q % (BM / 4);
           const int k = k0 + kk;
-          const bool ok = k < seg_end && aok[i];
+          const bool ok = k < seg_end && aok[ASAME ? 0 : i];
           const float* src = a.wtt + (ok ? aoff + k * a.mg4 + 4 * m4 : 0);
           if ((BK * BM / 4) % NT == 0 || q < BK * BM / 4) cp_async16(as + kk * AS + 4 * m4, src, ok);
         }
@@ -344,8 +351,8 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
           const int q = tid + i * NT;
           const int kk = q / (BN / 4), c4 = q % (BN / 4);
           const int k = k0 + kk;
-          const bool ok = vok[i] && k < seg_end;
-          const float* src = a.xw + (ok ? uoff[i] + ktab[k - kseg].x : 0);
+          const bool ok = vok[VSAME ? 0 : i] && k < seg_end;
+          const float* src = a.xw + (ok ? uoff[VSAME ? 0 : i] + ktab[k - kseg].x : 0);
           if ((BK * BN / 4) % NT == 0 || q < BK * BN / 4) cp_async16(bs + kk * BN + 4 * c4, src, ok);
         }
       } else if constexpr (BMODE == kBPointwise) {
@@ -355,8 +362,8 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
           const int q = tid + i * NT;
           const int kk = q / (BN / 4), c4 = q % (BN / 4);
           const int k = k0 + kk;
-          const bool ok = vok[i] && k < seg_end;
-          const float* src = ok ? xb + vbase[i] + ktab[k - kseg].x : xb;
+          const bool ok = vok[VSAME ? 0 : i] && k < seg_end;
+          const float* src = ok ? xb + vbase[VSAME ? 0 : i] + ktab[k - kseg].x : xb;
           if (q < BK * BN / 4) cp_async16(bs + kk * BN + 4 * c4, src, ok);
         }
       } else if (bloader) {
@@ -394,7 +401,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN)) __maxnreg__(ffma_maxreg
       cp_async_commit();
       const float* as = As + (c % S) * BK * AS;
       const float* bs = Bs + (c % S) * BK * BN;
-#pragma unroll
+#pragma unroll 8
       for (int kk = 0; kk < BK; ++kk) {
         float ra[TM], rb[TN];
         const float4 a0 = *reinterpret_cast<const float4*>(as + kk * AS + ty * 4);
