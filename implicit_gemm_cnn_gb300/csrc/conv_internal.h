@@ -17,7 +17,7 @@ struct FfmaCfg {
   int bm, bn, tm, tn;
   int threads() const { return (bm / tm) * (bn / tn); }
 };
-constexpr int kFfmaBK = 8;          // k terms per pipeline stage
+constexpr int kFfmaBK = 16;         // k terms per pipeline stage
 constexpr int kFfmaBKU = 16;        // k terms per stage with unfolded B (16-byte copies only)
 constexpr int kFfmaStages = 4;      // pipeline depth
 constexpr int kFfmaKTab = 2304;     // k entries of the window table per segment
