@@ -138,9 +138,16 @@ typedef enum conv_status {
  * Variants: the variant a device runs is a function of the problem). */
 typedef enum conv_variant {
   CONV_VARIANT_IGEMM_FFMA = 0,     /* implicit GEMM on CUDA cores, fused epilogue */
-  CONV_VARIANT_IGEMM_FFMA_SPLIT = 1, /* the same with k split into ranges, each
-                                      into a float32 plane of scratch, then an
-                                      ordered sum + epilogue pass            */
+  CONV_VARIANT_IGEMM_FFMA_SPLIT = 1, /* the same with k split into ranges: the
+                                      ranges of a tile are one thread-block
+                                      cluster and add their float32 sums in
+                                      range order through distributed shared
+                                      memory, then the epilogue (one launch);
+                                      or (CONV_FLAG_NO_CLUSTER_K, more than 16
+                                      ranges, no such cluster on the device)
+                                      each range into a float32 plane of
+                                      scratch, then an ordered sum + epilogue
+                                      pass; both give the same bits          */
   CONV_VARIANT_DEPTHWISE = 2,      /* direct halo-tiled kernel (one input channel
                                       per group, any channel multiplier)     */
   CONV_VARIANT_IGEMM_TC = 3,       /* implicit GEMM on tcgen05 tensor cores,
@@ -219,7 +226,10 @@ CONV_API conv_status conv_plan(const conv_problem* p, int32_t sm_count, conv_pla
 
 /* Scratch bytes conv_forward needs for `p` on the current CUDA device
  * ("Convolution, pooling and resize", Layout and operands: the scratch
- * query): the float32 partial planes of split k (ranges x output elements),
+ * query): the float32 partial planes of split k (ranges x output elements;
+ * reported even where the ranges are reduced within a thread-block cluster,
+ * which leaves them unused, so that a device where no such cluster fits can
+ * still run the call),
  * the repacked weights of the shifted-window variant (channel tiles x k
  * blocks x tile channels x 16 bytes), the CUDA-core kernel's unfolded input
  * (float32, n x c_in x kw x padded rows x Wo) and transposed weights when it
