@@ -196,7 +196,7 @@ void plan_ffma(const conv_problem* p, const Shape& s, int sm, Plan* out) {
   const long long ctas = ((s.mg + c.bm - 1) / c.bm) * ((s.npix + c.bn - 1) / c.bn) * p->groups;
   // split k ("Convolution, pooling and resize", split k for small grids): a
   // grid smaller than the device whose k has at least 256 terms runs k in at
-  // most 16 ranges of at least 128 terms, each a whole number of 8-term stages,
+  // most 16 ranges of at least 128 terms, each a whole number of stages,
   // aiming at about two blocks per SM; the cut is a function of (shape, SM
   // count) only.
   int split = 1;

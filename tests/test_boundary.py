@@ -213,7 +213,7 @@ def test_split_k_rule(lib):
     p = _layer_problem(L)
     a, b = conv.conv_plan(p, 152), conv.conv_plan(p, 148)
     assert a["split_k"] > 1 and b["split_k"] > 1
-    # every range but the last is a multiple of the 8-term stage; ranges cover k
+    # at most 16 ranges of at least 128 terms each (whole pipeline stages), covering k
     K = a["gemm_k"]
     per = -(-K // a["split_k"])
     assert a["split_k"] <= 16 and K / a["split_k"] >= 128
