@@ -72,14 +72,20 @@ def _check(case, extra_flags=0):
 
 
 def test_fixed_scratch_split_k_alternating_inputs():
-    """Split-k planes in the array: three calls, the middle one on another
-    shape and other values, each equal to conv_forward's bits."""
-    a = _case((1, 2048, 7, 7), (512, 2048, 1, 1), "f32", seed=41)
-    b = _case((1, 1024, 9, 9), (96, 1024, 3, 3), "f32", seed=42, flags=conv.FLAG_NO_WINOGRAD, pads=1, act="relu")
-    for c in (a, b):
+    """Split-k planes in the array (the planes form of the split, forced by
+    CONV_FLAG_NO_CLUSTER_K): calls alternating between two shapes and values,
+    each equal to conv_forward's bits; then the default form, whose ranges
+    are reduced within a thread-block cluster and leave the array unread."""
+    a = _case((1, 2048, 7, 7), (512, 2048, 1, 1), "f32", seed=41, flags=conv.FLAG_NO_CLUSTER_K)
+    b = _case((1, 1024, 9, 9), (96, 1024, 3, 3), "f32", seed=42,
+              flags=conv.FLAG_NO_WINOGRAD | conv.FLAG_NO_CLUSTER_K, pads=1, act="relu")
+    a_cluster = _case((1, 2048, 7, 7), (512, 2048, 1, 1), "f32", seed=49)
+    for c in (a, b, a_cluster):
         assert conv.conv_plan(c[0], torch.cuda.get_device_properties(0).multi_processor_count)["split_k"] > 1
         assert 0 < conv.conv_scratch_bytes(c[0]) <= conv.FIXED_SCRATCH_BYTES
-    for c in (a, b, a):
+    assert "reduce=planes" in conv.conv_describe_variant(a[0])
+    assert "reduce=cluster" in conv.conv_describe_variant(a_cluster[0])
+    for c in (a, b, a, a_cluster, b):
         _check(c)
 
 
