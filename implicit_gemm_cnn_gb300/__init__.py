@@ -23,7 +23,7 @@ __all__ = [
     "ConvError", "ConvLibraryError", "ConvProblem", "ConvPlanInfo", "ACTIVATIONS", "DTYPES",
     "FLAG_FORCE_FFMA", "FLAG_NO_SPLIT_K", "FLAG_NO_WINDOW", "FLAG_NO_UNFOLD", "FLAG_FORCE_UNFOLD", "FLAG_WINOGRAD",
     "FLAG_NO_WINOGRAD", "FLAG_NO_DW_MMA", "FLAG_NO_PW_MMA", "FLAG_NO_CLUSTER_K", "VARIANTS", "conv_abi_version", "conv_status_string",
-    "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
+    "conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant", "conv_describe_plan",
     "conv_forward", "conv_device_error", "conv_selftest_bounded_wait", "conv_forward_fixed_scratch",
     "FIXED_SCRATCH_BYTES",
     "conv_apply_auto_pad", "AUTO_PAD", "conv_scratch_bytes_per_image",
@@ -130,6 +130,7 @@ def load() -> ctypes.CDLL:
         lib.conv_plan.argtypes = [P(ConvProblem), ctypes.c_int32, P(ConvPlanInfo)]
         lib.conv_scratch_bytes.argtypes = [P(ConvProblem), P(ctypes.c_size_t)]
         lib.conv_describe_variant.argtypes = [P(ConvProblem), ctypes.c_char_p, ctypes.c_size_t]
+        lib.conv_describe_plan.argtypes = [P(ConvProblem), ctypes.c_int32, ctypes.c_char_p, ctypes.c_size_t]
         lib.conv_forward.argtypes = [P(ConvProblem), vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.conv_device_error.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         lib.conv_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P(ctypes.c_uint32)]
@@ -144,7 +145,7 @@ def load() -> ctypes.CDLL:
         lib.conv_integer_forward.argtypes = [P(ConvProblem), ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
                                              ctypes.c_int32, vp, vp, ctypes.c_size_t, vp]
         for f in ("conv_output_shape", "conv_plan", "conv_scratch_bytes", "conv_describe_variant",
-                  "conv_forward", "conv_device_error", "conv_selftest_bounded_wait",
+                  "conv_describe_plan", "conv_forward", "conv_device_error", "conv_selftest_bounded_wait",
                   "conv_forward_fixed_scratch", "conv_apply_auto_pad",
                   "conv_scratch_bytes_per_image", "conv_integer_scratch_bytes", "conv_integer_forward",
                   "conv_transpose_output_shape", "conv_transpose_scratch_bytes", "conv_transpose_forward"):
@@ -212,6 +213,14 @@ def conv_scratch_bytes_per_image(p: ConvProblem) -> int:
 def conv_describe_variant(p: ConvProblem) -> str:
     buf = ctypes.create_string_buffer(512)
     _check(load().conv_describe_variant(ctypes.byref(p), buf, len(buf)), "conv_describe_variant")
+    return buf.value.decode()
+
+
+def conv_describe_plan(p: ConvProblem, sm_count: int) -> str:
+    """conv_describe_variant's description for a device with ``sm_count`` SMs,
+    computed on the host only."""
+    buf = ctypes.create_string_buffer(512)
+    _check(load().conv_describe_plan(ctypes.byref(p), int(sm_count), buf, len(buf)), "conv_describe_plan")
     return buf.value.decode()
 
 

@@ -726,6 +726,15 @@ conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len) 
   int dev, sm;
   st = device_info(&dev, &sm);
   if (st != CONV_OK) return st;
+  return conv_describe_plan(p, sm, buf, len);
+}
+
+conv_status conv_describe_plan(const conv_problem* p, int32_t sm_count, char* buf, size_t len) {
+  if (!buf || !len) return CONV_ERR_NULL;
+  const int sm = sm_count;
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
   Plan plan;
   st = make_plan(p, sm, &plan, nullptr);
   if (st != CONV_OK) return st;

@@ -252,8 +252,20 @@ CONV_API conv_status conv_scratch_bytes_per_image(const conv_problem* p, size_t*
 
 /* Writes a one-line description of what conv_forward runs for `p` on the
  * current device into buf (NUL-terminated, truncated to len), ending with
- * "launches=N", the number of kernels one conv_forward call launches. */
+ * "launches=N", the number of kernels one conv_forward call launches
+ * ("Convolution, pooling and resize", Variants: the library reports which
+ * variant a problem runs). */
 CONV_API conv_status conv_describe_variant(const conv_problem* p, char* buf, size_t len);
+
+/* The same description for a device with `sm_count` SMs, on the host only
+ * (no device is touched): the plan conv_plan makes for (p, sm_count), in
+ * the words of conv_describe_variant.  Where the variant's choice depends on
+ * the device beyond its SM count (whether a thread-block cluster of the k
+ * ranges fits, checked when the call is launched) the description assumes
+ * the sm_103 case.
+ * Errors: CONV_ERR_NULL without buf or len, CONV_ERR_ARG for sm_count < 1,
+ * the shape errors of conv_plan. */
+CONV_API conv_status conv_describe_plan(const conv_problem* p, int32_t sm_count, char* buf, size_t len);
 
 /* Enqueue y = conv(x, w) + bias + residual, activated, on `stream`.
  *   x, w, y     device pointers (required);

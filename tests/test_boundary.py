@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 17, names
+    assert len(names) == 18, names
     for name in names:
         assert hasattr(lib, name), name           # dlsym succeeds
     assert conv.conv_abi_version() == 1
@@ -377,3 +377,67 @@ def test_auto_pad_c_abi_matches_oracle(lib):
     assert (p.pad_top, p.pad_left, p.pad_bottom, p.pad_right) == (1, 2, 3, 4)
     assert conv.STATUS[lib.conv_apply_auto_pad(ctypes.byref(p), 7)] == "CONV_ERR_ARG"
     assert conv.STATUS[lib.conv_apply_auto_pad(None, 1)] == "CONV_ERR_NULL"
+
+
+# ---- the description of a plan, on the host -----------------------------------
+def test_describe_plan_matches_plan(lib):
+    """conv_describe_plan (host only) names the planned variant, its blocks,
+    split and scratch as conv_plan reports them, and ends with the launch count."""
+    for name, L in LAYERS.items():
+        if name not in EXPECTED_VARIANT:
+            continue
+        p = _layer_problem(L)
+        plan = conv.conv_plan(p, 152)
+        desc = conv.conv_describe_plan(p, 152)
+        assert desc.split()[0] == plan["variant_name"] == EXPECTED_VARIANT[name], (name, desc)
+        assert desc.endswith(" launches=%d" % int(re.search(r"launches=(\d+)$", desc).group(1)))
+        assert "sms=152" in desc, desc
+        if plan["variant_name"].startswith("igemm_ffma") and "grouped" not in desc:
+            assert "split_k=%d" % plan["split_k"] in desc and "blocks=%d" % plan["ctas"] in desc, desc
+            assert "scratch=%d" % plan["scratch_bytes"] in desc, desc
+        assert conv.conv_describe_plan(p, 152) == desc      # a pure function of (problem, SMs)
+
+
+def test_describe_plan_launch_counts(lib):
+    """Kernels one call launches, per variant: the shifted-window kernel and its
+    weight repack 2, Winograd's transforms and products 4, the unfolded CUDA-core
+    path (pre-pass, kernel, tail reduction) 3, a single kernel otherwise."""
+    want = {"resnet50_stem_f16": 2, "resnet50_3x3_f16": 2, "resnet50_1x1_res_f16": 2,
+            "mbv3_dw5x5_f32": 1, "mbv3_dw5x5_f16": 1, "mbv3_pw1x1_f16": 1, "mbv3_pw1x1_f32": 1,
+            "grouped_dil2_f32": 1, "small_3x3_f32": 1, "strided_3x3_s2_f32": 3,
+            "resnet50_3x3_256_f32": 4}
+    for name, n in want.items():
+        desc = conv.conv_describe_plan(_layer_problem(LAYERS[name]), 152)
+        assert desc.endswith("launches=%d" % n), (name, desc)
+
+
+def test_describe_plan_split_k_reduction(lib):
+    """Split k: the ranges of a tile reduced within a thread-block cluster (one
+    launch) up to 16 ranges; the float32 planes and a second kernel under
+    CONV_FLAG_NO_CLUSTER_K or past 16 ranges."""
+    L = LAYERS["late_1x1_splitk_f32"]
+    desc = conv.conv_describe_plan(_layer_problem(L), 152)
+    assert "split_k=16 reduce=cluster" in desc and desc.endswith("launches=1"), desc
+    desc = conv.conv_describe_plan(_layer_problem(L, flags=conv.FLAG_NO_CLUSTER_K), 152)
+    assert "split_k=16 reduce=planes" in desc and desc.endswith("launches=2"), desc
+    desc = conv.conv_describe_plan(_layer_problem(L, flags=32 << conv.SPLIT_K_SHIFT), 152)
+    assert "split_k=32 reduce=planes" in desc and desc.endswith("launches=2"), desc
+    desc = conv.conv_describe_plan(_layer_problem(L, flags=conv.FLAG_NO_SPLIT_K), 152)
+    assert "split_k=1 " in desc and "reduce=" not in desc and desc.endswith("launches=1"), desc
+    # the plan (and so the scratch figure) does not depend on the reduction's form
+    a = conv.conv_plan(_layer_problem(L), 152)
+    b = conv.conv_plan(_layer_problem(L, flags=conv.FLAG_NO_CLUSTER_K), 152)
+    assert a == b
+
+
+def test_describe_plan_errors(lib):
+    p = _layer_problem(LAYERS["small_3x3_f32"])
+    buf = ctypes.create_string_buffer(64)
+    assert lib.conv_describe_plan(ctypes.byref(p), 0, buf, len(buf)) == 10           # CONV_ERR_ARG
+    assert lib.conv_describe_plan(ctypes.byref(p), 152, None, 0) == 5               # CONV_ERR_NULL
+    short = ctypes.create_string_buffer(8)
+    assert lib.conv_describe_plan(ctypes.byref(p), 152, short, len(short)) == 0     # truncated, terminated
+    assert len(short.value) == 7
+    bad = conv.make_problem((1, 3, 2, 2), (16, 3, 3, 3))                            # no output position
+    with pytest.raises(conv.ConvError):
+        conv.conv_describe_plan(bad, 152)
